@@ -1,0 +1,257 @@
+/*
+ * fp8lin.h -- C ABI of libfp8lin, the float8 training Linear with tensorwise
+ * scaling on one GB300 (sm_103a).
+ *
+ * What the library computes (the hot path of the float8 training Linear that
+ * replaces nn.Linear in "Why swapping nn.Linear with FP8Linear brings
+ * throughput decrease for 7B LLAMA2-like model?" (pytorch/ao issue 1199)):
+ *
+ *   amax   a     = max |t|                      over a bf16 tensor t
+ *   scale  s     = fl32(F / max(a, eps)),  inv = fl32(1 / s)
+ *                  F = 448 (e4m3: input, weight) or 57344 (e5m2: grad_output)
+ *   cast   q     = sat_rne_fp8(fl32(t * s)), plus the transposed copy q^T
+ *   GEMMs  y     = (x8  . W8^T)  * inv_x  * inv_w     -> bf16 [M, N]
+ *          dX    = (dY8 . W8)    * inv_dy * inv_w     -> bf16 [M, K]
+ *          dW    = (dY8^T . x8)  * inv_dy * inv_x     -> bf16 [N, K]
+ *   with fp32 accumulation on the tensor cores.
+ *
+ * Sources, by page and section:
+ *   - "Integrate float8nocompile, an experimental feature for high
+ *     performance" (pytorch/torchtitan PR 778), Summary: tensorwise dynamic
+ *     scaling with hand-written conversion kernels; "Benchmarking single
+ *     linear layer forward+backward performance": the two amax algorithms
+ *     (KernelAlgorithm.ATOMIC_MAX, KernelAlgorithm.REDUCTION) and the
+ *     forward+backward scope of one Linear.
+ *   - "[float8] FP8 GPT 1.5B Delayed Scaling 2x Slower than BF16"
+ *     (pytorch/ao issue 1297), repro script: Float8LinearConfig with
+ *     CastConfig(scaling_type=ScalingType.DELAYED) per tensor role,
+ *     enable_amax_init, and sync_float8_amax_and_scale_history(model) after
+ *     loss.backward().
+ * The pages print no numerics; the formulas above are the plain reading
+ * (formats e4m3/e5m2 with saturation to the largest finite value,
+ * round-to-nearest-even, no power-of-two rounding of the scale).
+ *
+ * Conventions for every entry point:
+ *   - Layout: row-major. A "[R, C] bf16 tensor with row stride ld" has
+ *     element (i, j) at ((const uint16_t*)p)[i * ld + j].  fp8 outputs are
+ *     dense row-major bytes (row stride = number of columns).  W is [N, K]
+ *     (out_features x in_features) as in nn.Linear.
+ *   - Ownership: every pointer is a caller-owned DEVICE pointer (except the
+ *     fp8lin_scaling_state struct itself, which lives in host memory).  The
+ *     library allocates no device memory and keeps no per-call state.
+ *   - Asynchrony: every call enqueues work on `stream` and returns without
+ *     synchronising; scalars (amax, scale, ...) stay on the device.
+ *   - Errors: arguments are checked before anything is enqueued; a bad call
+ *     returns FP8LIN_EINVAL (null/misaligned pointer, negative size, stride
+ *     smaller than the row) or FP8LIN_EUNSUPPORTED (shape or format the
+ *     kernels do not take) and enqueues nothing.  A failed launch returns
+ *     FP8LIN_ECUDA (fp8lin_last_cuda_error() gives the cudaError_t).
+ *     Device-side waits are bounded: a wait that runs out records a code in
+ *     the workspace and the kernel returns; fp8lin_check() reports it as
+ *     FP8LIN_ETIMEOUT.  Nothing traps on the device.
+ *   - Alignment: every device pointer 16-byte aligned; bf16 row strides a
+ *     multiple of 8 elements; columns a multiple of 16; rows a multiple of 16
+ *     wherever a transposed copy (or a GEMM operand) has them as its row
+ *     length.  In practice: M, K, N multiples of 16.
+ *   - Inputs are NaN-free by contract; NaN propagation is not specified.
+ */
+#ifndef FP8LIN_H
+#define FP8LIN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FP8LIN_OK = 0,
+  FP8LIN_EINVAL = 1,        /* bad argument; nothing enqueued */
+  FP8LIN_EUNSUPPORTED = 2,  /* valid but not handled (shape/format/size); nothing enqueued */
+  FP8LIN_ECUDA = 3,         /* a CUDA call failed; see fp8lin_last_cuda_error() */
+  FP8LIN_ETIMEOUT = 4       /* a bounded device wait ran out (reported by fp8lin_check) */
+} fp8lin_status;
+
+/* 8-bit formats: e4m3 (max 448, no infinity) for input and weight, e5m2 (max
+ * 57344) for grad_output. */
+typedef enum { FP8LIN_E4M3 = 0, FP8LIN_E5M2 = 1 } fp8lin_fmt;
+
+/* amax algorithms, after the KernelAlgorithm choice of the single-linear
+ * benchmark table in "Integrate float8nocompile ..." (torchtitan PR 778):
+ *   ATOMIC      one pass; each CTA folds its block maximum into the result
+ *               with one atomic max;
+ *   REDUCTION   each CTA writes its partial maximum to the workspace and a
+ *               second, one-CTA kernel reduces them;
+ *   SINGLE_PASS (dynamic scaling only, fp8lin_forward/backward/cast_fused)
+ *               amax -> scale -> cast (+transpose) in one cooperative launch
+ *               that keeps the bf16 tensor on chip between the phases; only
+ *               for tensors that fit (fp8lin_single_pass_max_elems()); larger
+ *               tensors fall back to ATOMIC inside forward/backward. */
+typedef enum {
+  FP8LIN_AMAX_ATOMIC = 0,
+  FP8LIN_AMAX_REDUCTION = 1,
+  FP8LIN_AMAX_SINGLE_PASS = 2
+} fp8lin_amax_algo;
+
+/* Scaling type per tensor, after CastConfig(scaling_type=...) in the repro
+ * script of "[float8] FP8 GPT 1.5B Delayed Scaling 2x Slower than BF16". */
+typedef enum { FP8LIN_DYNAMIC = 0, FP8LIN_DELAYED = 1 } fp8lin_scaling;
+
+/* Per-tensor scaling state.  The struct is host memory; the pointers in it
+ * are caller-owned device buffers (fp32 / int32).
+ *   amax          fp32[1]  amax of the tensor last cast with this state
+ *   scale         fp32[1]  scale the next cast uses (delayed) / last used (dynamic)
+ *   inv_scale     fp32[1]  fl32(1 / scale), folded into the GEMM epilogues
+ *   amax_history  fp32[history_len]  delayed only: ring of past amaxes, zero-filled
+ *                 by the caller before the first step
+ *   head          int32[1] delayed only: next ring slot, 0 before the first step
+ *   history_len   delayed only: ring length H >= 1
+ *   fmt           fp8lin_fmt of the cast
+ *   kind          fp8lin_scaling
+ *   amax_algo     fp8lin_amax_algo used by fp8lin_forward/backward
+ *   needs_init    delayed only, host flag: when nonzero the next forward or
+ *                 backward cast first takes the scale from the tensor's own
+ *                 amax (enable_amax_init in the repro script) without
+ *                 touching the ring, and the library then sets it to 0
+ *   eps           floor of the amax in the scale (1e-12 is the usual value) */
+typedef struct fp8lin_scaling_state {
+  float* amax;
+  float* scale;
+  float* inv_scale;
+  float* amax_history;
+  int32_t* head;
+  int32_t history_len;
+  int32_t fmt;
+  int32_t kind;
+  int32_t amax_algo;
+  int32_t needs_init;
+  float eps;
+} fp8lin_scaling_state;
+
+/* ---- library information ------------------------------------------- */
+
+/* Human-readable name of a status code (static string). */
+const char* fp8lin_status_string(int status);
+
+/* cudaError_t of the last failed CUDA call made by this thread (0 if none). */
+int fp8lin_last_cuda_error(void);
+
+/* ABI version: 100 * major + minor. */
+int fp8lin_version(void);
+
+/* Bytes of workspace `ws` the calls below need for these Linear sizes.  The
+ * workspace is caller-owned device memory, 256-byte aligned, zero-filled by
+ * the caller ONCE after allocation; the library keeps it consistent after
+ * that.  Calls that share one workspace must not overlap on the GPU. */
+size_t fp8lin_workspace_bytes(int64_t M, int64_t K, int64_t N);
+
+/* Largest tensor (elements) FP8LIN_AMAX_SINGLE_PASS handles on the current
+ * device (0 if the device cannot run it). */
+int64_t fp8lin_single_pass_max_elems(void);
+
+/* Synchronise `stream`, then read and clear the workspace's device error
+ * record.  Returns FP8LIN_OK, FP8LIN_ETIMEOUT (a bounded wait ran out) or
+ * FP8LIN_ECUDA. */
+fp8lin_status fp8lin_check(void* ws, cudaStream_t stream);
+
+/* ---- steps of the path ---------------------------------------------- */
+
+/* amax (row a1 of the path): *amax_out = max |x[i, j]| over the bf16
+ * [rows, cols] tensor x with row stride ld, as fp32 (exact: the maximum of
+ * bf16 magnitudes widened to fp32).  An empty tensor gives 0.
+ * algo: FP8LIN_AMAX_ATOMIC or FP8LIN_AMAX_REDUCTION (same bits).
+ * ws: workspace (REDUCTION keeps its partial maxima there).
+ * Source: "Integrate float8nocompile ..." (torchtitan PR 778), Summary and
+ * the single-linear benchmark table (ATOMIC_MAX / REDUCTION). */
+fp8lin_status fp8lin_amax(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                          float* amax_out, int32_t algo, void* ws, cudaStream_t stream);
+
+/* scale (rows a2 / a2' of the path).  Dynamic: reads *st->amax and writes
+ * scale = fl32(F / max(amax, eps)) and inv_scale = fl32(1 / scale).
+ * Delayed: ring[head] = *amax; head = (head + 1) % H; then the same formula
+ * on max(ring) -- the per-tensor work of sync_float8_amax_and_scale_history
+ * after backward in "[float8] FP8 GPT 1.5B Delayed Scaling 2x Slower than
+ * BF16" (pytorch/ao issue 1297), repro script. */
+fp8lin_status fp8lin_scale(const fp8lin_scaling_state* st, cudaStream_t stream);
+
+/* cast (row a3): out[i, j] = sat_rne_fp8(fl32(x[i, j] * (*scale))) into the
+ * dense [rows, cols] byte array out; if out_t is not NULL also
+ * out_t[j, i] = out[i, j] (dense [cols, rows]).  If amax_out is not NULL the
+ * amax of x is recorded in the same pass (delayed scaling's single pass).
+ * fmt: fp8lin_fmt.  out may be NULL when out_t is not.
+ * Source: "Integrate float8nocompile ..." (torchtitan PR 778), Summary
+ * (float8 conversion kernels). */
+fp8lin_status fp8lin_cast(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                          int32_t fmt, const float* scale, uint8_t* out, uint8_t* out_t,
+                          float* amax_out, cudaStream_t stream);
+
+/* Dynamic scaling in one call: amax -> scale -> cast (+ transpose) with
+ * st->amax_algo (ATOMIC, REDUCTION or SINGLE_PASS); writes *st->amax,
+ * *st->scale, *st->inv_scale, out and (if not NULL) out_t.  st->kind must
+ * be FP8LIN_DYNAMIC.  SINGLE_PASS returns FP8LIN_EUNSUPPORTED (nothing
+ * enqueued) for tensors above fp8lin_single_pass_max_elems(). */
+fp8lin_status fp8lin_cast_dynamic(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                  const fp8lin_scaling_state* st, uint8_t* out,
+                                  uint8_t* out_t, void* ws, cudaStream_t stream);
+
+/* FP8 GEMM (rows a4-a6): d[m, n] = bf16( (sum_k A[m, k] * B[n, k]) *
+ * fl32(inv_a * inv_b) ), accumulated in fp32 on the tensor cores.
+ * a: fp8 [M, K] row stride lda bytes; b: fp8 [N, K] row stride ldb bytes
+ * (both with the contraction index fastest); fmt_a, fmt_b: fp8lin_fmt;
+ * inv_a, inv_b: device fp32[1]; d: bf16 [M, N] row stride ldd elements.
+ * K == 0 writes zeros.  Requires lda, ldb multiples of 16, ldd a multiple
+ * of 8, N and K multiples of 16. */
+fp8lin_status fp8lin_gemm(const uint8_t* a, const uint8_t* b, int64_t M, int64_t N, int64_t K,
+                          int64_t lda, int64_t ldb, int32_t fmt_a, int32_t fmt_b,
+                          const float* inv_a, const float* inv_b, void* d, int64_t ldd,
+                          void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Forward of the Linear: amax/scale/cast of x ([M, K], e4m3, state sx) and
+ * W ([N, K], e4m3, state sw), then y = x8 . W8^T * inv_x * inv_w (bf16
+ * [M, N]).  Writes the fp8 copies x8 [M, K], x8t [K, M], w8 [N, K],
+ * w8t [K, N]; x8t and w8t are what fp8lin_backward needs.  Dynamic states
+ * take their scale from this call's amax; delayed states cast with their
+ * stored scale and record this call's amax (and do the amax init first when
+ * needs_init is set).  All buffers dense row-major. */
+fp8lin_status fp8lin_forward(const void* x, const void* w, int64_t M, int64_t K, int64_t N,
+                             fp8lin_scaling_state* sx, fp8lin_scaling_state* sw,
+                             void* y, uint8_t* x8, uint8_t* x8t, uint8_t* w8, uint8_t* w8t,
+                             void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Backward of the Linear: amax/scale/cast of dY ([M, N], e5m2, state sdy)
+ * into dy8 [M, N] and dy8t [N, M], then
+ *   dX = dY8 . W8 * inv_dy * inv_w     (bf16 [M, K], skipped if dx == NULL)
+ *   dW = dY8^T . x8 * inv_dy * inv_x   (bf16 [N, K], skipped if dw == NULL)
+ * from the x8t / w8t written by fp8lin_forward and the inv_scale of sx, sw. */
+fp8lin_status fp8lin_backward(const void* dy, int64_t M, int64_t K, int64_t N,
+                              const uint8_t* x8t, const uint8_t* w8t,
+                              const fp8lin_scaling_state* sx, const fp8lin_scaling_state* sw,
+                              fp8lin_scaling_state* sdy, uint8_t* dy8, uint8_t* dy8t,
+                              void* dx, void* dw, void* ws, size_t ws_bytes,
+                              cudaStream_t stream);
+
+/* ---- measurement hooks ------------------------------------------------ */
+
+/* Count of kernels this library has launched in the process. */
+uint64_t fp8lin_launch_count(void);
+
+/* Kernel timing: while enabled, every kernel launch of the library is
+ * bracketed by a pair of CUDA events on its stream (up to a fixed number of
+ * pairs).  fp8lin_profile_collect() synchronises those events, adds up the
+ * milliseconds per kernel kind into ms[kind] and launches into count[kind]
+ * (arrays of FP8LIN_PROF_KINDS entries), and clears the record.  Not
+ * thread-safe; not for use under CUDA graph capture. */
+enum {
+  FP8LIN_PROF_AMAX = 0, FP8LIN_PROF_SCALE = 1, FP8LIN_PROF_CAST = 2,
+  FP8LIN_PROF_CAST_FUSED = 3, FP8LIN_PROF_GEMM = 4, FP8LIN_PROF_KINDS = 5
+};
+void fp8lin_profile_enable(int on);
+fp8lin_status fp8lin_profile_collect(double* ms, int64_t* count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8LIN_H */

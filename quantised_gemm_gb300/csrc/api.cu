@@ -1,0 +1,557 @@
+// api.cu -- the C ABI of libfp8lin: argument checks, orchestration of the
+// forward and backward of the fp8 Linear on the caller's stream, workspace
+// layout, error reporting and the measurement hooks.  No device memory is
+// allocated here; every buffer comes from the caller.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <initializer_list>
+#include <mutex>
+
+#include "../../include/fp8lin.h"
+#include "internal.h"
+
+namespace fp8lin {
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+std::atomic<uint64_t> g_launches{0};
+
+fp8lin_status cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return FP8LIN_ECUDA;
+}
+
+// ---------------------------------------------------------------- profiling
+
+constexpr int kProfPairs = 8192;
+struct ProfRecord {
+  cudaEvent_t start, stop;
+  int kind;
+};
+bool g_prof_on = false;
+int g_prof_used = 0;
+ProfRecord g_prof[kProfPairs];
+bool g_prof_created[kProfPairs];
+
+struct ProfScope {
+  ProfRecord* rec = nullptr;
+  cudaStream_t stream;
+  ProfScope(int kind, cudaStream_t s) : stream(s) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (!g_prof_on || g_prof_used >= kProfPairs) return;
+    const int i = g_prof_used;
+    if (!g_prof_created[i]) {
+      if (cudaEventCreate(&g_prof[i].start) != cudaSuccess) return;
+      if (cudaEventCreate(&g_prof[i].stop) != cudaSuccess) return;
+      g_prof_created[i] = true;
+    }
+    rec = &g_prof[i];
+    rec->kind = kind;
+    ++g_prof_used;
+    cudaEventRecord(rec->start, stream);
+  }
+  ~ProfScope() {
+    if (rec) cudaEventRecord(rec->stop, stream);
+  }
+};
+
+// ---------------------------------------------------------------- helpers
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int* ws_error(void* ws) {
+  return reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + kWsErrorOffset);
+}
+uint32_t* ws_u32(void* ws, size_t off) {
+  return reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + off);
+}
+
+bool valid_fmt(int32_t f) { return f == FP8LIN_E4M3 || f == FP8LIN_E5M2; }
+
+// Checks shared by amax and cast: bf16 [rows, cols] with row stride ld.
+fp8lin_status check_bf16(const void* x, int64_t rows, int64_t cols, int64_t ld) {
+  if (rows < 0 || cols < 0) return FP8LIN_EINVAL;
+  if (rows == 0 || cols == 0) return FP8LIN_OK;
+  if (x == nullptr || !aligned16(x)) return FP8LIN_EINVAL;
+  if (ld < cols) return FP8LIN_EINVAL;
+  if (cols % 16 != 0 || ld % 8 != 0) return FP8LIN_EUNSUPPORTED;
+  if (rows > (int64_t(1) << 31) || cols > (int64_t(1) << 31)) return FP8LIN_EUNSUPPORTED;
+  return FP8LIN_OK;
+}
+
+fp8lin_status check_state(const fp8lin_scaling_state* st, bool need_delayed_buffers) {
+  if (st == nullptr) return FP8LIN_EINVAL;
+  if (!valid_fmt(st->fmt)) return FP8LIN_EUNSUPPORTED;
+  if (st->kind != FP8LIN_DYNAMIC && st->kind != FP8LIN_DELAYED) return FP8LIN_EUNSUPPORTED;
+  if (st->amax == nullptr || st->scale == nullptr || st->inv_scale == nullptr)
+    return FP8LIN_EINVAL;
+  if (!(st->eps > 0.0f)) return FP8LIN_EINVAL;
+  if (st->kind == FP8LIN_DELAYED && need_delayed_buffers) {
+    if (st->history_len < 1) return FP8LIN_EINVAL;
+    if (st->amax_history == nullptr || st->head == nullptr) return FP8LIN_EINVAL;
+  }
+  if (st->amax_algo < FP8LIN_AMAX_ATOMIC || st->amax_algo > FP8LIN_AMAX_SINGLE_PASS)
+    return FP8LIN_EUNSUPPORTED;
+  return FP8LIN_OK;
+}
+
+// amax into a device fp32 (ATOMIC or REDUCTION).
+fp8lin_status do_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, float* amax_out,
+                      int32_t algo, void* ws, const DeviceInfo& dev, cudaStream_t stream) {
+  uint32_t* out_bits = reinterpret_cast<uint32_t*>(amax_out);
+  if (rows == 0 || cols == 0) {
+    cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), stream);
+    return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);
+  }
+  const int grid = amax_grid(dev, rows, cols);
+  if (algo == FP8LIN_AMAX_REDUCTION) {
+    uint32_t* part = ws_u32(ws, kWsPartialOffset);
+    {
+      ProfScope ps(FP8LIN_PROF_AMAX, stream);
+      cudaError_t e = launch_amax(static_cast<const uint16_t*>(x), rows, cols, ld, part, false,
+                                  grid, stream);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    ProfScope ps(FP8LIN_PROF_AMAX, stream);
+    cudaError_t e = launch_amax_final(part, grid, out_bits, stream);
+    return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);
+  }
+  cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  ProfScope ps(FP8LIN_PROF_AMAX, stream);
+  e = launch_amax(static_cast<const uint16_t*>(x), rows, cols, ld, out_bits, true, grid, stream);
+  return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);
+}
+
+fp8lin_status do_cast(const CastArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
+  if (a.rows == 0 || a.cols == 0) return FP8LIN_OK;
+  ProfScope ps(FP8LIN_PROF_CAST, stream);
+  cudaError_t e = launch_cast(a, dev, stream);
+  return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);
+}
+
+// Dynamic scaling of one tensor: amax -> scale -> cast (+T) per st->amax_algo.
+// SINGLE_PASS falls back to ATOMIC when the tensor does not fit on chip and
+// `allow_fallback` is set.
+fp8lin_status cast_dynamic_scaled(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                           const fp8lin_scaling_state* st, uint8_t* out, uint8_t* out_t, void* ws,
+                           const DeviceInfo& dev, cudaStream_t stream, bool allow_fallback) {
+  int32_t algo = st->amax_algo;
+  if (algo == FP8LIN_AMAX_SINGLE_PASS && rows > 0 && cols > 0) {
+    if (single_pass_fits(dev, rows, cols)) {
+      cudaError_t e = cudaMemsetAsync(ws_u32(ws, kWsBarrierOffset), 0,
+                                      kWsPartialOffset - kWsBarrierOffset, stream);
+      if (e != cudaSuccess) return cuda_fail(e);
+      SinglePassArgs sp;
+      sp.x = static_cast<const uint16_t*>(x);
+      sp.rows = rows;
+      sp.cols = cols;
+      sp.ld = ld;
+      sp.fmt = st->fmt;
+      sp.eps = st->eps;
+      sp.amax_out = st->amax;
+      sp.scale_out = st->scale;
+      sp.inv_out = st->inv_scale;
+      sp.out = out;
+      sp.out_t = out_t;
+      sp.ws_barrier = ws_u32(ws, kWsBarrierOffset);
+      sp.ws_amax = ws_u32(ws, kWsAmaxOffset);
+      sp.ws_error = ws_error(ws);
+      ProfScope ps(FP8LIN_PROF_CAST_FUSED, stream);
+      e = launch_cast_single_pass(sp, dev, stream);
+      return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);
+    }
+    if (!allow_fallback) return FP8LIN_EUNSUPPORTED;
+    algo = FP8LIN_AMAX_ATOMIC;
+  }
+  fp8lin_status s = do_amax(x, rows, cols, ld, st->amax, algo, ws, dev, stream);
+  if (s != FP8LIN_OK) return s;
+  if (rows == 0 || cols == 0) {
+    ProfScope ps(FP8LIN_PROF_SCALE, stream);
+    cudaError_t e = launch_scale(st->amax, st->scale, st->inv_scale, nullptr, nullptr, 1, false,
+                                 st->fmt, st->eps, stream);
+    return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);
+  }
+  CastArgs c;
+  c.x = static_cast<const uint16_t*>(x);
+  c.rows = rows;
+  c.cols = cols;
+  c.ld = ld;
+  c.fmt = st->fmt;
+  c.scale_in = nullptr;
+  c.amax_in = st->amax;
+  c.derive_scale = true;
+  c.eps = st->eps;
+  c.scale_out = st->scale;
+  c.inv_out = st->inv_scale;
+  c.out = out;
+  c.out_t = out_t;
+  c.amax_rec = nullptr;
+  return do_cast(c, dev, stream);
+}
+
+// Delayed scaling of one tensor inside forward/backward: cast with the stored
+// scale and record this tensor's amax in the same pass; on the first step
+// (needs_init) take the scale from the tensor's own amax first.
+fp8lin_status delayed_cast(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                           fp8lin_scaling_state* st, uint8_t* out, uint8_t* out_t, void* ws,
+                           const DeviceInfo& dev, cudaStream_t stream) {
+  if (st->needs_init) {
+    fp8lin_status s = do_amax(x, rows, cols, ld, st->amax, FP8LIN_AMAX_ATOMIC, ws, dev, stream);
+    if (s != FP8LIN_OK) return s;
+    ProfScope ps(FP8LIN_PROF_SCALE, stream);
+    cudaError_t e = launch_scale(st->amax, st->scale, st->inv_scale, nullptr, nullptr, 1, false,
+                                 st->fmt, st->eps, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    st->needs_init = 0;
+  }
+  cudaError_t e = cudaMemsetAsync(st->amax, 0, sizeof(float), stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (rows == 0 || cols == 0) return FP8LIN_OK;
+  CastArgs c;
+  c.x = static_cast<const uint16_t*>(x);
+  c.rows = rows;
+  c.cols = cols;
+  c.ld = ld;
+  c.fmt = st->fmt;
+  c.scale_in = st->scale;
+  c.amax_in = nullptr;
+  c.derive_scale = false;
+  c.eps = st->eps;
+  c.scale_out = nullptr;
+  c.inv_out = nullptr;
+  c.out = out;
+  c.out_t = out_t;
+  c.amax_rec = reinterpret_cast<uint32_t*>(st->amax);
+  return do_cast(c, dev, stream);
+}
+
+fp8lin_status do_gemm(const uint8_t* a, const uint8_t* b, int64_t M, int64_t N, int64_t K,
+                      int64_t lda, int64_t ldb, int32_t fa, int32_t fb, const float* inv_a,
+                      const float* inv_b, void* d, int64_t ldd, void* ws, const DeviceInfo& dev,
+                      cudaStream_t stream) {
+  if (M == 0 || N == 0) return FP8LIN_OK;
+  if (K == 0) {
+    cudaError_t e = cudaMemset2DAsync(d, static_cast<size_t>(ldd) * 2, 0,
+                                      static_cast<size_t>(N) * 2, static_cast<size_t>(M), stream);
+    return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);
+  }
+  GemmArgs g;
+  g.a = a;
+  g.b = b;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.lda = lda;
+  g.ldb = ldb;
+  g.fmt_a = fa;
+  g.fmt_b = fb;
+  g.inv_a = inv_a;
+  g.inv_b = inv_b;
+  g.d = d;
+  g.ldd = ldd;
+  g.ws_error = ws_error(ws);
+  ProfScope ps(FP8LIN_PROF_GEMM, stream);
+  cudaError_t e = launch_gemm(g, dev, stream);
+  return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);
+}
+
+fp8lin_status get_dev(DeviceInfo* dev) {
+  cudaError_t e = current_device_info(dev);
+  return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);
+}
+
+bool ws_ok(const void* ws) {
+  return ws != nullptr && (reinterpret_cast<uintptr_t>(ws) & 255u) == 0;
+}
+
+}  // namespace
+
+cudaError_t current_device_info(DeviceInfo* info) {
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  static bool have[64] = {};
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) return e;
+  if (d < 0 || d >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!have[d]) {
+    DeviceInfo x;
+    x.device = d;
+    e = cudaDeviceGetAttribute(&x.num_sms, cudaDevAttrMultiProcessorCount, d);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&x.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
+    if (e != cudaSuccess) return e;
+    cache[d] = x;
+    have[d] = true;
+  }
+  *info = cache[d];
+  return cudaSuccess;
+}
+
+}  // namespace fp8lin
+
+using namespace fp8lin;
+
+extern "C" {
+
+const char* fp8lin_status_string(int status) {
+  switch (status) {
+    case FP8LIN_OK: return "FP8LIN_OK";
+    case FP8LIN_EINVAL: return "FP8LIN_EINVAL: invalid argument";
+    case FP8LIN_EUNSUPPORTED: return "FP8LIN_EUNSUPPORTED: shape, format or size not supported";
+    case FP8LIN_ECUDA: return "FP8LIN_ECUDA: a CUDA call failed";
+    case FP8LIN_ETIMEOUT: return "FP8LIN_ETIMEOUT: a bounded device wait ran out";
+    default: return "unknown fp8lin status";
+  }
+}
+
+int fp8lin_last_cuda_error(void) { return g_last_cuda_error; }
+
+int fp8lin_version(void) { return 100; }
+
+size_t fp8lin_workspace_bytes(int64_t M, int64_t K, int64_t N) {
+  (void)M;
+  (void)K;
+  (void)N;
+  return kWsFixedBytes;
+}
+
+int64_t fp8lin_single_pass_max_elems(void) {
+  DeviceInfo dev;
+  if (current_device_info(&dev) != cudaSuccess) return 0;
+  return single_pass_capacity_elems(dev);
+}
+
+fp8lin_status fp8lin_check(void* ws, cudaStream_t stream) {
+  if (!ws_ok(ws)) return FP8LIN_EINVAL;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  int code = 0;
+  e = cudaMemcpy(&code, ws_error(ws), sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (code == 0) return FP8LIN_OK;
+  e = cudaMemset(ws_error(ws), 0, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FP8LIN_ETIMEOUT;
+}
+
+fp8lin_status fp8lin_amax(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                          float* amax_out, int32_t algo, void* ws, cudaStream_t stream) {
+  fp8lin_status s = check_bf16(x, rows, cols, ld);
+  if (s != FP8LIN_OK) return s;
+  if (amax_out == nullptr || (reinterpret_cast<uintptr_t>(amax_out) & 3u)) return FP8LIN_EINVAL;
+  if (algo != FP8LIN_AMAX_ATOMIC && algo != FP8LIN_AMAX_REDUCTION) return FP8LIN_EUNSUPPORTED;
+  if (algo == FP8LIN_AMAX_REDUCTION && !ws_ok(ws)) return FP8LIN_EINVAL;
+  DeviceInfo dev;
+  if ((s = get_dev(&dev)) != FP8LIN_OK) return s;
+  return do_amax(x, rows, cols, ld, amax_out, algo, ws, dev, stream);
+}
+
+fp8lin_status fp8lin_scale(const fp8lin_scaling_state* st, cudaStream_t stream) {
+  fp8lin_status s = check_state(st, true);
+  if (s != FP8LIN_OK) return s;
+  const bool delayed = st->kind == FP8LIN_DELAYED;
+  ProfScope ps(FP8LIN_PROF_SCALE, stream);
+  cudaError_t e = launch_scale(st->amax, st->scale, st->inv_scale, st->amax_history, st->head,
+                               delayed ? st->history_len : 1, delayed, st->fmt, st->eps, stream);
+  return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);
+}
+
+fp8lin_status fp8lin_cast(const void* x, int64_t rows, int64_t cols, int64_t ld, int32_t fmt,
+                          const float* scale, uint8_t* out, uint8_t* out_t, float* amax_out,
+                          cudaStream_t stream) {
+  fp8lin_status s = check_bf16(x, rows, cols, ld);
+  if (s != FP8LIN_OK) return s;
+  if (!valid_fmt(fmt)) return FP8LIN_EUNSUPPORTED;
+  if (scale == nullptr) return FP8LIN_EINVAL;
+  if (out == nullptr && out_t == nullptr) return FP8LIN_EINVAL;
+  if (out != nullptr && !aligned16(out)) return FP8LIN_EINVAL;
+  if (out_t != nullptr) {
+    if (!aligned16(out_t)) return FP8LIN_EINVAL;
+    if (rows % 16 != 0) return FP8LIN_EUNSUPPORTED;
+  }
+  DeviceInfo dev;
+  if ((s = get_dev(&dev)) != FP8LIN_OK) return s;
+  if (amax_out != nullptr) {
+    cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  CastArgs c;
+  c.x = static_cast<const uint16_t*>(x);
+  c.rows = rows;
+  c.cols = cols;
+  c.ld = ld;
+  c.fmt = fmt;
+  c.scale_in = scale;
+  c.amax_in = nullptr;
+  c.derive_scale = false;
+  c.eps = 1e-12f;
+  c.scale_out = nullptr;
+  c.inv_out = nullptr;
+  c.out = out;
+  c.out_t = out_t;
+  c.amax_rec = reinterpret_cast<uint32_t*>(amax_out);
+  return do_cast(c, dev, stream);
+}
+
+fp8lin_status fp8lin_cast_dynamic(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                  const fp8lin_scaling_state* st, uint8_t* out, uint8_t* out_t,
+                                  void* ws, cudaStream_t stream) {
+  fp8lin_status s = check_bf16(x, rows, cols, ld);
+  if (s != FP8LIN_OK) return s;
+  if ((s = check_state(st, false)) != FP8LIN_OK) return s;
+  if (st->kind != FP8LIN_DYNAMIC) return FP8LIN_EINVAL;
+  if (!ws_ok(ws)) return FP8LIN_EINVAL;
+  if (out == nullptr && out_t == nullptr) return FP8LIN_EINVAL;
+  if (out != nullptr && !aligned16(out)) return FP8LIN_EINVAL;
+  if (out_t != nullptr) {
+    if (!aligned16(out_t)) return FP8LIN_EINVAL;
+    if (rows % 16 != 0) return FP8LIN_EUNSUPPORTED;
+  }
+  DeviceInfo dev;
+  if ((s = get_dev(&dev)) != FP8LIN_OK) return s;
+  return cast_dynamic_scaled(x, rows, cols, ld, st, out, out_t, ws, dev, stream, false);
+}
+
+fp8lin_status fp8lin_gemm(const uint8_t* a, const uint8_t* b, int64_t M, int64_t N, int64_t K,
+                          int64_t lda, int64_t ldb, int32_t fmt_a, int32_t fmt_b,
+                          const float* inv_a, const float* inv_b, void* d, int64_t ldd,
+                          void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (M < 0 || N < 0 || K < 0) return FP8LIN_EINVAL;
+  if (!valid_fmt(fmt_a) || !valid_fmt(fmt_b)) return FP8LIN_EUNSUPPORTED;
+  if (!ws_ok(ws) || ws_bytes < kWsFixedBytes) return FP8LIN_EINVAL;
+  if (M == 0 || N == 0) return FP8LIN_OK;
+  if (d == nullptr || !aligned16(d) || ldd < N) return FP8LIN_EINVAL;
+  if (inv_a == nullptr || inv_b == nullptr) return FP8LIN_EINVAL;
+  if (K > 0) {
+    if (a == nullptr || b == nullptr || !aligned16(a) || !aligned16(b)) return FP8LIN_EINVAL;
+    if (lda < K || ldb < K) return FP8LIN_EINVAL;
+    if (lda % 16 != 0 || ldb % 16 != 0 || K % 16 != 0) return FP8LIN_EUNSUPPORTED;
+  }
+  if (N % 16 != 0 || ldd % 8 != 0) return FP8LIN_EUNSUPPORTED;
+  if (M > (int64_t(1) << 31) - 256 || N > (int64_t(1) << 31) - 256 || K > (int64_t(1) << 31) - 256)
+    return FP8LIN_EUNSUPPORTED;
+  DeviceInfo dev;
+  fp8lin_status s = get_dev(&dev);
+  if (s != FP8LIN_OK) return s;
+  return do_gemm(a, b, M, N, K, lda, ldb, fmt_a, fmt_b, inv_a, inv_b, d, ldd, ws, dev, stream);
+}
+
+static fp8lin_status check_linear_sizes(int64_t M, int64_t K, int64_t N) {
+  if (M < 0 || K < 0 || N < 0) return FP8LIN_EINVAL;
+  if (M % 16 != 0 || K % 16 != 0 || N % 16 != 0) return FP8LIN_EUNSUPPORTED;
+  if (M > (int64_t(1) << 31) - 256 || K > (int64_t(1) << 31) - 256 ||
+      N > (int64_t(1) << 31) - 256)
+    return FP8LIN_EUNSUPPORTED;
+  return FP8LIN_OK;
+}
+
+static bool dev_ptrs_ok(std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (p == nullptr || !aligned16(p)) return false;
+  return true;
+}
+
+fp8lin_status fp8lin_forward(const void* x, const void* w, int64_t M, int64_t K, int64_t N,
+                             fp8lin_scaling_state* sx, fp8lin_scaling_state* sw, void* y,
+                             uint8_t* x8, uint8_t* x8t, uint8_t* w8, uint8_t* w8t, void* ws,
+                             size_t ws_bytes, cudaStream_t stream) {
+  fp8lin_status s = check_linear_sizes(M, K, N);
+  if (s != FP8LIN_OK) return s;
+  if ((s = check_state(sx, true)) != FP8LIN_OK) return s;
+  if ((s = check_state(sw, true)) != FP8LIN_OK) return s;
+  if (sx->fmt != FP8LIN_E4M3 || sw->fmt != FP8LIN_E4M3) return FP8LIN_EUNSUPPORTED;
+  if (!ws_ok(ws) || ws_bytes < kWsFixedBytes) return FP8LIN_EINVAL;
+  if (M * K > 0 && !dev_ptrs_ok({x, x8, x8t})) return FP8LIN_EINVAL;
+  if (N * K > 0 && !dev_ptrs_ok({w, w8, w8t})) return FP8LIN_EINVAL;
+  if (M * N > 0 && !dev_ptrs_ok({y})) return FP8LIN_EINVAL;
+  DeviceInfo dev;
+  if ((s = get_dev(&dev)) != FP8LIN_OK) return s;
+
+  if (sx->kind == FP8LIN_DYNAMIC)
+    s = cast_dynamic_scaled(x, M, K, K, sx, x8, x8t, ws, dev, stream, true);
+  else
+    s = delayed_cast(x, M, K, K, sx, x8, x8t, ws, dev, stream);
+  if (s != FP8LIN_OK) return s;
+  if (sw->kind == FP8LIN_DYNAMIC)
+    s = cast_dynamic_scaled(w, N, K, K, sw, w8, w8t, ws, dev, stream, true);
+  else
+    s = delayed_cast(w, N, K, K, sw, w8, w8t, ws, dev, stream);
+  if (s != FP8LIN_OK) return s;
+  // y = x8 . W8^T : A = x8 [M, K], B = W8 [N, K]
+  return do_gemm(x8, w8, M, N, K, K, K, FP8LIN_E4M3, FP8LIN_E4M3, sx->inv_scale, sw->inv_scale, y,
+                 N, ws, dev, stream);
+}
+
+fp8lin_status fp8lin_backward(const void* dy, int64_t M, int64_t K, int64_t N,
+                              const uint8_t* x8t, const uint8_t* w8t,
+                              const fp8lin_scaling_state* sx, const fp8lin_scaling_state* sw,
+                              fp8lin_scaling_state* sdy, uint8_t* dy8, uint8_t* dy8t, void* dx,
+                              void* dw, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  fp8lin_status s = check_linear_sizes(M, K, N);
+  if (s != FP8LIN_OK) return s;
+  if ((s = check_state(sx, false)) != FP8LIN_OK) return s;
+  if ((s = check_state(sw, false)) != FP8LIN_OK) return s;
+  if ((s = check_state(sdy, true)) != FP8LIN_OK) return s;
+  if (sdy->fmt != FP8LIN_E5M2) return FP8LIN_EUNSUPPORTED;
+  if (!ws_ok(ws) || ws_bytes < kWsFixedBytes) return FP8LIN_EINVAL;
+  if (M * N > 0 && !dev_ptrs_ok({dy, dy8, dy8t})) return FP8LIN_EINVAL;
+  if (dx != nullptr && M * K > 0 && !dev_ptrs_ok({dx})) return FP8LIN_EINVAL;
+  if (dx != nullptr && N * K > 0 && !dev_ptrs_ok({w8t})) return FP8LIN_EINVAL;
+  if (dw != nullptr && N * K > 0 && !dev_ptrs_ok({dw})) return FP8LIN_EINVAL;
+  if (dw != nullptr && M * K > 0 && !dev_ptrs_ok({x8t})) return FP8LIN_EINVAL;
+  DeviceInfo dev;
+  if ((s = get_dev(&dev)) != FP8LIN_OK) return s;
+
+  if (sdy->kind == FP8LIN_DYNAMIC)
+    s = cast_dynamic_scaled(dy, M, N, N, sdy, dy8, dy8t, ws, dev, stream, true);
+  else
+    s = delayed_cast(dy, M, N, N, sdy, dy8, dy8t, ws, dev, stream);
+  if (s != FP8LIN_OK) return s;
+  if (dx != nullptr) {
+    // dX = dY8 . W8 : A = dY8 [M, N], B = W8^T [K, N], contract over N
+    s = do_gemm(dy8, w8t, M, K, N, N, N, FP8LIN_E5M2, FP8LIN_E4M3, sdy->inv_scale, sw->inv_scale,
+                dx, K, ws, dev, stream);
+    if (s != FP8LIN_OK) return s;
+  }
+  if (dw != nullptr) {
+    // dW = dY8^T . x8 : A = dY8^T [N, M], B = x8^T [K, M], contract over M
+    s = do_gemm(dy8t, x8t, N, K, M, M, M, FP8LIN_E5M2, FP8LIN_E4M3, sdy->inv_scale, sx->inv_scale,
+                dw, K, ws, dev, stream);
+    if (s != FP8LIN_OK) return s;
+  }
+  return FP8LIN_OK;
+}
+
+uint64_t fp8lin_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+void fp8lin_profile_enable(int on) {
+  g_prof_on = on != 0;
+  if (g_prof_on) g_prof_used = 0;
+}
+
+fp8lin_status fp8lin_profile_collect(double* ms, int64_t* count) {
+  if (ms == nullptr || count == nullptr) return FP8LIN_EINVAL;
+  for (int k = 0; k < FP8LIN_PROF_KINDS; ++k) {
+    ms[k] = 0.0;
+    count[k] = 0;
+  }
+  for (int i = 0; i < g_prof_used; ++i) {
+    cudaError_t e = cudaEventSynchronize(g_prof[i].stop);
+    if (e != cudaSuccess) return cuda_fail(e);
+    float t = 0.0f;
+    e = cudaEventElapsedTime(&t, g_prof[i].start, g_prof[i].stop);
+    if (e != cudaSuccess) return cuda_fail(e);
+    ms[g_prof[i].kind] += t;
+    count[g_prof[i].kind] += 1;
+  }
+  g_prof_used = 0;
+  return FP8LIN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,533 @@
+// cast_kernels.cu -- HBM-bound kernels of the fp8 Linear: amax (one-pass
+// atomic and two-kernel reduction), scale (dynamic and delayed ring), cast
+// to e4m3/e5m2 with an optional transposed copy, and a cooperative single
+// pass amax -> scale -> cast that keeps the tensor in shared memory.
+//
+// Numerics (the plain reading of tensorwise scaling in "Integrate
+// float8nocompile, an experimental feature for high performance",
+// pytorch/torchtitan PR 778, Summary):
+//   amax  = max |x|, computed on the bf16 bit patterns (|x| is bits & 0x7FFF,
+//           whose unsigned order is the order of magnitudes), so it is exact;
+//   scale = __fdiv_rn(F, max(amax, eps)), inv = __fdiv_rn(1, scale);
+//   q     = cvt.rn.satfinite(x * scale) -- one RN fp32 product, then one
+//           saturating RNE rounding to the 8-bit format.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fp8lin {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTile = 128;          // cast tile: 128 rows x 128 columns
+constexpr int kSqWords = 33;        // shared fp8 tile row pitch: 132 bytes
+constexpr int kAmaxRows = 32;       // amax tile: 32 rows x 256 columns
+constexpr int kSinglePassTilesPerCta = 7;
+
+template <int kFmt>
+__device__ __forceinline__ float fp8_max() {
+  return kFmt == 0 ? 448.0f : 57344.0f;
+}
+
+__device__ __forceinline__ float scale_from_amax(float amax, float eps, float F) {
+  const float d = amax > eps ? amax : eps;
+  return __fdiv_rn(F, d);
+}
+
+// Max of the 16-bit magnitudes held in a 16-byte vector of 8 bf16 values.
+__device__ __forceinline__ uint32_t vec_absmax(uint32_t acc, const uint4& v) {
+  acc = __vmaxu2(acc, v.x & 0x7FFF7FFFu);
+  acc = __vmaxu2(acc, v.y & 0x7FFF7FFFu);
+  acc = __vmaxu2(acc, v.z & 0x7FFF7FFFu);
+  acc = __vmaxu2(acc, v.w & 0x7FFF7FFFu);
+  return acc;
+}
+
+// Block-wide max of per-thread 2x16-bit magnitudes; result (as fp32 bits)
+// valid in thread 0.
+__device__ __forceinline__ uint32_t block_absmax_bits(uint32_t acc) {
+  __shared__ uint32_t red[kThreads / 32];
+  uint32_t m = max(acc & 0xFFFFu, acc >> 16);
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  if (warp == 0) {
+    m = lane < kThreads / 32 ? red[lane] : 0u;
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+  }
+  return m << 16;
+}
+
+// 8 bf16 -> 8 fp8 codes (two words, element order preserved).
+template <int kFmt>
+__device__ __forceinline__ uint2 cast8(const uint4& v, float s) {
+  uint2 q;
+  q.x = static_cast<uint32_t>(cvt_fp8x2<kFmt>(__fmul_rn(bf16lo_to_f32(v.x), s),
+                                              __fmul_rn(bf16hi_to_f32(v.x), s))) |
+        (static_cast<uint32_t>(cvt_fp8x2<kFmt>(__fmul_rn(bf16lo_to_f32(v.y), s),
+                                               __fmul_rn(bf16hi_to_f32(v.y), s)))
+         << 16);
+  q.y = static_cast<uint32_t>(cvt_fp8x2<kFmt>(__fmul_rn(bf16lo_to_f32(v.z), s),
+                                              __fmul_rn(bf16hi_to_f32(v.z), s))) |
+        (static_cast<uint32_t>(cvt_fp8x2<kFmt>(__fmul_rn(bf16lo_to_f32(v.w), s),
+                                               __fmul_rn(bf16hi_to_f32(v.w), s)))
+         << 16);
+  return q;
+}
+
+// Transposed write of one 128x128 fp8 tile held in shared memory (rows of
+// kSqWords words).  Each thread moves a 16-row x 4-column block: 16 word
+// reads, a 4x4 byte transpose per 4 rows (prmt), four 16-byte stores.  Lane
+// pairs cover 32 contiguous output bytes; the pitch of 33 words makes the
+// reads of a warp hit 32 distinct banks.
+__device__ __forceinline__ void store_transposed_tile(const uint32_t* sq, uint8_t* out_t,
+                                                      int64_t rows, int64_t cols, int64_t r0,
+                                                      int64_t c0) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int jg = (warp & 1) * 16 + (lane >> 1);  // 4-column group 0..31
+  const int ig = (warp >> 1) * 2 + (lane & 1);   // 16-row group 0..7
+  const int i0 = ig * 16, j0 = jg * 4;
+  if (c0 + j0 >= cols || r0 + i0 >= rows) return;
+  uint32_t w[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) w[k] = sq[(i0 + k) * kSqWords + jg];
+  uint32_t o[4][4];
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const uint32_t t0 = __byte_perm(w[4 * g + 0], w[4 * g + 1], 0x5140);
+    const uint32_t t1 = __byte_perm(w[4 * g + 2], w[4 * g + 3], 0x5140);
+    const uint32_t t2 = __byte_perm(w[4 * g + 0], w[4 * g + 1], 0x7362);
+    const uint32_t t3 = __byte_perm(w[4 * g + 2], w[4 * g + 3], 0x7362);
+    o[0][g] = __byte_perm(t0, t1, 0x5410);
+    o[1][g] = __byte_perm(t0, t1, 0x7632);
+    o[2][g] = __byte_perm(t2, t3, 0x5410);
+    o[3][g] = __byte_perm(t2, t3, 0x7632);
+  }
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+    uint8_t* dst = out_t + (c0 + j0 + jj) * rows + r0 + i0;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(o[jj][0], o[jj][1], o[jj][2], o[jj][3]);
+  }
+}
+
+// ------------------------------------------------------------------ amax
+
+template <bool kAtomic>
+__global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t* __restrict__ x,
+                                                        int64_t rows, int64_t cols, int64_t ld,
+                                                        uint32_t* __restrict__ out) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t cvec = cols >> 3;                 // 8-element vectors per row
+  const int64_t ntc = (cvec + 31) >> 5;           // 32 vectors per tile row
+  const int64_t ntr = (rows + kAmaxRows - 1) / kAmaxRows;
+  const int64_t ntiles = ntr * ntc;
+  uint32_t acc = 0;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int64_t tr = t / ntc, tc = t - tr * ntc;
+    const int64_t c = (tc << 5) + lane;
+    if (c < cvec) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t r = tr * kAmaxRows + warp + u * 8;
+        v[u] = r < rows ? ld_stream_v4(x + r * ld + c * 8) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) acc = vec_absmax(acc, v[u]);
+    }
+  }
+  const uint32_t bits = block_absmax_bits(acc);
+  if (threadIdx.x == 0) {
+    if (kAtomic)
+      atomicMax(out, bits);
+    else
+      out[blockIdx.x] = bits;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) amax_final_kernel(const uint32_t* __restrict__ part,
+                                                              int n, uint32_t* __restrict__ out) {
+  uint32_t m = 0;
+  for (int i = threadIdx.x; i < n; i += kThreads) m = max(m, part[i]);
+  // part[] already holds fp32 bits of non-negative values: order-preserving.
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  __shared__ uint32_t red[kThreads / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t r = 0;
+    for (int w = 0; w < kThreads / 32; ++w) r = max(r, red[w]);
+    *out = r;
+  }
+}
+
+// ------------------------------------------------------------------ scale
+
+__global__ void scale_kernel(const float* __restrict__ amax, float* __restrict__ scale,
+                             float* __restrict__ inv, float* __restrict__ ring,
+                             int32_t* __restrict__ head, int32_t H, int delayed, float F,
+                             float eps) {
+  float a = *amax;
+  if (delayed) {
+    int32_t h = *head;
+    h = ((h % H) + H) % H;  // a corrupted head still indexes inside the ring
+    ring[h] = a;
+    *head = (h + 1 == H) ? 0 : h + 1;
+    float m = 0.0f;
+    for (int32_t i = 0; i < H; ++i) m = ring[i] > m ? ring[i] : m;
+    a = m;
+  }
+  const float s = scale_from_amax(a, eps, F);
+  *scale = s;
+  *inv = __fdiv_rn(1.0f, s);
+}
+
+// ------------------------------------------------------------------ cast
+
+struct CastParams {
+  const uint16_t* x;
+  int64_t rows, cols, ld;
+  const float* scale_in;
+  const float* amax_in;
+  int derive_scale;
+  float eps;
+  float* scale_out;
+  float* inv_out;
+  uint8_t* out;
+  uint8_t* out_t;
+  uint32_t* amax_rec;
+};
+
+template <int kFmt, bool kTrans>
+__global__ void __launch_bounds__(kThreads, 4) cast_kernel(const CastParams p) {
+  __shared__ __align__(16) uint32_t sq[kTrans ? kTile * kSqWords : 1];
+  float s;
+  if (p.derive_scale) {
+    s = scale_from_amax(*p.amax_in, p.eps, fp8_max<kFmt>());
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+      *p.scale_out = s;
+      *p.inv_out = __fdiv_rn(1.0f, s);
+    }
+  } else {
+    s = *p.scale_in;
+  }
+  const int64_t ntc = (p.cols + kTile - 1) / kTile;
+  const int64_t ntiles = ((p.rows + kTile - 1) / kTile) * ntc;
+  uint32_t acc = 0;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int64_t r0 = (t / ntc) * kTile, c0 = (t % ntc) * kTile;
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int vi = threadIdx.x + kThreads * u;
+      const int64_t row = r0 + (vi >> 4), col = c0 + (vi & 15) * 8;
+      v[u] = (row < p.rows && col < p.cols) ? ld_stream_v4(p.x + row * p.ld + col)
+                                             : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int vi = threadIdx.x + kThreads * u;
+      const int rl = vi >> 4, cv = vi & 15;
+      const int64_t row = r0 + rl, col = c0 + cv * 8;
+      acc = vec_absmax(acc, v[u]);
+      const uint2 q = cast8<kFmt>(v[u], s);
+      if (p.out != nullptr && row < p.rows && col < p.cols)
+        *reinterpret_cast<uint2*>(p.out + row * p.cols + col) = q;
+      if (kTrans) {
+        sq[rl * kSqWords + cv * 2] = q.x;
+        sq[rl * kSqWords + cv * 2 + 1] = q.y;
+      }
+    }
+    if (kTrans) {
+      __syncthreads();
+      store_transposed_tile(sq, p.out_t, p.rows, p.cols, r0, c0);
+      __syncthreads();
+    }
+  }
+  if (p.amax_rec != nullptr) {
+    const uint32_t bits = block_absmax_bits(acc);
+    if (threadIdx.x == 0) atomicMax(p.amax_rec, bits);
+  }
+}
+
+// ------------------------------------------------------------------ single pass
+
+struct SinglePassParams {
+  const uint16_t* x;
+  int64_t rows, cols, ld;
+  float eps;
+  float* amax_out;
+  float* scale_out;
+  float* inv_out;
+  uint8_t* out;
+  uint8_t* out_t;
+  uint32_t* ws_barrier;
+  uint32_t* ws_amax;
+  int* ws_error;
+};
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
+
+// Phase 1 copies this CTA's tiles (tile t = blockIdx.x + k * gridDim.x) into
+// shared memory and folds their amax into ws_amax; a bounded grid barrier
+// waits for every CTA; phase 2 derives the scale from the global amax and
+// casts the tiles from shared memory.  Launched cooperatively, so all CTAs
+// are co-resident and the barrier completes; the time limit only guards
+// against a launch that broke that promise.
+template <int kFmt, bool kTrans>
+__global__ void __launch_bounds__(kThreads, 1) cast_single_pass_kernel(const SinglePassParams p) {
+  extern __shared__ __align__(128) uint8_t tiles[];  // kSinglePassTilesPerCta x 32 KB
+  __shared__ uint32_t s_amax_bits;
+  __shared__ int s_abort;
+  const int64_t ntc = (p.cols + kTile - 1) / kTile;
+  const int64_t ntiles = ((p.rows + kTile - 1) / kTile) * ntc;
+  uint32_t acc = 0;
+
+  for (int k = 0; k < kSinglePassTilesPerCta; ++k) {
+    const int64_t t = blockIdx.x + static_cast<int64_t>(k) * gridDim.x;
+    if (t >= ntiles) break;
+    uint8_t* buf = tiles + k * (kTile * kTile * 2);
+    const int64_t r0 = (t / ntc) * kTile, c0 = (t % ntc) * kTile;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int vi = threadIdx.x + kThreads * u;
+      const int64_t row = r0 + (vi >> 4), col = c0 + (vi & 15) * 8;
+      uint8_t* dst = buf + (vi >> 4) * (kTile * 2) + (vi & 15) * 16;
+      if (row < p.rows && col < p.cols)
+        cp_async_16(dst, p.x + row * p.ld + col);
+      else
+        *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+    }
+  }
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+  for (int k = 0; k < kSinglePassTilesPerCta; ++k) {
+    const int64_t t = blockIdx.x + static_cast<int64_t>(k) * gridDim.x;
+    if (t >= ntiles) break;
+    const uint8_t* buf = tiles + k * (kTile * kTile * 2);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int vi = threadIdx.x + kThreads * u;  // the vectors this thread copied
+      acc = vec_absmax(acc, *reinterpret_cast<const uint4*>(buf + (vi >> 4) * (kTile * 2) +
+                                                          (vi & 15) * 16));
+    }
+  }
+  const uint32_t bits = block_absmax_bits(acc);
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    atomicMax(p.ws_amax, bits);
+    __threadfence();
+    atomicAdd(p.ws_barrier, 1u);
+    const uint64_t t0 = global_timer_ns();
+    while (ld_acquire_u32(p.ws_barrier) < gridDim.x) {
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        atomicCAS(p.ws_error, 0, kErrGridBarrier);
+        s_abort = 1;
+        break;
+      }
+    }
+    s_amax_bits = ld_acquire_u32(p.ws_amax);
+  }
+  __syncthreads();
+  if (s_abort) return;
+
+  const float amax = __uint_as_float(s_amax_bits);
+  const float s = scale_from_amax(amax, p.eps, fp8_max<kFmt>());
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    *p.amax_out = amax;
+    *p.scale_out = s;
+    *p.inv_out = __fdiv_rn(1.0f, s);
+  }
+  for (int k = 0; k < kSinglePassTilesPerCta; ++k) {
+    const int64_t t = blockIdx.x + static_cast<int64_t>(k) * gridDim.x;
+    if (t >= ntiles) break;
+    uint8_t* buf = tiles + k * (kTile * kTile * 2);
+    const int64_t r0 = (t / ntc) * kTile, c0 = (t % ntc) * kTile;
+    uint2 q[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int vi = threadIdx.x + kThreads * u;
+      const uint4 v = *reinterpret_cast<const uint4*>(buf + (vi >> 4) * (kTile * 2) +
+                                                      (vi & 15) * 16);
+      q[u] = cast8<kFmt>(v, s);
+      const int64_t row = r0 + (vi >> 4), col = c0 + (vi & 15) * 8;
+      if (p.out != nullptr && row < p.rows && col < p.cols)
+        *reinterpret_cast<uint2*>(p.out + row * p.cols + col) = q[u];
+    }
+    if (kTrans) {
+      // The bf16 tile is no longer needed: reuse its buffer for the fp8 tile.
+      __syncthreads();
+      uint32_t* sq = reinterpret_cast<uint32_t*>(buf);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int vi = threadIdx.x + kThreads * u;
+        sq[(vi >> 4) * kSqWords + (vi & 15) * 2] = q[u].x;
+        sq[(vi >> 4) * kSqWords + (vi & 15) * 2 + 1] = q[u].y;
+      }
+      __syncthreads();
+      store_transposed_tile(sq, p.out_t, p.rows, p.cols, r0, c0);
+    }
+  }
+}
+
+template <typename Kernel>
+int resident_ctas(Kernel k, int threads, size_t smem) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, threads, smem) != cudaSuccess) return 0;
+  return n;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ launchers
+
+int amax_grid(const DeviceInfo& dev, int64_t rows, int64_t cols) {
+  const int64_t cvec = cols >> 3;
+  const int64_t ntiles = ((rows + kAmaxRows - 1) / kAmaxRows) * ((cvec + 31) >> 5);
+  int64_t g = static_cast<int64_t>(dev.num_sms) * 8;
+  if (g > kMaxPartials) g = kMaxPartials;
+  if (ntiles < g) g = ntiles;
+  return g < 1 ? 1 : static_cast<int>(g);
+}
+
+cudaError_t launch_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, uint32_t* out,
+                        bool atomic, int grid, cudaStream_t stream) {
+  if (atomic)
+    amax_kernel<true><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld, out);
+  else
+    amax_kernel<false><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_amax_final(const uint32_t* partials, int n, uint32_t* amax_bits,
+                              cudaStream_t stream) {
+  amax_final_kernel<<<1, kThreads, 0, stream>>>(partials, n, amax_bits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale(const float* amax, float* scale, float* inv, float* ring, int32_t* head,
+                         int32_t history_len, bool delayed, int fmt, float eps,
+                         cudaStream_t stream) {
+  const float F = fmt == 0 ? 448.0f : 57344.0f;
+  scale_kernel<<<1, 1, 0, stream>>>(amax, scale, inv, ring, head, history_len, delayed ? 1 : 0,
+                                    F, eps);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cast(const CastArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
+  CastParams p;
+  p.x = a.x;
+  p.rows = a.rows;
+  p.cols = a.cols;
+  p.ld = a.ld;
+  p.scale_in = a.scale_in;
+  p.amax_in = a.amax_in;
+  p.derive_scale = a.derive_scale ? 1 : 0;
+  p.eps = a.eps;
+  p.scale_out = a.scale_out;
+  p.inv_out = a.inv_out;
+  p.out = a.out;
+  p.out_t = a.out_t;
+  p.amax_rec = a.amax_rec;
+  const int64_t ntiles = ((a.rows + kTile - 1) / kTile) * ((a.cols + kTile - 1) / kTile);
+  int64_t grid = static_cast<int64_t>(dev.num_sms) * 4;
+  if (ntiles < grid) grid = ntiles;
+  if (grid < 1) grid = 1;
+  const bool trans = a.out_t != nullptr;
+  if (a.fmt == 0) {
+    if (trans)
+      cast_kernel<0, true><<<static_cast<int>(grid), kThreads, 0, stream>>>(p);
+    else
+      cast_kernel<0, false><<<static_cast<int>(grid), kThreads, 0, stream>>>(p);
+  } else {
+    if (trans)
+      cast_kernel<1, true><<<static_cast<int>(grid), kThreads, 0, stream>>>(p);
+    else
+      cast_kernel<1, false><<<static_cast<int>(grid), kThreads, 0, stream>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+namespace {
+constexpr size_t kSinglePassSmem = static_cast<size_t>(kSinglePassTilesPerCta) * kTile * kTile * 2;
+
+template <int kFmt, bool kTrans>
+cudaError_t single_pass_prepare(int* ctas_per_sm) {
+  auto k = cast_single_pass_kernel<kFmt, kTrans>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSinglePassSmem));
+  if (e != cudaSuccess) return e;
+  *ctas_per_sm = resident_ctas(k, kThreads, kSinglePassSmem);
+  return cudaSuccess;
+}
+}  // namespace
+
+int64_t single_pass_capacity_elems(const DeviceInfo& dev) {
+  if (static_cast<size_t>(dev.max_smem_optin) < kSinglePassSmem + 1024) return 0;
+  int per_sm = 0;
+  if (single_pass_prepare<0, true>(&per_sm) != cudaSuccess || per_sm < 1) return 0;
+  return static_cast<int64_t>(dev.num_sms) * per_sm * kSinglePassTilesPerCta * kTile * kTile;
+}
+
+bool single_pass_fits(const DeviceInfo& dev, int64_t rows, int64_t cols) {
+  const int64_t ntiles = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
+  return ntiles * kTile * kTile <= single_pass_capacity_elems(dev);
+}
+
+cudaError_t launch_cast_single_pass(const SinglePassArgs& a, const DeviceInfo& dev,
+                                    cudaStream_t stream) {
+  SinglePassParams p;
+  p.x = a.x;
+  p.rows = a.rows;
+  p.cols = a.cols;
+  p.ld = a.ld;
+  p.eps = a.eps;
+  p.amax_out = a.amax_out;
+  p.scale_out = a.scale_out;
+  p.inv_out = a.inv_out;
+  p.out = a.out;
+  p.out_t = a.out_t;
+  p.ws_barrier = a.ws_barrier;
+  p.ws_amax = a.ws_amax;
+  p.ws_error = a.ws_error;
+  const bool trans = a.out_t != nullptr;
+  int per_sm = 0;
+  cudaError_t e;
+  void* fn;
+  if (a.fmt == 0) {
+    e = trans ? single_pass_prepare<0, true>(&per_sm) : single_pass_prepare<0, false>(&per_sm);
+    fn = trans ? reinterpret_cast<void*>(cast_single_pass_kernel<0, true>)
+               : reinterpret_cast<void*>(cast_single_pass_kernel<0, false>);
+  } else {
+    e = trans ? single_pass_prepare<1, true>(&per_sm) : single_pass_prepare<1, false>(&per_sm);
+    fn = trans ? reinterpret_cast<void*>(cast_single_pass_kernel<1, true>)
+               : reinterpret_cast<void*>(cast_single_pass_kernel<1, false>);
+  }
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+  const int64_t ntiles = ((a.rows + kTile - 1) / kTile) * ((a.cols + kTile - 1) / kTile);
+  int64_t grid = (ntiles + kSinglePassTilesPerCta - 1) / kSinglePassTilesPerCta;
+  const int64_t max_grid = static_cast<int64_t>(dev.num_sms) * per_sm;
+  if (grid > max_grid) return cudaErrorCooperativeLaunchTooLarge;
+  // Spread the tiles over as many SMs as possible (fewer tiles per CTA).
+  grid = ntiles < max_grid ? ntiles : max_grid;
+  if (grid < 1) grid = 1;
+  void* args[] = {&p};
+  return cudaLaunchCooperativeKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(kThreads), args,
+                                     kSinglePassSmem, stream);
+}
+
+}  // namespace fp8lin

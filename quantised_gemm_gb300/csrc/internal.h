@@ -1,0 +1,112 @@
+// internal.h -- launchers shared between the C ABI layer and the kernel
+// translation units.  Not part of the public interface.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace fp8lin {
+
+// Workspace layout (bytes from the 256-byte aligned base).
+constexpr size_t kWsErrorOffset = 0;      // int32: first device error code (0 = none)
+constexpr size_t kWsBarrierOffset = 64;   // uint32: grid barrier arrivals (single pass)
+constexpr size_t kWsAmaxOffset = 128;     // uint32: amax bits (single pass)
+constexpr size_t kWsPartialOffset = 256;  // uint32[kMaxPartials]: REDUCTION partial maxima
+constexpr int kMaxPartials = 4096;
+constexpr size_t kWsFixedBytes = kWsPartialOffset + sizeof(uint32_t) * kMaxPartials;
+
+// Device error codes written at kWsErrorOffset.
+enum DeviceError : int {
+  kErrNone = 0,
+  kErrGemmProducerWait = 1,
+  kErrGemmMmaWait = 2,
+  kErrGemmEpilogueWait = 3,
+  kErrGridBarrier = 4,
+};
+
+struct DeviceInfo {
+  int device;
+  int num_sms;
+  int max_smem_optin;
+};
+// Properties of the current device (cached per device).
+cudaError_t current_device_info(DeviceInfo* info);
+
+// ---- amax / scale / cast (cast_kernels.cu)
+
+// Grid size the amax kernel uses for this tensor.
+int amax_grid(const DeviceInfo& dev, int64_t rows, int64_t cols);
+
+// Block maxima of |x| as fp32 bits.  atomic: one atomicMax per CTA into
+// out[0] (which must hold 0 beforehand); otherwise out[blockIdx.x] = partial.
+cudaError_t launch_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, uint32_t* out,
+                        bool atomic, int grid, cudaStream_t stream);
+
+// amax = max(partials[0..n)) written as fp32 bits into *amax_bits.
+cudaError_t launch_amax_final(const uint32_t* partials, int n, uint32_t* amax_bits,
+                              cudaStream_t stream);
+
+// One-thread scale update (dynamic or delayed ring).
+cudaError_t launch_scale(const float* amax, float* scale, float* inv, float* ring, int32_t* head,
+                         int32_t history_len, bool delayed, int fmt, float eps,
+                         cudaStream_t stream);
+
+// Cast (+ transpose) of a bf16 tensor.
+//   derive_scale == false: scale read from scale_in[0];
+//   derive_scale == true:  scale = F / max(amax_in[0], eps), and CTA 0 writes
+//                          scale_out[0] / inv_out[0].
+//   amax_rec != nullptr: atomicMax of the tensor's amax bits (pre-zeroed).
+struct CastArgs {
+  const uint16_t* x;
+  int64_t rows, cols, ld;
+  int fmt;
+  const float* scale_in;
+  const float* amax_in;
+  bool derive_scale;
+  float eps;
+  float* scale_out;
+  float* inv_out;
+  uint8_t* out;
+  uint8_t* out_t;
+  uint32_t* amax_rec;
+};
+cudaError_t launch_cast(const CastArgs& a, const DeviceInfo& dev, cudaStream_t stream);
+
+// Cooperative single pass: amax -> scale -> cast (+T) with the tensor held in
+// shared memory.  Writes amax/scale/inv.  Requires tiles <= capacity.
+struct SinglePassArgs {
+  const uint16_t* x;
+  int64_t rows, cols, ld;
+  int fmt;
+  float eps;
+  float* amax_out;
+  float* scale_out;
+  float* inv_out;
+  uint8_t* out;
+  uint8_t* out_t;
+  uint32_t* ws_barrier;   // zeroed before launch
+  uint32_t* ws_amax;      // zeroed before launch
+  int* ws_error;
+};
+int64_t single_pass_capacity_elems(const DeviceInfo& dev);
+bool single_pass_fits(const DeviceInfo& dev, int64_t rows, int64_t cols);
+cudaError_t launch_cast_single_pass(const SinglePassArgs& a, const DeviceInfo& dev,
+                                    cudaStream_t stream);
+
+// ---- GEMM (gemm_tcgen05.cu)
+
+struct GemmArgs {
+  const uint8_t* a;   // [M, K] K fastest, row stride lda bytes
+  const uint8_t* b;   // [N, K] K fastest, row stride ldb bytes
+  int64_t M, N, K, lda, ldb;
+  int fmt_a, fmt_b;
+  const float* inv_a;
+  const float* inv_b;
+  void* d;            // bf16 [M, N], row stride ldd elements
+  int64_t ldd;
+  int* ws_error;
+};
+cudaError_t launch_gemm(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t stream);
+
+}  // namespace fp8lin

@@ -1,0 +1,63 @@
+"""Fp8Linear: the buffers and scaling states of one float8 training Linear,
+driving libfp8lin's forward / backward / delayed-scale update.
+
+Mirrors the user-facing flow of the pages' float8 Linear: a config per
+tensor role (input, weight, grad_output) with dynamic or delayed scaling
+("[float8] FP8 GPT 1.5B Delayed Scaling 2x Slower than BF16", pytorch/ao
+issue 1297, repro script: Float8LinearConfig / CastConfig / ScalingType), a
+forward and backward, and after backward the per-tensor history sync
+(sync_float8_amax_and_scale_history).  All device memory is allocated here,
+once, through PyTorch; the library itself allocates nothing.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (AMAX_ATOMIC, DELAYED, DYNAMIC, E4M3, E5M2, ScalingState, Workspace, backward,
+               forward, scale)
+
+
+class Fp8Linear:
+    """One Linear y = x W^T with x [M, K], W [N, K], fp8 tensorwise scaling."""
+
+    def __init__(self, M: int, K: int, N: int, *, scaling: str = "dynamic", history_len: int = 16,
+                 amax_algo: int = AMAX_ATOMIC, eps: float = 1e-12, device="cuda"):
+        kind = {"dynamic": DYNAMIC, "delayed": DELAYED}[scaling]
+        self.M, self.K, self.N = M, K, N
+        u8 = dict(dtype=torch.uint8, device=device)
+        bf = dict(dtype=torch.bfloat16, device=device)
+        self.x8 = torch.empty((M, K), **u8)
+        self.x8t = torch.empty((K, M), **u8)
+        self.w8 = torch.empty((N, K), **u8)
+        self.w8t = torch.empty((K, N), **u8)
+        self.dy8 = torch.empty((M, N), **u8)
+        self.dy8t = torch.empty((N, M), **u8)
+        self.y = torch.empty((M, N), **bf)
+        self.dx = torch.empty((M, K), **bf)
+        self.dw = torch.empty((N, K), **bf)
+        self.ws = Workspace(M, K, N, device=device)
+        mk = lambda fmt: ScalingState(fmt, kind, history_len, amax_algo, eps, device)  # noqa: E731
+        self.sx, self.sw, self.sdy = mk(E4M3), mk(E4M3), mk(E5M2)
+
+    def forward(self, x: torch.Tensor, w: torch.Tensor, stream=None) -> torch.Tensor:
+        return forward(x, w, self.sx, self.sw, self.y, self.x8, self.x8t, self.w8, self.w8t,
+                       self.ws, stream)
+
+    def backward(self, dy: torch.Tensor, need_dx: bool = True, need_dw: bool = True, stream=None):
+        return backward(dy, self.x8t, self.w8t, self.sx, self.sw, self.sdy, self.dy8, self.dy8t,
+                        self.dx if need_dx else None, self.dw if need_dw else None, self.ws,
+                        stream)
+
+    def sync_scales(self, stream=None):
+        """Delayed scaling: push this step's amaxes into the histories and
+        recompute the scales (a no-op for dynamic scaling)."""
+        for st in (self.sx, self.sw, self.sdy):
+            if st.kind == DELAYED:
+                scale(st, stream)
+
+    def step(self, x, w, dy, stream=None):
+        """One forward + backward (+ delayed sync)."""
+        self.forward(x, w, stream)
+        self.backward(dy, stream=stream)
+        self.sync_scales(stream)
+        return self.y, self.dx, self.dw

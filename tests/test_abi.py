@@ -1,0 +1,111 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds, loads,
+exports every entry point include/*.h declares, and rejects bad arguments
+with the documented status before touching the device."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from quantised_gemm_gb300 import build as qb
+    qb.build()
+    import quantised_gemm_gb300 as q
+    return q.library()
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(fp8lin_[a-z0-9_]+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_path():
+    names = _declared_functions()
+    for required in ("fp8lin_amax", "fp8lin_scale", "fp8lin_cast", "fp8lin_forward",
+                     "fp8lin_backward", "fp8lin_gemm"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        assert lib.fp8lin_status_string(code).startswith(b"FP8LIN_")
+    assert b"unknown" in lib.fp8lin_status_string(99)
+    assert lib.fp8lin_version() == 100
+    assert lib.fp8lin_workspace_bytes(65536, 4096, 4096) >= 256
+
+
+def test_argument_errors_before_any_cuda_call(lib):
+    import quantised_gemm_gb300._lib as L
+    fake = ctypes.c_void_p(0x10000)        # never dereferenced: checks fail first
+    odd = ctypes.c_void_p(0x10008)
+    # amax: negative size, null input, misaligned input, columns not multiple of 16
+    assert lib.fp8lin_amax(fake, -1, 16, 16, fake, 0, None, None) == L.EINVAL
+    assert lib.fp8lin_amax(None, 16, 16, 16, fake, 0, None, None) == L.EINVAL
+    assert lib.fp8lin_amax(odd, 16, 16, 16, fake, 0, None, None) == L.EINVAL
+    assert lib.fp8lin_amax(fake, 16, 24, 24, fake, 0, None, None) == L.EUNSUPPORTED
+    assert lib.fp8lin_amax(fake, 16, 16, 8, fake, 0, None, None) == L.EINVAL       # ld < cols
+    assert lib.fp8lin_amax(fake, 16, 16, 16, fake, 7, None, None) == L.EUNSUPPORTED
+    assert lib.fp8lin_amax(fake, 16, 16, 16, fake, 1, None, None) == L.EINVAL      # no ws
+    # cast: bad format, no outputs, transposed copy needs rows % 16 == 0
+    assert lib.fp8lin_cast(fake, 16, 16, 16, 5, fake, fake, None, None, None) == L.EUNSUPPORTED
+    assert lib.fp8lin_cast(fake, 16, 16, 16, 0, fake, None, None, None, None) == L.EINVAL
+    assert lib.fp8lin_cast(fake, 8, 16, 16, 0, fake, fake, fake, None, None) == L.EUNSUPPORTED
+    # gemm: no workspace, K not multiple of 16, misaligned output
+    assert lib.fp8lin_gemm(fake, fake, 16, 16, 16, 16, 16, 0, 0, fake, fake, fake, 16,
+                           None, 0, None) == L.EINVAL
+    ws = ctypes.c_void_p(0x20000)
+    nb = lib.fp8lin_workspace_bytes(16, 16, 16)
+    assert lib.fp8lin_gemm(fake, fake, 16, 16, 24, 32, 32, 0, 0, fake, fake, fake, 16,
+                           ws, nb, None) == L.EUNSUPPORTED
+    assert lib.fp8lin_gemm(fake, fake, 16, 16, 16, 16, 16, 0, 0, fake, fake, odd, 16,
+                           ws, nb, None) == L.EINVAL
+    assert lib.fp8lin_gemm(fake, fake, 16, 16, 16, 16, 16, 0, 3, fake, fake, fake, 16,
+                           ws, nb, None) == L.EUNSUPPORTED
+
+
+def _state(fmt, kind=0, H=1, eps=1e-12, algo=0):
+    import quantised_gemm_gb300._lib as L
+    s = L.ScalingStateC()
+    s.amax = s.scale = s.inv_scale = 0x30000
+    s.amax_history = 0x40000 if kind == 1 else 0
+    s.head = 0x50000 if kind == 1 else 0
+    s.history_len, s.fmt, s.kind, s.amax_algo, s.needs_init, s.eps = H, fmt, kind, algo, 0, eps
+    return s
+
+
+def test_forward_backward_argument_errors(lib):
+    import quantised_gemm_gb300._lib as L
+    p = ctypes.c_void_p(0x10000)
+    ws = ctypes.c_void_p(0x20000)
+    nb = lib.fp8lin_workspace_bytes(128, 128, 128)
+    sx, sw, sd = _state(0), _state(0), _state(1)
+    fwd = lambda M, K, N, a, b: lib.fp8lin_forward(p, p, M, K, N, ctypes.byref(a), ctypes.byref(b),
+                                                   p, p, p, p, p, ws, nb, None)
+    assert fwd(100, 128, 128, sx, sw) == L.EUNSUPPORTED            # M % 16
+    assert fwd(-16, 128, 128, sx, sw) == L.EINVAL
+    assert fwd(128, 128, 128, _state(1), sw) == L.EUNSUPPORTED     # x must be e4m3
+    assert fwd(128, 128, 128, _state(0, eps=0.0), sw) == L.EINVAL  # eps must be > 0
+    assert fwd(128, 128, 128, _state(0, kind=1, H=0), sw) == L.EINVAL   # delayed H >= 1
+    assert fwd(128, 128, 128, _state(0, algo=9), sw) == L.EUNSUPPORTED
+    assert lib.fp8lin_forward(p, p, 128, 128, 128, ctypes.byref(sx), ctypes.byref(sw), p, p, p,
+                              p, p, None, nb, None) == L.EINVAL    # no workspace
+    bwd = lambda d: lib.fp8lin_backward(p, 128, 128, 128, p, p, ctypes.byref(sx), ctypes.byref(sw),
+                                        ctypes.byref(d), p, p, p, p, ws, nb, None)
+    assert bwd(_state(0)) == L.EUNSUPPORTED                        # grad_output must be e5m2
+    assert lib.fp8lin_scale(None, None) == L.EINVAL
+    assert lib.fp8lin_scale(ctypes.byref(_state(0, kind=1, H=0)), None) == L.EINVAL

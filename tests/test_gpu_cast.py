@@ -1,0 +1,160 @@
+"""GPU parity of amax, scale and cast (+transpose) against the oracle:
+bit-exact for every amax, scale, inverse scale and fp8 byte."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import quantised_gemm_gb300 as q
+import synth_inputs as si
+from helpers import dev_f32_bits, f32_bits, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+E4M3, E5M2 = oracle.E4M3, oracle.E5M2
+SHAPES = [(16, 16), (128, 128), (144, 272), (272, 144), (48, 4096), (4096, 48), (1040, 1552)]
+
+
+@pytest.fixture(scope="module")
+def ws():
+    return q.Workspace()
+
+
+def _tensor(shape, seed, outliers=True):
+    x = si.normal_bf16(shape, 1.0, seed, 1)
+    if outliers:
+        x = si.add_outliers(x, 1e-3, 50.0, seed)
+    return x
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("algo", [q.AMAX_ATOMIC, q.AMAX_REDUCTION])
+def test_amax_bit_exact(shape, algo, ws):
+    x = _tensor(shape, seed=shape[0] * 7 + shape[1])
+    out = torch.full((1,), -1.0, device="cuda")
+    q.amax(to_dev_bf16(x), out, algo, ws)
+    assert dev_f32_bits(out) == f32_bits(oracle.amax(x))
+
+
+@pytest.mark.parametrize("kind", si.EDGE_KINDS)
+def test_amax_edge_tensors(kind, ws):
+    x = si.edge_tensor(kind, 256, 4096, seed=3)
+    ref = f32_bits(oracle.amax(x))
+    for algo in (q.AMAX_ATOMIC, q.AMAX_REDUCTION):
+        out = torch.full((1,), -1.0, device="cuda")
+        q.amax(to_dev_bf16(x), out, algo, ws)
+        assert dev_f32_bits(out) == ref, (kind, algo)
+
+
+def test_amax_strided_and_empty(ws):
+    full = _tensor((64, 512), seed=5)
+    full[:, 256:] = si.f32_to_bf16_bits(np.full((64, 256), 1e6, dtype=np.float32))
+    d = to_dev_bf16(full)[:, :256]                 # row stride 512, 256 columns
+    out = torch.zeros(1, device="cuda")
+    q.amax(d, out, q.AMAX_ATOMIC, ws)
+    assert dev_f32_bits(out) == f32_bits(oracle.amax(full[:, :256]))
+    out.fill_(7.0)
+    q.amax(torch.empty((0, 64), dtype=torch.bfloat16, device="cuda"), out, q.AMAX_ATOMIC, ws)
+    assert out.item() == 0.0
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_scale_dynamic_bit_exact(fmt):
+    g = np.random.default_rng(17)
+    amaxes = np.concatenate([[0.0, 1e-30, 0.5, 1.0, 3.0e38],
+                             np.exp2(g.uniform(-30, 30, 40))]).astype(np.float32)
+    st = q.ScalingState(fmt, q.DYNAMIC)
+    for a in amaxes:
+        st.amax.fill_(float(a))
+        q.scale(st)
+        s, inv = oracle.scale_dynamic(float(a), fmt)
+        assert dev_f32_bits(st.scale) == f32_bits(s), a
+        assert dev_f32_bits(st.inv_scale) == f32_bits(inv), a
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_scale_delayed_ring_matches_oracle(fmt):
+    g = np.random.default_rng(23)
+    amaxes = np.exp2(g.uniform(-6, 6, 25)).astype(np.float32)
+    H = 16
+    st = q.ScalingState(fmt, q.DELAYED, history_len=H)
+    ref = oracle.DelayedState(H, fmt)
+    for a in amaxes:
+        st.amax.fill_(float(a))
+        q.scale(st)
+        ref.update(float(a))
+        assert dev_f32_bits(st.scale) == f32_bits(ref.scale)
+        assert dev_f32_bits(st.inv_scale) == f32_bits(ref.inv_scale)
+        assert int(st.head.item()) == ref.head
+        assert np.array_equal(st.amax_history.cpu().numpy().view(np.uint32),
+                              ref.ring.view(np.uint32))
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+@pytest.mark.parametrize("trans", [False, True])
+@pytest.mark.parametrize("shape", SHAPES)
+def test_cast_bit_exact(fmt, trans, shape):
+    x = _tensor(shape, seed=11 + shape[0])
+    s, _ = oracle.scale_dynamic(oracle.amax(x), fmt)
+    qr, qtr, a = oracle.cast(x, s, fmt, transpose=True)
+    rows, cols = shape
+    out = torch.full((rows, cols), 0xAA, dtype=torch.uint8, device="cuda")
+    out_t = torch.full((cols, rows), 0xAA, dtype=torch.uint8, device="cuda") if trans else None
+    amax_out = torch.zeros(1, device="cuda")
+    q.cast(to_dev_bf16(x), fmt, torch.tensor([s], device="cuda"), out, out_t, amax_out)
+    assert np.array_equal(out.cpu().numpy(), qr)
+    if trans:
+        assert np.array_equal(out_t.cpu().numpy(), qtr)
+    assert dev_f32_bits(amax_out) == f32_bits(a)
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_cast_every_bf16_pattern(fmt):
+    """All 65536 bf16 patterns except NaN (infinities included) under a set
+    of scales: exercises ties, subnormals, saturation and signed zero."""
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    f = si.bf16_bits_to_f32(pats)
+    pats = np.where(np.isnan(f), np.uint16(0), pats).reshape(256, 256)
+    dx = to_dev_bf16(pats)
+    scales = [1.0, 448.0, 1.0 / 448, 2.0 ** -20, 2.0 ** 20, 3.7e-3, 12345.678, 0.999999, 57344.0]
+    for sv in scales:
+        s32 = np.float32(sv)
+        qr, qtr, _ = oracle.cast(pats, s32, fmt, transpose=True)
+        out = torch.empty((256, 256), dtype=torch.uint8, device="cuda")
+        out_t = torch.empty((256, 256), dtype=torch.uint8, device="cuda")
+        q.cast(dx, fmt, torch.tensor([s32], device="cuda"), out, out_t)
+        got = out.cpu().numpy()
+        assert np.array_equal(got, qr), (sv, np.argwhere(got != qr)[:4].tolist())
+        assert np.array_equal(out_t.cpu().numpy(), qtr), sv
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+@pytest.mark.parametrize("algo", [q.AMAX_ATOMIC, q.AMAX_REDUCTION, q.AMAX_SINGLE_PASS])
+@pytest.mark.parametrize("shape", [(144, 272), (1024, 4096), (4096, 1024)])
+def test_cast_dynamic_all_algorithms(fmt, algo, shape, ws):
+    x = _tensor(shape, seed=29)
+    a = oracle.amax(x)
+    s, inv = oracle.scale_dynamic(a, fmt)
+    qr, qtr, _ = oracle.cast(x, s, fmt, transpose=True)
+    st = q.ScalingState(fmt, q.DYNAMIC, amax_algo=algo)
+    out = torch.empty(shape, dtype=torch.uint8, device="cuda")
+    out_t = torch.empty(shape[::-1], dtype=torch.uint8, device="cuda")
+    q.cast_dynamic(to_dev_bf16(x), st, out, out_t, ws)
+    q.check(ws)
+    assert dev_f32_bits(st.amax) == f32_bits(a)
+    assert dev_f32_bits(st.scale) == f32_bits(s)
+    assert dev_f32_bits(st.inv_scale) == f32_bits(inv)
+    assert np.array_equal(out.cpu().numpy(), qr)
+    assert np.array_equal(out_t.cpu().numpy(), qtr)
+
+
+def test_single_pass_capacity_and_refusal(ws):
+    cap = q.single_pass_max_elems()
+    assert cap >= 4096 * 4096, cap             # holds a 4096 x 4096 weight
+    rows = ((cap // 4096) // 128 + 8) * 128     # just above capacity
+    x = torch.zeros((rows, 4096), dtype=torch.bfloat16, device="cuda")
+    st = q.ScalingState(E4M3, q.DYNAMIC, amax_algo=q.AMAX_SINGLE_PASS)
+    out = torch.empty((rows, 4096), dtype=torch.uint8, device="cuda")
+    with pytest.raises(q.Fp8linError) as ei:
+        q.cast_dynamic(x, st, out, None, ws)
+    assert ei.value.status == 2     # FP8LIN_EUNSUPPORTED, nothing enqueued

@@ -1,0 +1,99 @@
+"""GPU parity of the tcgen05 FP8 GEMM against the oracle:
+|d - d_ref| <= 2^-7 |d_ref| + 1e-4 sum_k |a_k b_k| for every entry, on
+shapes that span several tiles with ragged M, N and K edges, both operand
+format pairs, the few-row (swapped) path, the 128-wide N path, K = 16 and
+K = 0."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import quantised_gemm_gb300 as q
+import synth_inputs as si
+from helpers import assert_within_bound, bf16_to_f64
+
+pytestmark = pytest.mark.gpu
+
+E4M3, E5M2 = oracle.E4M3, oracle.E5M2
+
+
+@pytest.fixture(scope="module")
+def ws():
+    return q.Workspace()
+
+
+def _operand(rows, k, fmt, seed, std=1.0):
+    x = si.normal_bf16((rows, k), std, seed, 1)
+    s, inv = oracle.scale_dynamic(oracle.amax(x), fmt)
+    q8, _, _ = oracle.cast(x, s, fmt, transpose=False)
+    return q8, s, inv
+
+
+CASES = [
+    # (M, N, K)
+    (128, 256, 128),        # one tile, one k-block
+    (256, 512, 1024),       # several tiles
+    (200, 272, 336),        # ragged M, N, K
+    (384, 1600, 1600),      # N = 1600: 128-wide tiles, K tail of 64
+    (144, 4096, 16),        # K = 16 (one partial k-block)
+    (16, 4096, 4096),       # few rows: swapped operands, transposed store
+    (48, 208, 160),         # few rows, ragged
+    (64, 272, 320),
+    (1040, 784, 512),
+]
+
+
+@pytest.mark.parametrize("fmts", [(E4M3, E4M3), (E5M2, E4M3)])
+@pytest.mark.parametrize("mnk", CASES)
+def test_gemm_matches_oracle(mnk, fmts, ws):
+    M, N, K = mnk
+    fa, fb = fmts
+    a8, sa, inva = _operand(M, K, fa, seed=M + K)
+    b8, sb, invb = _operand(N, K, fb, seed=N + 3 * K)
+    d = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    q.gemm(torch.from_numpy(a8).cuda(), torch.from_numpy(b8).cuda(), fa, fb,
+           torch.tensor([inva], device="cuda"), torch.tensor([invb], device="cuda"), d, ws)
+    q.check(ws)
+    y, s = oracle.gemm(a8, b8, fa, fb, sa, sb)
+    assert_within_bound(bf16_to_f64(d), y, s, "gemm %s" % (mnk,))
+
+
+def test_gemm_strided_output_and_operands(ws):
+    M, N, K = 256, 256, 256
+    a8, sa, inva = _operand(M, K, E4M3, seed=1)
+    b8, sb, invb = _operand(N, K, E4M3, seed=2)
+    abig = torch.zeros((M, K + 64), dtype=torch.uint8, device="cuda")
+    abig[:, :K] = torch.from_numpy(a8).cuda()
+    dbig = torch.full((M, N + 32), 7.0, dtype=torch.bfloat16, device="cuda")
+    q.gemm(abig[:, :K], torch.from_numpy(b8).cuda(), E4M3, E4M3,
+           torch.tensor([inva], device="cuda"), torch.tensor([invb], device="cuda"),
+           dbig[:, :N], ws)
+    y, s = oracle.gemm(a8, b8, E4M3, E4M3, sa, sb)
+    assert_within_bound(bf16_to_f64(dbig[:, :N]), y, s, "strided")
+    assert torch.all(dbig[:, N:] == 7.0)        # padding untouched
+
+
+def test_gemm_k_zero_writes_zeros(ws):
+    d = torch.full((32, 48), 3.0, dtype=torch.bfloat16, device="cuda")
+    a = torch.empty((32, 0), dtype=torch.uint8, device="cuda")
+    b = torch.empty((48, 0), dtype=torch.uint8, device="cuda")
+    one = torch.ones(1, device="cuda")
+    q.gemm(a, b, E4M3, E4M3, one, one, d, ws)
+    assert torch.all(d == 0)
+
+
+def test_gemm_exact_small_integers(ws):
+    """Integer-valued fp8 codes with unit scales: every product and partial
+    sum is exact in fp32, so the result equals the exact product rounded
+    once to bf16."""
+    g = np.random.default_rng(3)
+    M, N, K = 256, 256, 512
+    ints = np.array([0x38, 0x40, 0x44, 0xB8, 0xC0, 0x00], dtype=np.uint8)  # 1,2,3,-1,-2,0
+    a8 = ints[g.integers(0, ints.size, (M, K))]
+    b8 = ints[g.integers(0, ints.size, (N, K))]
+    d = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    one = torch.ones(1, device="cuda")
+    q.gemm(torch.from_numpy(a8).cuda(), torch.from_numpy(b8).cuda(), E4M3, E4M3, one, one, d, ws)
+    y, _ = oracle.gemm(a8, b8, E4M3, E4M3, 1.0, 1.0)
+    ref = torch.from_numpy(y.astype(np.float32)).to(torch.bfloat16).float().numpy()
+    assert np.array_equal(d.float().cpu().numpy(), ref)
