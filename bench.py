@@ -1,0 +1,525 @@
+#!/usr/bin/env python3
+"""Benchmark of the fp8 training Linear (libfp8lin) on GB300.
+
+One step = one forward + backward of the 4096->4096 Linear at M = 65536
+tokens with tensorwise dynamic scaling: amax, scale, e4m3/e5m2 casts with
+transposed copies, and the three FP8 GEMMs (y = x W^T, dX = dY W,
+dW = dY^T x).  The workload is the largest row of the single-linear table of
+"Integrate float8nocompile, an experimental feature for high performance"
+(pytorch/torchtitan PR 778), with inputs that exceed L2 (x and dY are
+512 MiB each), so no L2 flush is needed between steps.
+
+Prints ONE JSON line: value = TFLOP/s of the whole job (6 M N K per step),
+plus the GEMM kernel's roofline (tensor pipe vs measured peak), the cast
+kernel's HBM roofline, an end-to-end figure through the host-buffer API,
+the oracle timed on the host cores, SM clocks sampled during the timed
+region, and a sweep of the other workloads (M = 16 / 256 / 4096, GPT-1.5B
+block Linears with delayed scaling, Llama-3-8B FFN Linears, cast-only
+bandwidth).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+  python -m torch.distributed.run --nproc-per-node N bench.py --gpus N ...
+
+With N > 1 every rank runs an independent replica on its own GPU (the path
+has no exchange step); value is the sum over ranks, time the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "FP8 Linear fwd+bwd µs & TFLOP/s (vs FP8 peak); amax+cast GB/s vs HBM"
+HEADLINE = "linear4096_m65536"
+L2_BYTES = 129 * 1024 * 1024
+FP8_OVER_BF16 = 2.0      # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--full-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=HEADLINE)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def load_traffic(kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current source of the kernel (else None)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    srcs = {"gemm": "gemm_tcgen05.cu", "cast": "cast_kernels.cu"}
+    with open(os.path.join(ROOT, "quantised_gemm_gb300", "csrc", srcs[kernel]), "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if line.startswith("{"):
+                rec = json.loads(line)
+                if rec.get("kernel") == kernel and rec.get("src_sha") == sha:
+                    return rec
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(f[1]), smax=float(f[2]),
+                                 power=float(f[3]) if f[3] not in ("[N/A]", "N/A") else None,
+                                 hw=f[5], hwt=f[6], swt=f[7], swp=f[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        loaded = [r for r in rows if r["power"] is None or r["power"] > 300] or rows
+        reasons = set()
+        for r in loaded:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+                "sm_max_mhz": max(r["smax"] for r in rows), "reasons": sorted(reasons),
+                "samples": len(loaded)}
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ------------------------------------------------------------------ native arm
+
+def make_inputs(name, idx=0, step=0):
+    import synth_inputs as si
+    return si.workload_inputs(name, idx, step=step)
+
+
+def to_dev(a, dev):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def time_region(fn, steps, flush=None):
+    """Device time (ms) of `steps` calls of fn on the current stream.  With a
+    flush function, each step is timed alone and the flush runs between."""
+    import torch
+    stream = torch.cuda.current_stream()
+    if flush is None:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1)
+    evs = []
+    for _ in range(steps):
+        flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        evs.append((a, b))
+    evs[-1][1].synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs)
+
+
+def linear_sweep_entry(q, torch, dev, name, steps, warmup, flush, use_graph=True):
+    """fwd+bwd time of every Linear of a workload (sum over its Linears)."""
+    import synth_inputs as si
+    wl = si.WORKLOADS[name]
+    delayed = wl.get("delayed", False)
+    total_ms, total_flop = 0.0, 0.0
+    for idx, (M, K, N) in enumerate(wl["shapes"]):
+        x, w, dy = make_inputs(name, idx)
+        xd, wd, dyd = to_dev(x, dev), to_dev(w, dev), to_dev(dy, dev)
+        del x, w, dy
+        lin = q.Fp8Linear(M, K, N, scaling="delayed" if delayed else "dynamic",
+                          history_len=wl.get("history_len", 16), device=dev)
+
+        def step():
+            lin.forward(xd, wd)
+            lin.backward(dyd)
+            lin.sync_scales()
+
+        for _ in range(warmup):
+            step()
+        fn = step
+        if use_graph:
+            g = torch.cuda.CUDAGraph()
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                step()
+            torch.cuda.current_stream().wait_stream(s)
+            with torch.cuda.graph(g):
+                step()
+            fn = g.replay
+            for _ in range(2):
+                fn()
+        torch.cuda.synchronize()
+        ms = time_region(fn, steps, flush)
+        q.check(lin.ws)
+        total_ms += ms / steps
+        total_flop += 6.0 * M * N * K
+        del lin, xd, wd, dyd
+        torch.cuda.empty_cache()
+    return {"workload": name, "us_per_fwd_bwd": round(total_ms * 1e3, 2),
+            "tflops": round(total_flop / (total_ms * 1e-3) / 1e12, 1),
+            "scaling": "delayed" if delayed else "dynamic",
+            "l2": "flushed between steps" if flush else "inputs larger than L2",
+            "cuda_graph": use_graph}
+
+
+def cast_sweep(q, torch, dev, peaks, full):
+    """amax + scale + cast (+T) of [R, 4096] / [4096, R] tensors: GB/s of the
+    algorithmic bytes (2 B read + 1 B per fp8 copy) and fraction of HBM."""
+    import synth_inputs as si
+    sizes = [1 << 20, 1 << 22, 1 << 24, 1 << 26, 1 << 28, 1 << 30] if full else \
+        [1 << 20, 1 << 24, 1 << 28]
+    fmts = [q.E4M3, q.E5M2] if full else [q.E4M3]
+    shapes = ["rows", "cols"] if full else ["rows"]
+    ws = q.Workspace(device=dev)
+    flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    out = []
+    for n in sizes:
+        for shp in shapes:
+            R = n // 4096
+            rows, cols = (R, 4096) if shp == "rows" else (4096, R)
+            x = si.normal_bf16((rows, cols), 1.0, 0, 1)
+            xd = to_dev(x, dev)
+            del x
+            o = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+            ot = torch.empty((cols, rows), dtype=torch.uint8, device=dev)
+            for fmt in fmts:
+                for trans in (True, False):
+                    for algo in (q.AMAX_ATOMIC, q.AMAX_REDUCTION, q.AMAX_SINGLE_PASS):
+                        if algo == q.AMAX_SINGLE_PASS and n > q.single_pass_max_elems():
+                            continue
+                        if algo == q.AMAX_REDUCTION and not full:
+                            continue
+                        st = q.ScalingState(fmt, q.DYNAMIC, amax_algo=algo, device=dev)
+                        fn = lambda: q.cast_dynamic(xd, st, o, ot if trans else None, ws)  # noqa
+                        for _ in range(3):
+                            fn()
+                        flush = (lambda: flush_buf.zero_()) if n * 2 < 2 * L2_BYTES else None
+                        steps = 20 if n >= (1 << 28) else 50
+                        torch.cuda.synchronize()
+                        ms = time_region(fn, steps, flush) / steps
+                        q.check(ws)
+                        alg_bytes = n * (2 + 1 + (1 if trans else 0))
+                        gbs = alg_bytes / (ms * 1e-3) / 1e9
+                        out.append({"elems": n, "shape": [rows, cols],
+                                    "fmt": "e4m3" if fmt == q.E4M3 else "e5m2",
+                                    "transpose": trans,
+                                    "amax": {0: "atomic", 1: "reduction", 2: "single_pass"}[algo],
+                                    "us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
+                                    "frac_hbm": round(gbs / peaks["hbm_gbs"], 3)})
+            del xd, o, ot
+            torch.cuda.empty_cache()
+    return out
+
+
+def cpu_baseline_sample(name, budget_s=12.0):
+    """The oracle, as it stands, on host cores: fwd+bwd of the workload's
+    Linear on its first Ms tokens (doubling Ms until the budget is used).
+    Returns (TFLOP/s, description, threads)."""
+    import oracle
+    import synth_inputs as si
+    oracle.build()
+    wl = si.WORKLOADS[name]
+    M, K, N = wl["shapes"][0]
+    w = si.weight(K, N, w_init=wl["w_init"], w_std=wl.get("w_std", 0.02))
+    Ms, spent, flop, elapsed = 64, 0.0, 0.0, 0.0
+    while True:
+        x = si.normal_bf16((Ms, K), 1.0, 0, si.STREAM_X)
+        dy = si.normal_bf16((Ms, N), 1e-3, 0, si.STREAM_DY)
+        t0 = time.perf_counter()
+        sx = oracle.scale_dynamic(oracle.amax(x), oracle.E4M3)[0]
+        sw = oracle.scale_dynamic(oracle.amax(w), oracle.E4M3)[0]
+        sd = oracle.scale_dynamic(oracle.amax(dy), oracle.E5M2)[0]
+        oracle.linear_fwd_bwd(x, w, dy, sx, sw, sd)
+        dt = time.perf_counter() - t0
+        spent += dt
+        flop, elapsed = 6.0 * Ms * N * K, dt
+        if spent > budget_s or Ms >= M or dt > budget_s / 3:
+            break
+        Ms *= 2
+    desc = ("oracle fwd+bwd (C casts + numpy fp64 GEMMs) of the %dx%d Linear on the first %d "
+            "of %d tokens, %.2f s" % (K, N, Ms, M, elapsed))
+    return flop / elapsed / 1e12, desc, oracle.num_threads()
+
+
+def run_native(args):
+    import torch
+    import quantised_gemm_gb300 as q
+    import synth_inputs as si
+
+    world, rank, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    wl = si.WORKLOADS[args.workload]
+    M, K, N = wl["shapes"][0]
+
+    x, w, dy = make_inputs(args.workload, 0)
+    xd, wd, dyd = to_dev(x, dev), to_dev(w, dev), to_dev(dy, dev)
+    lin = q.Fp8Linear(M, K, N, device=dev)
+
+    def step():
+        lin.forward(xd, wd)
+        lin.backward(dyd)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    q.check(lin.ws)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches0 = q.launch_count()
+    q.profile_enable(True)
+    sampler.mark("t0")
+    ms = time_region(step, args.steps)
+    sampler.mark("t1")
+    torch.cuda.synchronize()
+    prof = q.profile_collect()
+    q.profile_enable(False)
+    launches = q.launch_count() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    q.check(lin.ws)
+    ms_step = ms / args.steps
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+    flop_step = 6.0 * M * N * K
+    value = world * flop_step / (ms_step * 1e-3) / 1e12
+
+    gemm_ms, gemm_n = prof["gemm"]
+    gemm_avg = gemm_ms / max(1, gemm_n)
+    gemm_flop = 2.0 * M * N * K          # each of the three GEMMs of this square Linear
+    achieved = gemm_flop / (gemm_avg * 1e-3) / 1e12
+    peak = peaks["bf16_tflops_sustained"] * FP8_OVER_BF16
+    tr = load_traffic("gemm")
+    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 3),
+                "traffic": tr["bytes_per_launch"] if tr else None,
+                "kernel": "gemm_fp8_kernel (tcgen05, e4m3/e5m2 x e4m3 -> bf16)",
+                "launch_us": round(gemm_avg * 1e3, 1),
+                "peak_basis": "%s bf16 sustained %.1f TFLOP/s x %.0f (nominal fp8/bf16)" % (
+                    peaks["source"], peaks["bf16_tflops_sustained"], FP8_OVER_BF16)}
+    cast_ms, cast_n = prof["cast"]
+    cast_avg = cast_ms / max(1, cast_n)
+    # casts per step: x [M,K], W [N,K], dY [M,N] with transposed copies; the
+    # average launch moves 2 B read + 2 B written per element
+    cast_elems = (M * K + N * K + M * N) / 3.0
+    cast_gbs = cast_elems * 4 / (cast_avg * 1e-3) / 1e9
+    trc = load_traffic("cast")
+    cast_roofline = {"bound": "hbm", "achieved": round(cast_gbs, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(cast_gbs / peaks["hbm_gbs"], 3),
+                     "traffic": trc["bytes_per_launch"] if trc else None,
+                     "kernel": "cast_kernel (+transpose)", "launch_us": round(cast_avg * 1e3, 1)}
+    kernel_ms = {k: round(v[0] / args.steps, 4) for k, v in prof.items()}
+
+    # end to end through the host-buffer API
+    import torch as _t
+    hx = _t.from_numpy(x.view(np.int16)).view(_t.bfloat16).pin_memory()
+    hw = _t.from_numpy(w.view(np.int16)).view(_t.bfloat16).pin_memory()
+    hdy = _t.from_numpy(dy.view(np.int16)).view(_t.bfloat16).pin_memory()
+    hy = _t.empty((M, N), dtype=_t.bfloat16).pin_memory()
+    hdx = _t.empty((M, K), dtype=_t.bfloat16).pin_memory()
+    hdw = _t.empty((N, K), dtype=_t.bfloat16).pin_memory()
+    del x, w, dy
+    e2e_steps = max(3, min(20, args.steps // 10))
+    for _ in range(2):
+        lin.step_host(hx, hw, hdy, hy, hdx, hdw)
+    torch.cuda.synchronize()
+    e2e_ms = time_region(lambda: lin.step_host(hx, hw, hdy, hy, hdx, hdw), e2e_steps) / e2e_steps
+    e2e_value = world * flop_step / (e2e_ms * 1e-3) / 1e12
+    h2d = 2 * (M * K + N * K + M * N)
+    d2h = 2 * (M * N + M * K + N * K)
+    del lin, xd, wd, dyd, hx, hw, hdy, hy, hdx, hdw
+    torch.cuda.empty_cache()
+
+    sweep = None
+    if not args.no_sweep:
+        flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+        flush = lambda: flush_buf.zero_()  # noqa: E731
+        sweep = {"linears": [], "cast": None}
+        for name in ("linear4096_m16", "linear4096_m256", "linear4096_m4096",
+                     "gpt1.5b_linears_m12288", "llama3_8b_ffn_m8192"):
+            small = si.WORKLOADS[name]["shapes"][0][0] <= 4096
+            sweep["linears"].append(linear_sweep_entry(
+                q, torch, dev, name, steps=50 if small else 20, warmup=5,
+                flush=flush if small else None))
+        del flush_buf
+        torch.cuda.empty_cache()
+        sweep["cast"] = cast_sweep(q, torch, dev, peaks, args.full_sweep)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, desc, cores = cpu_baseline_sample(args.workload)
+        cpu = {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": desc}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup),
+            "ms_per_step": round(ms_step, 4), "us_per_fwd_bwd": round(ms_step * 1e3, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8",
+            "data": "synthetic",
+            "config": {"workload": "%s: Linear 4096->4096, M=%d tokens, dynamic tensorwise "
+                                   "scaling, x~N(0,1)+0.1%% N(0,50) outliers, W~U(+-1/64), "
+                                   "dY~N(0,1e-3)" % (args.workload, M),
+                       "M": M, "K": K, "N": N, "l2": "inputs larger than L2 (x, dY 512 MiB)",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": roofline, "cast_roofline": cast_roofline,
+            "kernel_ms_per_step": kernel_ms,
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": round(e2e_ms, 3)},
+            "gpu_launches": int(launches), "clocks": clocks, "peaks": peaks,
+            "sweep": sweep,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    """The oracle on host cores, same metric / unit / config, each step a
+    bounded sample of the workload (the first tokens of the Linear)."""
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return
+    import oracle
+    import synth_inputs as si
+    oracle.build()
+    wl = si.WORKLOADS[args.workload]
+    M, K, N = wl["shapes"][0]
+    Ms = 128
+    w = si.weight(K, N, w_init=wl["w_init"], w_std=wl.get("w_std", 0.02))
+    x = si.normal_bf16((Ms, K), 1.0, 0, si.STREAM_X)
+    dy = si.normal_bf16((Ms, N), 1e-3, 0, si.STREAM_DY)
+
+    def step():
+        sx = oracle.scale_dynamic(oracle.amax(x), oracle.E4M3)[0]
+        sw = oracle.scale_dynamic(oracle.amax(w), oracle.E4M3)[0]
+        sd = oracle.scale_dynamic(oracle.amax(dy), oracle.E5M2)[0]
+        oracle.linear_fwd_bwd(x, w, dy, sx, sw, sd)
+
+    for _ in range(max(1, min(args.warmup, 3))):
+        step()
+    steps = max(1, min(args.steps, 10))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    dt = (time.perf_counter() - t0) / steps
+    value = 6.0 * Ms * N * K / dt / 1e12
+    sample = ("oracle fwd+bwd of the %dx%d Linear on the first %d of %d tokens per step" %
+              (K, N, Ms, M))
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": steps, "warmup": max(1, min(args.warmup, 3)),
+            "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "%s: Linear 4096->4096, M=%d tokens (sampled %d)" %
+                                   (args.workload, M, Ms), "M": M, "K": K, "N": N},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "kind": "oracle",
+                             "cores": oracle.num_threads(), "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

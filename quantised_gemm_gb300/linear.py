@@ -55,9 +55,38 @@ class Fp8Linear:
             if st.kind == DELAYED:
                 scale(st, stream)
 
+    def step_host(self, x_h, w_h, dy_h, y_h, dx_h, dw_h, stream=None):
+        """End-to-end step from host buffers (pinned for asynchronous copies):
+        copy x, W, dY in, forward + backward (+ delayed sync), copy y, dX, dW
+        out, all on one stream.  Device staging buffers are allocated on the
+        first call."""
+        if not hasattr(self, "_xd"):
+            dev = self.y.device
+            self._xd = torch.empty((self.M, self.K), dtype=torch.bfloat16, device=dev)
+            self._wd = torch.empty((self.N, self.K), dtype=torch.bfloat16, device=dev)
+            self._dyd = torch.empty((self.M, self.N), dtype=torch.bfloat16, device=dev)
+        ctx = torch.cuda.stream(stream) if stream is not None else _NullCtx()
+        with ctx:
+            self._xd.copy_(x_h, non_blocking=True)
+            self._wd.copy_(w_h, non_blocking=True)
+            self._dyd.copy_(dy_h, non_blocking=True)
+            self.step(self._xd, self._wd, self._dyd)
+            y_h.copy_(self.y, non_blocking=True)
+            dx_h.copy_(self.dx, non_blocking=True)
+            dw_h.copy_(self.dw, non_blocking=True)
+        return y_h, dx_h, dw_h
+
     def step(self, x, w, dy, stream=None):
         """One forward + backward (+ delayed sync)."""
         self.forward(x, w, stream)
         self.backward(dy, stream=stream)
         self.sync_scales(stream)
         return self.y, self.dx, self.dw
+
+
+class _NullCtx:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False

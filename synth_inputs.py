@@ -88,17 +88,21 @@ def linear_inputs(M: int, K: int, N: int, *, w_init: str, x_std: float = 1.0,
     x = normal_bf16((M, K), x_std, s, STREAM_X)
     if outlier_frac > 0:
         x = add_outliers(x, outlier_frac, outlier_std, s)
-    if w_init == "uniform64":
-        w = uniform_bf16((N, K), -1.0 / 64, 1.0 / 64, seed, STREAM_W)
-    elif w_init == "kaiming":
-        b = 1.0 / np.sqrt(K)
-        w = uniform_bf16((N, K), -b, b, seed, STREAM_W)
-    elif w_init == "normal":
-        w = normal_bf16((N, K), w_std, seed, STREAM_W)
-    else:
-        raise ValueError(w_init)
+    w = weight(K, N, w_init=w_init, w_std=w_std, seed=seed)
     dy = normal_bf16((M, N), dy_std, s, STREAM_DY)
     return x, w, dy
+
+
+def weight(K: int, N: int, *, w_init: str, w_std: float = 0.02, seed: int = 0) -> np.ndarray:
+    """W [N, K] as bf16 bits (see linear_inputs for the recipes)."""
+    if w_init == "uniform64":
+        return uniform_bf16((N, K), -1.0 / 64, 1.0 / 64, seed, STREAM_W)
+    if w_init == "kaiming":
+        b = 1.0 / np.sqrt(K)
+        return uniform_bf16((N, K), -b, b, seed, STREAM_W)
+    if w_init == "normal":
+        return normal_bf16((N, K), w_std, seed, STREAM_W)
+    raise ValueError(w_init)
 
 
 # Named workloads: (M, K, N) per Linear and the value recipe.
