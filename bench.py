@@ -54,6 +54,7 @@ def parse():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--full-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--workload", default=HEADLINE)
     return ap.parse_args()
 
@@ -318,6 +319,27 @@ def cpu_baseline_sample(name, budget_s=12.0):
     return flop / elapsed / 1e12, desc, oracle.num_threads()
 
 
+def end_to_end(q, lin, x, w, dy, M, K, N, world, flop_step, steps):
+    """The same step through the host-buffer API (Fp8Linear.step_host):
+    pinned host inputs copied in and y, dX, dW copied out every step."""
+    import torch
+    hx = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hw = torch.from_numpy(w.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hdy = torch.from_numpy(dy.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hy = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    hdx = torch.empty((M, K), dtype=torch.bfloat16).pin_memory()
+    hdw = torch.empty((N, K), dtype=torch.bfloat16).pin_memory()
+    n = max(3, min(20, steps // 10))
+    for _ in range(2):
+        lin.step_host(hx, hw, hdy, hy, hdx, hdw)
+    torch.cuda.synchronize()
+    ms = time_region(lambda: lin.step_host(hx, hw, hdy, hy, hdx, hdw), n) / n
+    return {"value": round(world * flop_step / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": 2 * (M * K + N * K + M * N),
+            "d2h_bytes_per_step": 2 * (M * N + M * K + N * K), "ms_per_step": round(ms, 3),
+            "steps": n}
+
+
 def run_native(args):
     import torch
     import quantised_gemm_gb300 as q
@@ -399,24 +421,11 @@ def run_native(args):
                      "kernel": "cast_kernel (+transpose)", "launch_us": round(cast_avg * 1e3, 1)}
     kernel_ms = {k: round(v[0] / args.steps, 4) for k, v in prof.items()}
 
-    # end to end through the host-buffer API
-    import torch as _t
-    hx = _t.from_numpy(x.view(np.int16)).view(_t.bfloat16).pin_memory()
-    hw = _t.from_numpy(w.view(np.int16)).view(_t.bfloat16).pin_memory()
-    hdy = _t.from_numpy(dy.view(np.int16)).view(_t.bfloat16).pin_memory()
-    hy = _t.empty((M, N), dtype=_t.bfloat16).pin_memory()
-    hdx = _t.empty((M, K), dtype=_t.bfloat16).pin_memory()
-    hdw = _t.empty((N, K), dtype=_t.bfloat16).pin_memory()
+    e2e = None
+    if not args.no_e2e:
+        e2e = end_to_end(q, lin, x, w, dy, M, K, N, world, flop_step, args.steps)
     del x, w, dy
-    e2e_steps = max(3, min(20, args.steps // 10))
-    for _ in range(2):
-        lin.step_host(hx, hw, hdy, hy, hdx, hdw)
-    torch.cuda.synchronize()
-    e2e_ms = time_region(lambda: lin.step_host(hx, hw, hdy, hy, hdx, hdw), e2e_steps) / e2e_steps
-    e2e_value = world * flop_step / (e2e_ms * 1e-3) / 1e12
-    h2d = 2 * (M * K + N * K + M * N)
-    d2h = 2 * (M * N + M * K + N * K)
-    del lin, xd, wd, dyd, hx, hw, hdy, hy, hdx, hdw
+    del lin, xd, wd, dyd
     torch.cuda.empty_cache()
 
     sweep = None
@@ -455,9 +464,7 @@ def run_native(args):
             "roofline": roofline, "cast_roofline": cast_roofline,
             "kernel_ms_per_step": kernel_ms,
             "cpu_baseline": cpu,
-            "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": round(e2e_ms, 3)},
+            "e2e": e2e,
             "gpu_launches": int(launches), "clocks": clocks, "peaks": peaks,
             "sweep": sweep,
         }

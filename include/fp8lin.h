@@ -84,7 +84,8 @@ typedef enum { FP8LIN_E4M3 = 0, FP8LIN_E5M2 = 1 } fp8lin_fmt;
  *               with one atomic max;
  *   REDUCTION   each CTA writes its partial maximum to the workspace and a
  *               second, one-CTA kernel reduces them;
- *   SINGLE_PASS (dynamic scaling only, fp8lin_forward/backward/cast_fused)
+ *   SINGLE_PASS (dynamic scaling only: fp8lin_forward, fp8lin_backward,
+ *               fp8lin_cast_dynamic)
  *               amax -> scale -> cast (+transpose) in one cooperative launch
  *               that keeps the bf16 tensor on chip between the phases; only
  *               for tensors that fit (fp8lin_single_pass_max_elems()); larger

@@ -112,6 +112,8 @@ WORKLOADS = {
                             outlier_frac=1e-3),
     "linear4096_m4096": dict(shapes=[(4096, 4096, 4096)], w_init="uniform64", dy_std=1e-3,
                              outlier_frac=1e-3),
+    "linear4096_m16384": dict(shapes=[(16384, 4096, 4096)], w_init="uniform64", dy_std=1e-3,
+                              outlier_frac=1e-3),
     "linear4096_m65536": dict(shapes=[(65536, 4096, 4096)], w_init="uniform64", dy_std=1e-3,
                               outlier_frac=1e-3),
     "gpt1.5b_linears_m12288": dict(shapes=[(12288, 1600, 4800), (12288, 1600, 1600),
