@@ -169,6 +169,31 @@ fp8lin_status fp8lin_check(void* ws, cudaStream_t stream);
 fp8lin_status fp8lin_amax(const void* x, int64_t rows, int64_t cols, int64_t ld,
                           float* amax_out, int32_t algo, void* ws, cudaStream_t stream);
 
+/* amax without workspace or allocation.  The pages have no counterpart of
+ * this entry point; it exists for callers that cannot call cudaMalloc and
+ * have no workspace to pass -- for example a plug-in running inside a host
+ * framework that owns all device memory through its own pool (a direct
+ * cudaMalloc would bypass that pool's accounting, or fail because the pool
+ * has reserved the memory), or a tool allowed to touch only the buffers it
+ * was handed.
+ * Computes exactly what fp8lin_amax(..., FP8LIN_AMAX_REDUCTION, ws, ...)
+ * computes (same bits), with the partial maxima kept in a static device
+ * array of the library instead of `ws`: 4096 slots of 4 bytes (16 KiB),
+ * one per CTA, held on every GPU that loads the library until the process
+ * exits.  It allocates nothing and calls no allocating routine.
+ * Limits: the shape rules of fp8lin_amax; a launch that would need more
+ * than 4096 CTAs (a device with more than 512 SMs) returns
+ * FP8LIN_EUNSUPPORTED with nothing enqueued.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls on a device share the one array,
+ * which keeps the last call's contents (nothing in it needs clearing: each
+ * call writes every slot it reads); calls that overlap on the GPU -- on two
+ * streams, or from two host threads -- race on it and must be serialised
+ * by the caller. */
+fp8lin_status fp8lin_amax_noalloc(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                  float* amax_out, cudaStream_t stream);
+
 /* scale (rows a2 / a2' of the path).  Dynamic: reads *st->amax and writes
  * scale = fl32(F / max(amax, eps)) and inv_scale = fl32(1 / scale).
  * Delayed: ring[head] = *amax; head = (head + 1) % H; then the same formula

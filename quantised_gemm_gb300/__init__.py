@@ -31,7 +31,7 @@ from ._lib import (AMAX_ATOMIC, AMAX_REDUCTION, AMAX_SINGLE_PASS, DELAYED, DYNAM
 
 __all__ = [
     "E4M3", "E5M2", "AMAX_ATOMIC", "AMAX_REDUCTION", "AMAX_SINGLE_PASS", "DYNAMIC", "DELAYED",
-    "Fp8linError", "ScalingState", "Workspace", "amax", "scale", "cast", "cast_dynamic", "gemm",
+    "Fp8linError", "ScalingState", "Workspace", "amax", "amax_noalloc", "scale", "cast", "cast_dynamic", "gemm",
     "forward", "backward", "check", "workspace_bytes", "single_pass_max_elems", "launch_count",
     "profile_enable", "profile_collect", "Fp8Linear", "library",
 ]
@@ -138,6 +138,16 @@ def amax(x: torch.Tensor, out: torch.Tensor, algo: int = AMAX_ATOMIC, ws: Worksp
     st = lib.fp8lin_amax(px, rows, cols, ld, _dev(out, "out", torch.float32), algo,
                          ws.ptr if ws is not None else None, _stream(stream))
     _lib.check(st, "fp8lin_amax")
+    return out
+
+
+def amax_noalloc(x: torch.Tensor, out: torch.Tensor, stream=None):
+    """amax with no workspace and no allocation (static scratch in the
+    library; calls that overlap on the GPU race on it)."""
+    px, rows, cols, ld = _bf16_2d(x, "x")
+    st = library().fp8lin_amax_noalloc(px, rows, cols, ld, _dev(out, "out", torch.float32),
+                                       _stream(stream))
+    _lib.check(st, "fp8lin_amax_noalloc")
     return out
 
 

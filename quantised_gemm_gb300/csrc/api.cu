@@ -352,6 +352,25 @@ fp8lin_status fp8lin_amax(const void* x, int64_t rows, int64_t cols, int64_t ld,
   return do_amax(x, rows, cols, ld, amax_out, algo, ws, dev, stream);
 }
 
+fp8lin_status fp8lin_amax_noalloc(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                  float* amax_out, cudaStream_t stream) {
+  fp8lin_status s = check_bf16(x, rows, cols, ld);
+  if (s != FP8LIN_OK) return s;
+  if (amax_out == nullptr || (reinterpret_cast<uintptr_t>(amax_out) & 3u)) return FP8LIN_EINVAL;
+  DeviceInfo dev;
+  if ((s = get_dev(&dev)) != FP8LIN_OK) return s;
+  if (rows == 0 || cols == 0) {
+    cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), stream);
+    return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);
+  }
+  const int grid = amax_grid(dev, rows, cols);
+  if (grid > kStaticAmaxPartials) return FP8LIN_EUNSUPPORTED;  // more CTAs than scratch slots
+  g_launches.fetch_add(2, std::memory_order_relaxed);
+  cudaError_t e = launch_amax_static_scratch(static_cast<const uint16_t*>(x), rows, cols, ld,
+                                             amax_out, grid, stream);
+  return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);
+}
+
 fp8lin_status fp8lin_scale(const fp8lin_scaling_state* st, cudaStream_t stream) {
   fp8lin_status s = check_state(st, true);
   if (s != FP8LIN_OK) return s;

@@ -14,6 +14,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -415,6 +416,56 @@ cudaError_t launch_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t l
 cudaError_t launch_amax_final(const uint32_t* partials, int n, uint32_t* amax_bits,
                               cudaStream_t stream) {
   amax_final_kernel<<<1, kThreads, 0, stream>>>(partials, n, amax_bits);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ amax without a workspace
+//
+// The two-kernel REDUCTION amax needs somewhere to keep one partial maximum
+// per CTA.  For callers that cannot allocate device memory and have no
+// workspace to hand over, that scratch lives in this file-scope array instead:
+// kStaticAmaxPartials words (16 KiB), resident on every GPU that loads the
+// library until the process exits.  Host code must not pass the array's name
+// to a kernel (on the host it only stands in for the symbol); the device
+// address is looked up once per device with cudaGetSymbolAddress.
+static __device__ __align__(256) uint32_t g_static_amax_partials[kStaticAmaxPartials];
+
+namespace {
+
+// Device address of g_static_amax_partials on the current device, looked up
+// on the first call for each device.
+cudaError_t static_partials(uint32_t** out) {
+  static std::mutex mu;
+  static uint32_t* addr[64] = {};
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) return e;
+  if (d < 0 || d >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[d] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_amax_partials);
+    if (e != cudaSuccess) return e;
+    addr[d] = static_cast<uint32_t*>(p);
+  }
+  *out = addr[d];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_amax_static_scratch(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                                       float* amax_out, int grid, cudaStream_t stream) {
+  if (grid < 1 || grid > kStaticAmaxPartials) return cudaErrorInvalidValue;
+  uint32_t* part = nullptr;
+  cudaError_t e = static_partials(&part);
+  if (e != cudaSuccess) return e;
+  // Every CTA of the first kernel writes its own slot before the second
+  // kernel reads slots [0, grid): nothing in the array has to start at zero.
+  amax_kernel<false><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld, part);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  amax_final_kernel<<<1, kThreads, 0, stream>>>(part, grid, reinterpret_cast<uint32_t*>(amax_out));
   return cudaGetLastError();
 }
 

@@ -47,6 +47,12 @@ cudaError_t launch_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t l
 cudaError_t launch_amax_final(const uint32_t* partials, int n, uint32_t* amax_bits,
                               cudaStream_t stream);
 
+// REDUCTION amax with its partial maxima in a static device array instead of
+// a workspace (at most kStaticAmaxPartials CTAs); two launches.
+constexpr int kStaticAmaxPartials = 4096;
+cudaError_t launch_amax_static_scratch(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                                       float* amax_out, int grid, cudaStream_t stream);
+
 // One-thread scale update (dynamic or delayed ring).
 cudaError_t launch_scale(const float* amax, float* scale, float* inv, float* ring, int32_t* head,
                          int32_t history_len, bool delayed, int fmt, float eps,
