@@ -293,6 +293,224 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
+// ------------------------------------------------------------------ CTA-pair kernel
+//
+// Two CTAs of a cluster share one 256 x BN tile: each CTA loads 128 rows of
+// A and BN/2 rows of B per stage (so a stage is 16 KB + BN/2 * 128 B per
+// CTA instead of 16 KB + BN * 128 B), and the even CTA issues
+// tcgen05.mma.cta_group::2 (M = 256) reading both CTAs' shared memory; each
+// CTA's TMEM receives its 128 rows of the accumulator.
+//   full[s]      lives in the even CTA; both CTAs' TMA loads count their
+//                bytes on it (the even producer arms it for both);
+//   empty[s]     one per CTA; the MMA commit arrives on both (multicast);
+//   acc_full[a]  one per CTA; the MMA commit arrives on both (multicast);
+//   acc_empty[a] lives in the even CTA; all 8 epilogue warps arrive on it.
+
+template <int BN, int STAGES>
+struct PairCfg {
+  static constexpr int kABytes = kBM * kBK;             // 128 rows of A per CTA
+  static constexpr int kBBytes = (BN / 2) * kBK;        // BN/2 rows of B per CTA
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 2 * BN <= 256 ? 256 : 512;
+  static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(STAGES) * kStageBytes + 256;
+  static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "MMA N for M=256");
+  static_assert(kBBytes % 1024 == 0, "B tiles keep 1024-byte alignment");
+};
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_fp8_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                         const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+  using C = PairCfg<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * C::kABytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * C::kBBytes);
+  uint64_t* empty = full + STAGES;
+  uint64_t* acc_full = empty + STAGES;   // [2]
+  uint64_t* acc_empty = acc_full + 2;    // [2]
+  uint64_t* drain = acc_empty + 2;       // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();      // 0: issues the MMAs
+  const int pair = static_cast<int>(cluster_id_x());
+  const int num_pairs = static_cast<int>(cluster_count_x());
+  const int num_m = (p.M + 2 * kBM - 1) / (2 * kBM);
+  const int num_n = (p.N + BN - 1) / BN;
+  const int num_tiles = num_m * num_n;
+  const int num_kb = (p.K + kBK - 1) / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 8);  // 4 epilogue warps x 2 CTAs
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_map(&tmA);
+    tma_prefetch_map(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, C::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before_sync();
+  cluster_sync_all();  // barriers of both CTAs initialised before any remote use
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producers (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs) {
+        const int m_blk = tile / num_n, n_blk = tile % num_n;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait_cluster_bounded(&empty[stage], phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full_even = map_to_cta(smem_addr(&full[stage]), 0);
+          if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * C::kStageBytes);
+          tma_load_2d_pair(sA + stage * C::kABytes, &tmA, full_even, kb * kBK,
+                           m_blk * 2 * kBM + static_cast<int>(rank) * kBM);
+          tma_load_2d_pair(sB + stage * C::kBBytes, &tmB, full_even, kb * kBK,
+                           n_blk * BN + static_cast<int>(rank) * (BN / 2));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) record_error(p.err, abort_flag, kErrGemmProducerWait);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (lane == 0 && rank == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      bool issued = false;
+      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs) {
+        if (!mbar_wait_cluster_bounded(&acc_empty[acc], acc_phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait_cluster_bounded(&full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint64_t a_desc = smem_desc_k_sw128(smem_addr(sA + stage * C::kABytes));
+          const uint64_t b_desc = smem_desc_k_sw128(smem_addr(sB + stage * C::kBBytes));
+#pragma unroll
+          for (int k = 0; k < kBK / kMmaK; ++k) {
+            mma_f8f6f4_pair(d_tmem, a_desc + static_cast<uint64_t>(k * (kMmaK >> 4)),
+                            b_desc + static_cast<uint64_t>(k * (kMmaK >> 4)), p.idesc,
+                            (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          issued = true;
+          mma_commit_pair_multicast(&empty[stage], 0x3);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair_multicast(&acc_full[acc], 0x3);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        record_error(p.err, abort_flag, kErrGemmMmaWait);
+        if (issued) {
+          volatile int never = 0;
+          mma_commit_pair_multicast(drain, 0x1);
+          mbar_wait_bounded(drain, 0, &never);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int quarter = warp & 3;
+    const float alpha = __fmul_rn(*p.inv_a, *p.inv_b);
+    const uint32_t acc_empty_even0 = map_to_cta(smem_addr(&acc_empty[0]), 0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = pair; tile < num_tiles; tile += num_pairs) {
+      const int m_blk = tile / num_n, n_blk = tile % num_n;
+      const bool ready = __all_sync(
+          0xFFFFFFFFu, mbar_wait_cluster_bounded(&acc_full[acc], acc_phase, abort_flag));
+      if (!ready) {
+        if (lane == 0) record_error(p.err, abort_flag, kErrGemmEpilogueWait);
+        break;
+      }
+      tc_fence_after_sync();
+      const int row = m_blk * 2 * kBM + static_cast<int>(rank) * kBM + quarter * 32 + lane;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_load_32cols(t_row + c * 32, r);
+        tmem_load_wait();
+        const int col0 = n_blk * BN + c * 32;
+        if (row < p.M) {
+          uint16_t* dst = p.d + static_cast<int64_t>(row) * p.ldd + col0;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            if (col0 + g * 8 + 8 <= p.N) {
+              uint4 w;
+              w.x = cvt_bf16x2(__fmul_rn(__uint_as_float(r[g * 8 + 0]), alpha),
+                               __fmul_rn(__uint_as_float(r[g * 8 + 1]), alpha));
+              w.y = cvt_bf16x2(__fmul_rn(__uint_as_float(r[g * 8 + 2]), alpha),
+                               __fmul_rn(__uint_as_float(r[g * 8 + 3]), alpha));
+              w.z = cvt_bf16x2(__fmul_rn(__uint_as_float(r[g * 8 + 4]), alpha),
+                               __fmul_rn(__uint_as_float(r[g * 8 + 5]), alpha));
+              w.w = cvt_bf16x2(__fmul_rn(__uint_as_float(r[g * 8 + 6]), alpha),
+                               __fmul_rn(__uint_as_float(r[g * 8 + 7]), alpha));
+              *reinterpret_cast<uint4*>(dst + g * 8) = w;
+            }
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc_empty_even0 + static_cast<uint32_t>(acc * 8));
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before_sync();
+  cluster_sync_all();  // no CTA leaves while its peer may still read its shared memory
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, C::kTmemCols);
+  }
+}
+
 // ------------------------------------------------------------------ host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -351,6 +569,58 @@ cudaError_t run(const uint8_t* a, int64_t lda, const uint8_t* b, int64_t ldb, co
   return cudaGetLastError();
 }
 
+template <int BN, int STAGES>
+cudaError_t run_pair(const uint8_t* a, int64_t lda, const uint8_t* b, int64_t ldb,
+                     const GemmParams& p, const DeviceInfo& dev, cudaStream_t stream) {
+  using C = PairCfg<BN, STAGES>;
+  auto kernel = gemm_fp8_pair_kernel<BN, STAGES>;
+  static int configured_device = -1;
+  static int max_pairs = 0;
+  if (configured_device != dev.device) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(C::kSmemBytes));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+    (void)e;
+    cudaLaunchConfig_t probe = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    probe.gridDim = dim3(2 * (dev.num_sms / 2));
+    probe.blockDim = dim3(kGemmThreads);
+    probe.dynamicSmemBytes = C::kSmemBytes;
+    probe.attrs = attr;
+    probe.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &probe) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      n = dev.num_sms / 2;
+    }
+    max_pairs = n;
+    configured_device = dev.device;
+  }
+  CUtensorMap ma, mb;
+  if (!make_map_k_major(&ma, a, p.M, p.K, lda, kBM)) return cudaErrorInvalidValue;
+  if (!make_map_k_major(&mb, b, p.N, p.K, ldb, BN / 2)) return cudaErrorInvalidValue;
+  const int tiles = ((p.M + 2 * kBM - 1) / (2 * kBM)) * ((p.N + BN - 1) / BN);
+  const int pairs = tiles < max_pairs ? tiles : max_pairs;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, ma, mb, p);
+}
+
 }  // namespace
 
 cudaError_t launch_gemm(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t stream) {
@@ -381,7 +651,17 @@ cudaError_t launch_gemm(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t s
   p.N = static_cast<int>(g.N);
   // BN = 256 unless 128 pads the N edge clearly less (e.g. N = 1600).
   const int64_t pad256 = (g.N + 255) / 256 * 256, pad128 = (g.N + 127) / 128 * 128;
-  if (pad256 * 100 > pad128 * 105) {
+  const bool narrow = pad256 * 100 > pad128 * 105;
+  if (g.M > kBM) {
+    // CTA pairs: 256-row tiles.
+    if (narrow) {
+      p.idesc = make_idesc_f8(g.fmt_a, g.fmt_b, 2 * kBM, 128);
+      return run_pair<128, 8>(g.a, g.lda, g.b, g.ldb, p, dev, stream);
+    }
+    p.idesc = make_idesc_f8(g.fmt_a, g.fmt_b, 2 * kBM, 256);
+    return run_pair<256, 6>(g.a, g.lda, g.b, g.ldb, p, dev, stream);
+  }
+  if (narrow) {
     p.idesc = make_idesc_f8(g.fmt_a, g.fmt_b, kBM, 128);
     return run<128, 6, false>(g.a, g.lda, g.b, g.ldb, p, dev, stream);
   }
