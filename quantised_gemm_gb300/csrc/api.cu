@@ -231,8 +231,8 @@ fp8lin_status delayed_cast(const void* x, int64_t rows, int64_t cols, int64_t ld
 
 fp8lin_status do_gemm(const uint8_t* a, const uint8_t* b, int64_t M, int64_t N, int64_t K,
                       int64_t lda, int64_t ldb, int32_t fa, int32_t fb, const float* inv_a,
-                      const float* inv_b, void* d, int64_t ldd, void* ws, const DeviceInfo& dev,
-                      cudaStream_t stream) {
+                      const float* inv_b, void* d, int64_t ldd, void* ws, size_t ws_bytes,
+                      const DeviceInfo& dev, cudaStream_t stream) {
   if (M == 0 || N == 0) return FP8LIN_OK;
   if (K == 0) {
     cudaError_t e = cudaMemset2DAsync(d, static_cast<size_t>(ldd) * 2, 0,
@@ -254,6 +254,15 @@ fp8lin_status do_gemm(const uint8_t* a, const uint8_t* b, int64_t M, int64_t N, 
   g.d = d;
   g.ldd = ldd;
   g.ws_error = ws_error(ws);
+  if (ws_bytes > kWsSplitOffset) {
+    g.ws_tickets = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + kWsTicketOffset);
+    g.ws_split = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kWsSplitOffset);
+    g.ws_split_bytes = ws_bytes - kWsSplitOffset;
+  } else {
+    g.ws_tickets = nullptr;
+    g.ws_split = nullptr;
+    g.ws_split_bytes = 0;
+  }
   ProfScope ps(FP8LIN_PROF_GEMM, stream);
   cudaError_t e = launch_gemm(g, dev, stream);
   return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);
@@ -318,7 +327,13 @@ size_t fp8lin_workspace_bytes(int64_t M, int64_t K, int64_t N) {
   (void)M;
   (void)K;
   (void)N;
-  return kWsFixedBytes;
+  // Fixed part (error word, grid barrier, amax partials), the K-split tickets
+  // and room for the K-split partials of the GEMMs' tail wave.
+  int num_sms = 152;
+  DeviceInfo dev;
+  if (current_device_info(&dev) == cudaSuccess) num_sms = dev.num_sms;
+  else cudaGetLastError();
+  return kWsSplitOffset + gemm_split_workspace_bytes(num_sms);
 }
 
 int64_t fp8lin_single_pass_max_elems(void) {
@@ -335,7 +350,11 @@ fp8lin_status fp8lin_check(void* ws, cudaStream_t stream) {
   e = cudaMemcpy(&code, ws_error(ws), sizeof(int), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e);
   if (code == 0) return FP8LIN_OK;
+  // A wait that ran out can leave counters of the workspace mid-count: clear
+  // the error word and the GEMM split tickets so the workspace is usable again.
   e = cudaMemset(ws_error(ws), 0, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = cudaMemset(static_cast<uint8_t*>(ws) + kWsTicketOffset, 0, sizeof(int) * kWsTickets);
   if (e != cudaSuccess) return cuda_fail(e);
   return FP8LIN_ETIMEOUT;
 }
@@ -458,7 +477,8 @@ fp8lin_status fp8lin_gemm(const uint8_t* a, const uint8_t* b, int64_t M, int64_t
   DeviceInfo dev;
   fp8lin_status s = get_dev(&dev);
   if (s != FP8LIN_OK) return s;
-  return do_gemm(a, b, M, N, K, lda, ldb, fmt_a, fmt_b, inv_a, inv_b, d, ldd, ws, dev, stream);
+  return do_gemm(a, b, M, N, K, lda, ldb, fmt_a, fmt_b, inv_a, inv_b, d, ldd, ws, ws_bytes, dev,
+                 stream);
 }
 
 static fp8lin_status check_linear_sizes(int64_t M, int64_t K, int64_t N) {
@@ -504,7 +524,7 @@ fp8lin_status fp8lin_forward(const void* x, const void* w, int64_t M, int64_t K,
   if (s != FP8LIN_OK) return s;
   // y = x8 . W8^T : A = x8 [M, K], B = W8 [N, K]
   return do_gemm(x8, w8, M, N, K, K, K, FP8LIN_E4M3, FP8LIN_E4M3, sx->inv_scale, sw->inv_scale, y,
-                 N, ws, dev, stream);
+                 N, ws, ws_bytes, dev, stream);
 }
 
 fp8lin_status fp8lin_backward(const void* dy, int64_t M, int64_t K, int64_t N,
@@ -535,13 +555,13 @@ fp8lin_status fp8lin_backward(const void* dy, int64_t M, int64_t K, int64_t N,
   if (dx != nullptr) {
     // dX = dY8 . W8 : A = dY8 [M, N], B = W8^T [K, N], contract over N
     s = do_gemm(dy8, w8t, M, K, N, N, N, FP8LIN_E5M2, FP8LIN_E4M3, sdy->inv_scale, sw->inv_scale,
-                dx, K, ws, dev, stream);
+                dx, K, ws, ws_bytes, dev, stream);
     if (s != FP8LIN_OK) return s;
   }
   if (dw != nullptr) {
     // dW = dY8^T . x8 : A = dY8^T [N, M], B = x8^T [K, M], contract over M
     s = do_gemm(dy8t, x8t, N, K, M, M, M, FP8LIN_E5M2, FP8LIN_E4M3, sdy->inv_scale, sx->inv_scale,
-                dw, K, ws, dev, stream);
+                dw, K, ws, ws_bytes, dev, stream);
     if (s != FP8LIN_OK) return s;
   }
   return FP8LIN_OK;

@@ -6,19 +6,29 @@
 // LLAMA2-like model?", pytorch/ao issue 1199: the FP8Linear that replaces
 // nn.Linear) all take this form once the transposed fp8 copies exist.
 //
-// Design (one CTA per SM, persistent over output tiles):
-//   warp 0      TMA producer: 128-byte-swizzled K-major tiles of A (128 rows)
-//               and B (BN rows), 128 bytes of K per stage, STAGES-deep ring;
-//   warp 1      allocates TMEM (two BN-column fp32 accumulators) and one
-//               elected lane issues tcgen05.mma.kind::f8f6f4 (M=128, N=BN,
-//               K=32 per instruction), committing each stage back to the
-//               producer and each finished accumulator to the epilogue;
-//   warps 2..5  epilogue: tcgen05.ld of their 32 TMEM lanes, multiply by
-//               alpha = inv_a * inv_b, convert to bf16, 16-byte stores.
-// The double-buffered accumulator lets the epilogue of tile i overlap the
-// main loop of tile i+1.  For a handful of rows (small token counts) the
-// operands are swapped so the weight fills the 128-row MMA and the epilogue
-// stores the transposed result.
+// Two persistent, warp-specialised kernels (192 threads):
+//   gemm_fp8_pair_kernel  clusters of 2 CTAs sharing a 256 x BN tile
+//                         (tcgen05.mma.cta_group::2), for more than 128 rows;
+//   gemm_fp8_kernel       one CTA per 128 x BN tile (cta_group::1), for up to
+//                         128 rows; with at most 64 rows the operands are
+//                         swapped (D^T = B . A^T) so the weight fills the
+//                         128-row MMA, and the epilogue stores transposed.
+// Roles: warp 0 is the TMA producer (128-byte-swizzled K-major boxes, 128
+// bytes of K per stage, STAGES-deep mbarrier ring); warp 1 allocates TMEM
+// (two BN-column fp32 accumulators) and one lane issues the MMAs; warps 2..5
+// are the epilogue (tcgen05.ld of their 32 TMEM lanes, scale by
+// alpha = inv_a * inv_b, bf16, TMA stores of 32 x 32 boxes staged in shared
+// memory).  The double-buffered accumulator overlaps the epilogue of one work
+// unit with the main loop of the next.
+//
+// Work units: the tiles are dealt round-robin to the persistent CTAs (pairs).
+// When the tiles do not fill one wave (few rows: M = 16 or 256 against a
+// 4096-wide weight) and the K loop is long, each of the R tiles is split into
+// S slices of the K loop (S = floor(slots / R)), so the work runs on all slots;
+// every slice writes its fp32 partial to the workspace, waits (bounded) until
+// all S slices of its 32-row group have written theirs, then sums all S
+// partials of its own 1/S share of the columns in slice order --
+// deterministic -- and writes the bf16 result.
 //
 // Every wait on an mbarrier is bounded (kWaitLimitNs); a wait that runs out
 // records an error code in the workspace, raises a CTA-wide abort flag, lets
@@ -35,10 +45,292 @@
 namespace fp8lin {
 namespace {
 
-constexpr int kBM = 128;           // tile rows (MMA M)
+constexpr int kBM = 128;           // rows of A per CTA (MMA M per CTA)
 constexpr int kBK = 128;           // bytes (= 8-bit elements) of K per stage
 constexpr int kMmaK = 32;          // K of one kind::f8f6f4 MMA
 constexpr int kGemmThreads = 192;  // 6 warps
+constexpr int kBoxBytes = 32 * 32 * 2;              // one 32x32 bf16 epilogue box
+constexpr int kEpiStagingBytes = 4 * 2 * kBoxBytes;  // two boxes per epilogue warp
+constexpr int kMaxSplit = 8;
+
+struct GemmParams {
+  int M, N, K;          // kernel view: A has M rows, B has N rows, contraction K
+  uint32_t idesc;
+  const float* inv_a;
+  const float* inv_b;
+  uint16_t* d;          // bf16 output
+  int64_t ldd;          // elements
+  int* err;
+  int t_full;           // tiles [0, t_full) run whole
+  int s_tail;           // tiles [t_full, tiles) run as s_tail K slices each
+  float* partials;      // split slices' fp32 partials (workspace)
+  int* tickets;         // per (tail tile, 32-row group): arrivals, finished (workspace, zero)
+};
+
+struct Unit {
+  int tile, split, nsplit, kb0, kb1;
+};
+
+__device__ __forceinline__ Unit unit_of(int u, const GemmParams& p, int num_kb) {
+  Unit r;
+  if (u < p.t_full) {
+    r.tile = u;
+    r.split = 0;
+    r.nsplit = 1;
+    r.kb0 = 0;
+    r.kb1 = num_kb;
+  } else {
+    const int v = u - p.t_full;
+    r.tile = p.t_full + v / p.s_tail;
+    r.split = v % p.s_tail;
+    r.nsplit = p.s_tail;
+    const int per = (num_kb + p.s_tail - 1) / p.s_tail;
+    r.kb0 = r.split * per;
+    r.kb1 = min(num_kb, r.kb0 + per);
+  }
+  return r;
+}
+
+__device__ __forceinline__ int num_units(const GemmParams& p, int num_tiles) {
+  return p.t_full + (num_tiles - p.t_full) * p.s_tail;
+}
+
+__device__ __forceinline__ void record_error(int* err, volatile int* abort_flag, int code) {
+  atomicCAS(err, 0, code);
+  *abort_flag = 1;
+}
+
+template <int kChunk>
+__device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, uint32_t (&r)[kChunk]) {
+  if constexpr (kChunk == 32)
+    tmem_load_32cols(taddr, r);
+  else
+    tmem_load_16cols(taddr, r);
+  tmem_load_wait();
+}
+
+// Scale one 32-row x 32-column accumulator chunk (this lane's row in r[]),
+// convert to bf16, stage it in `box` and store it at (row0, col0) of D with
+// TMA.  The box's rows are 64 bytes with 16-byte chunks swizzled as the
+// 64-byte TMA swizzle expects (chunk ^= (row >> 1) & 3), which also keeps the
+// warp's shared-memory writes free of bank conflicts.
+__device__ __forceinline__ void store_chunk_tma(const uint32_t (&r)[32], float alpha, uint8_t* box,
+                                                const CUtensorMap* tmD, int row0, int col0,
+                                                int lane) {
+  uint32_t w[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    w[j] = cvt_bf16x2(__fmul_rn(__uint_as_float(r[2 * j]), alpha),
+                      __fmul_rn(__uint_as_float(r[2 * j + 1]), alpha));
+  if (lane == 0) bulk_wait_group_read<1>();  // this box's previous store has read it
+  __syncwarp();
+  uint8_t* rowp = box + lane * 64;
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    *reinterpret_cast<uint4*>(rowp + ((q ^ sw) << 4)) =
+        make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+  fence_proxy_async_shared();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tmD, box, col0, row0);
+    bulk_commit_group();
+  }
+}
+
+// Final bf16 output of one chunk of raw fp32 accumulators (this lane's row).
+template <int kChunk, bool kTransStore>
+__device__ __forceinline__ void emit_chunk(const uint32_t (&r)[kChunk], float alpha,
+                                           const GemmParams& p, const CUtensorMap* tmD,
+                                           uint8_t* boxes, uint32_t& chunk_no, int row0, int col0,
+                                           int lane) {
+  if constexpr (!kTransStore) {
+    static_assert(kChunk == 32, "TMA-store epilogue works on 32-column chunks");
+    store_chunk_tma(r, alpha, boxes + (chunk_no & 1) * kBoxBytes, tmD, row0, col0, lane);
+    ++chunk_no;
+  } else {
+    // kernel element (row, col) is output element (col, row)
+    const int row = row0 + lane;
+    if (row < p.M) {
+#pragma unroll
+      for (int j = 0; j < kChunk; ++j) {
+        if (col0 + j < p.N) {
+          const uint32_t b = cvt_bf16x2(__fmul_rn(__uint_as_float(r[j]), alpha), 0.0f) & 0xFFFFu;
+          p.d[static_cast<int64_t>(col0 + j) * p.ldd + row] = static_cast<uint16_t>(b);
+        }
+      }
+    }
+  }
+}
+
+// Partial of one (slice, 32-row group): chunk c is stored as [c][q][lane][4]
+// floats so a warp's 16-byte stores and loads are contiguous.
+template <int kChunk>
+__device__ __forceinline__ void store_partial(float* region, int c, const uint32_t (&r)[kChunk],
+                                              int lane) {
+#pragma unroll
+  for (int q = 0; q < kChunk / 4; ++q)
+    __stcg(reinterpret_cast<float4*>(region + ((c * (kChunk / 4) + q) * 32 + lane) * 4),
+           make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                       __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3])));
+}
+
+template <int kChunk>
+__device__ __forceinline__ void add_partial(const float* region, int c, float (&acc)[kChunk],
+                                            int lane) {
+#pragma unroll
+  for (int q = 0; q < kChunk / 4; ++q) {
+    const float4 v =
+        __ldcg(reinterpret_cast<const float4*>(region + ((c * (kChunk / 4) + q) * 32 + lane) * 4));
+    acc[4 * q] += v.x;
+    acc[4 * q + 1] += v.y;
+    acc[4 * q + 2] += v.z;
+    acc[4 * q + 3] += v.w;
+  }
+}
+
+__device__ __forceinline__ int ld_acquire_int(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Epilogue of one work unit for one warp: 32 rows (row0..row0+31) x BN
+// columns starting at col_base, accumulator at TMEM address t_row.  `group`
+// identifies the 32-row group inside the tile (G groups per tile).  Arrives on
+// the accumulator-empty barrier (via `release`) as soon as TMEM is read.
+//
+// A K slice of a split tail tile writes its raw fp32 partial, announces it on
+// the group's ticket, waits (bounded) until all S slices have done so, then
+// reduces its own 1/S share of the columns: every slice sums all S partials
+// of those columns in slice order (deterministic) and stores the bf16
+// result.  The slices of a tail tile run on distinct CTAs as their last unit,
+// all resident at once, so the wait cannot block on itself.  The last slice to
+// finish clears both counters for the next call.
+template <int BN, bool kTransStore, typename Release>
+__device__ __forceinline__ void epilogue_unit(const GemmParams& p, const Unit& u, int G, int group,
+                                              int row0, int col_base, uint32_t t_row, float alpha,
+                                              const CUtensorMap* tmD, uint8_t* boxes,
+                                              uint32_t& chunk_no, int lane,
+                                              volatile int* abort_flag, Release release) {
+  constexpr int kChunk = (BN % 32 == 0) ? 32 : 16;
+  const bool active = row0 < p.M;  // warp-uniform
+  int nch = 0;                     // chunks with at least one column inside D
+  while (nch < BN / kChunk && col_base + nch * kChunk < p.N) ++nch;
+  if (u.nsplit == 1) {
+    if (active && nch > 0) {
+      // Two chunks per iteration: the TMEM load of the second is in flight
+      // while the first is converted and stored.
+      uint32_t ra[kChunk], rb[kChunk];
+#pragma unroll 1
+      for (int c = 0; c < nch; c += 2) {
+        if (c + 1 < nch) {
+          if constexpr (kChunk == 32) {
+            tmem_load_32cols(t_row + c * kChunk, ra);
+            tmem_load_32cols(t_row + (c + 1) * kChunk, rb);
+          } else {
+            tmem_load_16cols(t_row + c * kChunk, ra);
+            tmem_load_16cols(t_row + (c + 1) * kChunk, rb);
+          }
+          tmem_load_wait();
+          emit_chunk<kChunk, kTransStore>(ra, alpha, p, tmD, boxes, chunk_no, row0,
+                                          col_base + c * kChunk, lane);
+          emit_chunk<kChunk, kTransStore>(rb, alpha, p, tmD, boxes, chunk_no, row0,
+                                          col_base + (c + 1) * kChunk, lane);
+        } else {
+          tmem_load_chunk<kChunk>(t_row + c * kChunk, ra);
+          emit_chunk<kChunk, kTransStore>(ra, alpha, p, tmD, boxes, chunk_no, row0,
+                                          col_base + c * kChunk, lane);
+        }
+      }
+    }
+    release();
+    return;
+  }
+  const int tail_tile = u.tile - p.t_full;
+  const size_t region_floats = static_cast<size_t>(32) * BN;
+  float* mine = p.partials + ((static_cast<size_t>(tail_tile) * u.nsplit + u.split) * G + group) *
+                                 region_floats;
+  if (active) {
+    uint32_t ra[kChunk], rb[kChunk];
+#pragma unroll 1
+    for (int c = 0; c < nch; c += 2) {
+      if (c + 1 < nch) {
+        if constexpr (kChunk == 32) {
+          tmem_load_32cols(t_row + c * kChunk, ra);
+          tmem_load_32cols(t_row + (c + 1) * kChunk, rb);
+        } else {
+          tmem_load_16cols(t_row + c * kChunk, ra);
+          tmem_load_16cols(t_row + (c + 1) * kChunk, rb);
+        }
+        tmem_load_wait();
+        store_partial<kChunk>(mine, c, ra, lane);
+        store_partial<kChunk>(mine, c + 1, rb, lane);
+      } else {
+        tmem_load_chunk<kChunk>(t_row + c * kChunk, ra);
+        store_partial<kChunk>(mine, c, ra, lane);
+      }
+    }
+  }
+  release();
+  if (!active) return;
+  __threadfence();
+  __syncwarp();
+  int* ticket = p.tickets + 2 * (tail_tile * G + group);
+  int* done = ticket + 1;
+  bool all_in = true;
+  if (lane == 0) {
+    atomicAdd(ticket, 1);
+    if (ld_acquire_int(ticket) < u.nsplit) {
+      const uint64_t t0 = global_timer_ns();
+      while (ld_acquire_int(ticket) < u.nsplit) {
+        if (*abort_flag || global_timer_ns() - t0 > kWaitLimitNs) {
+          all_in = false;
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+  }
+  all_in = __shfl_sync(0xFFFFFFFFu, all_in ? 1 : 0, 0) != 0;
+  if (!all_in) {
+    if (lane == 0) record_error(p.err, abort_flag, kErrGemmEpilogueWait);
+    return;
+  }
+  __threadfence();
+  // This slice's share of the chunks.
+  const int share = (nch + u.nsplit - 1) / u.nsplit;
+  const int c_lo = u.split * share;
+  const int c_hi = min(nch, c_lo + share);
+#pragma unroll 1
+  for (int c = c_lo; c < c_hi; ++c) {
+    float acc[kChunk];
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) acc[j] = 0.0f;
+    for (int s2 = 0; s2 < u.nsplit; ++s2) {  // fixed slice order: deterministic sums
+      const float* region =
+          p.partials + ((static_cast<size_t>(tail_tile) * u.nsplit + s2) * G + group) *
+                           region_floats;
+      add_partial<kChunk>(region, c, acc, lane);
+    }
+    uint32_t r[kChunk];
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) r[j] = __float_as_uint(acc[j]);
+    emit_chunk<kChunk, kTransStore>(r, alpha, p, tmD, boxes, chunk_no, row0,
+                                    col_base + c * kChunk, lane);
+  }
+  __syncwarp();
+  if (lane == 0) {
+    // Everyone has read the ticket before anyone can finish: the last to
+    // finish may clear both counters.
+    if (atomicAdd(done, 1) == u.nsplit - 1) {
+      atomicExch(ticket, 0);
+      atomicExch(done, 0);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ one-CTA kernel
 
 template <int BN, int STAGES>
 struct Cfg {
@@ -51,37 +343,24 @@ struct Cfg {
                                    : 2 * BN <= 256 ? 256
                                                    : 512;
   static constexpr int kBarrierBytes = 256;
-  static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(STAGES) * kStageBytes + kBarrierBytes;
+  static constexpr size_t kSmemBytes =
+      1024 + static_cast<size_t>(STAGES) * kStageBytes + kEpiStagingBytes + kBarrierBytes;
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128");
   static_assert(kBBytes % 1024 == 0, "B tiles keep 1024-byte alignment");
 };
 
-struct GemmParams {
-  int M, N, K;          // kernel view: A has M rows, B has N rows, contraction K
-  uint32_t idesc;
-  const float* inv_a;
-  const float* inv_b;
-  uint16_t* d;          // bf16 output
-  int64_t ldd;          // elements
-  int* err;
-};
-
-__device__ __forceinline__ void record_error(int* err, volatile int* abort_flag, int code) {
-  atomicCAS(err, 0, code);
-  *abort_flag = 1;
-}
-
 template <int BN, int STAGES, bool kTransStore>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const GemmParams p) {
+                    const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
   using C = Cfg<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * C::kABytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * C::kBBytes);
+  uint8_t* sEpi = sB + STAGES * C::kBBytes;  // 1024-aligned
+  uint64_t* full = reinterpret_cast<uint64_t*>(sEpi + kEpiStagingBytes);
   uint64_t* empty = full + STAGES;
   uint64_t* acc_full = empty + STAGES;   // [2]
   uint64_t* acc_empty = acc_full + 2;    // [2]
@@ -90,10 +369,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int num_m = (p.M + kBM - 1) / kBM;
   const int num_n = (p.N + BN - 1) / BN;
-  const int num_tiles = num_m * num_n;
+  const int num_tiles = ((p.M + kBM - 1) / kBM) * num_n;
   const int num_kb = (p.K + kBK - 1) / kBK;
+  const int units = num_units(p, num_tiles);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -109,6 +388,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     fence_barrier_init();
     tma_prefetch_map(&tmA);
     tma_prefetch_map(&tmB);
+    if (!kTransStore) tma_prefetch_map(&tmD);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::kTmemCols);
@@ -128,9 +408,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int m_blk = tile / num_n, n_blk = tile % num_n;
-        for (int kb = 0; kb < num_kb; ++kb) {
+      for (int ui = blockIdx.x; ui < units && ok; ui += gridDim.x) {
+        const Unit u = unit_of(ui, p, num_kb);
+        const int m_blk = u.tile / num_n, n_blk = u.tile % num_n;
+        for (int kb = u.kb0; kb < u.kb1; ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
             break;
@@ -165,14 +446,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       bool issued = false;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      for (int ui = blockIdx.x; ui < units && ok; ui += gridDim.x) {
+        const Unit u = unit_of(ui, p, num_kb);
         if (!mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = u.kb0; kb < u.kb1; ++kb) {
           if (!mbar_wait_bounded(&full[stage], phase, abort_flag)) {
             ok = false;
             break;
@@ -185,7 +467,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // advance the start address by k * 32 bytes (encoded >> 4)
             mma_f8f6f4(d_tmem, a_desc + static_cast<uint64_t>(k * (kMmaK >> 4)),
                        b_desc + static_cast<uint64_t>(k * (kMmaK >> 4)), p.idesc,
-                       (kb > 0 || k > 0) ? 1u : 0u);
+                       (kb > u.kb0 || k > 0) ? 1u : 0u);
           }
           issued = true;
           mma_commit(&empty[stage]);
@@ -215,10 +497,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;  // TMEM lanes this warp may read: 32*quarter..+31
     const float alpha = __fmul_rn(*p.inv_a, *p.inv_b);
+    uint8_t* boxes = sEpi + (warp - 2) * 2 * kBoxBytes;
+    uint32_t chunk_no = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      const int m_blk = tile / num_n, n_blk = tile % num_n;
+    for (int ui = blockIdx.x; ui < units; ui += gridDim.x) {
+      const Unit u = unit_of(ui, p, num_kb);
+      const int m_blk = u.tile / num_n, n_blk = u.tile % num_n;
       // tcgen05.ld below is warp-collective: take the decision warp-uniformly.
       const bool ready = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&acc_full[acc], acc_phase,
                                                                   abort_flag));
@@ -227,61 +512,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         break;
       }
       tc_fence_after_sync();
-      const int row = m_blk * kBM + quarter * 32 + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
-      constexpr int kChunk = (BN % 32 == 0) ? 32 : 16;
-#pragma unroll 1
-      for (int c = 0; c < BN / kChunk; ++c) {
-        float v[kChunk];
-        if constexpr (kChunk == 32) {
-          uint32_t r[32];
-          tmem_load_32cols(t_row + c * 32, r);
-          tmem_load_wait();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__uint_as_float(r[j]), alpha);
-        } else {
-          uint32_t r[16];
-          tmem_load_16cols(t_row + c * 16, r);
-          tmem_load_wait();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(__uint_as_float(r[j]), alpha);
-        }
-        const int col0 = n_blk * BN + c * kChunk;
-        if (row < p.M) {
-          if constexpr (!kTransStore) {
-            uint16_t* dst = p.d + static_cast<int64_t>(row) * p.ldd + col0;
-#pragma unroll
-            for (int g = 0; g < kChunk / 8; ++g) {
-              if (col0 + g * 8 + 8 <= p.N) {
-                uint4 w;
-                w.x = cvt_bf16x2(v[g * 8 + 0], v[g * 8 + 1]);
-                w.y = cvt_bf16x2(v[g * 8 + 2], v[g * 8 + 3]);
-                w.z = cvt_bf16x2(v[g * 8 + 4], v[g * 8 + 5]);
-                w.w = cvt_bf16x2(v[g * 8 + 6], v[g * 8 + 7]);
-                *reinterpret_cast<uint4*>(dst + g * 8) = w;
-              }
-            }
-          } else {
-            // kernel element (row, col) is output element (col, row)
-#pragma unroll
-            for (int j = 0; j < kChunk; ++j) {
-              if (col0 + j < p.N) {
-                const uint32_t b = cvt_bf16x2(v[j], 0.0f) & 0xFFFFu;
-                p.d[static_cast<int64_t>(col0 + j) * p.ldd + row] = static_cast<uint16_t>(b);
-              }
-            }
-          }
-        }
-      }
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      const int acc_now = acc;
+      epilogue_unit<BN, kTransStore>(p, u, 4, quarter, m_blk * kBM + quarter * 32, n_blk * BN,
+                                     t_row, alpha, &tmD, boxes, chunk_no, lane, abort_flag, [&] {
+                                       tc_fence_before_sync();
+                                       __syncwarp();
+                                       if (lane == 0) mbar_arrive(&acc_empty[acc_now]);
+                                     });
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
       }
     }
+    if (lane == 0) bulk_wait_group<0>();  // stores done before the staging memory goes away
   }
 
   __syncwarp();  // reconverge the producer / MMA warps around their elected lane
@@ -312,7 +557,8 @@ struct PairCfg {
   static constexpr int kBBytes = (BN / 2) * kBK;        // BN/2 rows of B per CTA
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 2 * BN <= 256 ? 256 : 512;
-  static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(STAGES) * kStageBytes + 256;
+  static constexpr size_t kSmemBytes =
+      1024 + static_cast<size_t>(STAGES) * kStageBytes + kEpiStagingBytes + 256;
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "MMA N for M=256");
   static_assert(kBBytes % 1024 == 0, "B tiles keep 1024-byte alignment");
 };
@@ -320,14 +566,16 @@ struct PairCfg {
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_fp8_pair_kernel(const __grid_constant__ CUtensorMap tmA,
-                         const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+                         const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
   using C = PairCfg<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * C::kABytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * C::kBBytes);
+  uint8_t* sEpi = sB + STAGES * C::kBBytes;  // 1024-aligned
+  uint64_t* full = reinterpret_cast<uint64_t*>(sEpi + kEpiStagingBytes);
   uint64_t* empty = full + STAGES;
   uint64_t* acc_full = empty + STAGES;   // [2]
   uint64_t* acc_empty = acc_full + 2;    // [2]
@@ -339,10 +587,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t rank = cluster_ctarank();      // 0: issues the MMAs
   const int pair = static_cast<int>(cluster_id_x());
   const int num_pairs = static_cast<int>(cluster_count_x());
-  const int num_m = (p.M + 2 * kBM - 1) / (2 * kBM);
   const int num_n = (p.N + BN - 1) / BN;
-  const int num_tiles = num_m * num_n;
+  const int num_tiles = ((p.M + 2 * kBM - 1) / (2 * kBM)) * num_n;
   const int num_kb = (p.K + kBK - 1) / kBK;
+  const int units = num_units(p, num_tiles);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -358,6 +606,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     fence_barrier_init();
     tma_prefetch_map(&tmA);
     tma_prefetch_map(&tmB);
+    tma_prefetch_map(&tmD);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, C::kTmemCols);
@@ -374,9 +623,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs) {
-        const int m_blk = tile / num_n, n_blk = tile % num_n;
-        for (int kb = 0; kb < num_kb; ++kb) {
+      for (int ui = pair; ui < units && ok; ui += num_pairs) {
+        const Unit u = unit_of(ui, p, num_kb);
+        const int m_blk = u.tile / num_n, n_blk = u.tile % num_n;
+        for (int kb = u.kb0; kb < u.kb1; ++kb) {
           if (!mbar_wait_cluster_bounded(&empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
             break;
@@ -404,14 +654,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       bool issued = false;
-      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs) {
+      for (int ui = pair; ui < units && ok; ui += num_pairs) {
+        const Unit u = unit_of(ui, p, num_kb);
         if (!mbar_wait_cluster_bounded(&acc_empty[acc], acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = u.kb0; kb < u.kb1; ++kb) {
           if (!mbar_wait_cluster_bounded(&full[stage], phase, abort_flag)) {
             ok = false;
             break;
@@ -423,7 +674,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           for (int k = 0; k < kBK / kMmaK; ++k) {
             mma_f8f6f4_pair(d_tmem, a_desc + static_cast<uint64_t>(k * (kMmaK >> 4)),
                             b_desc + static_cast<uint64_t>(k * (kMmaK >> 4)), p.idesc,
-                            (kb > 0 || k > 0) ? 1u : 0u);
+                            (kb > u.kb0 || k > 0) ? 1u : 0u);
           }
           issued = true;
           mma_commit_pair_multicast(&empty[stage], 0x3);
@@ -453,10 +704,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int quarter = warp & 3;
     const float alpha = __fmul_rn(*p.inv_a, *p.inv_b);
     const uint32_t acc_empty_even0 = map_to_cta(smem_addr(&acc_empty[0]), 0);
+    uint8_t* boxes = sEpi + (warp - 2) * 2 * kBoxBytes;
+    uint32_t chunk_no = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = pair; tile < num_tiles; tile += num_pairs) {
-      const int m_blk = tile / num_n, n_blk = tile % num_n;
+    for (int ui = pair; ui < units; ui += num_pairs) {
+      const Unit u = unit_of(ui, p, num_kb);
+      const int m_blk = u.tile / num_n, n_blk = u.tile % num_n;
       const bool ready = __all_sync(
           0xFFFFFFFFu, mbar_wait_cluster_bounded(&acc_full[acc], acc_phase, abort_flag));
       if (!ready) {
@@ -464,42 +718,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         break;
       }
       tc_fence_after_sync();
-      const int row = m_blk * 2 * kBM + static_cast<int>(rank) * kBM + quarter * 32 + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_load_32cols(t_row + c * 32, r);
-        tmem_load_wait();
-        const int col0 = n_blk * BN + c * 32;
-        if (row < p.M) {
-          uint16_t* dst = p.d + static_cast<int64_t>(row) * p.ldd + col0;
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            if (col0 + g * 8 + 8 <= p.N) {
-              uint4 w;
-              w.x = cvt_bf16x2(__fmul_rn(__uint_as_float(r[g * 8 + 0]), alpha),
-                               __fmul_rn(__uint_as_float(r[g * 8 + 1]), alpha));
-              w.y = cvt_bf16x2(__fmul_rn(__uint_as_float(r[g * 8 + 2]), alpha),
-                               __fmul_rn(__uint_as_float(r[g * 8 + 3]), alpha));
-              w.z = cvt_bf16x2(__fmul_rn(__uint_as_float(r[g * 8 + 4]), alpha),
-                               __fmul_rn(__uint_as_float(r[g * 8 + 5]), alpha));
-              w.w = cvt_bf16x2(__fmul_rn(__uint_as_float(r[g * 8 + 6]), alpha),
-                               __fmul_rn(__uint_as_float(r[g * 8 + 7]), alpha));
-              *reinterpret_cast<uint4*>(dst + g * 8) = w;
-            }
-          }
-        }
-      }
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(acc_empty_even0 + static_cast<uint32_t>(acc * 8));
+      const int group = static_cast<int>(rank) * 4 + quarter;
+      const uint32_t release_addr = acc_empty_even0 + static_cast<uint32_t>(acc * 8);
+      epilogue_unit<BN, false>(p, u, 8, group, m_blk * 2 * kBM + group * 32, n_blk * BN, t_row,
+                               alpha, &tmD, boxes, chunk_no, lane, abort_flag, [&] {
+                                 tc_fence_before_sync();
+                                 __syncwarp();
+                                 if (lane == 0) mbar_arrive_cluster(release_addr);
+                               });
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
       }
     }
+    if (lane == 0) bulk_wait_group<0>();  // stores done before the staging memory goes away
   }
 
   __syncwarp();
@@ -548,9 +782,55 @@ bool make_map_k_major(CUtensorMap* map, const uint8_t* base, int64_t rows, int64
   return r == CUDA_SUCCESS;
 }
 
+// 2-D map over the bf16 output [rows, cols] (row stride ldd elements), box
+// 32 x 32, 64-byte swizzle, for the epilogue's TMA stores.
+bool make_map_out(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ldd) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldd) * 2};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Choose the tail split: tiles beyond the last full wave of `slots`
+// persistent units are cut into S K-slices, if the workspace holds their
+// partials (`group_rows` rows of BN fp32 per slice and 32-row group).
+void plan_split(GemmParams& p, int tiles, int slots, int num_kb, int rows_per_tile, int bn,
+                const GemmArgs& g) {
+  p.t_full = tiles;
+  p.s_tail = 1;
+  p.partials = nullptr;
+  p.tickets = nullptr;
+  // Only when the tiles do not fill one wave and the K loop is long: splitting
+  // the tail of a multi-wave grid, or a short K loop, measured slower than
+  // running the tiles whole (the partial write and reduce cost more).
+  if (g.ws_split == nullptr || slots < 2 || tiles >= slots || num_kb < 16) return;
+  const int tail = tiles % slots;
+  int s = slots / tail;
+  if (s > kMaxSplit) s = kMaxSplit;
+  if (s > num_kb) s = num_kb;
+  if (s < 2) return;
+  const int per = (num_kb + s - 1) / s;
+  s = (num_kb + per - 1) / per;  // no empty slice
+  if (s < 2) return;
+  const size_t groups = static_cast<size_t>(rows_per_tile) / 32;
+  const size_t need_floats = static_cast<size_t>(tail) * s * rows_per_tile * bn;
+  const size_t need_tickets = 2 * static_cast<size_t>(tail) * groups;
+  if (need_floats * sizeof(float) > g.ws_split_bytes || need_tickets > kWsTickets) return;
+  p.t_full = tiles - tail;
+  p.s_tail = s;
+  p.partials = g.ws_split;
+  p.tickets = g.ws_tickets;
+}
+
 template <int BN, int STAGES, bool kTransStore>
-cudaError_t run(const uint8_t* a, int64_t lda, const uint8_t* b, int64_t ldb, const GemmParams& p,
-                const DeviceInfo& dev, cudaStream_t stream) {
+cudaError_t run(const uint8_t* a, int64_t lda, const uint8_t* b, int64_t ldb, GemmParams p,
+                const GemmArgs& g, const DeviceInfo& dev, cudaStream_t stream) {
   using C = Cfg<BN, STAGES>;
   auto kernel = gemm_fp8_kernel<BN, STAGES, kTransStore>;
   static int configured_device = -1;
@@ -560,18 +840,24 @@ cudaError_t run(const uint8_t* a, int64_t lda, const uint8_t* b, int64_t ldb, co
     if (e != cudaSuccess) return e;
     configured_device = dev.device;
   }
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, md;
   if (!make_map_k_major(&ma, a, p.M, p.K, lda, kBM)) return cudaErrorInvalidValue;
   if (!make_map_k_major(&mb, b, p.N, p.K, ldb, BN)) return cudaErrorInvalidValue;
+  if (kTransStore)
+    md = mb;  // unused: the transposed store writes D directly
+  else if (!make_map_out(&md, p.d, p.M, p.N, p.ldd))
+    return cudaErrorInvalidValue;
   const int tiles = ((p.M + kBM - 1) / kBM) * ((p.N + BN - 1) / BN);
-  const int grid = tiles < dev.num_sms ? tiles : dev.num_sms;
-  kernel<<<grid, kGemmThreads, C::kSmemBytes, stream>>>(ma, mb, p);
+  plan_split(p, tiles, dev.num_sms, (p.K + kBK - 1) / kBK, kBM, BN, g);
+  const int units = p.t_full + (tiles - p.t_full) * p.s_tail;
+  const int grid = units < dev.num_sms ? units : dev.num_sms;
+  kernel<<<grid, kGemmThreads, C::kSmemBytes, stream>>>(ma, mb, md, p);
   return cudaGetLastError();
 }
 
 template <int BN, int STAGES>
-cudaError_t run_pair(const uint8_t* a, int64_t lda, const uint8_t* b, int64_t ldb,
-                     const GemmParams& p, const DeviceInfo& dev, cudaStream_t stream) {
+cudaError_t run_pair(const uint8_t* a, int64_t lda, const uint8_t* b, int64_t ldb, GemmParams p,
+                     const GemmArgs& g, const DeviceInfo& dev, cudaStream_t stream) {
   using C = PairCfg<BN, STAGES>;
   auto kernel = gemm_fp8_pair_kernel<BN, STAGES>;
   static int configured_device = -1;
@@ -580,8 +866,6 @@ cudaError_t run_pair(const uint8_t* a, int64_t lda, const uint8_t* b, int64_t ld
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(C::kSmemBytes));
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
-    (void)e;
     cudaLaunchConfig_t probe = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -601,11 +885,14 @@ cudaError_t run_pair(const uint8_t* a, int64_t lda, const uint8_t* b, int64_t ld
     max_pairs = n;
     configured_device = dev.device;
   }
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, md;
   if (!make_map_k_major(&ma, a, p.M, p.K, lda, kBM)) return cudaErrorInvalidValue;
   if (!make_map_k_major(&mb, b, p.N, p.K, ldb, BN / 2)) return cudaErrorInvalidValue;
+  if (!make_map_out(&md, p.d, p.M, p.N, p.ldd)) return cudaErrorInvalidValue;
   const int tiles = ((p.M + 2 * kBM - 1) / (2 * kBM)) * ((p.N + BN - 1) / BN);
-  const int pairs = tiles < max_pairs ? tiles : max_pairs;
+  plan_split(p, tiles, max_pairs, (p.K + kBK - 1) / kBK, 2 * kBM, BN, g);
+  const int units = p.t_full + (tiles - p.t_full) * p.s_tail;
+  const int pairs = units < max_pairs ? units : max_pairs;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -618,10 +905,16 @@ cudaError_t run_pair(const uint8_t* a, int64_t lda, const uint8_t* b, int64_t ld
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, ma, mb, p);
+  return cudaLaunchKernelEx(&cfg, kernel, ma, mb, md, p);
 }
 
 }  // namespace
+
+size_t gemm_split_workspace_bytes(int num_sms) {
+  // At most `num_sms` one-CTA slices of 128 x 256 fp32 (or num_sms / 2 pair
+  // slices of 256 x 256): the tail split never has more slices than slots.
+  return static_cast<size_t>(num_sms) * kBM * 256 * sizeof(float);
+}
 
 cudaError_t launch_gemm(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t stream) {
   GemmParams p;
@@ -635,17 +928,16 @@ cudaError_t launch_gemm(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t s
     // Few rows: D^T = B . A^T, the weight-side operand fills the 128-row MMA.
     p.M = static_cast<int>(g.N);
     p.N = static_cast<int>(g.M);
-    p.idesc = 0;
     if (g.M <= 16) {
       p.idesc = make_idesc_f8(g.fmt_b, g.fmt_a, kBM, 16);
-      return run<16, 8, true>(g.b, g.ldb, g.a, g.lda, p, dev, stream);
+      return run<16, 8, true>(g.b, g.ldb, g.a, g.lda, p, g, dev, stream);
     }
     if (g.M <= 32) {
       p.idesc = make_idesc_f8(g.fmt_b, g.fmt_a, kBM, 32);
-      return run<32, 8, true>(g.b, g.ldb, g.a, g.lda, p, dev, stream);
+      return run<32, 8, true>(g.b, g.ldb, g.a, g.lda, p, g, dev, stream);
     }
     p.idesc = make_idesc_f8(g.fmt_b, g.fmt_a, kBM, 64);
-    return run<64, 8, true>(g.b, g.ldb, g.a, g.lda, p, dev, stream);
+    return run<64, 8, true>(g.b, g.ldb, g.a, g.lda, p, g, dev, stream);
   }
   p.M = static_cast<int>(g.M);
   p.N = static_cast<int>(g.N);
@@ -656,17 +948,17 @@ cudaError_t launch_gemm(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t s
     // CTA pairs: 256-row tiles.
     if (narrow) {
       p.idesc = make_idesc_f8(g.fmt_a, g.fmt_b, 2 * kBM, 128);
-      return run_pair<128, 8>(g.a, g.lda, g.b, g.ldb, p, dev, stream);
+      return run_pair<128, 8>(g.a, g.lda, g.b, g.ldb, p, g, dev, stream);
     }
     p.idesc = make_idesc_f8(g.fmt_a, g.fmt_b, 2 * kBM, 256);
-    return run_pair<256, 6>(g.a, g.lda, g.b, g.ldb, p, dev, stream);
+    return run_pair<256, 6>(g.a, g.lda, g.b, g.ldb, p, g, dev, stream);
   }
   if (narrow) {
     p.idesc = make_idesc_f8(g.fmt_a, g.fmt_b, kBM, 128);
-    return run<128, 6, false>(g.a, g.lda, g.b, g.ldb, p, dev, stream);
+    return run<128, 6, false>(g.a, g.lda, g.b, g.ldb, p, g, dev, stream);
   }
   p.idesc = make_idesc_f8(g.fmt_a, g.fmt_b, kBM, 256);
-  return run<256, 4, false>(g.a, g.lda, g.b, g.ldb, p, dev, stream);
+  return run<256, 4, false>(g.a, g.lda, g.b, g.ldb, p, g, dev, stream);
 }
 
 }  // namespace fp8lin

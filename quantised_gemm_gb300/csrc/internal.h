@@ -15,6 +15,9 @@ constexpr size_t kWsAmaxOffset = 128;     // uint32: amax bits (single pass)
 constexpr size_t kWsPartialOffset = 256;  // uint32[kMaxPartials]: REDUCTION partial maxima
 constexpr int kMaxPartials = 4096;
 constexpr size_t kWsFixedBytes = kWsPartialOffset + sizeof(uint32_t) * kMaxPartials;
+constexpr size_t kWsTicketOffset = (kWsFixedBytes + 255) / 256 * 256;  // int32[kWsTickets]
+constexpr int kWsTickets = 4096;
+constexpr size_t kWsSplitOffset = kWsTicketOffset + sizeof(int) * kWsTickets;  // fp32 partials
 
 // Device error codes written at kWsErrorOffset.
 enum DeviceError : int {
@@ -112,7 +115,13 @@ struct GemmArgs {
   void* d;            // bf16 [M, N], row stride ldd elements
   int64_t ldd;
   int* ws_error;
+  int* ws_tickets;     // kWsTickets zero-initialised counters (nullptr: no K split)
+  float* ws_split;     // fp32 partials of K-split tail tiles (nullptr: no K split)
+  size_t ws_split_bytes;
 };
 cudaError_t launch_gemm(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t stream);
+
+// Workspace bytes the tail K split can use at most on a device with num_sms SMs.
+size_t gemm_split_workspace_bytes(int num_sms);
 
 }  // namespace fp8lin

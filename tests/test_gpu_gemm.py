@@ -40,6 +40,8 @@ CASES = [
     (48, 208, 160),         # few rows, ragged
     (64, 272, 320),
     (1040, 784, 512),
+    (128, 4096, 1024),      # one-CTA tiles, 16 tiles: tail split into K slices
+    (2048, 2560, 256),      # pair tiles: one full wave plus a K-split tail
 ]
 
 
@@ -97,3 +99,43 @@ def test_gemm_exact_small_integers(ws):
     y, _ = oracle.gemm(a8, b8, E4M3, E4M3, 1.0, 1.0)
     ref = torch.from_numpy(y.astype(np.float32)).to(torch.bfloat16).float().numpy()
     assert np.array_equal(d.float().cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("mnk", [(256, 4096, 4096), (16, 4096, 4096), (4096, 4096, 4096)])
+def test_gemm_is_deterministic(mnk, ws):
+    """K-split tails sum their slices in a fixed order: repeated calls give
+    identical bits."""
+    M, N, K = mnk
+    a8, _, inva = _operand(M, K, E5M2, seed=7)
+    b8, _, invb = _operand(N, K, E4M3, seed=8)
+    a, b = torch.from_numpy(a8).cuda(), torch.from_numpy(b8).cuda()
+    ia, ib = torch.tensor([inva], device="cuda"), torch.tensor([invb], device="cuda")
+    d1 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    d2 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    q.gemm(a, b, E5M2, E4M3, ia, ib, d1, ws)
+    q.gemm(a, b, E5M2, E4M3, ia, ib, d2, ws)
+    q.check(ws)
+    assert torch.equal(d1.view(torch.int16), d2.view(torch.int16))
+
+
+def test_gemm_without_split_workspace_matches(ws):
+    """A workspace too small for the K-split partials falls back to whole
+    tiles; the result still meets the bound."""
+    M, N, K = 256, 4096, 1024
+    a8, sa, inva = _operand(M, K, E4M3, seed=11)
+    b8, sb, invb = _operand(N, K, E4M3, seed=12)
+    small = torch.zeros(20000, dtype=torch.uint8, device="cuda")   # fixed part only
+    d = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    lib = q.library()
+    a, b = torch.from_numpy(a8).cuda(), torch.from_numpy(b8).cuda()
+    ia, ib = torch.tensor([inva], device="cuda"), torch.tensor([invb], device="cuda")
+    st = lib.fp8lin_gemm(a.data_ptr(), None, 0, 0, 0, 0, 0, 0, 0, None, None, None, 0,
+                         small.data_ptr(), small.numel(), None)
+    assert st == 0          # M = N = 0: nothing to do
+    st = lib.fp8lin_gemm(a.data_ptr(), b.data_ptr(), M, N, K, K, K, 0, 0, ia.data_ptr(),
+                         ib.data_ptr(), d.data_ptr(), N, small.data_ptr(), small.numel(),
+                         torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    y, s = oracle.gemm(a8, b8, E4M3, E4M3, sa, sb)
+    assert_within_bound(bf16_to_f64(d), y, s, "no-split fallback")
