@@ -410,15 +410,19 @@ def run_native(args):
                     peaks["source"], peaks["bf16_tflops_sustained"], FP8_OVER_BF16)}
     cast_ms, cast_n = prof["cast"]
     cast_avg = cast_ms / max(1, cast_n)
-    # casts per step: x [M,K], W [N,K], dY [M,N] with transposed copies; the
-    # average launch moves 2 B read + 2 B written per element
-    cast_elems = (M * K + N * K + M * N) / 3.0
-    cast_gbs = cast_elems * 4 / (cast_avg * 1e-3) / 1e9
+    # Two-pass casts of the step (kind "cast"): x [M,K] and dY [M,N], plus W
+    # [N,K] when it is too large for the single-pass kernel (kind
+    # "cast_fused"); each moves 2 B read + 1 B + 1 B (transposed) per element.
+    two_pass = [M * K, M * N] + ([] if N * K <= q.single_pass_max_elems() else [N * K])
+    cast_bytes_per_step = 4.0 * sum(two_pass)
+    cast_gbs = cast_bytes_per_step / (cast_ms / args.steps * 1e-3) / 1e9
     trc = load_traffic("cast")
     cast_roofline = {"bound": "hbm", "achieved": round(cast_gbs, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(cast_gbs / peaks["hbm_gbs"], 3),
                      "traffic": trc["bytes_per_launch"] if trc else None,
-                     "kernel": "cast_kernel (+transpose)", "launch_us": round(cast_avg * 1e3, 1)}
+                     "kernel": "cast_kernel (+transpose), two-pass casts of x and dY",
+                     "launch_us": round(cast_avg * 1e3, 1),
+                     "bytes_per_launch": round(cast_bytes_per_step / max(1, cast_n / args.steps))}
     kernel_ms = {k: round(v[0] / args.steps, 4) for k, v in prof.items()}
 
     e2e = None

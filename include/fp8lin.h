@@ -81,7 +81,8 @@ typedef enum { FP8LIN_E4M3 = 0, FP8LIN_E5M2 = 1 } fp8lin_fmt;
 /* amax algorithms, after the KernelAlgorithm choice of the single-linear
  * benchmark table in "Integrate float8nocompile ..." (torchtitan PR 778):
  *   ATOMIC      one pass; each CTA folds its block maximum into the result
- *               with one atomic max;
+ *               with one atomic max (through self-cleaning workspace words
+ *               when a workspace is given, so no memset precedes it);
  *   REDUCTION   each CTA writes its partial maximum to the workspace and a
  *               second, one-CTA kernel reduces them;
  *   SINGLE_PASS (dynamic scaling only: fp8lin_forward, fp8lin_backward,
@@ -93,7 +94,8 @@ typedef enum { FP8LIN_E4M3 = 0, FP8LIN_E5M2 = 1 } fp8lin_fmt;
 typedef enum {
   FP8LIN_AMAX_ATOMIC = 0,
   FP8LIN_AMAX_REDUCTION = 1,
-  FP8LIN_AMAX_SINGLE_PASS = 2
+  FP8LIN_AMAX_SINGLE_PASS = 2,
+  FP8LIN_AMAX_AUTO = 3       /* SINGLE_PASS where the tensor fits, else ATOMIC */
 } fp8lin_amax_algo;
 
 /* Scaling type per tensor, after CastConfig(scaling_type=...) in the repro
@@ -214,7 +216,7 @@ fp8lin_status fp8lin_cast(const void* x, int64_t rows, int64_t cols, int64_t ld,
                           float* amax_out, cudaStream_t stream);
 
 /* Dynamic scaling in one call: amax -> scale -> cast (+ transpose) with
- * st->amax_algo (ATOMIC, REDUCTION or SINGLE_PASS); writes *st->amax,
+ * st->amax_algo (ATOMIC, REDUCTION, SINGLE_PASS or AUTO); writes *st->amax,
  * *st->scale, *st->inv_scale, out and (if not NULL) out_t.  st->kind must
  * be FP8LIN_DYNAMIC.  SINGLE_PASS returns FP8LIN_EUNSUPPORTED (nothing
  * enqueued) for tensors above fp8lin_single_pass_max_elems(). */

@@ -26,14 +26,17 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import (AMAX_ATOMIC, AMAX_REDUCTION, AMAX_SINGLE_PASS, DELAYED, DYNAMIC, E4M3, E5M2,
-                   Fp8linError, PROF_KINDS)
+from ._lib import (AMAX_ATOMIC, AMAX_AUTO, AMAX_REDUCTION, AMAX_SINGLE_PASS, DELAYED, DYNAMIC,
+                   E4M3, E5M2, Fp8linError, PROF_KINDS)
 
 __all__ = [
-    "E4M3", "E5M2", "AMAX_ATOMIC", "AMAX_REDUCTION", "AMAX_SINGLE_PASS", "DYNAMIC", "DELAYED",
+    "E4M3", "E5M2", "AMAX_ATOMIC", "AMAX_REDUCTION", "AMAX_SINGLE_PASS", "AMAX_AUTO", "DYNAMIC",
+    "DELAYED",
     "Fp8linError", "ScalingState", "Workspace", "amax", "amax_noalloc", "scale", "cast", "cast_dynamic", "gemm",
     "forward", "backward", "check", "workspace_bytes", "single_pass_max_elems", "launch_count",
-    "profile_enable", "profile_collect", "Fp8Linear", "library",
+    "profile_enable", "profile_collect", "Fp8Linear", "library", "Float8Linear",
+    "Float8LinearConfig", "CastConfig", "convert_to_float8_training",
+    "sync_float8_amax_and_scale_history",
 ]
 
 
@@ -250,3 +253,5 @@ def profile_collect() -> dict:
 
 
 from .linear import Fp8Linear  # noqa: E402
+from .nn import (CastConfig, Float8Linear, Float8LinearConfig,  # noqa: E402
+                 convert_to_float8_training, sync_float8_amax_and_scale_history)

@@ -17,7 +17,7 @@ OK, EINVAL, EUNSUPPORTED, ECUDA, ETIMEOUT = 0, 1, 2, 3, 4
 # fp8lin_fmt
 E4M3, E5M2 = 0, 1
 # fp8lin_amax_algo
-AMAX_ATOMIC, AMAX_REDUCTION, AMAX_SINGLE_PASS = 0, 1, 2
+AMAX_ATOMIC, AMAX_REDUCTION, AMAX_SINGLE_PASS, AMAX_AUTO = 0, 1, 2, 3
 # fp8lin_scaling
 DYNAMIC, DELAYED = 0, 1
 # profile kinds

@@ -93,7 +93,7 @@ fp8lin_status check_state(const fp8lin_scaling_state* st, bool need_delayed_buff
     if (st->history_len < 1) return FP8LIN_EINVAL;
     if (st->amax_history == nullptr || st->head == nullptr) return FP8LIN_EINVAL;
   }
-  if (st->amax_algo < FP8LIN_AMAX_ATOMIC || st->amax_algo > FP8LIN_AMAX_SINGLE_PASS)
+  if (st->amax_algo < FP8LIN_AMAX_ATOMIC || st->amax_algo > FP8LIN_AMAX_AUTO)
     return FP8LIN_EUNSUPPORTED;
   return FP8LIN_OK;
 }
@@ -119,6 +119,14 @@ fp8lin_status do_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, flo
     cudaError_t e = launch_amax_final(part, grid, out_bits, stream);
     return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);
   }
+  if (ws != nullptr) {
+    // One atomic max per CTA through the workspace's self-cleaning words.
+    ProfScope ps(FP8LIN_PROF_AMAX, stream);
+    cudaError_t e = launch_amax(static_cast<const uint16_t*>(x), rows, cols, ld, out_bits, true,
+                                grid, stream, ws_u32(ws, kWsAtomicAccOffset),
+                                ws_u32(ws, kWsAtomicTicketOffset));
+    return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);
+  }
   cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), stream);
   if (e != cudaSuccess) return cuda_fail(e);
   ProfScope ps(FP8LIN_PROF_AMAX, stream);
@@ -140,11 +148,8 @@ fp8lin_status cast_dynamic_scaled(const void* x, int64_t rows, int64_t cols, int
                            const fp8lin_scaling_state* st, uint8_t* out, uint8_t* out_t, void* ws,
                            const DeviceInfo& dev, cudaStream_t stream, bool allow_fallback) {
   int32_t algo = st->amax_algo;
-  if (algo == FP8LIN_AMAX_SINGLE_PASS && rows > 0 && cols > 0) {
+  if ((algo == FP8LIN_AMAX_SINGLE_PASS || algo == FP8LIN_AMAX_AUTO) && rows > 0 && cols > 0) {
     if (single_pass_fits(dev, rows, cols)) {
-      cudaError_t e = cudaMemsetAsync(ws_u32(ws, kWsBarrierOffset), 0,
-                                      kWsPartialOffset - kWsBarrierOffset, stream);
-      if (e != cudaSuccess) return cuda_fail(e);
       SinglePassArgs sp;
       sp.x = static_cast<const uint16_t*>(x);
       sp.rows = rows;
@@ -158,13 +163,14 @@ fp8lin_status cast_dynamic_scaled(const void* x, int64_t rows, int64_t cols, int
       sp.out = out;
       sp.out_t = out_t;
       sp.ws_barrier = ws_u32(ws, kWsBarrierOffset);
+      sp.ws_exits = ws_u32(ws, kWsExitsOffset);
       sp.ws_amax = ws_u32(ws, kWsAmaxOffset);
       sp.ws_error = ws_error(ws);
       ProfScope ps(FP8LIN_PROF_CAST_FUSED, stream);
-      e = launch_cast_single_pass(sp, dev, stream);
+      cudaError_t e = launch_cast_single_pass(sp, dev, stream);
       return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);
     }
-    if (!allow_fallback) return FP8LIN_EUNSUPPORTED;
+    if (!allow_fallback && algo == FP8LIN_AMAX_SINGLE_PASS) return FP8LIN_EUNSUPPORTED;
     algo = FP8LIN_AMAX_ATOMIC;
   }
   fp8lin_status s = do_amax(x, rows, cols, ld, st->amax, algo, ws, dev, stream);
@@ -208,9 +214,10 @@ fp8lin_status delayed_cast(const void* x, int64_t rows, int64_t cols, int64_t ld
     if (e != cudaSuccess) return cuda_fail(e);
     st->needs_init = 0;
   }
-  cudaError_t e = cudaMemsetAsync(st->amax, 0, sizeof(float), stream);
-  if (e != cudaSuccess) return cuda_fail(e);
-  if (rows == 0 || cols == 0) return FP8LIN_OK;
+  if (rows == 0 || cols == 0) {
+    cudaError_t e = cudaMemsetAsync(st->amax, 0, sizeof(float), stream);
+    return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);
+  }
   CastArgs c;
   c.x = static_cast<const uint16_t*>(x);
   c.rows = rows;
@@ -226,6 +233,8 @@ fp8lin_status delayed_cast(const void* x, int64_t rows, int64_t cols, int64_t ld
   c.out = out;
   c.out_t = out_t;
   c.amax_rec = reinterpret_cast<uint32_t*>(st->amax);
+  c.rec_acc = ws_u32(ws, kWsAtomicAccOffset);
+  c.rec_ticket = ws_u32(ws, kWsAtomicTicketOffset);
   return do_cast(c, dev, stream);
 }
 
@@ -355,6 +364,9 @@ fp8lin_status fp8lin_check(void* ws, cudaStream_t stream) {
   e = cudaMemset(ws_error(ws), 0, sizeof(int));
   if (e != cudaSuccess) return cuda_fail(e);
   e = cudaMemset(static_cast<uint8_t*>(ws) + kWsTicketOffset, 0, sizeof(int) * kWsTickets);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = cudaMemset(static_cast<uint8_t*>(ws) + kWsScratchBegin, 0,
+                 kWsPartialOffset - kWsScratchBegin);
   if (e != cudaSuccess) return cuda_fail(e);
   return FP8LIN_ETIMEOUT;
 }

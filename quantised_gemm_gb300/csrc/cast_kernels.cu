@@ -117,10 +117,28 @@ __device__ __forceinline__ void store_transposed_tile(const uint32_t* sq, uint8_
 
 // ------------------------------------------------------------------ amax
 
-template <bool kAtomic>
+// Ticketed atomic maximum: fold `bits` into *acc, and let the last of `n`
+// arrivals publish the result to *out and clear *acc and *ticket, so the
+// scratch words are zero again for the next launch (no memset needed).
+__device__ __forceinline__ void ticketed_max(uint32_t bits, uint32_t* acc, uint32_t* ticket,
+                                             uint32_t* out, unsigned n) {
+  atomicMax(acc, bits);
+  __threadfence();
+  if (atomicAdd(ticket, 1u) == n - 1) {
+    __threadfence();
+    *out = atomicExch(acc, 0u);
+    atomicExch(ticket, 0u);
+  }
+}
+
+// kMode: 0 = write this CTA's partial maximum to out[blockIdx.x];
+//        1 = atomicMax into out[0] (zero beforehand);
+//        2 = ticketed maximum through the workspace words acc / ticket.
+template <int kMode>
 __global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t* __restrict__ x,
                                                         int64_t rows, int64_t cols, int64_t ld,
-                                                        uint32_t* __restrict__ out) {
+                                                        uint32_t* __restrict__ out,
+                                                        uint32_t* acc_word, uint32_t* ticket) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t cvec = cols >> 3;                 // 8-element vectors per row
   const int64_t ntc = (cvec + 31) >> 5;           // 32 vectors per tile row
@@ -143,10 +161,12 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t* __restri
   }
   const uint32_t bits = block_absmax_bits(acc);
   if (threadIdx.x == 0) {
-    if (kAtomic)
+    if (kMode == 0)
+      out[blockIdx.x] = bits;
+    else if (kMode == 1)
       atomicMax(out, bits);
     else
-      out[blockIdx.x] = bits;
+      ticketed_max(bits, acc_word, ticket, out, gridDim.x);
   }
 }
 
@@ -202,6 +222,8 @@ struct CastParams {
   uint8_t* out;
   uint8_t* out_t;
   uint32_t* amax_rec;
+  uint32_t* rec_acc;     // non-null: ticketed recording through the workspace
+  uint32_t* rec_ticket;
 };
 
 template <int kFmt, bool kTrans>
@@ -252,23 +274,28 @@ __global__ void __launch_bounds__(kThreads, 4) cast_kernel(const CastParams p) {
   }
   if (p.amax_rec != nullptr) {
     const uint32_t bits = block_absmax_bits(acc);
-    if (threadIdx.x == 0) atomicMax(p.amax_rec, bits);
+    if (threadIdx.x == 0) {
+      if (p.rec_ticket != nullptr)
+        ticketed_max(bits, p.rec_acc, p.rec_ticket, p.amax_rec, gridDim.x);
+      else
+        atomicMax(p.amax_rec, bits);
+    }
   }
 }
 
 // ------------------------------------------------------------------ single pass
 
 struct SinglePassParams {
-  const uint16_t* x;
-  int64_t rows, cols, ld;
+  int64_t rows, cols;
   float eps;
   float* amax_out;
   float* scale_out;
   float* inv_out;
   uint8_t* out;
   uint8_t* out_t;
-  uint32_t* ws_barrier;
-  uint32_t* ws_amax;
+  uint32_t* ws_barrier;   // arrivals  } zero between launches: the last CTA
+  uint32_t* ws_exits;     // leavers   } past the barrier clears all three
+  uint32_t* ws_amax;      // amax bits }
   int* ws_error;
 };
 
@@ -278,57 +305,62 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
   return v;
 }
 
-__device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
-               : "memory");
-}
-
-// Phase 1 copies this CTA's tiles (tile t = blockIdx.x + k * gridDim.x) into
-// shared memory and folds their amax into ws_amax; a bounded grid barrier
-// waits for every CTA; phase 2 derives the scale from the global amax and
-// casts the tiles from shared memory.  Launched cooperatively, so all CTAs
-// are co-resident and the barrier completes; the time limit only guards
-// against a launch that broke that promise.
+// Phase 1: one TMA load per 128 x 128 bf16 tile brings this CTA's tiles
+// (tile t = blockIdx.x + k * gridDim.x) into shared memory; the CTA folds
+// their amax into ws_amax and arrives on a grid barrier.  Phase 2 derives the
+// scale from the global amax and casts the tiles from shared memory.
+// Launched cooperatively, so all CTAs are co-resident and the barrier
+// completes; its time limit only guards against a launch that broke that
+// promise.  The counters clean themselves: the last CTA past the barrier
+// resets them, so consecutive launches need no memset.
 template <int kFmt, bool kTrans>
-__global__ void __launch_bounds__(kThreads, 1) cast_single_pass_kernel(const SinglePassParams p) {
-  extern __shared__ __align__(128) uint8_t tiles[];  // kSinglePassTilesPerCta x 32 KB
+__global__ void __launch_bounds__(kThreads, 1)
+    cast_single_pass_kernel(const __grid_constant__ CUtensorMap tmX, const SinglePassParams p) {
+  extern __shared__ __align__(1024) uint8_t tiles_raw[];
+  uint8_t* tiles = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(tiles_raw) + 127) & ~static_cast<uintptr_t>(127));
+  __shared__ __align__(8) uint64_t loaded;
   __shared__ uint32_t s_amax_bits;
   __shared__ int s_abort;
   const int64_t ntc = (p.cols + kTile - 1) / kTile;
   const int64_t ntiles = ((p.rows + kTile - 1) / kTile) * ntc;
-  uint32_t acc = 0;
+  int mine = 0;
+  while (mine < kSinglePassTilesPerCta &&
+         blockIdx.x + static_cast<int64_t>(mine) * gridDim.x < ntiles)
+    ++mine;
 
-  for (int k = 0; k < kSinglePassTilesPerCta; ++k) {
-    const int64_t t = blockIdx.x + static_cast<int64_t>(k) * gridDim.x;
-    if (t >= ntiles) break;
-    uint8_t* buf = tiles + k * (kTile * kTile * 2);
-    const int64_t r0 = (t / ntc) * kTile, c0 = (t % ntc) * kTile;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int vi = threadIdx.x + kThreads * u;
-      const int64_t row = r0 + (vi >> 4), col = c0 + (vi & 15) * 8;
-      uint8_t* dst = buf + (vi >> 4) * (kTile * 2) + (vi & 15) * 16;
-      if (row < p.rows && col < p.cols)
-        cp_async_16(dst, p.x + row * p.ld + col);
-      else
-        *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    mbar_init(&loaded, 1);
+    fence_barrier_init();
+    mbar_arrive_expect_tx(&loaded, static_cast<uint32_t>(mine) * (kTile * kTile * 2));
+    for (int k = 0; k < mine; ++k) {
+      const int64_t t = blockIdx.x + static_cast<int64_t>(k) * gridDim.x;
+      tma_load_2d(tiles + k * (kTile * kTile * 2), &tmX, &loaded,
+                  static_cast<int32_t>((t % ntc) * kTile), static_cast<int32_t>((t / ntc) * kTile));
     }
   }
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
-  for (int k = 0; k < kSinglePassTilesPerCta; ++k) {
-    const int64_t t = blockIdx.x + static_cast<int64_t>(k) * gridDim.x;
-    if (t >= ntiles) break;
+  __syncthreads();
+  {
+    volatile int never = 0;
+    if (!mbar_wait_bounded(&loaded, 0, &never)) {
+      if (threadIdx.x == 0) atomicCAS(p.ws_error, 0, kErrGridBarrier);
+      mbar_wait_bounded(&loaded, 0, &never);  // give copies in flight a second chance to land
+      return;
+    }
+  }
+  uint32_t acc = 0;
+  for (int k = 0; k < mine; ++k) {
     const uint8_t* buf = tiles + k * (kTile * kTile * 2);
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const int vi = threadIdx.x + kThreads * u;  // the vectors this thread copied
+      const int vi = threadIdx.x + kThreads * u;
       acc = vec_absmax(acc, *reinterpret_cast<const uint4*>(buf + (vi >> 4) * (kTile * 2) +
                                                           (vi & 15) * 16));
     }
   }
   const uint32_t bits = block_absmax_bits(acc);
   if (threadIdx.x == 0) {
-    s_abort = 0;
     atomicMax(p.ws_amax, bits);
     __threadfence();
     atomicAdd(p.ws_barrier, 1u);
@@ -340,7 +372,14 @@ __global__ void __launch_bounds__(kThreads, 1) cast_single_pass_kernel(const Sin
         break;
       }
     }
-    s_amax_bits = ld_acquire_u32(p.ws_amax);
+    if (!s_abort) {
+      s_amax_bits = ld_acquire_u32(p.ws_amax);
+      if (atomicAdd(p.ws_exits, 1u) == gridDim.x - 1) {  // everyone has read the amax
+        atomicExch(p.ws_barrier, 0u);
+        atomicExch(p.ws_exits, 0u);
+        atomicExch(p.ws_amax, 0u);
+      }
+    }
   }
   __syncthreads();
   if (s_abort) return;
@@ -352,9 +391,8 @@ __global__ void __launch_bounds__(kThreads, 1) cast_single_pass_kernel(const Sin
     *p.scale_out = s;
     *p.inv_out = __fdiv_rn(1.0f, s);
   }
-  for (int k = 0; k < kSinglePassTilesPerCta; ++k) {
+  for (int k = 0; k < mine; ++k) {
     const int64_t t = blockIdx.x + static_cast<int64_t>(k) * gridDim.x;
-    if (t >= ntiles) break;
     uint8_t* buf = tiles + k * (kTile * kTile * 2);
     const int64_t r0 = (t / ntc) * kTile, c0 = (t % ntc) * kTile;
     uint2 q[8];
@@ -405,11 +443,14 @@ int amax_grid(const DeviceInfo& dev, int64_t rows, int64_t cols) {
 }
 
 cudaError_t launch_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, uint32_t* out,
-                        bool atomic, int grid, cudaStream_t stream) {
-  if (atomic)
-    amax_kernel<true><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld, out);
+                        bool atomic, int grid, cudaStream_t stream, uint32_t* ws_acc,
+                        uint32_t* ws_ticket) {
+  if (!atomic)
+    amax_kernel<0><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld, out, nullptr, nullptr);
+  else if (ws_ticket == nullptr)
+    amax_kernel<1><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld, out, nullptr, nullptr);
   else
-    amax_kernel<false><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld, out);
+    amax_kernel<2><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld, out, ws_acc, ws_ticket);
   return cudaGetLastError();
 }
 
@@ -462,7 +503,7 @@ cudaError_t launch_amax_static_scratch(const uint16_t* x, int64_t rows, int64_t 
   if (e != cudaSuccess) return e;
   // Every CTA of the first kernel writes its own slot before the second
   // kernel reads slots [0, grid): nothing in the array has to start at zero.
-  amax_kernel<false><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld, part);
+  amax_kernel<0><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld, part, nullptr, nullptr);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   amax_final_kernel<<<1, kThreads, 0, stream>>>(part, grid, reinterpret_cast<uint32_t*>(amax_out));
@@ -493,6 +534,8 @@ cudaError_t launch_cast(const CastArgs& a, const DeviceInfo& dev, cudaStream_t s
   p.out = a.out;
   p.out_t = a.out_t;
   p.amax_rec = a.amax_rec;
+  p.rec_acc = a.rec_acc;
+  p.rec_ticket = a.rec_ticket;
   const int64_t ntiles = ((a.rows + kTile - 1) / kTile) * ((a.cols + kTile - 1) / kTile);
   int64_t grid = static_cast<int64_t>(dev.num_sms) * 4;
   if (ntiles < grid) grid = ntiles;
@@ -513,7 +556,8 @@ cudaError_t launch_cast(const CastArgs& a, const DeviceInfo& dev, cudaStream_t s
 }
 
 namespace {
-constexpr size_t kSinglePassSmem = static_cast<size_t>(kSinglePassTilesPerCta) * kTile * kTile * 2;
+constexpr size_t kSinglePassSmem =
+    static_cast<size_t>(kSinglePassTilesPerCta) * kTile * kTile * 2 + 128;  // + alignment slack
 
 template <int kFmt, bool kTrans>
 cudaError_t single_pass_prepare(int* ctas_per_sm) {
@@ -541,10 +585,8 @@ bool single_pass_fits(const DeviceInfo& dev, int64_t rows, int64_t cols) {
 cudaError_t launch_cast_single_pass(const SinglePassArgs& a, const DeviceInfo& dev,
                                     cudaStream_t stream) {
   SinglePassParams p;
-  p.x = a.x;
   p.rows = a.rows;
   p.cols = a.cols;
-  p.ld = a.ld;
   p.eps = a.eps;
   p.amax_out = a.amax_out;
   p.scale_out = a.scale_out;
@@ -552,6 +594,7 @@ cudaError_t launch_cast_single_pass(const SinglePassArgs& a, const DeviceInfo& d
   p.out = a.out;
   p.out_t = a.out_t;
   p.ws_barrier = a.ws_barrier;
+  p.ws_exits = a.ws_exits;
   p.ws_amax = a.ws_amax;
   p.ws_error = a.ws_error;
   const bool trans = a.out_t != nullptr;
@@ -576,7 +619,12 @@ cudaError_t launch_cast_single_pass(const SinglePassArgs& a, const DeviceInfo& d
   // Spread the tiles over as many SMs as possible (fewer tiles per CTA).
   grid = ntiles < max_grid ? ntiles : max_grid;
   if (grid < 1) grid = 1;
-  void* args[] = {&p};
+  CUtensorMap tm;
+  if (!make_map_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, static_cast<uint64_t>(a.cols),
+                   static_cast<uint64_t>(a.rows), static_cast<uint64_t>(a.ld) * 2, kTile, kTile,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  void* args[] = {&tm, &p};
   return cudaLaunchCooperativeKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(kThreads), args,
                                      kSinglePassSmem, stream);
 }

@@ -2,6 +2,7 @@
 // translation units.  Not part of the public interface.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
@@ -11,7 +12,11 @@ namespace fp8lin {
 // Workspace layout (bytes from the 256-byte aligned base).
 constexpr size_t kWsErrorOffset = 0;      // int32: first device error code (0 = none)
 constexpr size_t kWsBarrierOffset = 64;   // uint32: grid barrier arrivals (single pass)
+constexpr size_t kWsExitsOffset = 68;     // uint32: CTAs past the barrier (single pass)
 constexpr size_t kWsAmaxOffset = 128;     // uint32: amax bits (single pass)
+constexpr size_t kWsAtomicAccOffset = 192;     // uint32: ticketed amax accumulator
+constexpr size_t kWsAtomicTicketOffset = 196;  // uint32: ticketed amax arrivals
+constexpr size_t kWsScratchBegin = 64;    // [64, 256): self-cleaning counters
 constexpr size_t kWsPartialOffset = 256;  // uint32[kMaxPartials]: REDUCTION partial maxima
 constexpr int kMaxPartials = 4096;
 constexpr size_t kWsFixedBytes = kWsPartialOffset + sizeof(uint32_t) * kMaxPartials;
@@ -41,10 +46,13 @@ cudaError_t current_device_info(DeviceInfo* info);
 // Grid size the amax kernel uses for this tensor.
 int amax_grid(const DeviceInfo& dev, int64_t rows, int64_t cols);
 
-// Block maxima of |x| as fp32 bits.  atomic: one atomicMax per CTA into
-// out[0] (which must hold 0 beforehand); otherwise out[blockIdx.x] = partial.
+// Block maxima of |x| as fp32 bits.  atomic: one atomicMax per CTA, either
+// into out[0] (which must hold 0 beforehand; ws_ticket == nullptr) or through
+// the self-cleaning workspace words ws_acc / ws_ticket (the last CTA writes
+// out[0]); otherwise out[blockIdx.x] = partial.
 cudaError_t launch_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, uint32_t* out,
-                        bool atomic, int grid, cudaStream_t stream);
+                        bool atomic, int grid, cudaStream_t stream, uint32_t* ws_acc = nullptr,
+                        uint32_t* ws_ticket = nullptr);
 
 // amax = max(partials[0..n)) written as fp32 bits into *amax_bits.
 cudaError_t launch_amax_final(const uint32_t* partials, int n, uint32_t* amax_bits,
@@ -79,6 +87,8 @@ struct CastArgs {
   uint8_t* out;
   uint8_t* out_t;
   uint32_t* amax_rec;
+  uint32_t* rec_acc = nullptr;     // non-null: record through the self-cleaning
+  uint32_t* rec_ticket = nullptr;  // workspace words instead of a pre-zeroed amax_rec
 };
 cudaError_t launch_cast(const CastArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 
@@ -94,14 +104,21 @@ struct SinglePassArgs {
   float* inv_out;
   uint8_t* out;
   uint8_t* out_t;
-  uint32_t* ws_barrier;   // zeroed before launch
-  uint32_t* ws_amax;      // zeroed before launch
+  uint32_t* ws_barrier;   // self-cleaning workspace counters (zero between launches)
+  uint32_t* ws_exits;
+  uint32_t* ws_amax;
   int* ws_error;
 };
 int64_t single_pass_capacity_elems(const DeviceInfo& dev);
 bool single_pass_fits(const DeviceInfo& dev, int64_t rows, int64_t cols);
 cudaError_t launch_cast_single_pass(const SinglePassArgs& a, const DeviceInfo& dev,
                                     cudaStream_t stream);
+
+// 2-D tiled TMA map over a row-major [rows, inner] tensor (row stride in
+// bytes), box [box_rows, box_inner], zero fill outside (gemm_tcgen05.cu).
+bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
+                 uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,
+                 CUtensorMapSwizzle swizzle);
 
 // ---- GEMM (gemm_tcgen05.cu)
 

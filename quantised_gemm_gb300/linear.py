@@ -13,7 +13,7 @@ from __future__ import annotations
 
 import torch
 
-from . import (AMAX_ATOMIC, DELAYED, DYNAMIC, E4M3, E5M2, ScalingState, Workspace, backward,
+from . import (AMAX_AUTO, DELAYED, DYNAMIC, E4M3, E5M2, ScalingState, Workspace, backward,
                forward, scale)
 
 
@@ -21,7 +21,7 @@ class Fp8Linear:
     """One Linear y = x W^T with x [M, K], W [N, K], fp8 tensorwise scaling."""
 
     def __init__(self, M: int, K: int, N: int, *, scaling: str = "dynamic", history_len: int = 16,
-                 amax_algo: int = AMAX_ATOMIC, eps: float = 1e-12, device="cuda"):
+                 amax_algo: int = AMAX_AUTO, eps: float = 1e-12, device="cuda"):
         kind = {"dynamic": DYNAMIC, "delayed": DELAYED}[scaling]
         self.M, self.K, self.N = M, K, N
         u8 = dict(dtype=torch.uint8, device=device)

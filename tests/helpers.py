@@ -12,7 +12,7 @@ def to_dev_bf16(a: np.ndarray, device="cuda") -> torch.Tensor:
 
 
 def bf16_to_f64(t: torch.Tensor) -> np.ndarray:
-    return t.float().cpu().numpy().astype(np.float64)
+    return t.detach().float().cpu().numpy().astype(np.float64)
 
 
 def f32_bits(v) -> int:

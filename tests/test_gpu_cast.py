@@ -129,8 +129,8 @@ def test_cast_every_bf16_pattern(fmt):
 
 
 @pytest.mark.parametrize("fmt", [E4M3, E5M2])
-@pytest.mark.parametrize("algo", [q.AMAX_ATOMIC, q.AMAX_REDUCTION, q.AMAX_SINGLE_PASS])
-@pytest.mark.parametrize("shape", [(144, 272), (1024, 4096), (4096, 1024)])
+@pytest.mark.parametrize("algo", [q.AMAX_ATOMIC, q.AMAX_REDUCTION, q.AMAX_SINGLE_PASS, q.AMAX_AUTO])
+@pytest.mark.parametrize("shape", [(144, 272), (1024, 4096), (4096, 1024), (4096, 4096)])
 def test_cast_dynamic_all_algorithms(fmt, algo, shape, ws):
     x = _tensor(shape, seed=29)
     a = oracle.amax(x)
@@ -158,3 +158,29 @@ def test_single_pass_capacity_and_refusal(ws):
     with pytest.raises(q.Fp8linError) as ei:
         q.cast_dynamic(x, st, out, None, ws)
     assert ei.value.status == 2     # FP8LIN_EUNSUPPORTED, nothing enqueued
+
+
+@pytest.mark.parametrize("algo", [q.AMAX_ATOMIC, q.AMAX_SINGLE_PASS, q.AMAX_AUTO])
+def test_workspace_counters_clean_themselves(algo, ws):
+    """Consecutive calls share the workspace's counters with no memset in
+    between: a large maximum, then a smaller one, then the large one again
+    must each come out exactly."""
+    big = _tensor((1024, 4096), seed=31)                       # outliers: amax ~ 200
+    small = si.normal_bf16((272, 1552), 0.5, 32, 1)            # amax ~ 2.5
+    for host in (big, small, big, small):
+        st = q.ScalingState(E4M3, q.DYNAMIC, amax_algo=algo)
+        rows, cols = host.shape
+        out = torch.empty((rows, cols), dtype=torch.uint8, device="cuda")
+        out_t = torch.empty((cols, rows), dtype=torch.uint8, device="cuda")
+        q.cast_dynamic(to_dev_bf16(host), st, out, out_t, ws)
+        a = oracle.amax(host)
+        s, _ = oracle.scale_dynamic(a, E4M3)
+        assert dev_f32_bits(st.amax) == f32_bits(a)
+        qr, qtr, _ = oracle.cast(host, s, E4M3, transpose=True)
+        assert np.array_equal(out.cpu().numpy(), qr)
+        assert np.array_equal(out_t.cpu().numpy(), qtr)
+    q.check(ws)
+    out = torch.full((1,), -1.0, device="cuda")
+    for host in (big, small):                                  # ticketed fp8lin_amax
+        q.amax(to_dev_bf16(host), out, q.AMAX_ATOMIC, ws)
+        assert dev_f32_bits(out) == f32_bits(oracle.amax(host))

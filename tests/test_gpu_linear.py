@@ -31,7 +31,7 @@ def _check_full(lin, x, w, dy, sx, sw, sd):
 
 @pytest.mark.parametrize("mkn", [(16, 4096, 4096), (256, 4096, 4096), (144, 272, 208),
                                  (48, 160, 96), (1040, 784, 512)])
-@pytest.mark.parametrize("algo", [q.AMAX_ATOMIC, q.AMAX_REDUCTION, q.AMAX_SINGLE_PASS])
+@pytest.mark.parametrize("algo", [q.AMAX_ATOMIC, q.AMAX_REDUCTION, q.AMAX_SINGLE_PASS, q.AMAX_AUTO])
 def test_linear_dynamic_full_compare(mkn, algo):
     M, K, N = mkn
     x, w, dy = si.linear_inputs(M, K, N, w_init="uniform64", outlier_frac=1e-3, seed=M + N)
