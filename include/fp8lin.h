@@ -141,6 +141,10 @@ const char* fp8lin_status_string(int status);
 /* cudaError_t of the last failed CUDA call made by this thread (0 if none). */
 int fp8lin_last_cuda_error(void);
 
+/* Which operation the last failed CUDA call of this thread was in, with the
+ * error's name (static per-thread string; "" if none). */
+const char* fp8lin_last_error_detail(void);
+
 /* ABI version: 100 * major + minor. */
 int fp8lin_version(void);
 

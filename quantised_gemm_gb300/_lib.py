@@ -46,7 +46,8 @@ class Fp8linError(RuntimeError):
         self.status = status
         msg = "%s failed: %s" % (what, status_string(status))
         if status == ECUDA and _lib is not None:
-            msg += " (cudaError %d)" % _lib.fp8lin_last_cuda_error()
+            msg += " (cudaError %d: %s)" % (_lib.fp8lin_last_cuda_error(),
+                                            _lib.fp8lin_last_error_detail().decode())
         super().__init__(msg)
 
 
@@ -61,6 +62,7 @@ _ST = ctypes.POINTER(ScalingStateC)
 _SIGNATURES = {
     "fp8lin_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fp8lin_last_cuda_error": (ctypes.c_int, []),
+    "fp8lin_last_error_detail": (ctypes.c_char_p, []),
     "fp8lin_version": (ctypes.c_int, []),
     "fp8lin_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
     "fp8lin_single_pass_max_elems": (_I64, []),

@@ -6,6 +6,8 @@
 
 #include <atomic>
 #include <cstdint>
+#include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <initializer_list>
 #include <mutex>
@@ -17,10 +19,21 @@ namespace fp8lin {
 namespace {
 
 thread_local int g_last_cuda_error = 0;
+thread_local const char* g_error_site = nullptr;
+thread_local char g_error_detail[256];
 std::atomic<uint64_t> g_launches{0};
 
-fp8lin_status cuda_fail(cudaError_t e) {
+// Record a failed CUDA call: its error, and where (the site a launcher named
+// with set_error_site, else the line of this file that saw the failure).
+fp8lin_status cuda_fail(cudaError_t e, int line = __builtin_LINE()) {
   g_last_cuda_error = static_cast<int>(e);
+  if (g_error_site != nullptr)
+    std::snprintf(g_error_detail, sizeof(g_error_detail), "%s in %s", cudaGetErrorName(e),
+                  g_error_site);
+  else
+    std::snprintf(g_error_detail, sizeof(g_error_detail), "%s at api.cu:%d", cudaGetErrorName(e),
+                  line);
+  g_error_site = nullptr;
   return FP8LIN_ECUDA;
 }
 
@@ -288,6 +301,16 @@ bool ws_ok(const void* ws) {
 
 }  // namespace
 
+void set_error_site(const char* site) { g_error_site = site; }
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("FP8LIN_PDL");
+    return !(v != nullptr && v[0] == '0');
+  }();
+  return on;
+}
+
 cudaError_t current_device_info(DeviceInfo* info) {
   static std::mutex mu;
   static DeviceInfo cache[64];
@@ -296,6 +319,11 @@ cudaError_t current_device_info(DeviceInfo* info) {
   cudaError_t e = cudaGetDevice(&d);
   if (e != cudaSuccess) return e;
   if (d < 0 || d >= 64) return cudaErrorInvalidDevice;
+  // Bind the device's primary context to this thread: a thread that never
+  // called cudaSetDevice (e.g. an autograd worker) may have none current, and
+  // the driver-level tensor-map encoding needs one.
+  e = cudaSetDevice(d);
+  if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
   if (!have[d]) {
     DeviceInfo x;
@@ -329,6 +357,10 @@ const char* fp8lin_status_string(int status) {
 }
 
 int fp8lin_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* fp8lin_last_error_detail(void) {
+  return g_last_cuda_error == 0 ? "" : g_error_detail;
+}
 
 int fp8lin_version(void) { return 100; }
 

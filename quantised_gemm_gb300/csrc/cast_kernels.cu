@@ -87,8 +87,8 @@ __device__ __forceinline__ uint2 cast8(const uint4& v, float s) {
 // reads of a warp hit 32 distinct banks.
 __device__ __forceinline__ void store_transposed_tile(const uint32_t* sq, uint8_t* out_t,
                                                       int64_t rows, int64_t cols, int64_t r0,
-                                                      int64_t c0) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+                                                      int64_t c0, int tid) {
+  const int lane = tid & 31, warp = tid >> 5;
   const int jg = (warp & 1) * 16 + (lane >> 1);  // 4-column group 0..31
   const int ig = (warp >> 1) * 2 + (lane & 1);   // 16-row group 0..7
   const int i0 = ig * 16, j0 = jg * 4;
@@ -139,6 +139,7 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t* __restri
                                                         int64_t rows, int64_t cols, int64_t ld,
                                                         uint32_t* __restrict__ out,
                                                         uint32_t* acc_word, uint32_t* ticket) {
+  griddep_wait();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t cvec = cols >> 3;                 // 8-element vectors per row
   const int64_t ntc = (cvec + 31) >> 5;           // 32 vectors per tile row
@@ -159,6 +160,7 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t* __restri
       for (int u = 0; u < 4; ++u) acc = vec_absmax(acc, v[u]);
     }
   }
+  griddep_launch_dependents();
   const uint32_t bits = block_absmax_bits(acc);
   if (threadIdx.x == 0) {
     if (kMode == 0)
@@ -172,6 +174,8 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t* __restri
 
 __global__ void __launch_bounds__(kThreads) amax_final_kernel(const uint32_t* __restrict__ part,
                                                               int n, uint32_t* __restrict__ out) {
+  griddep_wait();
+  griddep_launch_dependents();
   uint32_t m = 0;
   for (int i = threadIdx.x; i < n; i += kThreads) m = max(m, part[i]);
   // part[] already holds fp32 bits of non-negative values: order-preserving.
@@ -193,6 +197,8 @@ __global__ void scale_kernel(const float* __restrict__ amax, float* __restrict__
                              float* __restrict__ inv, float* __restrict__ ring,
                              int32_t* __restrict__ head, int32_t H, int delayed, float F,
                              float eps) {
+  griddep_wait();
+  griddep_launch_dependents();
   float a = *amax;
   if (delayed) {
     int32_t h = *head;
@@ -229,6 +235,7 @@ struct CastParams {
 template <int kFmt, bool kTrans>
 __global__ void __launch_bounds__(kThreads, 4) cast_kernel(const CastParams p) {
   __shared__ __align__(16) uint32_t sq[kTrans ? kTile * kSqWords : 1];
+  griddep_wait();
   float s;
   if (p.derive_scale) {
     s = scale_from_amax(*p.amax_in, p.eps, fp8_max<kFmt>());
@@ -268,10 +275,11 @@ __global__ void __launch_bounds__(kThreads, 4) cast_kernel(const CastParams p) {
     }
     if (kTrans) {
       __syncthreads();
-      store_transposed_tile(sq, p.out_t, p.rows, p.cols, r0, c0);
+      store_transposed_tile(sq, p.out_t, p.rows, p.cols, r0, c0, threadIdx.x);
       __syncthreads();
     }
   }
+  griddep_launch_dependents();
   if (p.amax_rec != nullptr) {
     const uint32_t bits = block_absmax_bits(acc);
     if (threadIdx.x == 0) {
@@ -308,20 +316,31 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
 // Phase 1: one TMA load per 128 x 128 bf16 tile brings this CTA's tiles
 // (tile t = blockIdx.x + k * gridDim.x) into shared memory; the CTA folds
 // their amax into ws_amax and arrives on a grid barrier.  Phase 2 derives the
-// scale from the global amax and casts the tiles from shared memory.
-// Launched cooperatively, so all CTAs are co-resident and the barrier
-// completes; its time limit only guards against a launch that broke that
-// promise.  The counters clean themselves: the last CTA past the barrier
-// resets them, so consecutive launches need no memset.
+// scale from the global amax and casts the tiles from shared memory, the two
+// 256-thread groups of the CTA working on alternate tiles (each group
+// synchronises on its own named barrier).  Launched cooperatively, so all
+// CTAs are co-resident and the grid barrier completes; its time limit only
+// guards against a launch that broke that promise.  The counters clean
+// themselves: the last CTA past the barrier resets them, so consecutive
+// launches need no memset.
+constexpr int kSpGroups = 2;
+constexpr int kSpThreads = kSpGroups * kThreads;
+
+__device__ __forceinline__ void group_sync(int group) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(kThreads) : "memory");
+}
+
 template <int kFmt, bool kTrans>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kSpThreads, 1)
     cast_single_pass_kernel(const __grid_constant__ CUtensorMap tmX, const SinglePassParams p) {
   extern __shared__ __align__(1024) uint8_t tiles_raw[];
   uint8_t* tiles = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(tiles_raw) + 127) & ~static_cast<uintptr_t>(127));
   __shared__ __align__(8) uint64_t loaded;
   __shared__ uint32_t s_amax_bits;
+  __shared__ uint32_t s_red[kSpThreads / 32];
   __shared__ int s_abort;
+  const int group = threadIdx.x / kThreads, tid = threadIdx.x % kThreads;
   const int64_t ntc = (p.cols + kTile - 1) / kTile;
   const int64_t ntiles = ((p.rows + kTile - 1) / kTile) * ntc;
   int mine = 0;
@@ -329,6 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
          blockIdx.x + static_cast<int64_t>(mine) * gridDim.x < ntiles)
     ++mine;
 
+  griddep_wait();
   if (threadIdx.x == 0) {
     s_abort = 0;
     mbar_init(&loaded, 1);
@@ -350,18 +370,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   uint32_t acc = 0;
-  for (int k = 0; k < mine; ++k) {
+  for (int k = group; k < mine; k += kSpGroups) {
     const uint8_t* buf = tiles + k * (kTile * kTile * 2);
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const int vi = threadIdx.x + kThreads * u;
+      const int vi = tid + kThreads * u;
       acc = vec_absmax(acc, *reinterpret_cast<const uint4*>(buf + (vi >> 4) * (kTile * 2) +
                                                           (vi & 15) * 16));
     }
   }
-  const uint32_t bits = block_absmax_bits(acc);
+  {
+    uint32_t m = max(acc & 0xFFFFu, acc >> 16);
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = m;
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
-    atomicMax(p.ws_amax, bits);
+    uint32_t m = 0;
+    for (int w = 0; w < kSpThreads / 32; ++w) m = max(m, s_red[w]);
+    atomicMax(p.ws_amax, m << 16);
     __threadfence();
     atomicAdd(p.ws_barrier, 1u);
     const uint64_t t0 = global_timer_ns();
@@ -383,6 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   if (s_abort) return;
+  griddep_launch_dependents();
 
   const float amax = __uint_as_float(s_amax_bits);
   const float s = scale_from_amax(amax, p.eps, fp8_max<kFmt>());
@@ -391,14 +419,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     *p.scale_out = s;
     *p.inv_out = __fdiv_rn(1.0f, s);
   }
-  for (int k = 0; k < mine; ++k) {
+  for (int k = group; k < mine; k += kSpGroups) {
     const int64_t t = blockIdx.x + static_cast<int64_t>(k) * gridDim.x;
     uint8_t* buf = tiles + k * (kTile * kTile * 2);
     const int64_t r0 = (t / ntc) * kTile, c0 = (t % ntc) * kTile;
     uint2 q[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const int vi = threadIdx.x + kThreads * u;
+      const int vi = tid + kThreads * u;
       const uint4 v = *reinterpret_cast<const uint4*>(buf + (vi >> 4) * (kTile * 2) +
                                                       (vi & 15) * 16);
       q[u] = cast8<kFmt>(v, s);
@@ -408,16 +436,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (kTrans) {
       // The bf16 tile is no longer needed: reuse its buffer for the fp8 tile.
-      __syncthreads();
+      group_sync(group);
       uint32_t* sq = reinterpret_cast<uint32_t*>(buf);
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int vi = threadIdx.x + kThreads * u;
+        const int vi = tid + kThreads * u;
         sq[(vi >> 4) * kSqWords + (vi & 15) * 2] = q[u].x;
         sq[(vi >> 4) * kSqWords + (vi & 15) * 2 + 1] = q[u].y;
       }
-      __syncthreads();
-      store_transposed_tile(sq, p.out_t, p.rows, p.cols, r0, c0);
+      group_sync(group);
+      store_transposed_tile(sq, p.out_t, p.rows, p.cols, r0, c0, tid);
     }
   }
 }
@@ -445,19 +473,21 @@ int amax_grid(const DeviceInfo& dev, int64_t rows, int64_t cols) {
 cudaError_t launch_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, uint32_t* out,
                         bool atomic, int grid, cudaStream_t stream, uint32_t* ws_acc,
                         uint32_t* ws_ticket) {
+  uint32_t* none = nullptr;
   if (!atomic)
-    amax_kernel<0><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld, out, nullptr, nullptr);
-  else if (ws_ticket == nullptr)
-    amax_kernel<1><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld, out, nullptr, nullptr);
-  else
-    amax_kernel<2><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld, out, ws_acc, ws_ticket);
-  return cudaGetLastError();
+    return launch_kernel(amax_kernel<0>, dim3(grid), dim3(kThreads), 0, stream, 1, false, x, rows,
+                         cols, ld, out, none, none);
+  if (ws_ticket == nullptr)
+    return launch_kernel(amax_kernel<1>, dim3(grid), dim3(kThreads), 0, stream, 1, false, x, rows,
+                         cols, ld, out, none, none);
+  return launch_kernel(amax_kernel<2>, dim3(grid), dim3(kThreads), 0, stream, 1, false, x, rows,
+                       cols, ld, out, ws_acc, ws_ticket);
 }
 
 cudaError_t launch_amax_final(const uint32_t* partials, int n, uint32_t* amax_bits,
                               cudaStream_t stream) {
-  amax_final_kernel<<<1, kThreads, 0, stream>>>(partials, n, amax_bits);
-  return cudaGetLastError();
+  return launch_kernel(amax_final_kernel, dim3(1), dim3(kThreads), 0, stream, 1, false, partials, n,
+                       amax_bits);
 }
 
 // ------------------------------------------------------------------ amax without a workspace
@@ -514,9 +544,8 @@ cudaError_t launch_scale(const float* amax, float* scale, float* inv, float* rin
                          int32_t history_len, bool delayed, int fmt, float eps,
                          cudaStream_t stream) {
   const float F = fmt == 0 ? 448.0f : 57344.0f;
-  scale_kernel<<<1, 1, 0, stream>>>(amax, scale, inv, ring, head, history_len, delayed ? 1 : 0,
-                                    F, eps);
-  return cudaGetLastError();
+  return launch_kernel(scale_kernel, dim3(1), dim3(1), 0, stream, 1, false, amax, scale, inv, ring,
+                       head, history_len, delayed ? 1 : 0, F, eps);
 }
 
 cudaError_t launch_cast(const CastArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
@@ -541,31 +570,38 @@ cudaError_t launch_cast(const CastArgs& a, const DeviceInfo& dev, cudaStream_t s
   if (ntiles < grid) grid = ntiles;
   if (grid < 1) grid = 1;
   const bool trans = a.out_t != nullptr;
-  if (a.fmt == 0) {
-    if (trans)
-      cast_kernel<0, true><<<static_cast<int>(grid), kThreads, 0, stream>>>(p);
-    else
-      cast_kernel<0, false><<<static_cast<int>(grid), kThreads, 0, stream>>>(p);
-  } else {
-    if (trans)
-      cast_kernel<1, true><<<static_cast<int>(grid), kThreads, 0, stream>>>(p);
-    else
-      cast_kernel<1, false><<<static_cast<int>(grid), kThreads, 0, stream>>>(p);
-  }
-  return cudaGetLastError();
+  const dim3 g(static_cast<unsigned>(grid)), b(kThreads);
+  if (a.fmt == 0)
+    return trans ? launch_kernel(cast_kernel<0, true>, g, b, 0, stream, 1, false, p)
+                 : launch_kernel(cast_kernel<0, false>, g, b, 0, stream, 1, false, p);
+  return trans ? launch_kernel(cast_kernel<1, true>, g, b, 0, stream, 1, false, p)
+               : launch_kernel(cast_kernel<1, false>, g, b, 0, stream, 1, false, p);
 }
 
 namespace {
 constexpr size_t kSinglePassSmem =
     static_cast<size_t>(kSinglePassTilesPerCta) * kTile * kTile * 2 + 128;  // + alignment slack
 
+// Opt the kernel into its shared memory and count its resident CTAs per SM,
+// once per device (the answers do not change; the calls cost host time).
 template <int kFmt, bool kTrans>
 cudaError_t single_pass_prepare(int* ctas_per_sm) {
-  auto k = cast_single_pass_kernel<kFmt, kTrans>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSinglePassSmem));
+  static std::mutex mu;
+  static int ready_device = -1;
+  static int per_sm = 0;
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
   if (e != cudaSuccess) return e;
-  *ctas_per_sm = resident_ctas(k, kThreads, kSinglePassSmem);
+  std::lock_guard<std::mutex> lock(mu);
+  if (ready_device != d) {
+    auto k = cast_single_pass_kernel<kFmt, kTrans>;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSinglePassSmem));
+    if (e != cudaSuccess) return e;
+    per_sm = resident_ctas(k, kSpThreads, kSinglePassSmem);
+    ready_device = d;
+  }
+  *ctas_per_sm = per_sm;
   return cudaSuccess;
 }
 }  // namespace
@@ -600,17 +636,18 @@ cudaError_t launch_cast_single_pass(const SinglePassArgs& a, const DeviceInfo& d
   const bool trans = a.out_t != nullptr;
   int per_sm = 0;
   cudaError_t e;
-  void* fn;
+  void (*fn)(const CUtensorMap, const SinglePassParams);
   if (a.fmt == 0) {
     e = trans ? single_pass_prepare<0, true>(&per_sm) : single_pass_prepare<0, false>(&per_sm);
-    fn = trans ? reinterpret_cast<void*>(cast_single_pass_kernel<0, true>)
-               : reinterpret_cast<void*>(cast_single_pass_kernel<0, false>);
+    fn = trans ? cast_single_pass_kernel<0, true> : cast_single_pass_kernel<0, false>;
   } else {
     e = trans ? single_pass_prepare<1, true>(&per_sm) : single_pass_prepare<1, false>(&per_sm);
-    fn = trans ? reinterpret_cast<void*>(cast_single_pass_kernel<1, true>)
-               : reinterpret_cast<void*>(cast_single_pass_kernel<1, false>);
+    fn = trans ? cast_single_pass_kernel<1, true> : cast_single_pass_kernel<1, false>;
   }
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess) {
+    set_error_site("single-pass kernel set-up");
+    return e;
+  }
   if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
   const int64_t ntiles = ((a.rows + kTile - 1) / kTile) * ((a.cols + kTile - 1) / kTile);
   int64_t grid = (ntiles + kSinglePassTilesPerCta - 1) / kSinglePassTilesPerCta;
@@ -622,11 +659,12 @@ cudaError_t launch_cast_single_pass(const SinglePassArgs& a, const DeviceInfo& d
   CUtensorMap tm;
   if (!make_map_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, static_cast<uint64_t>(a.cols),
                    static_cast<uint64_t>(a.rows), static_cast<uint64_t>(a.ld) * 2, kTile, kTile,
-                   CU_TENSOR_MAP_SWIZZLE_NONE))
-    return cudaErrorInvalidValue;
-  void* args[] = {&tm, &p};
-  return cudaLaunchCooperativeKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(kThreads), args,
-                                     kSinglePassSmem, stream);
+                   CU_TENSOR_MAP_SWIZZLE_NONE)) {
+    return map_failed("single-pass input map");
+  }
+  set_error_site("single-pass cooperative launch");
+  return launch_kernel(fn, dim3(static_cast<unsigned>(grid)), dim3(kSpThreads), kSinglePassSmem,
+                       stream, 1, true, tm, p);
 }
 
 }  // namespace fp8lin

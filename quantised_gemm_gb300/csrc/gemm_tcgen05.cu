@@ -37,6 +37,8 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdio>
+#include <cstdlib>
 #include <mutex>
 
 #include "internal.h"
@@ -61,38 +63,49 @@ struct GemmParams {
   uint16_t* d;          // bf16 output
   int64_t ldd;          // elements
   int* err;
-  int t_full;           // tiles [0, t_full) run whole
-  int s_tail;           // tiles [t_full, tiles) run as s_tail K slices each
-  float* partials;      // split slices' fp32 partials (workspace)
-  int* tickets;         // per (tail tile, 32-row group): arrivals, finished (workspace, zero)
+  // Schedule: tiles [0, t_full) run whole; tiles [t_full, tiles) run as
+  // s_tail K slices each.
+  int t_full;
+  int s_tail;
+  float* partials;      // fp32 partials of split tiles (workspace)
+  int* tickets;         // per split tile and 32-row group counters (workspace, zero)
+};
+
+// What one work unit does with its accumulator.
+enum Role : int {
+  kWhole = 0,     // the whole K loop: store bf16
+  kSlice = 1,     // one of nsplit K slices of a few-tile GEMM
 };
 
 struct Unit {
-  int tile, split, nsplit, kb0, kb1;
+  int tile, split, nsplit, kb0, kb1, role;
 };
 
-__device__ __forceinline__ Unit unit_of(int u, const GemmParams& p, int num_kb) {
-  Unit r;
-  if (u < p.t_full) {
-    r.tile = u;
-    r.split = 0;
-    r.nsplit = 1;
-    r.kb0 = 0;
-    r.kb1 = num_kb;
+// The n-th work unit of persistent slot `slot` (a CTA, or a CTA pair) out of
+// `slots` (round-robin over the units); false when the slot has no n-th
+// unit.  All roles of a CTA walk the same sequence.
+__device__ __forceinline__ bool unit_at(int slot, int slots, int n, const GemmParams& p,
+                                        int num_tiles, int num_kb, Unit& u) {
+  const int ui = slot + n * slots;
+  if (ui >= p.t_full + (num_tiles - p.t_full) * p.s_tail) return false;
+  if (ui < p.t_full) {
+    u.tile = ui;
+    u.split = 0;
+    u.nsplit = 1;
+    u.kb0 = 0;
+    u.kb1 = num_kb;
+    u.role = kWhole;
   } else {
-    const int v = u - p.t_full;
-    r.tile = p.t_full + v / p.s_tail;
-    r.split = v % p.s_tail;
-    r.nsplit = p.s_tail;
+    const int v = ui - p.t_full;
+    u.tile = p.t_full + v / p.s_tail;
+    u.split = v % p.s_tail;
+    u.nsplit = p.s_tail;
     const int per = (num_kb + p.s_tail - 1) / p.s_tail;
-    r.kb0 = r.split * per;
-    r.kb1 = min(num_kb, r.kb0 + per);
+    u.kb0 = u.split * per;
+    u.kb1 = min(num_kb, u.kb0 + per);
+    u.role = kSlice;
   }
-  return r;
-}
-
-__device__ __forceinline__ int num_units(const GemmParams& p, int num_tiles) {
-  return p.t_full + (num_tiles - p.t_full) * p.s_tail;
+  return true;
 }
 
 __device__ __forceinline__ void record_error(int* err, volatile int* abort_flag, int code) {
@@ -208,16 +221,16 @@ __device__ __forceinline__ int ld_acquire_int(const int* p) {
 // all resident at once, so the wait cannot block on itself.  The last slice to
 // finish clears both counters for the next call.
 template <int BN, bool kTransStore, typename Release>
-__device__ __forceinline__ void epilogue_unit(const GemmParams& p, const Unit& u, int G, int group,
-                                              int row0, int col_base, uint32_t t_row, float alpha,
-                                              const CUtensorMap* tmD, uint8_t* boxes,
+__device__ __forceinline__ void epilogue_unit(const GemmParams& p, const Unit& u, int G,
+                                              int group, int row0, int col_base, uint32_t t_row,
+                                              float alpha, const CUtensorMap* tmD, uint8_t* boxes,
                                               uint32_t& chunk_no, int lane,
                                               volatile int* abort_flag, Release release) {
   constexpr int kChunk = (BN % 32 == 0) ? 32 : 16;
   const bool active = row0 < p.M;  // warp-uniform
   int nch = 0;                     // chunks with at least one column inside D
   while (nch < BN / kChunk && col_base + nch * kChunk < p.N) ++nch;
-  if (u.nsplit == 1) {
+  if (u.role == kWhole) {
     if (active && nch > 0) {
       // Two chunks per iteration: the TMEM load of the second is in flight
       // while the first is converted and stored.
@@ -247,8 +260,8 @@ __device__ __forceinline__ void epilogue_unit(const GemmParams& p, const Unit& u
     release();
     return;
   }
-  const int tail_tile = u.tile - p.t_full;
   const size_t region_floats = static_cast<size_t>(32) * BN;
+  const int tail_tile = u.tile - p.t_full;
   float* mine = p.partials + ((static_cast<size_t>(tail_tile) * u.nsplit + u.split) * G + group) *
                                  region_floats;
   if (active) {
@@ -372,7 +385,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int num_n = (p.N + BN - 1) / BN;
   const int num_tiles = ((p.M + kBM - 1) / kBM) * num_n;
   const int num_kb = (p.K + kBK - 1) / kBK;
-  const int units = num_units(p, num_tiles);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -398,6 +410,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  griddep_wait();               // operands, scales and D are ready / free
+  griddep_launch_dependents();  // the next kernel may start its prologue on freed SMs
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -408,8 +422,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int ui = blockIdx.x; ui < units && ok; ui += gridDim.x) {
-        const Unit u = unit_of(ui, p, num_kb);
+      Unit u;
+      for (int n = 0; ok && unit_at(blockIdx.x, gridDim.x, n, p, num_tiles, num_kb, u); ++n) {
         const int m_blk = u.tile / num_n, n_blk = u.tile % num_n;
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) {
@@ -446,8 +460,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       bool issued = false;
-      for (int ui = blockIdx.x; ui < units && ok; ui += gridDim.x) {
-        const Unit u = unit_of(ui, p, num_kb);
+      Unit u;
+      for (int n = 0; ok && unit_at(blockIdx.x, gridDim.x, n, p, num_tiles, num_kb, u); ++n) {
         if (!mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
@@ -501,8 +515,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t chunk_no = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int ui = blockIdx.x; ui < units; ui += gridDim.x) {
-      const Unit u = unit_of(ui, p, num_kb);
+    Unit u;
+    for (int n = 0; unit_at(blockIdx.x, gridDim.x, n, p, num_tiles, num_kb, u); ++n) {
       const int m_blk = u.tile / num_n, n_blk = u.tile % num_n;
       // tcgen05.ld below is warp-collective: take the decision warp-uniformly.
       const bool ready = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&acc_full[acc], acc_phase,
@@ -590,7 +604,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int num_n = (p.N + BN - 1) / BN;
   const int num_tiles = ((p.M + 2 * kBM - 1) / (2 * kBM)) * num_n;
   const int num_kb = (p.K + kBK - 1) / kBK;
-  const int units = num_units(p, num_tiles);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -616,6 +629,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   cluster_sync_all();  // barriers of both CTAs initialised before any remote use
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  griddep_wait();               // operands, scales and D are ready / free
+  griddep_launch_dependents();  // the next kernel may start its prologue on freed SMs
 
   if (warp == 0) {
     // ------------------------------------------------------------ producers (both CTAs)
@@ -623,8 +638,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int ui = pair; ui < units && ok; ui += num_pairs) {
-        const Unit u = unit_of(ui, p, num_kb);
+      Unit u;
+      for (int n = 0; ok && unit_at(pair, num_pairs, n, p, num_tiles, num_kb, u); ++n) {
         const int m_blk = u.tile / num_n, n_blk = u.tile % num_n;
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
           if (!mbar_wait_cluster_bounded(&empty[stage], phase ^ 1u, abort_flag)) {
@@ -654,8 +669,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       bool issued = false;
-      for (int ui = pair; ui < units && ok; ui += num_pairs) {
-        const Unit u = unit_of(ui, p, num_kb);
+      Unit u;
+      for (int n = 0; ok && unit_at(pair, num_pairs, n, p, num_tiles, num_kb, u); ++n) {
         if (!mbar_wait_cluster_bounded(&acc_empty[acc], acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
@@ -708,8 +723,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t chunk_no = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int ui = pair; ui < units; ui += num_pairs) {
-      const Unit u = unit_of(ui, p, num_kb);
+    Unit u;
+    for (int n = 0; unit_at(pair, num_pairs, n, p, num_tiles, num_kb, u); ++n) {
       const int m_blk = u.tile / num_n, n_blk = u.tile % num_n;
       const bool ready = __all_sync(
           0xFFFFFFFFu, mbar_wait_cluster_bounded(&acc_full[acc], acc_phase, abort_flag));
@@ -747,6 +762,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 // ------------------------------------------------------------------ host side
 
+thread_local CUresult g_last_encode_result = CUDA_SUCCESS;
+thread_local char g_map_site[128];
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -779,6 +797,7 @@ bool make_map_k_major(CUtensorMap* map, const uint8_t* base, int64_t rows, int64
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  g_last_encode_result = r;
   return r == CUDA_SUCCESS;
 }
 
@@ -794,35 +813,37 @@ bool make_map_out(CUtensorMap* map, const void* base, int64_t rows, int64_t cols
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  g_last_encode_result = r;
   return r == CUDA_SUCCESS;
 }
 
-// Choose the tail split: tiles beyond the last full wave of `slots`
-// persistent units are cut into S K-slices, if the workspace holds their
-// partials (`group_rows` rows of BN fp32 per slice and 32-row group).
-void plan_split(GemmParams& p, int tiles, int slots, int num_kb, int rows_per_tile, int bn,
-                const GemmArgs& g) {
+// Choose the schedule of `tiles` tiles on `slots` persistent units (CTAs or
+// pairs) with `num_kb` K blocks each: whole tiles round-robin, except that
+// when the tiles do not fill one wave and the K loop is long, each tile runs
+// as S K slices (S = slots / tiles) reduced by the slices together.  Splitting
+// the partial last wave of a multi-wave grid (stream-K style) was measured
+// slower on the Linear's shapes than leaving it partial: the extra epilogues
+// and partial traffic cost more than the idle tail.
+void plan_schedule(GemmParams& p, int tiles, int slots, int num_kb, int rows_per_tile, int bn,
+                   const GemmArgs& g) {
   p.t_full = tiles;
   p.s_tail = 1;
   p.partials = nullptr;
   p.tickets = nullptr;
-  // Only when the tiles do not fill one wave and the K loop is long: splitting
-  // the tail of a multi-wave grid, or a short K loop, measured slower than
-  // running the tiles whole (the partial write and reduce cost more).
   if (g.ws_split == nullptr || slots < 2 || tiles >= slots || num_kb < 16) return;
-  const int tail = tiles % slots;
-  int s = slots / tail;
+  const size_t groups = static_cast<size_t>(rows_per_tile) / 32;
+  const size_t tile_bytes = static_cast<size_t>(rows_per_tile) * bn * sizeof(float);
+  int s = slots / tiles;
   if (s > kMaxSplit) s = kMaxSplit;
   if (s > num_kb) s = num_kb;
   if (s < 2) return;
   const int per = (num_kb + s - 1) / s;
   s = (num_kb + per - 1) / per;  // no empty slice
   if (s < 2) return;
-  const size_t groups = static_cast<size_t>(rows_per_tile) / 32;
-  const size_t need_floats = static_cast<size_t>(tail) * s * rows_per_tile * bn;
-  const size_t need_tickets = 2 * static_cast<size_t>(tail) * groups;
-  if (need_floats * sizeof(float) > g.ws_split_bytes || need_tickets > kWsTickets) return;
-  p.t_full = tiles - tail;
+  const size_t need_tickets = 2 * static_cast<size_t>(tiles) * groups;
+  if (static_cast<size_t>(tiles) * s * tile_bytes > g.ws_split_bytes || need_tickets > kWsTickets)
+    return;
+  p.t_full = 0;
   p.s_tail = s;
   p.partials = g.ws_split;
   p.tickets = g.ws_tickets;
@@ -841,18 +862,19 @@ cudaError_t run(const uint8_t* a, int64_t lda, const uint8_t* b, int64_t ldb, Ge
     configured_device = dev.device;
   }
   CUtensorMap ma, mb, md;
-  if (!make_map_k_major(&ma, a, p.M, p.K, lda, kBM)) return cudaErrorInvalidValue;
-  if (!make_map_k_major(&mb, b, p.N, p.K, ldb, BN)) return cudaErrorInvalidValue;
+  if (!make_map_k_major(&ma, a, p.M, p.K, lda, kBM)) return map_failed("GEMM operand A map");
+  if (!make_map_k_major(&mb, b, p.N, p.K, ldb, BN)) return map_failed("GEMM operand B map");
   if (kTransStore)
     md = mb;  // unused: the transposed store writes D directly
   else if (!make_map_out(&md, p.d, p.M, p.N, p.ldd))
-    return cudaErrorInvalidValue;
+    return map_failed("GEMM output map");
   const int tiles = ((p.M + kBM - 1) / kBM) * ((p.N + BN - 1) / BN);
-  plan_split(p, tiles, dev.num_sms, (p.K + kBK - 1) / kBK, kBM, BN, g);
+  plan_schedule(p, tiles, dev.num_sms, (p.K + kBK - 1) / kBK, kBM, BN, g);
+  set_error_site("one-CTA GEMM launch");
   const int units = p.t_full + (tiles - p.t_full) * p.s_tail;
   const int grid = units < dev.num_sms ? units : dev.num_sms;
-  kernel<<<grid, kGemmThreads, C::kSmemBytes, stream>>>(ma, mb, md, p);
-  return cudaGetLastError();
+  return launch_kernel(kernel, dim3(grid), dim3(kGemmThreads), C::kSmemBytes, stream, 1, false, ma,
+                       mb, md, p);
 }
 
 template <int BN, int STAGES>
@@ -886,29 +908,27 @@ cudaError_t run_pair(const uint8_t* a, int64_t lda, const uint8_t* b, int64_t ld
     configured_device = dev.device;
   }
   CUtensorMap ma, mb, md;
-  if (!make_map_k_major(&ma, a, p.M, p.K, lda, kBM)) return cudaErrorInvalidValue;
-  if (!make_map_k_major(&mb, b, p.N, p.K, ldb, BN / 2)) return cudaErrorInvalidValue;
-  if (!make_map_out(&md, p.d, p.M, p.N, p.ldd)) return cudaErrorInvalidValue;
+  if (!make_map_k_major(&ma, a, p.M, p.K, lda, kBM)) return map_failed("pair GEMM operand A map");
+  if (!make_map_k_major(&mb, b, p.N, p.K, ldb, BN / 2))
+    return map_failed("pair GEMM operand B map");
+  if (!make_map_out(&md, p.d, p.M, p.N, p.ldd)) return map_failed("pair GEMM output map");
   const int tiles = ((p.M + 2 * kBM - 1) / (2 * kBM)) * ((p.N + BN - 1) / BN);
-  plan_split(p, tiles, max_pairs, (p.K + kBK - 1) / kBK, 2 * kBM, BN, g);
+  plan_schedule(p, tiles, max_pairs, (p.K + kBK - 1) / kBK, 2 * kBM, BN, g);
+  set_error_site("pair GEMM launch");
   const int units = p.t_full + (tiles - p.t_full) * p.s_tail;
   const int pairs = units < max_pairs ? units : max_pairs;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(2 * pairs);
-  cfg.blockDim = dim3(kGemmThreads);
-  cfg.dynamicSmemBytes = C::kSmemBytes;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, ma, mb, md, p);
+  return launch_kernel(kernel, dim3(2 * pairs), dim3(kGemmThreads), C::kSmemBytes, stream, 2, false,
+                       ma, mb, md, p);
 }
 
 }  // namespace
+
+cudaError_t map_failed(const char* what) {
+  std::snprintf(g_map_site, sizeof(g_map_site), "%s (cuTensorMapEncodeTiled CUresult %d)", what,
+                static_cast<int>(g_last_encode_result));
+  set_error_site(g_map_site);
+  return cudaErrorInvalidValue;
+}
 
 bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
                  uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,
@@ -922,6 +942,7 @@ bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, 
   CUresult r = fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  g_last_encode_result = r;
   return r == CUDA_SUCCESS;
 }
 

@@ -33,6 +33,49 @@ enum DeviceError : int {
   kErrGridBarrier = 4,
 };
 
+// Name the operation a launcher failed in (reported by
+// fp8lin_last_error_detail together with the cudaError_t).
+void set_error_site(const char* site);
+
+// Whether launches use programmatic dependent launch (default on; the
+// environment variable FP8LIN_PDL=0 turns it off).
+bool pdl_enabled();
+
+// Launch `kernel` on `stream` with cudaLaunchKernelEx: programmatic
+// dependent launch when enabled (not for cooperative grids), a cluster of
+// `cluster_x` CTAs when > 1, and a cooperative launch when `cooperative`.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, int cluster_x, bool cooperative, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[3];
+  unsigned n = 0;
+  if (pdl_enabled() && !cooperative) {  // a cooperative grid is launched whole
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (cooperative) {
+    attr[n].id = cudaLaunchAttributeCooperative;
+    attr[n].val.cooperative = 1;
+    ++n;
+  }
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 struct DeviceInfo {
   int device;
   int num_sms;
@@ -119,6 +162,10 @@ cudaError_t launch_cast_single_pass(const SinglePassArgs& a, const DeviceInfo& d
 bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
                  uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,
                  CUtensorMapSwizzle swizzle);
+
+// Record a failed tensor-map encoding (with its CUresult) as the error site;
+// returns cudaErrorInvalidValue.
+cudaError_t map_failed(const char* what);
 
 // ---- GEMM (gemm_tcgen05.cu)
 

@@ -21,6 +21,24 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// ---------------------------------------------------------------- dependent launch
+//
+// With programmatic dependent launch, a kernel may start before the kernel
+// ahead of it in the stream has finished.  Every kernel of the library calls
+// griddep_wait() before its first global-memory access (read or write), which
+// returns once the preceding grid has completed and its writes are visible;
+// since that grid did the same, all earlier work is complete too.  Without
+// programmatic launch both instructions are no-ops.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next kernel in the stream to begin launching (its CTAs run their
+// prologue and then wait in griddep_wait()).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

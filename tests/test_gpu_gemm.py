@@ -41,7 +41,10 @@ CASES = [
     (64, 272, 320),
     (1040, 784, 512),
     (128, 4096, 1024),      # one-CTA tiles, 16 tiles: tail split into K slices
-    (2048, 2560, 256),      # pair tiles: one full wave plus a K-split tail
+    (2048, 2560, 256),      # pair tiles: one full wave plus a partial one
+    (4096, 4096, 1024),     # 256 pair tiles: 3.4 waves
+    (128, 40960, 512),      # 160 one-CTA tiles: more tiles than CTAs
+    (16, 20480, 256),       # swapped operands, 160 tiles, transposed stores
 ]
 
 
