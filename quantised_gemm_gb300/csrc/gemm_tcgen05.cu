@@ -52,7 +52,8 @@ constexpr int kBK = 128;           // bytes (= 8-bit elements) of K per stage
 constexpr int kMmaK = 32;          // K of one kind::f8f6f4 MMA
 constexpr int kGemmThreads = 192;  // 6 warps
 constexpr int kBoxBytes = 32 * 32 * 2;              // one 32x32 bf16 epilogue box
-constexpr int kEpiStagingBytes = 4 * 2 * kBoxBytes;  // two boxes per epilogue warp
+constexpr int kBoxesPerWarp = 4;                     // TMA stores in flight per epilogue warp
+constexpr int kEpiStagingBytes = 4 * kBoxesPerWarp * kBoxBytes;
 constexpr int kMaxSplit = 8;
 
 struct GemmParams {
@@ -135,7 +136,7 @@ __device__ __forceinline__ void store_chunk_tma(const uint32_t (&r)[32], float a
   for (int j = 0; j < 16; ++j)
     w[j] = cvt_bf16x2(__fmul_rn(__uint_as_float(r[2 * j]), alpha),
                       __fmul_rn(__uint_as_float(r[2 * j + 1]), alpha));
-  if (lane == 0) bulk_wait_group_read<1>();  // this box's previous store has read it
+  if (lane == 0) bulk_wait_group_read<kBoxesPerWarp - 1>();  // this box's last store has read it
   __syncwarp();
   uint8_t* rowp = box + lane * 64;
   const int sw = (lane >> 1) & 3;
@@ -159,7 +160,8 @@ __device__ __forceinline__ void emit_chunk(const uint32_t (&r)[kChunk], float al
                                            int lane) {
   if constexpr (!kTransStore) {
     static_assert(kChunk == 32, "TMA-store epilogue works on 32-column chunks");
-    store_chunk_tma(r, alpha, boxes + (chunk_no & 1) * kBoxBytes, tmD, row0, col0, lane);
+    store_chunk_tma(r, alpha, boxes + (chunk_no % kBoxesPerWarp) * kBoxBytes, tmD, row0, col0,
+                    lane);
     ++chunk_no;
   } else {
     // kernel element (row, col) is output element (col, row)
@@ -511,7 +513,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;  // TMEM lanes this warp may read: 32*quarter..+31
     const float alpha = __fmul_rn(*p.inv_a, *p.inv_b);
-    uint8_t* boxes = sEpi + (warp - 2) * 2 * kBoxBytes;
+    uint8_t* boxes = sEpi + (warp - 2) * kBoxesPerWarp * kBoxBytes;
     uint32_t chunk_no = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -719,7 +721,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int quarter = warp & 3;
     const float alpha = __fmul_rn(*p.inv_a, *p.inv_b);
     const uint32_t acc_empty_even0 = map_to_cta(smem_addr(&acc_empty[0]), 0);
-    uint8_t* boxes = sEpi + (warp - 2) * 2 * kBoxBytes;
+    uint8_t* boxes = sEpi + (warp - 2) * kBoxesPerWarp * kBoxBytes;
     uint32_t chunk_no = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
