@@ -334,6 +334,9 @@ def end_to_end(q, lin, x, w, dy, M, K, N, world, flop_step, steps):
     hdx = torch.empty((M, K), dtype=torch.bfloat16).pin_memory()
     hdw = torch.empty((N, K), dtype=torch.bfloat16).pin_memory()
     n = max(3, min(20, steps // 10))
+    lanes = os.environ.get("FP8LIN_COPY_LANES")
+    if lanes:
+        lin.copy_lanes = int(lanes)
     for _ in range(2):
         lin.step_host(hx, hw, hdy, hy, hdx, hdw)
     torch.cuda.synchronize()
@@ -341,7 +344,8 @@ def end_to_end(q, lin, x, w, dy, M, K, N, world, flop_step, steps):
     return {"value": round(world * flop_step / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": 2 * (M * K + N * K + M * N),
             "d2h_bytes_per_step": 2 * (M * N + M * K + N * K), "ms_per_step": round(ms, 3),
-            "steps": n}
+            "steps": n, "copy_lanes": lin.copy_lanes,
+            "api": "Fp8Linear.step_host (pinned host buffers)"}
 
 
 def run_native(args):

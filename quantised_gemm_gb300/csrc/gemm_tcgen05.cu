@@ -50,10 +50,19 @@ namespace {
 constexpr int kBM = 128;           // rows of A per CTA (MMA M per CTA)
 constexpr int kBK = 128;           // bytes (= 8-bit elements) of K per stage
 constexpr int kMmaK = 32;          // K of one kind::f8f6f4 MMA
-constexpr int kGemmThreads = 192;  // 6 warps
+constexpr int kGemmThreads = 320;  // 10 warps: producer, MMA, 8 epilogue
+constexpr int kEpiWarps = 8;       // two per TMEM lane quarter, each on half the columns
 constexpr int kBoxBytes = 32 * 32 * 2;              // one 32x32 bf16 epilogue box
-constexpr int kBoxesPerWarp = 4;                     // TMA stores in flight per epilogue warp
-constexpr int kEpiStagingBytes = 4 * kBoxesPerWarp * kBoxBytes;
+constexpr int kBoxesPerWarp = 2;                     // staging boxes per epilogue warp
+constexpr int kEpiStagingBytes = kEpiWarps * kBoxesPerWarp * kBoxBytes;
+
+// Epilogue warps split the BN columns of a tile in two halves when each half
+// still holds whole 32-column chunks.
+template <int BN>
+struct EpiSplit {
+  static constexpr int kHalves = BN >= 64 ? 2 : 1;
+  static constexpr int kCols = BN / kHalves;
+};
 constexpr int kMaxSplit = 8;
 
 struct GemmParams {
@@ -222,16 +231,16 @@ __device__ __forceinline__ int ld_acquire_int(const int* p) {
 // result.  The slices of a tail tile run on distinct CTAs as their last unit,
 // all resident at once, so the wait cannot block on itself.  The last slice to
 // finish clears both counters for the next call.
-template <int BN, bool kTransStore, typename Release>
+template <int kCols, bool kTransStore, typename Release>
 __device__ __forceinline__ void epilogue_unit(const GemmParams& p, const Unit& u, int G,
                                               int group, int row0, int col_base, uint32_t t_row,
                                               float alpha, const CUtensorMap* tmD, uint8_t* boxes,
                                               uint32_t& chunk_no, int lane,
                                               volatile int* abort_flag, Release release) {
-  constexpr int kChunk = (BN % 32 == 0) ? 32 : 16;
+  constexpr int kChunk = (kCols % 32 == 0) ? 32 : 16;
   const bool active = row0 < p.M;  // warp-uniform
   int nch = 0;                     // chunks with at least one column inside D
-  while (nch < BN / kChunk && col_base + nch * kChunk < p.N) ++nch;
+  while (nch < kCols / kChunk && col_base + nch * kChunk < p.N) ++nch;
   if (u.role == kWhole) {
     if (active && nch > 0) {
       // Two chunks per iteration: the TMEM load of the second is in flight
@@ -262,7 +271,7 @@ __device__ __forceinline__ void epilogue_unit(const GemmParams& p, const Unit& u
     release();
     return;
   }
-  const size_t region_floats = static_cast<size_t>(32) * BN;
+  const size_t region_floats = static_cast<size_t>(32) * kCols;
   const int tail_tile = u.tile - p.t_full;
   float* mine = p.partials + ((static_cast<size_t>(tail_tile) * u.nsplit + u.split) * G + group) *
                                  region_floats;
@@ -395,7 +404,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 4);  // one arrival per epilogue warp
+      mbar_init(&acc_empty[a], kEpiWarps);  // one arrival per epilogue warp
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -511,7 +520,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int quarter = warp & 3;  // TMEM lanes this warp may read: 32*quarter..+31
+    using E = EpiSplit<BN>;
+    const int quarter = warp & 3;        // TMEM lanes this warp may read: 32*quarter..+31
+    const int half = (warp - 2) >> 2;    // which half of the columns (0 or 1)
+    const bool has_cols = half < E::kHalves;
     const float alpha = __fmul_rn(*p.inv_a, *p.inv_b);
     uint8_t* boxes = sEpi + (warp - 2) * kBoxesPerWarp * kBoxBytes;
     uint32_t chunk_no = 0;
@@ -529,14 +541,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       tc_fence_after_sync();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                             static_cast<uint32_t>(acc * BN);
+                             static_cast<uint32_t>(acc * BN + half * E::kCols);
       const int acc_now = acc;
-      epilogue_unit<BN, kTransStore>(p, u, 4, quarter, m_blk * kBM + quarter * 32, n_blk * BN,
-                                     t_row, alpha, &tmD, boxes, chunk_no, lane, abort_flag, [&] {
-                                       tc_fence_before_sync();
-                                       __syncwarp();
-                                       if (lane == 0) mbar_arrive(&acc_empty[acc_now]);
-                                     });
+      auto release = [&] {
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[acc_now]);
+      };
+      if (has_cols)
+        epilogue_unit<E::kCols, kTransStore>(p, u, 4 * E::kHalves, half * 4 + quarter,
+                                             m_blk * kBM + quarter * 32,
+                                             n_blk * BN + half * E::kCols, t_row, alpha, &tmD,
+                                             boxes, chunk_no, lane, abort_flag, release);
+      else
+        release();
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
@@ -614,7 +632,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 8);  // 4 epilogue warps x 2 CTAs
+      mbar_init(&acc_empty[a], 2 * kEpiWarps);  // every epilogue warp of both CTAs
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -718,7 +736,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
+    using E = EpiSplit<BN>;
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
     const float alpha = __fmul_rn(*p.inv_a, *p.inv_b);
     const uint32_t acc_empty_even0 = map_to_cta(smem_addr(&acc_empty[0]), 0);
     uint8_t* boxes = sEpi + (warp - 2) * kBoxesPerWarp * kBoxBytes;
@@ -736,15 +756,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       tc_fence_after_sync();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                             static_cast<uint32_t>(acc * BN);
-      const int group = static_cast<int>(rank) * 4 + quarter;
+                             static_cast<uint32_t>(acc * BN + half * E::kCols);
+      const int row_group = static_cast<int>(rank) * 4 + quarter;
       const uint32_t release_addr = acc_empty_even0 + static_cast<uint32_t>(acc * 8);
-      epilogue_unit<BN, false>(p, u, 8, group, m_blk * 2 * kBM + group * 32, n_blk * BN, t_row,
-                               alpha, &tmD, boxes, chunk_no, lane, abort_flag, [&] {
-                                 tc_fence_before_sync();
-                                 __syncwarp();
-                                 if (lane == 0) mbar_arrive_cluster(release_addr);
-                               });
+      epilogue_unit<E::kCols, false>(p, u, 8 * E::kHalves, half * 8 + row_group,
+                                     m_blk * 2 * kBM + row_group * 32, n_blk * BN + half * E::kCols,
+                                     t_row, alpha, &tmD, boxes, chunk_no, lane, abort_flag, [&] {
+                                       tc_fence_before_sync();
+                                       __syncwarp();
+                                       if (lane == 0) mbar_arrive_cluster(release_addr);
+                                     });
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
@@ -833,7 +854,7 @@ void plan_schedule(GemmParams& p, int tiles, int slots, int num_kb, int rows_per
   p.partials = nullptr;
   p.tickets = nullptr;
   if (g.ws_split == nullptr || slots < 2 || tiles >= slots || num_kb < 16) return;
-  const size_t groups = static_cast<size_t>(rows_per_tile) / 32;
+  const size_t groups = static_cast<size_t>(rows_per_tile) / 32 * (bn >= 64 ? 2 : 1);
   const size_t tile_bytes = static_cast<size_t>(rows_per_tile) * bn * sizeof(float);
   int s = slots / tiles;
   if (s > kMaxSplit) s = kMaxSplit;

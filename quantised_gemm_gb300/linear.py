@@ -55,25 +55,65 @@ class Fp8Linear:
             if st.kind == DELAYED:
                 scale(st, stream)
 
+    copy_lanes = 1   # copy streams per direction; with more, each tensor moves in row slices
+
     def step_host(self, x_h, w_h, dy_h, y_h, dx_h, dw_h, stream=None):
-        """End-to-end step from host buffers (pinned for asynchronous copies):
+        """End-to-end step from host buffers (pinned, for asynchronous copies):
         copy x, W, dY in, forward + backward (+ delayed sync), copy y, dX, dW
-        out, all on one stream.  Device staging buffers are allocated on the
-        first call."""
+        out.  The copies run on copy streams of their own (``copy_lanes`` per
+        direction, each moving a slice of rows, so several copy engines work
+        at once), ordered by events: dY's upload overlaps the forward, y's
+        download overlaps the backward, and the next step's uploads may start
+        while this step's downloads finish.  The compute runs on `stream`
+        (default: the current stream), which waits for the last download
+        before it goes on.  Device staging buffers and the copy streams are
+        created on the first call."""
+        main = stream if stream is not None else torch.cuda.current_stream()
+        n = self.copy_lanes
         if not hasattr(self, "_xd"):
             dev = self.y.device
             self._xd = torch.empty((self.M, self.K), dtype=torch.bfloat16, device=dev)
             self._wd = torch.empty((self.N, self.K), dtype=torch.bfloat16, device=dev)
             self._dyd = torch.empty((self.M, self.N), dtype=torch.bfloat16, device=dev)
-        ctx = torch.cuda.stream(stream) if stream is not None else _NullCtx()
-        with ctx:
-            self._xd.copy_(x_h, non_blocking=True)
-            self._wd.copy_(w_h, non_blocking=True)
-            self._dyd.copy_(dy_h, non_blocking=True)
-            self.step(self._xd, self._wd, self._dyd)
-            y_h.copy_(self.y, non_blocking=True)
-            dx_h.copy_(self.dx, non_blocking=True)
-            dw_h.copy_(self.dw, non_blocking=True)
+            self._up = [torch.cuda.Stream(device=dev) for _ in range(n)]
+            self._down = [torch.cuda.Stream(device=dev) for _ in range(n)]
+            self._fwd_done = torch.cuda.Event()
+            self._bwd_done = torch.cuda.Event()
+            self._fwd_done.record(main)
+            self._bwd_done.record(main)
+
+        def move(pairs, streams, after):
+            """Copy each (dst, src) in row slices over `streams` once `after`
+            has fired; returns the events marking each stream's end."""
+            done = []
+            for i, st in enumerate(streams):
+                st.wait_event(after)
+                with torch.cuda.stream(st):
+                    for dst, src in pairs:
+                        rows = dst.shape[0]
+                        lo, hi = rows * i // len(streams), rows * (i + 1) // len(streams)
+                        if hi > lo:
+                            dst[lo:hi].copy_(src[lo:hi], non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(st)
+                    done.append(ev)
+            return done
+
+        # the previous forward has read x and W; the previous backward dY
+        for ev in move([(self._xd, x_h), (self._wd, w_h)], self._up, self._fwd_done):
+            main.wait_event(ev)
+        dy_in = move([(self._dyd, dy_h)], self._up, self._bwd_done)
+        self.forward(self._xd, self._wd, main)
+        self._fwd_done.record(main)
+        y_out = move([(y_h, self.y)], self._down, self._fwd_done)
+        for ev in dy_in:
+            main.wait_event(ev)
+        self.backward(self._dyd, stream=main)
+        self.sync_scales(main)
+        self._bwd_done.record(main)
+        out = move([(dx_h, self.dx), (dw_h, self.dw)], self._down, self._bwd_done)
+        for ev in y_out + out:
+            main.wait_event(ev)                # host results complete; y, dX, dW free again
         return y_h, dx_h, dw_h
 
     def step(self, x, w, dy, stream=None):

@@ -204,3 +204,27 @@ def test_bad_arguments_raise_without_launch():
     with pytest.raises(q.Fp8linError):
         lin.forward(x, w)
     assert q.launch_count() == before
+
+
+@pytest.mark.parametrize("lanes", [1, 3])
+def test_step_host_matches_device_path(lanes):
+    """The host-buffer API (overlapped uploads / downloads on copy streams,
+    one stream per direction or row slices over three) returns the same
+    bits as the device path, over consecutive steps."""
+    M, K, N = 560, 768, 1024                      # 560 rows: slices of 186/187/187
+    dev_lin = q.Fp8Linear(M, K, N)
+    host_lin = q.Fp8Linear(M, K, N)
+    host_lin.copy_lanes = lanes
+    hy = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    hdx = torch.empty((M, K), dtype=torch.bfloat16).pin_memory()
+    hdw = torch.empty((N, K), dtype=torch.bfloat16).pin_memory()
+    for step in range(3):
+        x, w, dy = si.linear_inputs(M, K, N, w_init="uniform64", seed=3, step=step)
+        pin = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
+        host_lin.step_host(pin(x), pin(w), pin(dy), hy, hdx, hdw)
+        torch.cuda.current_stream().synchronize()
+        dev_lin.step(to_dev_bf16(x), to_dev_bf16(w), to_dev_bf16(dy))
+        torch.cuda.synchronize()
+        assert torch.equal(hy.view(torch.int16), dev_lin.y.cpu().view(torch.int16)), step
+        assert torch.equal(hdx.view(torch.int16), dev_lin.dx.cpu().view(torch.int16)), step
+        assert torch.equal(hdw.view(torch.int16), dev_lin.dw.cpu().view(torch.int16)), step
