@@ -412,7 +412,11 @@ def run_native(args):
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1),
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 3),
                 "traffic": tr["bytes_per_launch"] if tr else None,
-                "kernel": "gemm_fp8_kernel (tcgen05, e4m3/e5m2 x e4m3 -> bf16)",
+                "kernel": q.gemm_describe(M, N, K).split(":")[0] +
+                          " (tcgen05, e4m3/e5m2 x e4m3 -> bf16)",
+                "schedule": {"y = x8.W8^T": q.gemm_describe(M, N, K),
+                             "dX = dY8.W8t^T": q.gemm_describe(M, K, N),
+                             "dW = dY8t.x8t^T": q.gemm_describe(N, K, M)},
                 "launch_us": round(gemm_avg * 1e3, 1),
                 "peak_basis": "%s bf16 sustained %.1f TFLOP/s x %.0f (nominal fp8/bf16)" % (
                     peaks["source"], peaks["bf16_tflops_sustained"], FP8_OVER_BF16)}

@@ -240,6 +240,15 @@ fp8lin_status fp8lin_gemm(const uint8_t* a, const uint8_t* b, int64_t M, int64_t
                           const float* inv_a, const float* inv_b, void* d, int64_t ldd,
                           void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* Names the kernel, tile shape and schedule fp8lin_gemm uses on the current
+ * device for an M x N x K GEMM with a workspace of fp8lin_workspace_bytes,
+ * as one NUL-terminated line written into buf (caller-owned host memory of
+ * buf_len bytes; truncated to fit).  The kernel name is spelled as profilers
+ * list it, e.g. "gemm_fp8_pair_kernel<256, 6>".  Enqueues nothing.  Returns
+ * FP8LIN_EINVAL for negative sizes or a NULL / empty buffer, FP8LIN_ECUDA
+ * without a usable device. */
+fp8lin_status fp8lin_gemm_describe(int64_t M, int64_t N, int64_t K, char* buf, size_t buf_len);
+
 /* Forward of the Linear: amax/scale/cast of x ([M, K], e4m3, state sx) and
  * W ([N, K], e4m3, state sw), then y = x8 . W8^T * inv_x * inv_w (bf16
  * [M, N]).  Writes the fp8 copies x8 [M, K], x8t [K, M], w8 [N, K],

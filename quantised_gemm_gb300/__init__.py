@@ -33,6 +33,7 @@ __all__ = [
     "E4M3", "E5M2", "AMAX_ATOMIC", "AMAX_REDUCTION", "AMAX_SINGLE_PASS", "AMAX_AUTO", "DYNAMIC",
     "DELAYED",
     "Fp8linError", "ScalingState", "Workspace", "amax", "amax_noalloc", "scale", "cast", "cast_dynamic", "gemm",
+    "gemm_describe",
     "forward", "backward", "check", "workspace_bytes", "single_pass_max_elems", "launch_count",
     "profile_enable", "profile_collect", "Fp8Linear", "library", "Float8Linear",
     "Float8LinearConfig", "CastConfig", "convert_to_float8_training",
@@ -75,6 +76,14 @@ def workspace_bytes(M: int = 0, K: int = 0, N: int = 0) -> int:
 
 def single_pass_max_elems() -> int:
     return int(library().fp8lin_single_pass_max_elems())
+
+
+def gemm_describe(M: int, N: int, K: int) -> str:
+    """The kernel, tile shape and schedule gemm() uses for an M x N x K GEMM
+    on the current device."""
+    buf = ctypes.create_string_buffer(256)
+    _lib.check(library().fp8lin_gemm_describe(M, N, K, buf, len(buf)), "fp8lin_gemm_describe")
+    return buf.value.decode()
 
 
 class Workspace:

@@ -74,6 +74,7 @@ _SIGNATURES = {
     "fp8lin_cast_dynamic": (ctypes.c_int, [_P, _I64, _I64, _I64, _ST, _P, _P, _P, _P]),
     "fp8lin_gemm": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I64, _I64, _I32, _I32, _P, _P,
                                    _P, _I64, _P, _SZ, _P]),
+    "fp8lin_gemm_describe": (ctypes.c_int, [_I64, _I64, _I64, ctypes.c_char_p, _SZ]),
     "fp8lin_forward": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _ST, _ST, _P, _P, _P, _P, _P,
                                       _P, _SZ, _P]),
     "fp8lin_backward": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _ST, _ST, _ST, _P, _P,

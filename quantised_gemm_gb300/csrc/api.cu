@@ -525,6 +525,16 @@ fp8lin_status fp8lin_gemm(const uint8_t* a, const uint8_t* b, int64_t M, int64_t
                  stream);
 }
 
+fp8lin_status fp8lin_gemm_describe(int64_t M, int64_t N, int64_t K, char* buf, size_t buf_len) {
+  if (M < 0 || N < 0 || K < 0 || buf == nullptr || buf_len == 0) return FP8LIN_EINVAL;
+  buf[0] = '\0';
+  DeviceInfo dev;
+  fp8lin_status s = get_dev(&dev);
+  if (s != FP8LIN_OK) return s;
+  cudaError_t e = describe_gemm(M, N, K, dev, buf, buf_len);
+  return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);
+}
+
 static fp8lin_status check_linear_sizes(int64_t M, int64_t K, int64_t N) {
   if (M < 0 || K < 0 || N < 0) return FP8LIN_EINVAL;
   if (M % 16 != 0 || K % 16 != 0 || N % 16 != 0) return FP8LIN_EUNSUPPORTED;

@@ -840,69 +840,57 @@ bool make_map_out(CUtensorMap* map, const void* base, int64_t rows, int64_t cols
   return r == CUDA_SUCCESS;
 }
 
-// Choose the schedule of `tiles` tiles on `slots` persistent units (CTAs or
-// pairs) with `num_kb` K blocks each: whole tiles round-robin, except that
-// when the tiles do not fill one wave and the K loop is long, each tile runs
-// as S K slices (S = slots / tiles) reduced by the slices together.  Splitting
-// the partial last wave of a multi-wave grid (stream-K style) was measured
-// slower on the Linear's shapes than leaving it partial: the extra epilogues
-// and partial traffic cost more than the idle tail.
-void plan_schedule(GemmParams& p, int tiles, int slots, int num_kb, int rows_per_tile, int bn,
-                   const GemmArgs& g) {
-  p.t_full = tiles;
-  p.s_tail = 1;
-  p.partials = nullptr;
-  p.tickets = nullptr;
-  if (g.ws_split == nullptr || slots < 2 || tiles >= slots || num_kb < 16) return;
+// Number of K slices each tile runs as when `tiles` tiles of rows_per_tile x
+// bn are scheduled on `slots` persistent units (CTAs or pairs) with `num_kb`
+// K blocks each, given `split_bytes` of workspace for fp32 partials (1 = whole
+// tiles round-robin).  The K loop is split only when the tiles do not fill one
+// wave and the K loop is long: S = slots / tiles slices, reduced by the slices
+// together.  Splitting the partial last wave of a multi-wave grid (stream-K
+// style) was measured slower on the Linear's shapes than leaving it partial:
+// the extra epilogues and partial traffic cost more than the idle tail.
+int split_ways(int tiles, int slots, int num_kb, int rows_per_tile, int bn, size_t split_bytes) {
+  if (split_bytes == 0 || slots < 2 || tiles >= slots || num_kb < 16) return 1;
   const size_t groups = static_cast<size_t>(rows_per_tile) / 32 * (bn >= 64 ? 2 : 1);
   const size_t tile_bytes = static_cast<size_t>(rows_per_tile) * bn * sizeof(float);
   int s = slots / tiles;
   if (s > kMaxSplit) s = kMaxSplit;
   if (s > num_kb) s = num_kb;
-  if (s < 2) return;
+  if (s < 2) return 1;
   const int per = (num_kb + s - 1) / s;
   s = (num_kb + per - 1) / per;  // no empty slice
-  if (s < 2) return;
+  if (s < 2) return 1;
   const size_t need_tickets = 2 * static_cast<size_t>(tiles) * groups;
-  if (static_cast<size_t>(tiles) * s * tile_bytes > g.ws_split_bytes || need_tickets > kWsTickets)
-    return;
-  p.t_full = 0;
-  p.s_tail = s;
-  p.partials = g.ws_split;
-  p.tickets = g.ws_tickets;
+  if (static_cast<size_t>(tiles) * s * tile_bytes > split_bytes || need_tickets > kWsTickets)
+    return 1;
+  return s;
 }
 
+void plan_schedule(GemmParams& p, int tiles, int slots, int num_kb, int rows_per_tile, int bn,
+                   const GemmArgs& g) {
+  const bool can_split = g.ws_split != nullptr && g.ws_tickets != nullptr;
+  const int s =
+      split_ways(tiles, slots, num_kb, rows_per_tile, bn, can_split ? g.ws_split_bytes : 0);
+  p.t_full = s > 1 ? 0 : tiles;
+  p.s_tail = s;
+  p.partials = s > 1 ? g.ws_split : nullptr;
+  p.tickets = s > 1 ? g.ws_tickets : nullptr;
+}
+
+// One-time per-device set-up of a kernel's shared-memory limit (and, for the
+// pair kernel, the number of co-resident clusters of 2 it gets).
 template <int BN, int STAGES, bool kTransStore>
-cudaError_t run(const uint8_t* a, int64_t lda, const uint8_t* b, int64_t ldb, GemmParams p,
-                const GemmArgs& g, const DeviceInfo& dev, cudaStream_t stream) {
-  using C = Cfg<BN, STAGES>;
-  auto kernel = gemm_fp8_kernel<BN, STAGES, kTransStore>;
+cudaError_t one_cta_setup(const DeviceInfo& dev) {
   static int configured_device = -1;
-  if (configured_device != dev.device) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(C::kSmemBytes));
-    if (e != cudaSuccess) return e;
-    configured_device = dev.device;
-  }
-  CUtensorMap ma, mb, md;
-  if (!make_map_k_major(&ma, a, p.M, p.K, lda, kBM)) return map_failed("GEMM operand A map");
-  if (!make_map_k_major(&mb, b, p.N, p.K, ldb, BN)) return map_failed("GEMM operand B map");
-  if (kTransStore)
-    md = mb;  // unused: the transposed store writes D directly
-  else if (!make_map_out(&md, p.d, p.M, p.N, p.ldd))
-    return map_failed("GEMM output map");
-  const int tiles = ((p.M + kBM - 1) / kBM) * ((p.N + BN - 1) / BN);
-  plan_schedule(p, tiles, dev.num_sms, (p.K + kBK - 1) / kBK, kBM, BN, g);
-  set_error_site("one-CTA GEMM launch");
-  const int units = p.t_full + (tiles - p.t_full) * p.s_tail;
-  const int grid = units < dev.num_sms ? units : dev.num_sms;
-  return launch_kernel(kernel, dim3(grid), dim3(kGemmThreads), C::kSmemBytes, stream, 1, false, ma,
-                       mb, md, p);
+  if (configured_device == dev.device) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(gemm_fp8_kernel<BN, STAGES, kTransStore>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(Cfg<BN, STAGES>::kSmemBytes));
+  if (e == cudaSuccess) configured_device = dev.device;
+  return e;
 }
 
 template <int BN, int STAGES>
-cudaError_t run_pair(const uint8_t* a, int64_t lda, const uint8_t* b, int64_t ldb, GemmParams p,
-                     const GemmArgs& g, const DeviceInfo& dev, cudaStream_t stream) {
+cudaError_t pair_setup(const DeviceInfo& dev, int* slots) {
   using C = PairCfg<BN, STAGES>;
   auto kernel = gemm_fp8_pair_kernel<BN, STAGES>;
   static int configured_device = -1;
@@ -930,6 +918,41 @@ cudaError_t run_pair(const uint8_t* a, int64_t lda, const uint8_t* b, int64_t ld
     max_pairs = n;
     configured_device = dev.device;
   }
+  *slots = max_pairs;
+  return cudaSuccess;
+}
+
+template <int BN, int STAGES, bool kTransStore>
+cudaError_t run(const uint8_t* a, int64_t lda, const uint8_t* b, int64_t ldb, GemmParams p,
+                const GemmArgs& g, const DeviceInfo& dev, cudaStream_t stream) {
+  using C = Cfg<BN, STAGES>;
+  auto kernel = gemm_fp8_kernel<BN, STAGES, kTransStore>;
+  cudaError_t e = one_cta_setup<BN, STAGES, kTransStore>(dev);
+  if (e != cudaSuccess) return e;
+  CUtensorMap ma, mb, md;
+  if (!make_map_k_major(&ma, a, p.M, p.K, lda, kBM)) return map_failed("GEMM operand A map");
+  if (!make_map_k_major(&mb, b, p.N, p.K, ldb, BN)) return map_failed("GEMM operand B map");
+  if (kTransStore)
+    md = mb;  // unused: the transposed store writes D directly
+  else if (!make_map_out(&md, p.d, p.M, p.N, p.ldd))
+    return map_failed("GEMM output map");
+  const int tiles = ((p.M + kBM - 1) / kBM) * ((p.N + BN - 1) / BN);
+  plan_schedule(p, tiles, dev.num_sms, (p.K + kBK - 1) / kBK, kBM, BN, g);
+  set_error_site("one-CTA GEMM launch");
+  const int units = p.t_full + (tiles - p.t_full) * p.s_tail;
+  const int grid = units < dev.num_sms ? units : dev.num_sms;
+  return launch_kernel(kernel, dim3(grid), dim3(kGemmThreads), C::kSmemBytes, stream, 1, false, ma,
+                       mb, md, p);
+}
+
+template <int BN, int STAGES>
+cudaError_t run_pair(const uint8_t* a, int64_t lda, const uint8_t* b, int64_t ldb, GemmParams p,
+                     const GemmArgs& g, const DeviceInfo& dev, cudaStream_t stream) {
+  using C = PairCfg<BN, STAGES>;
+  auto kernel = gemm_fp8_pair_kernel<BN, STAGES>;
+  int max_pairs = 0;
+  cudaError_t e = pair_setup<BN, STAGES>(dev, &max_pairs);
+  if (e != cudaSuccess) return e;
   CUtensorMap ma, mb, md;
   if (!make_map_k_major(&ma, a, p.M, p.K, lda, kBM)) return map_failed("pair GEMM operand A map");
   if (!make_map_k_major(&mb, b, p.N, p.K, ldb, BN / 2))
@@ -975,6 +998,31 @@ size_t gemm_split_workspace_bytes(int num_sms) {
   return static_cast<size_t>(num_sms) * kBM * 256 * sizeof(float);
 }
 
+namespace {
+
+// The kernel and tile shape for a Linear GEMM of M rows and N columns:
+// swap-AB (D^T = B . A^T, the weight-side operand fills the 128-row MMA and
+// the few rows of A become N = 16 / 32 / 64) for M <= 64; one-CTA 128-row
+// tiles up to M = 128; CTA pairs with 256-row tiles above.  BN = 256 unless
+// 128 pads the N edge clearly less (e.g. N = 1600).
+enum class Variant { kSwap16, kSwap32, kSwap64, kOne128, kOne256, kPair128, kPair256 };
+
+Variant choose_variant(int64_t M, int64_t N) {
+  if (M <= 16) return Variant::kSwap16;
+  if (M <= 32) return Variant::kSwap32;
+  if (M <= 64) return Variant::kSwap64;
+  const int64_t pad256 = (N + 255) / 256 * 256, pad128 = (N + 127) / 128 * 128;
+  const bool narrow = pad256 * 100 > pad128 * 105;
+  if (M > kBM) return narrow ? Variant::kPair128 : Variant::kPair256;
+  return narrow ? Variant::kOne128 : Variant::kOne256;
+}
+
+bool is_swap(Variant v) {
+  return v == Variant::kSwap16 || v == Variant::kSwap32 || v == Variant::kSwap64;
+}
+
+}  // namespace
+
 cudaError_t launch_gemm(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t stream) {
   GemmParams p;
   p.inv_a = g.inv_a;
@@ -983,15 +1031,15 @@ cudaError_t launch_gemm(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t s
   p.ldd = g.ldd;
   p.err = g.ws_error;
   p.K = static_cast<int>(g.K);
-  if (g.M <= 64) {
-    // Few rows: D^T = B . A^T, the weight-side operand fills the 128-row MMA.
+  const Variant v = choose_variant(g.M, g.N);
+  if (is_swap(v)) {
     p.M = static_cast<int>(g.N);
     p.N = static_cast<int>(g.M);
-    if (g.M <= 16) {
+    if (v == Variant::kSwap16) {
       p.idesc = make_idesc_f8(g.fmt_b, g.fmt_a, kBM, 16);
       return run<16, 8, true>(g.b, g.ldb, g.a, g.lda, p, g, dev, stream);
     }
-    if (g.M <= 32) {
+    if (v == Variant::kSwap32) {
       p.idesc = make_idesc_f8(g.fmt_b, g.fmt_a, kBM, 32);
       return run<32, 8, true>(g.b, g.ldb, g.a, g.lda, p, g, dev, stream);
     }
@@ -1000,24 +1048,61 @@ cudaError_t launch_gemm(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t s
   }
   p.M = static_cast<int>(g.M);
   p.N = static_cast<int>(g.N);
-  // BN = 256 unless 128 pads the N edge clearly less (e.g. N = 1600).
-  const int64_t pad256 = (g.N + 255) / 256 * 256, pad128 = (g.N + 127) / 128 * 128;
-  const bool narrow = pad256 * 100 > pad128 * 105;
-  if (g.M > kBM) {
-    // CTA pairs: 256-row tiles.
-    if (narrow) {
+  switch (v) {
+    case Variant::kPair128:
       p.idesc = make_idesc_f8(g.fmt_a, g.fmt_b, 2 * kBM, 128);
       return run_pair<128, 8>(g.a, g.lda, g.b, g.ldb, p, g, dev, stream);
-    }
-    p.idesc = make_idesc_f8(g.fmt_a, g.fmt_b, 2 * kBM, 256);
-    return run_pair<256, 6>(g.a, g.lda, g.b, g.ldb, p, g, dev, stream);
+    case Variant::kPair256:
+      p.idesc = make_idesc_f8(g.fmt_a, g.fmt_b, 2 * kBM, 256);
+      return run_pair<256, 6>(g.a, g.lda, g.b, g.ldb, p, g, dev, stream);
+    case Variant::kOne128:
+      p.idesc = make_idesc_f8(g.fmt_a, g.fmt_b, kBM, 128);
+      return run<128, 6, false>(g.a, g.lda, g.b, g.ldb, p, g, dev, stream);
+    default:
+      p.idesc = make_idesc_f8(g.fmt_a, g.fmt_b, kBM, 256);
+      return run<256, 4, false>(g.a, g.lda, g.b, g.ldb, p, g, dev, stream);
   }
-  if (narrow) {
-    p.idesc = make_idesc_f8(g.fmt_a, g.fmt_b, kBM, 128);
-    return run<128, 6, false>(g.a, g.lda, g.b, g.ldb, p, g, dev, stream);
+}
+
+cudaError_t describe_gemm(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev, char* buf,
+                          size_t len) {
+  const Variant v = choose_variant(M, N);
+  const char* name = "";
+  int rows = kBM, bn = 256, slots = dev.num_sms;
+  cudaError_t e = cudaSuccess;
+  switch (v) {
+    case Variant::kSwap16: name = "gemm_fp8_kernel<16, 8, 1>"; bn = 16; break;
+    case Variant::kSwap32: name = "gemm_fp8_kernel<32, 8, 1>"; bn = 32; break;
+    case Variant::kSwap64: name = "gemm_fp8_kernel<64, 8, 1>"; bn = 64; break;
+    case Variant::kOne128: name = "gemm_fp8_kernel<128, 6, 0>"; bn = 128; break;
+    case Variant::kOne256: name = "gemm_fp8_kernel<256, 4, 0>"; break;
+    case Variant::kPair128:
+      name = "gemm_fp8_pair_kernel<128, 8>";
+      bn = 128;
+      rows = 2 * kBM;
+      e = pair_setup<128, 8>(dev, &slots);
+      break;
+    case Variant::kPair256:
+      name = "gemm_fp8_pair_kernel<256, 6>";
+      rows = 2 * kBM;
+      e = pair_setup<256, 6>(dev, &slots);
+      break;
   }
-  p.idesc = make_idesc_f8(g.fmt_a, g.fmt_b, kBM, 256);
-  return run<256, 4, false>(g.a, g.lda, g.b, g.ldb, p, g, dev, stream);
+  if (e != cudaSuccess) return e;
+  const int64_t tm = is_swap(v) ? N : M, tn = is_swap(v) ? M : N;  // as the kernel sees it
+  const int64_t tiles64 = ((tm + rows - 1) / rows) * ((tn + bn - 1) / bn);
+  const int tiles = tiles64 > (1 << 30) ? (1 << 30) : static_cast<int>(tiles64);
+  const int num_kb = static_cast<int>((K + kBK - 1) / kBK);
+  const int ways =
+      split_ways(tiles, slots, num_kb, rows, bn, gemm_split_workspace_bytes(dev.num_sms));
+  const int units = ways > 1 ? tiles * ways : tiles;
+  const int used = units < slots ? units : slots;
+  char sched[32] = "whole tiles";
+  if (ways > 1) std::snprintf(sched, sizeof(sched), "K split %d ways", ways);
+  std::snprintf(buf, len, "%s: %s%dx%d tiles, %d tiles on %d of %d %s, %s", name,
+                is_swap(v) ? "swap-AB (D^T = B.A^T), " : "", rows, bn, tiles, used, slots,
+                rows == 2 * kBM ? "CTA pairs" : "CTAs", sched);
+  return cudaSuccess;
 }
 
 }  // namespace fp8lin

@@ -185,6 +185,11 @@ struct GemmArgs {
 };
 cudaError_t launch_gemm(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t stream);
 
+// One line naming the kernel, tile shape and schedule launch_gemm uses for
+// an M x N x K GEMM (given a workspace of fp8lin_workspace_bytes).
+cudaError_t describe_gemm(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev, char* buf,
+                          size_t len);
+
 // Workspace bytes the tail K split can use at most on a device with num_sms SMs.
 size_t gemm_split_workspace_bytes(int num_sms);
 

@@ -40,7 +40,8 @@ CASES = [
     (48, 208, 160),         # few rows, ragged
     (64, 272, 320),
     (1040, 784, 512),
-    (128, 4096, 1024),      # one-CTA tiles, 16 tiles: tail split into K slices
+    (128, 4096, 1024),      # one-CTA tiles, 16 tiles, short K loop: whole tiles
+    (128, 4096, 4096),      # one-CTA tiles, 16 tiles, 32 k-blocks: K split 8 ways
     (2048, 2560, 256),      # pair tiles: one full wave plus a partial one
     (4096, 4096, 1024),     # 256 pair tiles: 3.4 waves
     (128, 40960, 512),      # 160 one-CTA tiles: more tiles than CTAs
@@ -142,3 +143,40 @@ def test_gemm_without_split_workspace_matches(ws):
     torch.cuda.synchronize()
     y, s = oracle.gemm(a8, b8, E4M3, E4M3, sa, sb)
     assert_within_bound(bf16_to_f64(d), y, s, "no-split fallback")
+
+
+@pytest.mark.parametrize("mnk,kernel,sched", [
+    ((16, 4096, 4096), "gemm_fp8_kernel<16, 8, 1>", "K split 4 ways"),
+    ((48, 208, 160), "gemm_fp8_kernel<64, 8, 1>", "whole tiles"),
+    ((128, 4096, 4096), "gemm_fp8_kernel<256, 4, 0>", "K split 8 ways"),
+    ((128, 1600, 512), "gemm_fp8_kernel<128, 6, 0>", "whole tiles"),
+    ((384, 1600, 1600), "gemm_fp8_pair_kernel<128, 8>", "whole tiles"),
+    ((4096, 4096, 1024), "gemm_fp8_pair_kernel<256, 6>", "whole tiles"),
+])
+def test_gemm_describe_names_the_launched_kernel(mnk, kernel, sched, ws):
+    """gemm_describe() reports the kernel and schedule gemm() runs; the
+    profiler's kernel records confirm the kernel."""
+    from torch.profiler import ProfilerActivity, profile
+    M, N, K = mnk
+    desc = q.gemm_describe(M, N, K)
+    assert desc.startswith(kernel + ":") and desc.endswith(sched), desc
+    a = torch.zeros((M, K), dtype=torch.uint8, device="cuda")
+    b = torch.zeros((N, K), dtype=torch.uint8, device="cuda")
+    one = torch.ones(1, device="cuda")
+    d = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    names = []
+    for _ in range(2):      # the first profiling session of a process may miss kernels
+        torch.cuda.synchronize()
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            q.gemm(a, b, E4M3, E4M3, one, one, d, ws)
+            torch.cuda.synchronize()
+        names = [e.name for e in prof.events() if "gemm_fp8" in e.name]
+        if names:
+            break
+    q.check(ws)
+    assert torch.count_nonzero(d.float()).item() == 0
+    if not names:
+        pytest.skip("the profiler recorded no kernels (no CUPTI activity on this host)")
+    # the profiler spells a bool template argument as true / false, ncu as 1 / 0
+    names = [n.replace(", true>", ", 1>").replace(", false>", ", 0>") for n in names]
+    assert all(kernel in n for n in names), names
