@@ -243,6 +243,64 @@ def linear_sweep_entry(q, torch, dev, name, steps, warmup, flush, use_graph=True
             "cuda_graph": use_graph}
 
 
+def chain_sweep_entry(q, torch, dev, name, steps, warmup, flush, rounds=3):
+    """Two Linears of a workload's shape in a chain (the second consumes the
+    first's y, the first's grad_output is the second's dX), fwd+bwd of both,
+    with the amax of y and dX taken in the GEMM epilogues (link_linears: those
+    two casts read their tensor once) and with separate amax passes.  The two
+    variants alternate over `rounds` rounds (median reported), so clock drift
+    under the power cap does not favour either; a profiled pass of each gives
+    its time per kernel kind."""
+    import statistics
+    import synth_inputs as si
+    M, K, N = si.WORKLOADS[name]["shapes"][0]
+    assert K == N, "a chain of square Linears"
+    x, w, dy = make_inputs(name, 0)
+    xd, wd, dyd = to_dev(x, dev), to_dev(w, dev), to_dev(dy, dev)
+    del x, w, dy
+    variants = {}
+    for linked in (False, True):
+        l1, l2 = q.Fp8Linear(M, K, N, device=dev), q.Fp8Linear(M, N, N, device=dev)
+        if linked:
+            q.link_linears(l1, l2)
+
+        def step(l1=l1, l2=l2):
+            l1.forward(xd, wd)
+            l2.forward(l1.y, wd)
+            l2.backward(dyd)
+            l1.backward(l2.dx)
+
+        for _ in range(warmup):
+            step()
+        q.profile_enable(True)
+        for _ in range(2):
+            step()
+        prof = q.profile_collect()
+        q.profile_enable(False)
+        variants["fused_amax" if linked else "separate_amax"] = {
+            "step": step, "graph": graphed(torch, step), "lins": (l1, l2), "ms": [],
+            "kernel_us_per_step": {k: round(v[0] * 1e3 / 2, 1) for k, v in prof.items()
+                                   if v[1] > 0}}
+    torch.cuda.synchronize()
+    for _ in range(rounds):
+        for v in variants.values():
+            v["ms"].append(time_region(v["graph"], steps, flush) / steps)
+    res = {"workload": "2 x %s chained" % name, "l2": "flushed between steps" if flush else
+           "inputs larger than L2", "cuda_graph": True, "rounds": rounds}
+    for key, v in variants.items():
+        for lin in v["lins"]:
+            q.check(lin.ws)
+        ms = statistics.median(v["ms"])
+        res[key] = {"us_per_fwd_bwd": round(ms * 1e3, 2),
+                    "tflops": round(2 * 6.0 * M * N * K / (ms * 1e-3) / 1e12, 1),
+                    "kernel_us_per_step": v["kernel_us_per_step"]}
+    res["saved_us"] = round(res["separate_amax"]["us_per_fwd_bwd"] -
+                            res["fused_amax"]["us_per_fwd_bwd"], 2)
+    del variants, xd, wd, dyd
+    torch.cuda.empty_cache()
+    return res
+
+
 def cast_sweep(q, torch, dev, peaks, full):
     """amax + scale + cast (+T) of [R, 4096] / [4096, R] tensors: GB/s of the
     algorithmic bytes (2 B read + 1 B per fp8 copy) and fraction of HBM."""
@@ -466,13 +524,16 @@ def run_native(args):
     if not args.no_sweep:
         flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
         flush = lambda: flush_buf.zero_()  # noqa: E731
-        sweep = {"linears": [], "cast": None}
+        sweep = {"linears": [], "chains": None, "cast": None}
         for name in ("linear4096_m16", "linear4096_m256", "linear4096_m4096",
                      "gpt1.5b_linears_m12288", "llama3_8b_ffn_m8192"):
             small = si.WORKLOADS[name]["shapes"][0][0] <= 4096
             sweep["linears"].append(linear_sweep_entry(
                 q, torch, dev, name, steps=50 if small else 20, warmup=5,
                 flush=flush if small else None))
+        sweep["chains"] = [
+            chain_sweep_entry(q, torch, dev, "linear4096_m4096", steps=50, warmup=5, flush=flush),
+            chain_sweep_entry(q, torch, dev, "linear4096_m65536", steps=10, warmup=3, flush=None)]
         del flush_buf
         torch.cuda.empty_cache()
         sweep["cast"] = cast_sweep(q, torch, dev, peaks, args.full_sweep)

@@ -90,12 +90,22 @@ typedef enum { FP8LIN_E4M3 = 0, FP8LIN_E5M2 = 1 } fp8lin_fmt;
  *               amax -> scale -> cast (+transpose) in one cooperative launch
  *               that keeps the bf16 tensor on chip between the phases; only
  *               for tensors that fit (fp8lin_single_pass_max_elems()); larger
- *               tensors fall back to ATOMIC inside forward/backward. */
+ *               tensors fall back to ATOMIC inside forward/backward;
+ *   PRECOMPUTED (dynamic scaling only, not fp8lin_amax) *amax already holds
+ *               the tensor's amax -- the GEMM that produced the tensor wrote
+ *               it from its epilogue (the y_amax / dx_amax outputs below)
+ *               -- so the cast reads the tensor once: scale, then cast
+ *               (+transpose).  This moves the amax into the producer: the
+ *               diagnosis in "Why swapping nn.Linear with FP8Linear brings
+ *               throughput decrease ..." (pytorch/ao issue 1199) is that the
+ *               eager float8 casts run as kernels of their own, apart from
+ *               the ops around them. */
 typedef enum {
   FP8LIN_AMAX_ATOMIC = 0,
   FP8LIN_AMAX_REDUCTION = 1,
   FP8LIN_AMAX_SINGLE_PASS = 2,
-  FP8LIN_AMAX_AUTO = 3       /* SINGLE_PASS where the tensor fits, else ATOMIC */
+  FP8LIN_AMAX_AUTO = 3,      /* SINGLE_PASS where the tensor fits, else ATOMIC */
+  FP8LIN_AMAX_PRECOMPUTED = 4
 } fp8lin_amax_algo;
 
 /* Scaling type per tensor, after CastConfig(scaling_type=...) in the repro
@@ -233,12 +243,15 @@ fp8lin_status fp8lin_cast_dynamic(const void* x, int64_t rows, int64_t cols, int
  * a: fp8 [M, K] row stride lda bytes; b: fp8 [N, K] row stride ldb bytes
  * (both with the contraction index fastest); fmt_a, fmt_b: fp8lin_fmt;
  * inv_a, inv_b: device fp32[1]; d: bf16 [M, N] row stride ldd elements.
+ * d_amax: NULL, or device fp32[1] that receives max |d| over the stored
+ * bf16 values, computed in the epilogue (no extra pass over d); 0 when d is
+ * empty or K == 0.
  * K == 0 writes zeros.  Requires lda, ldb multiples of 16, ldd a multiple
  * of 8, N and K multiples of 16. */
 fp8lin_status fp8lin_gemm(const uint8_t* a, const uint8_t* b, int64_t M, int64_t N, int64_t K,
                           int64_t lda, int64_t ldb, int32_t fmt_a, int32_t fmt_b,
                           const float* inv_a, const float* inv_b, void* d, int64_t ldd,
-                          void* ws, size_t ws_bytes, cudaStream_t stream);
+                          float* d_amax, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Names the kernel, tile shape and schedule fp8lin_gemm uses on the current
  * device for an M x N x K GEMM with a workspace of fp8lin_workspace_bytes,
@@ -255,23 +268,29 @@ fp8lin_status fp8lin_gemm_describe(int64_t M, int64_t N, int64_t K, char* buf, s
  * w8t [K, N]; x8t and w8t are what fp8lin_backward needs.  Dynamic states
  * take their scale from this call's amax; delayed states cast with their
  * stored scale and record this call's amax (and do the amax init first when
- * needs_init is set).  All buffers dense row-major. */
+ * needs_init is set).  All buffers dense row-major.
+ * y_amax: NULL, or device fp32[1] that receives max |y| from the GEMM
+ * epilogue -- point it at the amax of the next layer's input state and give
+ * that state FP8LIN_AMAX_PRECOMPUTED to cast y in one pass. */
 fp8lin_status fp8lin_forward(const void* x, const void* w, int64_t M, int64_t K, int64_t N,
                              fp8lin_scaling_state* sx, fp8lin_scaling_state* sw,
-                             void* y, uint8_t* x8, uint8_t* x8t, uint8_t* w8, uint8_t* w8t,
-                             void* ws, size_t ws_bytes, cudaStream_t stream);
+                             void* y, float* y_amax, uint8_t* x8, uint8_t* x8t, uint8_t* w8,
+                             uint8_t* w8t, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Backward of the Linear: amax/scale/cast of dY ([M, N], e5m2, state sdy)
  * into dy8 [M, N] and dy8t [N, M], then
  *   dX = dY8 . W8 * inv_dy * inv_w     (bf16 [M, K], skipped if dx == NULL)
  *   dW = dY8^T . x8 * inv_dy * inv_x   (bf16 [N, K], skipped if dw == NULL)
- * from the x8t / w8t written by fp8lin_forward and the inv_scale of sx, sw. */
+ * from the x8t / w8t written by fp8lin_forward and the inv_scale of sx, sw.
+ * dx_amax, dw_amax: NULL, or device fp32[1] receiving max |dX| / max |dW|
+ * from the GEMM epilogues (each needs its GEMM: dx / dw not NULL); dx_amax
+ * can feed the previous layer's grad_output state as PRECOMPUTED. */
 fp8lin_status fp8lin_backward(const void* dy, int64_t M, int64_t K, int64_t N,
                               const uint8_t* x8t, const uint8_t* w8t,
                               const fp8lin_scaling_state* sx, const fp8lin_scaling_state* sw,
                               fp8lin_scaling_state* sdy, uint8_t* dy8, uint8_t* dy8t,
-                              void* dx, void* dw, void* ws, size_t ws_bytes,
-                              cudaStream_t stream);
+                              void* dx, void* dw, float* dx_amax, float* dw_amax, void* ws,
+                              size_t ws_bytes, cudaStream_t stream);
 
 /* ---- measurement hooks ------------------------------------------------ */
 

@@ -26,16 +26,18 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import (AMAX_ATOMIC, AMAX_AUTO, AMAX_REDUCTION, AMAX_SINGLE_PASS, DELAYED, DYNAMIC,
+from ._lib import (AMAX_ATOMIC, AMAX_AUTO, AMAX_PRECOMPUTED, AMAX_REDUCTION, AMAX_SINGLE_PASS,
+                   DELAYED, DYNAMIC,
                    E4M3, E5M2, Fp8linError, PROF_KINDS)
 
 __all__ = [
-    "E4M3", "E5M2", "AMAX_ATOMIC", "AMAX_REDUCTION", "AMAX_SINGLE_PASS", "AMAX_AUTO", "DYNAMIC",
+    "E4M3", "E5M2", "AMAX_ATOMIC", "AMAX_REDUCTION", "AMAX_SINGLE_PASS", "AMAX_AUTO",
+    "AMAX_PRECOMPUTED", "DYNAMIC",
     "DELAYED",
     "Fp8linError", "ScalingState", "Workspace", "amax", "amax_noalloc", "scale", "cast", "cast_dynamic", "gemm",
     "gemm_describe",
     "forward", "backward", "check", "workspace_bytes", "single_pass_max_elems", "launch_count",
-    "profile_enable", "profile_collect", "Fp8Linear", "library", "Float8Linear",
+    "profile_enable", "profile_collect", "Fp8Linear", "link_linears", "library", "Float8Linear",
     "Float8LinearConfig", "CastConfig", "convert_to_float8_training",
     "sync_float8_amax_and_scale_history",
 ]
@@ -102,7 +104,9 @@ class ScalingState:
     """Per-tensor scaling state with its device buffers.
 
     kind: DYNAMIC or DELAYED; fmt: E4M3 or E5M2; history_len: ring length
-    for DELAYED; amax_algo: AMAX_ATOMIC, AMAX_REDUCTION or AMAX_SINGLE_PASS.
+    for DELAYED; amax_algo: AMAX_ATOMIC, AMAX_REDUCTION, AMAX_SINGLE_PASS,
+    AMAX_AUTO, or AMAX_PRECOMPUTED (``amax`` is written by the producing
+    GEMM's epilogue before the cast).
     Delayed states start with ``needs_init`` set (amax init on the first
     cast)."""
 
@@ -187,8 +191,10 @@ def cast_dynamic(x: torch.Tensor, state: ScalingState, out: torch.Tensor | None,
 
 
 def gemm(a8: torch.Tensor, b8: torch.Tensor, fmt_a: int, fmt_b: int, inv_a: torch.Tensor,
-         inv_b: torch.Tensor, out: torch.Tensor, ws: Workspace, stream=None):
-    """out[m, n] = bf16(sum_k a8[m, k] b8[n, k] * inv_a * inv_b)."""
+         inv_b: torch.Tensor, out: torch.Tensor, ws: Workspace, stream=None,
+         amax_out: torch.Tensor | None = None):
+    """out[m, n] = bf16(sum_k a8[m, k] b8[n, k] * inv_a * inv_b); amax_out
+    (fp32[1], optional) receives max |out| from the epilogue."""
     if a8.dim() != 2 or b8.dim() != 2 or a8.shape[1] != b8.shape[1]:
         raise ValueError("a8 [M, K] and b8 [N, K] expected")
     M, K = a8.shape
@@ -200,14 +206,14 @@ def gemm(a8: torch.Tensor, b8: torch.Tensor, fmt_a: int, fmt_b: int, inv_a: torc
                                max(a8.stride(0), K), max(b8.stride(0), K), fmt_a, fmt_b,
                                _dev(inv_a, "inv_a", torch.float32),
                                _dev(inv_b, "inv_b", torch.float32),
-                               _dev(out, "out", torch.bfloat16), max(out.stride(0), N), pw, nb,
-                               _stream(stream))
+                               _dev(out, "out", torch.bfloat16), max(out.stride(0), N),
+                               _dev(amax_out, "amax_out", torch.float32), pw, nb, _stream(stream))
     _lib.check(st, "fp8lin_gemm")
     return out
 
 
 def forward(x, w, sx: ScalingState, sw: ScalingState, y, x8, x8t, w8, w8t, ws: Workspace,
-            stream=None):
+            stream=None, y_amax: torch.Tensor | None = None):
     M, K = x.shape
     N = w.shape[0]
     for t, n in ((x, "x"), (w, "w"), (y, "y")):
@@ -217,7 +223,9 @@ def forward(x, w, sx: ScalingState, sw: ScalingState, y, x8, x8t, w8, w8t, ws: W
     cx, cw = sx.c_struct(), sw.c_struct()
     st = library().fp8lin_forward(_dev(x, "x", torch.bfloat16), _dev(w, "w", torch.bfloat16), M, K,
                                   N, ctypes.byref(cx), ctypes.byref(cw),
-                                  _dev(y, "y", torch.bfloat16), _dev(x8, "x8", torch.uint8),
+                                  _dev(y, "y", torch.bfloat16),
+                                  _dev(y_amax, "y_amax", torch.float32),
+                                  _dev(x8, "x8", torch.uint8),
                                   _dev(x8t, "x8t", torch.uint8), _dev(w8, "w8", torch.uint8),
                                   _dev(w8t, "w8t", torch.uint8), pw, nb, _stream(stream))
     sx._pull()
@@ -227,7 +235,8 @@ def forward(x, w, sx: ScalingState, sw: ScalingState, y, x8, x8t, w8, w8t, ws: W
 
 
 def backward(dy, x8t, w8t, sx: ScalingState, sw: ScalingState, sdy: ScalingState, dy8, dy8t,
-             dx, dw, ws: Workspace, stream=None):
+             dx, dw, ws: Workspace, stream=None, dx_amax: torch.Tensor | None = None,
+             dw_amax: torch.Tensor | None = None):
     M, N = dy.shape
     K = x8t.shape[0] if x8t is not None else w8t.shape[0]
     if not dy.is_contiguous():
@@ -239,7 +248,10 @@ def backward(dy, x8t, w8t, sx: ScalingState, sw: ScalingState, sdy: ScalingState
                                    ctypes.byref(sx.c_struct()), ctypes.byref(sw.c_struct()),
                                    ctypes.byref(cd), _dev(dy8, "dy8", torch.uint8),
                                    _dev(dy8t, "dy8t", torch.uint8), _dev(dx, "dx", torch.bfloat16),
-                                   _dev(dw, "dw", torch.bfloat16), pw, nb, _stream(stream))
+                                   _dev(dw, "dw", torch.bfloat16),
+                                   _dev(dx_amax, "dx_amax", torch.float32),
+                                   _dev(dw_amax, "dw_amax", torch.float32), pw, nb,
+                                   _stream(stream))
     sdy._pull()
     _lib.check(st, "fp8lin_backward")
     return dx, dw
@@ -261,6 +273,6 @@ def profile_collect() -> dict:
     return {k: (ms[i], cnt[i]) for i, k in enumerate(PROF_KINDS)}
 
 
-from .linear import Fp8Linear  # noqa: E402
+from .linear import Fp8Linear, link_linears  # noqa: E402
 from .nn import (CastConfig, Float8Linear, Float8LinearConfig,  # noqa: E402
                  convert_to_float8_training, sync_float8_amax_and_scale_history)

@@ -17,7 +17,7 @@ OK, EINVAL, EUNSUPPORTED, ECUDA, ETIMEOUT = 0, 1, 2, 3, 4
 # fp8lin_fmt
 E4M3, E5M2 = 0, 1
 # fp8lin_amax_algo
-AMAX_ATOMIC, AMAX_REDUCTION, AMAX_SINGLE_PASS, AMAX_AUTO = 0, 1, 2, 3
+AMAX_ATOMIC, AMAX_REDUCTION, AMAX_SINGLE_PASS, AMAX_AUTO, AMAX_PRECOMPUTED = 0, 1, 2, 3, 4
 # fp8lin_scaling
 DYNAMIC, DELAYED = 0, 1
 # profile kinds
@@ -73,12 +73,12 @@ _SIGNATURES = {
     "fp8lin_cast": (ctypes.c_int, [_P, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P]),
     "fp8lin_cast_dynamic": (ctypes.c_int, [_P, _I64, _I64, _I64, _ST, _P, _P, _P, _P]),
     "fp8lin_gemm": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I64, _I64, _I32, _I32, _P, _P,
-                                   _P, _I64, _P, _SZ, _P]),
+                                   _P, _I64, _P, _P, _SZ, _P]),
     "fp8lin_gemm_describe": (ctypes.c_int, [_I64, _I64, _I64, ctypes.c_char_p, _SZ]),
     "fp8lin_forward": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _ST, _ST, _P, _P, _P, _P, _P,
-                                      _P, _SZ, _P]),
+                                      _P, _P, _SZ, _P]),
     "fp8lin_backward": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _ST, _ST, _ST, _P, _P,
-                                       _P, _P, _P, _SZ, _P]),
+                                       _P, _P, _P, _P, _P, _SZ, _P]),
     "fp8lin_launch_count": (ctypes.c_uint64, []),
     "fp8lin_profile_enable": (None, [ctypes.c_int]),
     "fp8lin_profile_collect": (ctypes.c_int, [_P, _P]),

@@ -106,8 +106,10 @@ fp8lin_status check_state(const fp8lin_scaling_state* st, bool need_delayed_buff
     if (st->history_len < 1) return FP8LIN_EINVAL;
     if (st->amax_history == nullptr || st->head == nullptr) return FP8LIN_EINVAL;
   }
-  if (st->amax_algo < FP8LIN_AMAX_ATOMIC || st->amax_algo > FP8LIN_AMAX_AUTO)
+  if (st->amax_algo < FP8LIN_AMAX_ATOMIC || st->amax_algo > FP8LIN_AMAX_PRECOMPUTED)
     return FP8LIN_EUNSUPPORTED;
+  if (st->amax_algo == FP8LIN_AMAX_PRECOMPUTED && st->kind != FP8LIN_DYNAMIC)
+    return FP8LIN_EUNSUPPORTED;  // delayed scaling records the amax in its own cast pass
   return FP8LIN_OK;
 }
 
@@ -156,7 +158,8 @@ fp8lin_status do_cast(const CastArgs& a, const DeviceInfo& dev, cudaStream_t str
 
 // Dynamic scaling of one tensor: amax -> scale -> cast (+T) per st->amax_algo.
 // SINGLE_PASS falls back to ATOMIC when the tensor does not fit on chip and
-// `allow_fallback` is set.
+// `allow_fallback` is set.  PRECOMPUTED takes *st->amax as given (written by
+// the producer of x, e.g. a GEMM epilogue) and runs scale + cast only.
 fp8lin_status cast_dynamic_scaled(const void* x, int64_t rows, int64_t cols, int64_t ld,
                            const fp8lin_scaling_state* st, uint8_t* out, uint8_t* out_t, void* ws,
                            const DeviceInfo& dev, cudaStream_t stream, bool allow_fallback) {
@@ -186,8 +189,10 @@ fp8lin_status cast_dynamic_scaled(const void* x, int64_t rows, int64_t cols, int
     if (!allow_fallback && algo == FP8LIN_AMAX_SINGLE_PASS) return FP8LIN_EUNSUPPORTED;
     algo = FP8LIN_AMAX_ATOMIC;
   }
-  fp8lin_status s = do_amax(x, rows, cols, ld, st->amax, algo, ws, dev, stream);
-  if (s != FP8LIN_OK) return s;
+  if (algo != FP8LIN_AMAX_PRECOMPUTED) {
+    fp8lin_status s = do_amax(x, rows, cols, ld, st->amax, algo, ws, dev, stream);
+    if (s != FP8LIN_OK) return s;
+  }
   if (rows == 0 || cols == 0) {
     ProfScope ps(FP8LIN_PROF_SCALE, stream);
     cudaError_t e = launch_scale(st->amax, st->scale, st->inv_scale, nullptr, nullptr, 1, false,
@@ -253,12 +258,16 @@ fp8lin_status delayed_cast(const void* x, int64_t rows, int64_t cols, int64_t ld
 
 fp8lin_status do_gemm(const uint8_t* a, const uint8_t* b, int64_t M, int64_t N, int64_t K,
                       int64_t lda, int64_t ldb, int32_t fa, int32_t fb, const float* inv_a,
-                      const float* inv_b, void* d, int64_t ldd, void* ws, size_t ws_bytes,
-                      const DeviceInfo& dev, cudaStream_t stream) {
-  if (M == 0 || N == 0) return FP8LIN_OK;
-  if (K == 0) {
-    cudaError_t e = cudaMemset2DAsync(d, static_cast<size_t>(ldd) * 2, 0,
-                                      static_cast<size_t>(N) * 2, static_cast<size_t>(M), stream);
+                      const float* inv_b, void* d, int64_t ldd, float* d_amax, void* ws,
+                      size_t ws_bytes, const DeviceInfo& dev, cudaStream_t stream) {
+  if (M == 0 || N == 0 || K == 0) {
+    // Nothing to multiply: D (if any) is zeros, and so is its amax.
+    cudaError_t e = cudaSuccess;
+    if (M > 0 && N > 0)
+      e = cudaMemset2DAsync(d, static_cast<size_t>(ldd) * 2, 0, static_cast<size_t>(N) * 2,
+                            static_cast<size_t>(M), stream);
+    if (e == cudaSuccess && d_amax != nullptr)
+      e = cudaMemsetAsync(d_amax, 0, sizeof(float), stream);
     return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);
   }
   GemmArgs g;
@@ -275,6 +284,9 @@ fp8lin_status do_gemm(const uint8_t* a, const uint8_t* b, int64_t M, int64_t N, 
   g.inv_b = inv_b;
   g.d = d;
   g.ldd = ldd;
+  g.d_amax = reinterpret_cast<uint32_t*>(d_amax);
+  g.ws_amax_acc = ws_u32(ws, kWsGemmAmaxAccOffset);
+  g.ws_amax_ticket = ws_u32(ws, kWsGemmAmaxTicketOffset);
   g.ws_error = ws_error(ws);
   if (ws_bytes > kWsSplitOffset) {
     g.ws_tickets = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + kWsTicketOffset);
@@ -503,11 +515,19 @@ fp8lin_status fp8lin_cast_dynamic(const void* x, int64_t rows, int64_t cols, int
 fp8lin_status fp8lin_gemm(const uint8_t* a, const uint8_t* b, int64_t M, int64_t N, int64_t K,
                           int64_t lda, int64_t ldb, int32_t fmt_a, int32_t fmt_b,
                           const float* inv_a, const float* inv_b, void* d, int64_t ldd,
-                          void* ws, size_t ws_bytes, cudaStream_t stream) {
+                          float* d_amax, void* ws, size_t ws_bytes, cudaStream_t stream) {
   if (M < 0 || N < 0 || K < 0) return FP8LIN_EINVAL;
   if (!valid_fmt(fmt_a) || !valid_fmt(fmt_b)) return FP8LIN_EUNSUPPORTED;
   if (!ws_ok(ws) || ws_bytes < kWsFixedBytes) return FP8LIN_EINVAL;
-  if (M == 0 || N == 0) return FP8LIN_OK;
+  if (d_amax != nullptr && (reinterpret_cast<uintptr_t>(d_amax) & 3u) != 0) return FP8LIN_EINVAL;
+  if (M == 0 || N == 0) {
+    if (d_amax == nullptr) return FP8LIN_OK;
+    DeviceInfo dev;
+    fp8lin_status s = get_dev(&dev);
+    if (s != FP8LIN_OK) return s;
+    return do_gemm(a, b, M, N, K, lda, ldb, fmt_a, fmt_b, inv_a, inv_b, d, ldd, d_amax, ws,
+                   ws_bytes, dev, stream);
+  }
   if (d == nullptr || !aligned16(d) || ldd < N) return FP8LIN_EINVAL;
   if (inv_a == nullptr || inv_b == nullptr) return FP8LIN_EINVAL;
   if (K > 0) {
@@ -521,8 +541,8 @@ fp8lin_status fp8lin_gemm(const uint8_t* a, const uint8_t* b, int64_t M, int64_t
   DeviceInfo dev;
   fp8lin_status s = get_dev(&dev);
   if (s != FP8LIN_OK) return s;
-  return do_gemm(a, b, M, N, K, lda, ldb, fmt_a, fmt_b, inv_a, inv_b, d, ldd, ws, ws_bytes, dev,
-                 stream);
+  return do_gemm(a, b, M, N, K, lda, ldb, fmt_a, fmt_b, inv_a, inv_b, d, ldd, d_amax, ws, ws_bytes,
+                 dev, stream);
 }
 
 fp8lin_status fp8lin_gemm_describe(int64_t M, int64_t N, int64_t K, char* buf, size_t buf_len) {
@@ -552,8 +572,8 @@ static bool dev_ptrs_ok(std::initializer_list<const void*> ps) {
 
 fp8lin_status fp8lin_forward(const void* x, const void* w, int64_t M, int64_t K, int64_t N,
                              fp8lin_scaling_state* sx, fp8lin_scaling_state* sw, void* y,
-                             uint8_t* x8, uint8_t* x8t, uint8_t* w8, uint8_t* w8t, void* ws,
-                             size_t ws_bytes, cudaStream_t stream) {
+                             float* y_amax, uint8_t* x8, uint8_t* x8t, uint8_t* w8, uint8_t* w8t,
+                             void* ws, size_t ws_bytes, cudaStream_t stream) {
   fp8lin_status s = check_linear_sizes(M, K, N);
   if (s != FP8LIN_OK) return s;
   if ((s = check_state(sx, true)) != FP8LIN_OK) return s;
@@ -563,6 +583,7 @@ fp8lin_status fp8lin_forward(const void* x, const void* w, int64_t M, int64_t K,
   if (M * K > 0 && !dev_ptrs_ok({x, x8, x8t})) return FP8LIN_EINVAL;
   if (N * K > 0 && !dev_ptrs_ok({w, w8, w8t})) return FP8LIN_EINVAL;
   if (M * N > 0 && !dev_ptrs_ok({y})) return FP8LIN_EINVAL;
+  if (y_amax != nullptr && (reinterpret_cast<uintptr_t>(y_amax) & 3u) != 0) return FP8LIN_EINVAL;
   DeviceInfo dev;
   if ((s = get_dev(&dev)) != FP8LIN_OK) return s;
 
@@ -578,14 +599,15 @@ fp8lin_status fp8lin_forward(const void* x, const void* w, int64_t M, int64_t K,
   if (s != FP8LIN_OK) return s;
   // y = x8 . W8^T : A = x8 [M, K], B = W8 [N, K]
   return do_gemm(x8, w8, M, N, K, K, K, FP8LIN_E4M3, FP8LIN_E4M3, sx->inv_scale, sw->inv_scale, y,
-                 N, ws, ws_bytes, dev, stream);
+                 N, y_amax, ws, ws_bytes, dev, stream);
 }
 
 fp8lin_status fp8lin_backward(const void* dy, int64_t M, int64_t K, int64_t N,
                               const uint8_t* x8t, const uint8_t* w8t,
                               const fp8lin_scaling_state* sx, const fp8lin_scaling_state* sw,
                               fp8lin_scaling_state* sdy, uint8_t* dy8, uint8_t* dy8t, void* dx,
-                              void* dw, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                              void* dw, float* dx_amax, float* dw_amax, void* ws, size_t ws_bytes,
+                              cudaStream_t stream) {
   fp8lin_status s = check_linear_sizes(M, K, N);
   if (s != FP8LIN_OK) return s;
   if ((s = check_state(sx, false)) != FP8LIN_OK) return s;
@@ -598,6 +620,9 @@ fp8lin_status fp8lin_backward(const void* dy, int64_t M, int64_t K, int64_t N,
   if (dx != nullptr && N * K > 0 && !dev_ptrs_ok({w8t})) return FP8LIN_EINVAL;
   if (dw != nullptr && N * K > 0 && !dev_ptrs_ok({dw})) return FP8LIN_EINVAL;
   if (dw != nullptr && M * K > 0 && !dev_ptrs_ok({x8t})) return FP8LIN_EINVAL;
+  if ((dx_amax != nullptr && (dx == nullptr || (reinterpret_cast<uintptr_t>(dx_amax) & 3u))) ||
+      (dw_amax != nullptr && (dw == nullptr || (reinterpret_cast<uintptr_t>(dw_amax) & 3u))))
+    return FP8LIN_EINVAL;
   DeviceInfo dev;
   if ((s = get_dev(&dev)) != FP8LIN_OK) return s;
 
@@ -609,13 +634,13 @@ fp8lin_status fp8lin_backward(const void* dy, int64_t M, int64_t K, int64_t N,
   if (dx != nullptr) {
     // dX = dY8 . W8 : A = dY8 [M, N], B = W8^T [K, N], contract over N
     s = do_gemm(dy8, w8t, M, K, N, N, N, FP8LIN_E5M2, FP8LIN_E4M3, sdy->inv_scale, sw->inv_scale,
-                dx, K, ws, ws_bytes, dev, stream);
+                dx, K, dx_amax, ws, ws_bytes, dev, stream);
     if (s != FP8LIN_OK) return s;
   }
   if (dw != nullptr) {
     // dW = dY8^T . x8 : A = dY8^T [N, M], B = x8^T [K, M], contract over M
     s = do_gemm(dy8t, x8t, N, K, M, M, M, FP8LIN_E5M2, FP8LIN_E4M3, sdy->inv_scale, sx->inv_scale,
-                dw, K, ws, ws_bytes, dev, stream);
+                dw, K, dw_amax, ws, ws_bytes, dev, stream);
     if (s != FP8LIN_OK) return s;
   }
   return FP8LIN_OK;

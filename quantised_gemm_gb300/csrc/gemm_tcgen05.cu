@@ -79,6 +79,11 @@ struct GemmParams {
   int s_tail;
   float* partials;      // fp32 partials of split tiles (workspace)
   int* tickets;         // per split tile and 32-row group counters (workspace, zero)
+  // max |D| over the stored bf16 values, as fp32 bits (nullptr: not wanted),
+  // published by the last epilogue warp through two self-cleaning words.
+  uint32_t* amax_out;
+  uint32_t* amax_acc;
+  uint32_t* amax_ticket;
 };
 
 // What one work unit does with its accumulator.
@@ -139,12 +144,15 @@ __device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, uint32_t (&r)[kC
 // warp's shared-memory writes free of bank conflicts.
 __device__ __forceinline__ void store_chunk_tma(const uint32_t (&r)[32], float alpha, uint8_t* box,
                                                 const CUtensorMap* tmD, int row0, int col0,
-                                                int lane) {
+                                                int lane, bool track, float& vmax) {
   uint32_t w[16];
 #pragma unroll
-  for (int j = 0; j < 16; ++j)
-    w[j] = cvt_bf16x2(__fmul_rn(__uint_as_float(r[2 * j]), alpha),
-                      __fmul_rn(__uint_as_float(r[2 * j + 1]), alpha));
+  for (int j = 0; j < 16; ++j) {
+    const float v0 = __fmul_rn(__uint_as_float(r[2 * j]), alpha);
+    const float v1 = __fmul_rn(__uint_as_float(r[2 * j + 1]), alpha);
+    w[j] = cvt_bf16x2(v0, v1);
+    if (track) vmax = fmaxf(vmax, fmaxf(fabsf(v0), fabsf(v1)));
+  }
   if (lane == 0) bulk_wait_group_read<kBoxesPerWarp - 1>();  // this box's last store has read it
   __syncwarp();
   uint8_t* rowp = box + lane * 64;
@@ -162,15 +170,22 @@ __device__ __forceinline__ void store_chunk_tma(const uint32_t (&r)[32], float a
 }
 
 // Final bf16 output of one chunk of raw fp32 accumulators (this lane's row).
+// When D's amax is wanted (p.amax_out, warp-uniform), vmax collects the
+// largest |v| of the fp32 values before their rounding to bf16: rounding to
+// nearest even is monotone and odd, so max |bf16(v)| = bf16(max |v|), and one
+// rounding at the end gives the amax of the stored bf16 D exactly.  Elements
+// outside D come from zero-filled operand rows or columns, hence are zero and
+// cannot raise it.
 template <int kChunk, bool kTransStore>
 __device__ __forceinline__ void emit_chunk(const uint32_t (&r)[kChunk], float alpha,
                                            const GemmParams& p, const CUtensorMap* tmD,
                                            uint8_t* boxes, uint32_t& chunk_no, int row0, int col0,
-                                           int lane) {
+                                           int lane, float& vmax) {
+  const bool track = p.amax_out != nullptr;
   if constexpr (!kTransStore) {
     static_assert(kChunk == 32, "TMA-store epilogue works on 32-column chunks");
     store_chunk_tma(r, alpha, boxes + (chunk_no % kBoxesPerWarp) * kBoxBytes, tmD, row0, col0,
-                    lane);
+                    lane, track, vmax);
     ++chunk_no;
   } else {
     // kernel element (row, col) is output element (col, row)
@@ -179,8 +194,10 @@ __device__ __forceinline__ void emit_chunk(const uint32_t (&r)[kChunk], float al
 #pragma unroll
       for (int j = 0; j < kChunk; ++j) {
         if (col0 + j < p.N) {
-          const uint32_t b = cvt_bf16x2(__fmul_rn(__uint_as_float(r[j]), alpha), 0.0f) & 0xFFFFu;
+          const float v = __fmul_rn(__uint_as_float(r[j]), alpha);
+          const uint32_t b = cvt_bf16x2(v, 0.0f) & 0xFFFFu;
           p.d[static_cast<int64_t>(col0 + j) * p.ldd + row] = static_cast<uint16_t>(b);
+          if (track) vmax = fmaxf(vmax, fabsf(v));
         }
       }
     }
@@ -236,7 +253,8 @@ __device__ __forceinline__ void epilogue_unit(const GemmParams& p, const Unit& u
                                               int group, int row0, int col_base, uint32_t t_row,
                                               float alpha, const CUtensorMap* tmD, uint8_t* boxes,
                                               uint32_t& chunk_no, int lane,
-                                              volatile int* abort_flag, Release release) {
+                                              volatile int* abort_flag, float& vmax,
+                                              Release release) {
   constexpr int kChunk = (kCols % 32 == 0) ? 32 : 16;
   const bool active = row0 < p.M;  // warp-uniform
   int nch = 0;                     // chunks with at least one column inside D
@@ -258,13 +276,13 @@ __device__ __forceinline__ void epilogue_unit(const GemmParams& p, const Unit& u
           }
           tmem_load_wait();
           emit_chunk<kChunk, kTransStore>(ra, alpha, p, tmD, boxes, chunk_no, row0,
-                                          col_base + c * kChunk, lane);
+                                          col_base + c * kChunk, lane, vmax);
           emit_chunk<kChunk, kTransStore>(rb, alpha, p, tmD, boxes, chunk_no, row0,
-                                          col_base + (c + 1) * kChunk, lane);
+                                          col_base + (c + 1) * kChunk, lane, vmax);
         } else {
           tmem_load_chunk<kChunk>(t_row + c * kChunk, ra);
           emit_chunk<kChunk, kTransStore>(ra, alpha, p, tmD, boxes, chunk_no, row0,
-                                          col_base + c * kChunk, lane);
+                                          col_base + c * kChunk, lane, vmax);
         }
       }
     }
@@ -341,7 +359,7 @@ __device__ __forceinline__ void epilogue_unit(const GemmParams& p, const Unit& u
 #pragma unroll
     for (int j = 0; j < kChunk; ++j) r[j] = __float_as_uint(acc[j]);
     emit_chunk<kChunk, kTransStore>(r, alpha, p, tmD, boxes, chunk_no, row0,
-                                    col_base + c * kChunk, lane);
+                                    col_base + c * kChunk, lane, vmax);
   }
   __syncwarp();
   if (lane == 0) {
@@ -350,6 +368,26 @@ __device__ __forceinline__ void epilogue_unit(const GemmParams& p, const Unit& u
     if (atomicAdd(done, 1) == u.nsplit - 1) {
       atomicExch(ticket, 0);
       atomicExch(done, 0);
+    }
+  }
+}
+
+// Every epilogue warp of the grid arrives here once, after its last unit:
+// the warp's maximum, rounded to bf16 as D was, joins the grid's through an
+// atomic max on the workspace accumulator, and the last warp to arrive
+// publishes it to p.amax_out and clears both words for the next call.  A bf16
+// bit pattern shifted up by 16 is the fp32 bit pattern of the same value, and
+// non-negative values order like their bits.
+__device__ __forceinline__ void publish_amax(const GemmParams& p, float vmax, int lane) {
+  if (p.amax_out == nullptr) return;
+  const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, cvt_bf16x2(vmax, 0.0f) & 0xFFFFu);
+  if (lane == 0) {
+    atomicMax(p.amax_acc, m << 16);
+    __threadfence();
+    if (atomicAdd(p.amax_ticket, 1u) == gridDim.x * static_cast<unsigned>(kEpiWarps) - 1u) {
+      __threadfence();
+      *p.amax_out = atomicExch(p.amax_acc, 0u);
+      atomicExch(p.amax_ticket, 0u);
     }
   }
 }
@@ -527,6 +565,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const float alpha = __fmul_rn(*p.inv_a, *p.inv_b);
     uint8_t* boxes = sEpi + (warp - 2) * kBoxesPerWarp * kBoxBytes;
     uint32_t chunk_no = 0;
+    float vmax = 0.0f;
     int acc = 0;
     uint32_t acc_phase = 0;
     Unit u;
@@ -552,7 +591,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         epilogue_unit<E::kCols, kTransStore>(p, u, 4 * E::kHalves, half * 4 + quarter,
                                              m_blk * kBM + quarter * 32,
                                              n_blk * BN + half * E::kCols, t_row, alpha, &tmD,
-                                             boxes, chunk_no, lane, abort_flag, release);
+                                             boxes, chunk_no, lane, abort_flag, vmax, release);
       else
         release();
       if (++acc == 2) {
@@ -560,6 +599,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         acc_phase ^= 1u;
       }
     }
+    publish_amax(p, vmax, lane);
     if (lane == 0) bulk_wait_group<0>();  // stores done before the staging memory goes away
   }
 
@@ -743,6 +783,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t acc_empty_even0 = map_to_cta(smem_addr(&acc_empty[0]), 0);
     uint8_t* boxes = sEpi + (warp - 2) * kBoxesPerWarp * kBoxBytes;
     uint32_t chunk_no = 0;
+    float vmax = 0.0f;
     int acc = 0;
     uint32_t acc_phase = 0;
     Unit u;
@@ -761,7 +802,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t release_addr = acc_empty_even0 + static_cast<uint32_t>(acc * 8);
       epilogue_unit<E::kCols, false>(p, u, 8 * E::kHalves, half * 8 + row_group,
                                      m_blk * 2 * kBM + row_group * 32, n_blk * BN + half * E::kCols,
-                                     t_row, alpha, &tmD, boxes, chunk_no, lane, abort_flag, [&] {
+                                     t_row, alpha, &tmD, boxes, chunk_no, lane, abort_flag, vmax,
+                                     [&] {
                                        tc_fence_before_sync();
                                        __syncwarp();
                                        if (lane == 0) mbar_arrive_cluster(release_addr);
@@ -771,6 +813,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         acc_phase ^= 1u;
       }
     }
+    publish_amax(p, vmax, lane);
     if (lane == 0) bulk_wait_group<0>();  // stores done before the staging memory goes away
   }
 
@@ -1031,6 +1074,9 @@ cudaError_t launch_gemm(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t s
   p.ldd = g.ldd;
   p.err = g.ws_error;
   p.K = static_cast<int>(g.K);
+  p.amax_out = g.d_amax;
+  p.amax_acc = g.ws_amax_acc;
+  p.amax_ticket = g.ws_amax_ticket;
   const Variant v = choose_variant(g.M, g.N);
   if (is_swap(v)) {
     p.M = static_cast<int>(g.N);

@@ -16,6 +16,8 @@ constexpr size_t kWsExitsOffset = 68;     // uint32: CTAs past the barrier (sing
 constexpr size_t kWsAmaxOffset = 128;     // uint32: amax bits (single pass)
 constexpr size_t kWsAtomicAccOffset = 192;     // uint32: ticketed amax accumulator
 constexpr size_t kWsAtomicTicketOffset = 196;  // uint32: ticketed amax arrivals
+constexpr size_t kWsGemmAmaxAccOffset = 200;     // uint32: GEMM output amax accumulator
+constexpr size_t kWsGemmAmaxTicketOffset = 204;  // uint32: GEMM epilogue warps arrived
 constexpr size_t kWsScratchBegin = 64;    // [64, 256): self-cleaning counters
 constexpr size_t kWsPartialOffset = 256;  // uint32[kMaxPartials]: REDUCTION partial maxima
 constexpr int kMaxPartials = 4096;
@@ -178,6 +180,9 @@ struct GemmArgs {
   const float* inv_b;
   void* d;            // bf16 [M, N], row stride ldd elements
   int64_t ldd;
+  uint32_t* d_amax;   // fp32 bits of max |d| over the stored bf16 values (nullptr: not wanted)
+  uint32_t* ws_amax_acc;     // self-cleaning words of the ticketed d_amax
+  uint32_t* ws_amax_ticket;
   int* ws_error;
   int* ws_tickets;     // kWsTickets zero-initialised counters (nullptr: no K split)
   float* ws_split;     // fp32 partials of K-split tail tiles (nullptr: no K split)

@@ -13,8 +13,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (AMAX_AUTO, DELAYED, DYNAMIC, E4M3, E5M2, ScalingState, Workspace, backward,
-               forward, scale)
+from . import (AMAX_AUTO, AMAX_PRECOMPUTED, DELAYED, DYNAMIC, E4M3, E5M2, ScalingState,
+               Workspace, backward, forward, scale)
 
 
 class Fp8Linear:
@@ -38,15 +38,18 @@ class Fp8Linear:
         self.ws = Workspace(M, K, N, device=device)
         mk = lambda fmt: ScalingState(fmt, kind, history_len, amax_algo, eps, device)  # noqa: E731
         self.sx, self.sw, self.sdy = mk(E4M3), mk(E4M3), mk(E5M2)
+        # Where the GEMM epilogues deliver max |y| and max |dX| (set by link_linears()).
+        self.y_amax_to = None
+        self.dx_amax_to = None
 
     def forward(self, x: torch.Tensor, w: torch.Tensor, stream=None) -> torch.Tensor:
         return forward(x, w, self.sx, self.sw, self.y, self.x8, self.x8t, self.w8, self.w8t,
-                       self.ws, stream)
+                       self.ws, stream, y_amax=self.y_amax_to)
 
     def backward(self, dy: torch.Tensor, need_dx: bool = True, need_dw: bool = True, stream=None):
         return backward(dy, self.x8t, self.w8t, self.sx, self.sw, self.sdy, self.dy8, self.dy8t,
                         self.dx if need_dx else None, self.dw if need_dw else None, self.ws,
-                        stream)
+                        stream, dx_amax=self.dx_amax_to if need_dx else None)
 
     def sync_scales(self, stream=None):
         """Delayed scaling: push this step's amaxes into the histories and
@@ -130,3 +133,21 @@ class _NullCtx:
 
     def __exit__(self, *a):
         return False
+
+
+def link_linears(prev: Fp8Linear, nxt: Fp8Linear):
+    """Chain two Linears, nxt consuming prev's output: nxt's input is
+    ``prev.y`` and prev's grad_output is ``nxt.dx``.  prev's forward GEMM then
+    writes max |y| straight into nxt's input amax, and nxt's dX GEMM writes
+    max |dX| into prev's grad_output amax, both from their epilogues; the two
+    states switch to AMAX_PRECOMPUTED, so each of those casts reads its tensor
+    once instead of twice.  Both states must use dynamic scaling, and the
+    caller must feed exactly prev.y / nxt.dx to the linked layer."""
+    if prev.N != nxt.K or prev.M != nxt.M:
+        raise ValueError("prev [M, N] output must be nxt's [M, K] input")
+    if nxt.sx.kind != DYNAMIC or prev.sdy.kind != DYNAMIC:
+        raise ValueError("a producer-computed amax needs dynamic scaling")
+    nxt.sx.amax_algo = AMAX_PRECOMPUTED
+    prev.sdy.amax_algo = AMAX_PRECOMPUTED
+    prev.y_amax_to = nxt.sx.amax
+    nxt.dx_amax_to = prev.sdy.amax

@@ -66,15 +66,17 @@ def test_argument_errors_before_any_cuda_call(lib):
     assert lib.fp8lin_cast(fake, 16, 16, 16, 0, fake, None, None, None, None) == L.EINVAL
     assert lib.fp8lin_cast(fake, 8, 16, 16, 0, fake, fake, fake, None, None) == L.EUNSUPPORTED
     # gemm: no workspace, K not multiple of 16, misaligned output
-    assert lib.fp8lin_gemm(fake, fake, 16, 16, 16, 16, 16, 0, 0, fake, fake, fake, 16,
+    assert lib.fp8lin_gemm(fake, fake, 16, 16, 16, 16, 16, 0, 0, fake, fake, fake, 16, None,
                            None, 0, None) == L.EINVAL
     ws = ctypes.c_void_p(0x20000)
     nb = lib.fp8lin_workspace_bytes(16, 16, 16)
-    assert lib.fp8lin_gemm(fake, fake, 16, 16, 24, 32, 32, 0, 0, fake, fake, fake, 16,
+    assert lib.fp8lin_gemm(fake, fake, 16, 16, 24, 32, 32, 0, 0, fake, fake, fake, 16, None,
                            ws, nb, None) == L.EUNSUPPORTED
-    assert lib.fp8lin_gemm(fake, fake, 16, 16, 16, 16, 16, 0, 0, fake, fake, odd, 16,
+    assert lib.fp8lin_gemm(fake, fake, 16, 16, 16, 16, 16, 0, 0, fake, fake, odd, 16, None,
                            ws, nb, None) == L.EINVAL
-    assert lib.fp8lin_gemm(fake, fake, 16, 16, 16, 16, 16, 0, 3, fake, fake, fake, 16,
+    assert lib.fp8lin_gemm(fake, fake, 16, 16, 16, 16, 16, 0, 0, fake, fake, fake, 16,
+                           ctypes.c_void_p(0x10002), ws, nb, None) == L.EINVAL  # misaligned amax
+    assert lib.fp8lin_gemm(fake, fake, 16, 16, 16, 16, 16, 0, 3, fake, fake, fake, 16, None,
                            ws, nb, None) == L.EUNSUPPORTED
 
 
@@ -94,18 +96,25 @@ def test_forward_backward_argument_errors(lib):
     ws = ctypes.c_void_p(0x20000)
     nb = lib.fp8lin_workspace_bytes(128, 128, 128)
     sx, sw, sd = _state(0), _state(0), _state(1)
-    fwd = lambda M, K, N, a, b: lib.fp8lin_forward(p, p, M, K, N, ctypes.byref(a), ctypes.byref(b),
-                                                   p, p, p, p, p, ws, nb, None)
+    fwd = lambda M, K, N, a, b, ya=None: lib.fp8lin_forward(
+        p, p, M, K, N, ctypes.byref(a), ctypes.byref(b), p, ya, p, p, p, p, ws, nb, None)
     assert fwd(100, 128, 128, sx, sw) == L.EUNSUPPORTED            # M % 16
     assert fwd(-16, 128, 128, sx, sw) == L.EINVAL
     assert fwd(128, 128, 128, _state(1), sw) == L.EUNSUPPORTED     # x must be e4m3
     assert fwd(128, 128, 128, _state(0, eps=0.0), sw) == L.EINVAL  # eps must be > 0
     assert fwd(128, 128, 128, _state(0, kind=1, H=0), sw) == L.EINVAL   # delayed H >= 1
     assert fwd(128, 128, 128, _state(0, algo=9), sw) == L.EUNSUPPORTED
-    assert lib.fp8lin_forward(p, p, 128, 128, 128, ctypes.byref(sx), ctypes.byref(sw), p, p, p,
-                              p, p, None, nb, None) == L.EINVAL    # no workspace
-    bwd = lambda d: lib.fp8lin_backward(p, 128, 128, 128, p, p, ctypes.byref(sx), ctypes.byref(sw),
-                                        ctypes.byref(d), p, p, p, p, ws, nb, None)
+    # a precomputed amax is a dynamic-scaling mode only
+    assert fwd(128, 128, 128, _state(0, kind=1, H=4, algo=L.AMAX_PRECOMPUTED), sw) == \
+        L.EUNSUPPORTED
+    assert fwd(128, 128, 128, sx, sw, ctypes.c_void_p(0x10001)) == L.EINVAL   # misaligned y_amax
+    assert lib.fp8lin_forward(p, p, 128, 128, 128, ctypes.byref(sx), ctypes.byref(sw), p, None, p,
+                              p, p, p, None, nb, None) == L.EINVAL    # no workspace
+    bwd = lambda d, dxa=None, dwa=None, dx=p, dw=p: lib.fp8lin_backward(
+        p, 128, 128, 128, p, p, ctypes.byref(sx), ctypes.byref(sw), ctypes.byref(d), p, p, dx, dw,
+        dxa, dwa, ws, nb, None)
     assert bwd(_state(0)) == L.EUNSUPPORTED                        # grad_output must be e5m2
+    assert bwd(sd, dxa=p, dx=None) == L.EINVAL                     # dX amax without dX
+    assert bwd(sd, dwa=p, dw=None) == L.EINVAL                     # dW amax without dW
     assert lib.fp8lin_scale(None, None) == L.EINVAL
     assert lib.fp8lin_scale(ctypes.byref(_state(0, kind=1, H=0)), None) == L.EINVAL

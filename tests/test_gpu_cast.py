@@ -184,3 +184,26 @@ def test_workspace_counters_clean_themselves(algo, ws):
     for host in (big, small):                                  # ticketed fp8lin_amax
         q.amax(to_dev_bf16(host), out, q.AMAX_ATOMIC, ws)
         assert dev_f32_bits(out) == f32_bits(oracle.amax(host))
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+@pytest.mark.parametrize("shape", [(144, 272), (1040, 1552), (4096, 4096)])
+def test_cast_dynamic_precomputed_amax(fmt, shape, ws):
+    """AMAX_PRECOMPUTED takes the amax already in the state (as a producing
+    GEMM's epilogue leaves it) and runs scale + cast only: same scale, same
+    bytes as the oracle; the amax is left as given."""
+    x = _tensor(shape, seed=41)
+    a = oracle.amax(x)
+    s, inv = oracle.scale_dynamic(a, fmt)
+    qr, qtr, _ = oracle.cast(x, s, fmt, transpose=True)
+    st = q.ScalingState(fmt, q.DYNAMIC, amax_algo=q.AMAX_PRECOMPUTED)
+    st.amax.fill_(a)                              # a bf16 magnitude: exact in fp32
+    out = torch.empty(shape, dtype=torch.uint8, device="cuda")
+    out_t = torch.empty(shape[::-1], dtype=torch.uint8, device="cuda")
+    q.cast_dynamic(to_dev_bf16(x), st, out, out_t, ws)
+    q.check(ws)
+    assert dev_f32_bits(st.amax) == f32_bits(a)
+    assert dev_f32_bits(st.scale) == f32_bits(s)
+    assert dev_f32_bits(st.inv_scale) == f32_bits(inv)
+    assert np.array_equal(out.cpu().numpy(), qr)
+    assert np.array_equal(out_t.cpu().numpy(), qtr)

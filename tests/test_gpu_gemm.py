@@ -10,7 +10,7 @@ import torch
 import oracle
 import quantised_gemm_gb300 as q
 import synth_inputs as si
-from helpers import assert_within_bound, bf16_to_f64
+from helpers import assert_within_bound, bf16_to_f64, dev_f32_bits, f32_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -133,11 +133,11 @@ def test_gemm_without_split_workspace_matches(ws):
     lib = q.library()
     a, b = torch.from_numpy(a8).cuda(), torch.from_numpy(b8).cuda()
     ia, ib = torch.tensor([inva], device="cuda"), torch.tensor([invb], device="cuda")
-    st = lib.fp8lin_gemm(a.data_ptr(), None, 0, 0, 0, 0, 0, 0, 0, None, None, None, 0,
+    st = lib.fp8lin_gemm(a.data_ptr(), None, 0, 0, 0, 0, 0, 0, 0, None, None, None, 0, None,
                          small.data_ptr(), small.numel(), None)
     assert st == 0          # M = N = 0: nothing to do
     st = lib.fp8lin_gemm(a.data_ptr(), b.data_ptr(), M, N, K, K, K, 0, 0, ia.data_ptr(),
-                         ib.data_ptr(), d.data_ptr(), N, small.data_ptr(), small.numel(),
+                         ib.data_ptr(), d.data_ptr(), N, None, small.data_ptr(), small.numel(),
                          torch.cuda.current_stream().cuda_stream)
     assert st == 0
     torch.cuda.synchronize()
@@ -180,3 +180,52 @@ def test_gemm_describe_names_the_launched_kernel(mnk, kernel, sched, ws):
     # the profiler spells a bool template argument as true / false, ncu as 1 / 0
     names = [n.replace(", true>", ", 1>").replace(", false>", ", 0>") for n in names]
     assert all(kernel in n for n in names), names
+
+
+def _bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("mnk", [
+    (16, 4096, 4096),      # swapped operands, K split 4 ways, transposed stores
+    (48, 208, 160),        # swapped operands, ragged
+    (128, 4096, 4096),     # one-CTA tiles, K split 8 ways
+    (128, 1600, 512),      # one-CTA 128-wide tiles, ragged N edge
+    (200, 272, 336),       # CTA pairs, ragged M, N, K
+    (384, 1600, 1600),     # CTA pairs, 128-wide tiles
+    (2048, 2560, 256),     # CTA pairs, more than one wave
+])
+def test_gemm_output_amax(mnk, ws):
+    """max |D| from the epilogue equals the amax of the bf16 D it stored (the
+    oracle's amax of those bits) for every kernel and schedule; a large
+    maximum followed by a smaller one checks that the workspace words it goes
+    through start clean for each call."""
+    M, N, K = mnk
+    amax_out = torch.full((1,), -1.0, device="cuda")
+    for seed, std in ((21, 4.0), (22, 0.25)):
+        a8, _, inva = _operand(M, K, E4M3, seed=seed, std=std)
+        b8, _, invb = _operand(N, K, E4M3, seed=seed + 100)
+        d = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        q.gemm(torch.from_numpy(a8).cuda(), torch.from_numpy(b8).cuda(), E4M3, E4M3,
+               torch.tensor([inva], device="cuda"), torch.tensor([invb], device="cuda"), d,
+               ws, amax_out=amax_out)
+        q.check(ws)
+        assert dev_f32_bits(amax_out) == f32_bits(oracle.amax(_bf16_bits(d))), (mnk, seed)
+
+
+def test_gemm_output_amax_of_empty_products(ws):
+    """K = 0 (all-zero D) and M = 0 (no D) both report an amax of 0."""
+    one = torch.ones(1, device="cuda")
+    amax_out = torch.full((1,), 5.0, device="cuda")
+    d = torch.full((32, 64), 1.0, dtype=torch.bfloat16, device="cuda")
+    q.gemm(torch.empty((32, 0), dtype=torch.uint8, device="cuda"),
+           torch.empty((64, 0), dtype=torch.uint8, device="cuda"), E4M3, E4M3, one, one, d, ws,
+           amax_out=amax_out)
+    torch.cuda.synchronize()
+    assert amax_out.item() == 0.0 and torch.count_nonzero(d.float()).item() == 0
+    amax_out.fill_(5.0)
+    q.gemm(torch.empty((0, 16), dtype=torch.uint8, device="cuda"),
+           torch.zeros((64, 16), dtype=torch.uint8, device="cuda"), E4M3, E4M3, one, one,
+           torch.empty((0, 64), dtype=torch.bfloat16, device="cuda"), ws, amax_out=amax_out)
+    torch.cuda.synchronize()
+    assert amax_out.item() == 0.0

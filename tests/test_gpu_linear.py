@@ -228,3 +228,58 @@ def test_step_host_matches_device_path(lanes):
         assert torch.equal(hy.view(torch.int16), dev_lin.y.cpu().view(torch.int16)), step
         assert torch.equal(hdx.view(torch.int16), dev_lin.dx.cpu().view(torch.int16)), step
         assert torch.equal(hdw.view(torch.int16), dev_lin.dw.cpu().view(torch.int16)), step
+
+
+def _bits(t: torch.Tensor) -> np.ndarray:
+    return t.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def test_forward_backward_output_amaxes():
+    """y_amax, dx_amax and dw_amax from the GEMM epilogues equal the oracle's
+    amax of the y, dX and dW the GPU stored."""
+    M, K, N = 560, 768, 1024
+    lin = q.Fp8Linear(M, K, N)
+    ya, dxa, dwa = (torch.full((1,), -1.0, device="cuda") for _ in range(3))
+    x, w, dy = si.linear_inputs(M, K, N, w_init="uniform64", seed=5)
+    q.forward(to_dev_bf16(x), to_dev_bf16(w), lin.sx, lin.sw, lin.y, lin.x8, lin.x8t, lin.w8,
+              lin.w8t, lin.ws, y_amax=ya)
+    q.backward(to_dev_bf16(dy), lin.x8t, lin.w8t, lin.sx, lin.sw, lin.sdy, lin.dy8, lin.dy8t,
+               lin.dx, lin.dw, lin.ws, dx_amax=dxa, dw_amax=dwa)
+    q.check(lin.ws)
+    for t, a, what in ((lin.y, ya, "y"), (lin.dx, dxa, "dX"), (lin.dw, dwa, "dW")):
+        assert dev_f32_bits(a) == f32_bits(oracle.amax(_bits(t))), what
+
+
+@pytest.mark.parametrize("M", [16, 560])
+def test_linked_linears_match_unlinked(M):
+    """Two Linears chained with link_linears (amax of y and dX from the GEMM
+    epilogues, casts of y and dX in one pass) give the same bits as the same
+    chain with separate amax passes, over two steps; the linked states hold
+    the oracle's amax of the tensors they cast."""
+    K, N1, N2 = 768, 1024, 512
+    x, w1, _ = si.linear_inputs(M, K, N1, w_init="uniform64", seed=8)
+    _, w2, dy2 = si.linear_inputs(M, N1, N2, w_init="uniform64", seed=9)
+    xd, w1d, w2d, dy2d = (to_dev_bf16(a) for a in (x, w1, w2, dy2))
+
+    def run(linked):
+        l1, l2 = q.Fp8Linear(M, K, N1), q.Fp8Linear(M, N1, N2)
+        if linked:
+            q.link_linears(l1, l2)
+        for _ in range(2):
+            l1.forward(xd, w1d)
+            l2.forward(l1.y, w2d)
+            l2.backward(dy2d)
+            l1.backward(l2.dx)
+        q.check(l1.ws)
+        q.check(l2.ws)
+        outs = [_bits(t) for t in (l1.y, l2.y, l2.dx, l1.dx, l1.dw, l2.dw)]
+        scalars = [dev_f32_bits(t) for t in (l2.sx.amax, l2.sx.scale, l1.sdy.amax, l1.sdy.scale)]
+        if linked:
+            assert scalars[0] == f32_bits(oracle.amax(outs[0]))     # amax of y1
+            assert scalars[2] == f32_bits(oracle.amax(outs[2]))     # amax of dX2
+        return outs, scalars
+
+    (o1, s1), (o2, s2) = run(True), run(False)
+    for i, (u, v) in enumerate(zip(o1, o2)):
+        assert np.array_equal(u, v), i
+    assert s1 == s2
