@@ -399,11 +399,63 @@ def end_to_end(q, lin, x, w, dy, M, K, N, world, flop_step, steps):
         lin.step_host(hx, hw, hdy, hy, hdx, hdw)
     torch.cuda.synchronize()
     ms = time_region(lambda: lin.step_host(hx, hw, hdy, hy, hdx, hdw), n) / n
+    h2d = 2 * (M * K + N * K + M * N)
+    d2h = 2 * (M * N + M * K + N * K)
+    link = host_link_rates(torch, hx, lin.y.device)
+    floor_ms = max(h2d / (link["h2d_gbs"] * 1e9), d2h / (link["d2h_gbs"] * 1e9),
+                   (h2d + d2h) / (link["both_gbs"] * 1e9)) * 1e3
     return {"value": round(world * flop_step / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-            "h2d_bytes_per_step": 2 * (M * K + N * K + M * N),
-            "d2h_bytes_per_step": 2 * (M * N + M * K + N * K), "ms_per_step": round(ms, 3),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3),
             "steps": n, "copy_lanes": lin.copy_lanes,
-            "api": "Fp8Linear.step_host (pinned host buffers)"}
+            "api": "Fp8Linear.step_host (pinned host buffers)",
+            "host_link": link, "copy_floor_ms": round(floor_ms, 3),
+            "frac_of_copy_floor": round(floor_ms / ms, 3)}
+
+
+def host_link_rates(torch, host, dev):
+    """Copy rate of the host link with pinned buffers (GB/s): host -> device,
+    device -> host, and both at once on two streams (the rate the step's
+    copies can reach at best)."""
+    nbytes = host.numel() * host.element_size()
+    d = torch.empty_like(host, device=dev)
+    back = torch.empty_like(host).pin_memory()
+    s1, s2 = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def timed(fn, reps=3):
+        fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s1)
+        for _ in range(reps):
+            fn()
+        s1.wait_stream(s2)
+        b.record(s1)
+        b.synchronize()
+        return a.elapsed_time(b) / reps
+
+    def up():
+        with torch.cuda.stream(s1):
+            d.copy_(host, non_blocking=True)
+
+    def down():
+        with torch.cuda.stream(s1):
+            back.copy_(d, non_blocking=True)
+
+    def both():
+        s2.wait_stream(s1)
+        with torch.cuda.stream(s1):
+            d.copy_(host, non_blocking=True)
+        with torch.cuda.stream(s2):
+            back.copy_(d2, non_blocking=True)
+
+    d2 = torch.empty_like(d)
+    t_up, t_down, t_both = timed(up), timed(down), timed(both)
+    torch.cuda.synchronize()
+    del d, d2, back
+    return {"h2d_gbs": round(nbytes / (t_up * 1e-3) / 1e9, 1),
+            "d2h_gbs": round(nbytes / (t_down * 1e-3) / 1e9, 1),
+            "both_gbs": round(2 * nbytes / (t_both * 1e-3) / 1e9, 1),
+            "bytes": nbytes}
 
 
 def run_native(args):
