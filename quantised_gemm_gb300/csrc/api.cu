@@ -165,7 +165,8 @@ fp8lin_status cast_dynamic_scaled(const void* x, int64_t rows, int64_t cols, int
                            const DeviceInfo& dev, cudaStream_t stream, bool allow_fallback) {
   int32_t algo = st->amax_algo;
   if ((algo == FP8LIN_AMAX_SINGLE_PASS || algo == FP8LIN_AMAX_AUTO) && rows > 0 && cols > 0) {
-    if (single_pass_fits(dev, rows, cols)) {
+    const bool cluster = cluster_cast_fits(rows, cols);
+    if (cluster || single_pass_fits(dev, rows, cols)) {
       SinglePassArgs sp;
       sp.x = static_cast<const uint16_t*>(x);
       sp.rows = rows;
@@ -183,7 +184,8 @@ fp8lin_status cast_dynamic_scaled(const void* x, int64_t rows, int64_t cols, int
       sp.ws_amax = ws_u32(ws, kWsAmaxOffset);
       sp.ws_error = ws_error(ws);
       ProfScope ps(FP8LIN_PROF_CAST_FUSED, stream);
-      cudaError_t e = launch_cast_single_pass(sp, dev, stream);
+      cudaError_t e =
+          cluster ? launch_cast_cluster(sp, stream) : launch_cast_single_pass(sp, dev, stream);
       return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);
     }
     if (!allow_fallback && algo == FP8LIN_AMAX_SINGLE_PASS) return FP8LIN_EUNSUPPORTED;

@@ -450,6 +450,150 @@ __global__ void __launch_bounds__(kSpThreads, 1)
   }
 }
 
+// ------------------------------------------------------------------ cluster single pass
+//
+// Dynamic amax -> scale -> cast (+ transpose) of a small tensor in ONE
+// thread-block cluster of at most kClusterCtas CTAs.  Each CTA loads its
+// tiles into registers and takes their maximum; the CTAs exchange their
+// maxima through distributed shared memory between two cluster barriers; each
+// then casts from registers.  No grid barrier, no global atomics and no
+// workspace words, so the latency of a few-token tensor is one load, one
+// cluster exchange and one store.  Tiles are kTR rows x (16384 / kTR) columns,
+// kTR the smallest of 16, 32, 64, 128 covering the rows, so that a short,
+// wide tensor (a few tokens x 4096) is not padded to 128-row tiles.
+constexpr int kClusterCtas = 8;
+constexpr int kClusterTilesPerCta = 2;
+constexpr int kClusterTileElems = kThreads * 8 * 8;  // 8 vectors of 8 values per thread
+
+struct ClusterCastParams {
+  const uint16_t* x;
+  int64_t rows, cols, ld;
+  float eps;
+  float* amax_out;
+  float* scale_out;
+  float* inv_out;
+  uint8_t* out;
+  uint8_t* out_t;
+};
+
+// Transposed write of one kTR x kTC fp8 tile held in shared memory (rows of
+// kTC / 4 + 1 words): each thread moves one 16-row x 4-column block with the
+// same 4x4 byte transposes as store_transposed_tile.  A warp reads 32
+// consecutive words of a row: conflict-free.
+template <int kTR, int kTC>
+__device__ __forceinline__ void store_transposed_block(const uint32_t* sq, uint8_t* out_t,
+                                                       int64_t rows, int64_t cols, int64_t r0,
+                                                       int64_t c0, int tid) {
+  constexpr int kPitch = kTC / 4 + 1;
+  const int jg = tid % (kTC / 4), ig = tid / (kTC / 4);
+  const int i0 = ig * 16, j0 = jg * 4;
+  if (c0 + j0 >= cols || r0 + i0 >= rows) return;
+  uint32_t w[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) w[k] = sq[(i0 + k) * kPitch + jg];
+  uint32_t o[4][4];
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const uint32_t t0 = __byte_perm(w[4 * g + 0], w[4 * g + 1], 0x5140);
+    const uint32_t t1 = __byte_perm(w[4 * g + 2], w[4 * g + 3], 0x5140);
+    const uint32_t t2 = __byte_perm(w[4 * g + 0], w[4 * g + 1], 0x7362);
+    const uint32_t t3 = __byte_perm(w[4 * g + 2], w[4 * g + 3], 0x7362);
+    o[0][g] = __byte_perm(t0, t1, 0x5410);
+    o[1][g] = __byte_perm(t0, t1, 0x7632);
+    o[2][g] = __byte_perm(t2, t3, 0x5410);
+    o[3][g] = __byte_perm(t2, t3, 0x7632);
+  }
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+    uint8_t* dst = out_t + (c0 + j0 + jj) * rows + r0 + i0;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(o[jj][0], o[jj][1], o[jj][2], o[jj][3]);
+  }
+}
+
+template <int kFmt, bool kTrans, int kTR>
+__global__ void __launch_bounds__(kThreads, 1) cast_cluster_kernel(const ClusterCastParams p) {
+  constexpr int kTC = kClusterTileElems / kTR;
+  constexpr int kVR = kTC / 8;  // 8-value vectors per tile row
+  constexpr int kPitch = kTC / 4 + 1;
+  static_assert(kTR % 16 == 0 && kTC % 128 == 0, "tile shape");
+  __shared__ __align__(16) uint32_t sq[kTrans ? kTR * kPitch : 1];
+  __shared__ uint32_t s_max;  // this CTA's maximum, read by every CTA of the cluster
+  __shared__ uint32_t s_all;
+  const uint32_t rank = cluster_ctarank();
+  const int nctas = static_cast<int>(gridDim.x);  // the grid is one cluster
+  const int64_t ntc = (p.cols + kTC - 1) / kTC;
+  const int64_t ntiles = ((p.rows + kTR - 1) / kTR) * ntc;
+  griddep_wait();
+  uint4 v[kClusterTilesPerCta][8];
+  uint32_t acc = 0;
+#pragma unroll
+  for (int k = 0; k < kClusterTilesPerCta; ++k) {
+    const int64_t t = rank + static_cast<int64_t>(k) * nctas;
+    const int64_t r0 = (t / ntc) * kTR, c0 = (t % ntc) * kTC;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int vi = threadIdx.x + kThreads * u;
+      const int64_t row = r0 + vi / kVR, col = c0 + (vi % kVR) * 8;
+      v[k][u] = (t < ntiles && row < p.rows && col < p.cols)
+                    ? ld_stream_v4(p.x + row * p.ld + col)
+                    : make_uint4(0, 0, 0, 0);
+      acc = vec_absmax(acc, v[k][u]);
+    }
+  }
+  const uint32_t bits = block_absmax_bits(acc);
+  if (threadIdx.x == 0) s_max = bits;
+  // A lone CTA (launched without a cluster) keeps to CTA-scope barriers.
+  if (nctas > 1)
+    cluster_sync_all();  // every CTA's s_max is written
+  else
+    __syncthreads();
+  if (threadIdx.x < 32) {
+    uint32_t m = 0;
+    if (static_cast<int>(threadIdx.x) < nctas)
+      m = nctas > 1 ? ld_shared_cluster_u32(map_to_cta(smem_addr(&s_max), threadIdx.x)) : s_max;
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if (threadIdx.x == 0) s_all = m;
+  }
+  if (nctas > 1)
+    cluster_sync_all();  // no CTA leaves or moves on while a peer may read its s_max
+  else
+    __syncthreads();
+  griddep_launch_dependents();
+
+  const float amax = __uint_as_float(s_all);
+  const float s = scale_from_amax(amax, p.eps, fp8_max<kFmt>());
+  if (rank == 0 && threadIdx.x == 0) {
+    *p.amax_out = amax;
+    *p.scale_out = s;
+    *p.inv_out = __fdiv_rn(1.0f, s);
+  }
+#pragma unroll
+  for (int k = 0; k < kClusterTilesPerCta; ++k) {
+    const int64_t t = rank + static_cast<int64_t>(k) * nctas;
+    if (t < ntiles) {  // uniform in the CTA
+      const int64_t r0 = (t / ntc) * kTR, c0 = (t % ntc) * kTC;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int vi = threadIdx.x + kThreads * u;
+        const int rl = vi / kVR, cv = vi % kVR;
+        const int64_t row = r0 + rl, col = c0 + cv * 8;
+        const uint2 q = cast8<kFmt>(v[k][u], s);
+        if (p.out != nullptr && row < p.rows && col < p.cols)
+          *reinterpret_cast<uint2*>(p.out + row * p.cols + col) = q;
+        if (kTrans) {
+          sq[rl * kPitch + cv * 2] = q.x;
+          sq[rl * kPitch + cv * 2 + 1] = q.y;
+        }
+      }
+      if (kTrans) {
+        __syncthreads();
+        store_transposed_block<kTR, kTC>(sq, p.out_t, p.rows, p.cols, r0, c0, threadIdx.x);
+        __syncthreads();
+      }
+    }
+  }
+}
+
 template <typename Kernel>
 int resident_ctas(Kernel k, int threads, size_t smem) {
   int n = 0;
@@ -616,6 +760,59 @@ int64_t single_pass_capacity_elems(const DeviceInfo& dev) {
 bool single_pass_fits(const DeviceInfo& dev, int64_t rows, int64_t cols) {
   const int64_t ntiles = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
   return ntiles * kTile * kTile <= single_pass_capacity_elems(dev);
+}
+
+namespace {
+int cluster_tile_rows(int64_t rows) {
+  return rows <= 16 ? 16 : rows <= 32 ? 32 : rows <= 64 ? 64 : 128;
+}
+
+int64_t cluster_tiles(int64_t rows, int64_t cols) {
+  const int tr = cluster_tile_rows(rows);
+  const int64_t tc = kClusterTileElems / tr;
+  return ((rows + tr - 1) / tr) * ((cols + tc - 1) / tc);
+}
+
+template <int kFmt, bool kTrans>
+void (*cluster_kernel_for(int tr))(const ClusterCastParams) {
+  switch (tr) {
+    case 16: return cast_cluster_kernel<kFmt, kTrans, 16>;
+    case 32: return cast_cluster_kernel<kFmt, kTrans, 32>;
+    case 64: return cast_cluster_kernel<kFmt, kTrans, 64>;
+    default: return cast_cluster_kernel<kFmt, kTrans, 128>;
+  }
+}
+}  // namespace
+
+bool cluster_cast_fits(int64_t rows, int64_t cols) {
+  return rows > 0 && cols > 0 && cluster_tiles(rows, cols) <= kClusterCtas * kClusterTilesPerCta;
+}
+
+cudaError_t launch_cast_cluster(const SinglePassArgs& a, cudaStream_t stream) {
+  if (!cluster_cast_fits(a.rows, a.cols)) return cudaErrorInvalidValue;
+  ClusterCastParams p;
+  p.x = a.x;
+  p.rows = a.rows;
+  p.cols = a.cols;
+  p.ld = a.ld;
+  p.eps = a.eps;
+  p.amax_out = a.amax_out;
+  p.scale_out = a.scale_out;
+  p.inv_out = a.inv_out;
+  p.out = a.out;
+  p.out_t = a.out_t;
+  const int tr = cluster_tile_rows(a.rows);
+  const int64_t ntiles = cluster_tiles(a.rows, a.cols);
+  const int ctas = static_cast<int>(ntiles < kClusterCtas ? ntiles : kClusterCtas);
+  const bool trans = a.out_t != nullptr;
+  void (*fn)(const ClusterCastParams);
+  if (a.fmt == 0)
+    fn = trans ? cluster_kernel_for<0, true>(tr) : cluster_kernel_for<0, false>(tr);
+  else
+    fn = trans ? cluster_kernel_for<1, true>(tr) : cluster_kernel_for<1, false>(tr);
+  set_error_site("cluster single-pass launch");
+  return launch_kernel(fn, dim3(static_cast<unsigned>(ctas)), dim3(kThreads), 0, stream, ctas,
+                       false, p);
 }
 
 cudaError_t launch_cast_single_pass(const SinglePassArgs& a, const DeviceInfo& dev,

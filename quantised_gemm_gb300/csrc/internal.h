@@ -156,6 +156,10 @@ struct SinglePassArgs {
 };
 int64_t single_pass_capacity_elems(const DeviceInfo& dev);
 bool single_pass_fits(const DeviceInfo& dev, int64_t rows, int64_t cols);
+// Small tensors: the same single pass in one thread-block cluster (no grid
+// barrier, no workspace).  Results are identical to the cooperative kernel's.
+bool cluster_cast_fits(int64_t rows, int64_t cols);
+cudaError_t launch_cast_cluster(const SinglePassArgs& a, cudaStream_t stream);
 cudaError_t launch_cast_single_pass(const SinglePassArgs& a, const DeviceInfo& dev,
                                     cudaStream_t stream);
 

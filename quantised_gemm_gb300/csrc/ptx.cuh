@@ -271,6 +271,13 @@ __device__ __forceinline__ uint32_t map_to_cta(uint32_t local_saddr, uint32_t ra
   return r;
 }
 
+// 32-bit load from shared memory of a CTA of the cluster (address from map_to_cta).
+__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_saddr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_saddr) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_saddr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_saddr)
                : "memory");

@@ -207,3 +207,72 @@ def test_cast_dynamic_precomputed_amax(fmt, shape, ws):
     assert dev_f32_bits(st.inv_scale) == f32_bits(inv)
     assert np.array_equal(out.cpu().numpy(), qr)
     assert np.array_equal(out_t.cpu().numpy(), qtr)
+
+
+# Shapes that the one-cluster single pass takes (up to 16 tiles of 16384
+# elements: 16-row tiles for 16 rows, ... 128-row tiles above 64 rows), and
+# one just past it that goes to the cooperative single pass.
+CLUSTER_SHAPES = [(16, 16), (16, 4096), (16, 16384), (32, 1552), (48, 4096), (64, 4096),
+                  (80, 2048), (128, 2048)]
+
+
+@pytest.mark.parametrize("trans", [False, True])
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+@pytest.mark.parametrize("shape", CLUSTER_SHAPES + [(128, 2176)])
+def test_small_tensor_single_pass(shape, fmt, trans, ws):
+    x = _tensor(shape, seed=53 + shape[0])
+    a = oracle.amax(x)
+    s, inv = oracle.scale_dynamic(a, fmt)
+    qr, qtr, _ = oracle.cast(x, s, fmt, transpose=True)
+    for algo in (q.AMAX_SINGLE_PASS, q.AMAX_AUTO):
+        st = q.ScalingState(fmt, q.DYNAMIC, amax_algo=algo)
+        out = torch.full(shape, 0xAA, dtype=torch.uint8, device="cuda")
+        out_t = torch.full(shape[::-1], 0xAA, dtype=torch.uint8, device="cuda") if trans else None
+        q.cast_dynamic(to_dev_bf16(x), st, out, out_t, ws)
+        q.check(ws)
+        assert dev_f32_bits(st.amax) == f32_bits(a)
+        assert dev_f32_bits(st.scale) == f32_bits(s)
+        assert dev_f32_bits(st.inv_scale) == f32_bits(inv)
+        assert np.array_equal(out.cpu().numpy(), qr)
+        if trans:
+            assert np.array_equal(out_t.cpu().numpy(), qtr)
+
+
+@pytest.mark.parametrize("kind", si.EDGE_KINDS)
+def test_small_tensor_single_pass_edge_tensors(kind, ws):
+    x = si.edge_tensor(kind, 64, 4096, seed=6)
+    for fmt in (E4M3, E5M2):
+        a = oracle.amax(x)
+        s, inv = oracle.scale_dynamic(a, fmt)
+        qr, qtr, _ = oracle.cast(x, s, fmt, transpose=True)
+        st = q.ScalingState(fmt, q.DYNAMIC, amax_algo=q.AMAX_AUTO)
+        out = torch.empty((64, 4096), dtype=torch.uint8, device="cuda")
+        out_t = torch.empty((4096, 64), dtype=torch.uint8, device="cuda")
+        q.cast_dynamic(to_dev_bf16(x), st, out, out_t, ws)
+        assert dev_f32_bits(st.amax) == f32_bits(a), kind
+        assert dev_f32_bits(st.scale) == f32_bits(s), kind
+        assert np.array_equal(out.cpu().numpy(), qr), kind
+        assert np.array_equal(out_t.cpu().numpy(), qtr), kind
+
+
+@pytest.mark.parametrize("shape,kernel", [((16, 4096), "cast_cluster_kernel"),
+                                          ((128, 2048), "cast_cluster_kernel"),
+                                          ((128, 2176), "cast_single_pass_kernel")])
+def test_small_tensor_single_pass_kernel_choice(shape, kernel, ws):
+    """Up to 16 tiles the single pass runs in one cluster; above, cooperatively."""
+    from torch.profiler import ProfilerActivity, profile
+    x = to_dev_bf16(_tensor(shape, seed=3))
+    out = torch.empty(shape, dtype=torch.uint8, device="cuda")
+    st = q.ScalingState(E4M3, q.DYNAMIC, amax_algo=q.AMAX_AUTO)
+    names = []
+    for _ in range(2):      # the first profiling session of a process may miss kernels
+        torch.cuda.synchronize()
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            q.cast_dynamic(x, st, out, None, ws)
+            torch.cuda.synchronize()
+        names = [e.name for e in prof.events() if "cast" in e.name]
+        if names:
+            break
+    if not names:
+        pytest.skip("the profiler recorded no kernels (no CUPTI activity on this host)")
+    assert len(names) == 1 and kernel in names[0], names
