@@ -208,8 +208,11 @@ def graphed(torch, fn):
     return g.replay
 
 
-def linear_sweep_entry(q, torch, dev, name, steps, warmup, flush, use_graph=True):
-    """fwd+bwd time of every Linear of a workload (sum over its Linears)."""
+def linear_sweep_entry(q, torch, dev, name, steps, warmup, flush, use_graph=True,
+                       cache_weight=False):
+    """fwd+bwd time of every Linear of a workload (sum over its Linears).
+    cache_weight: W is cast once and reused by every step, as over the
+    micro-batches of one optimizer step (not the full step of the headline)."""
     import synth_inputs as si
     wl = si.WORKLOADS[name]
     delayed = wl.get("delayed", False)
@@ -219,7 +222,8 @@ def linear_sweep_entry(q, torch, dev, name, steps, warmup, flush, use_graph=True
         xd, wd, dyd = to_dev(x, dev), to_dev(w, dev), to_dev(dy, dev)
         del x, w, dy
         lin = q.Fp8Linear(M, K, N, scaling="delayed" if delayed else "dynamic",
-                          history_len=wl.get("history_len", 16), device=dev)
+                          history_len=wl.get("history_len", 16), cache_weight=cache_weight,
+                          device=dev)
 
         def step():
             lin.forward(xd, wd)
@@ -236,7 +240,9 @@ def linear_sweep_entry(q, torch, dev, name, steps, warmup, flush, use_graph=True
         total_flop += 6.0 * M * N * K
         del lin, xd, wd, dyd
         torch.cuda.empty_cache()
-    return {"workload": name, "us_per_fwd_bwd": round(total_ms * 1e3, 2),
+    return {"workload": name + (" (W cast once, reused: micro-batches of one optimizer step)"
+                                if cache_weight else ""),
+            "us_per_fwd_bwd": round(total_ms * 1e3, 2),
             "tflops": round(total_flop / (total_ms * 1e-3) / 1e12, 1),
             "scaling": "delayed" if delayed else "dynamic",
             "l2": "flushed between steps" if flush else "inputs larger than L2",
@@ -583,6 +589,9 @@ def run_native(args):
             sweep["linears"].append(linear_sweep_entry(
                 q, torch, dev, name, steps=50 if small else 20, warmup=5,
                 flush=flush if small else None))
+        for name in ("linear4096_m16", "linear4096_m256"):
+            sweep["linears"].append(linear_sweep_entry(
+                q, torch, dev, name, steps=50, warmup=5, flush=flush, cache_weight=True))
         sweep["chains"] = [
             chain_sweep_entry(q, torch, dev, "linear4096_m4096", steps=50, warmup=5, flush=flush),
             chain_sweep_entry(q, torch, dev, "linear4096_m65536", steps=10, warmup=3, flush=None)]

@@ -271,7 +271,14 @@ fp8lin_status fp8lin_gemm_describe(int64_t M, int64_t N, int64_t K, char* buf, s
  * needs_init is set).  All buffers dense row-major.
  * y_amax: NULL, or device fp32[1] that receives max |y| from the GEMM
  * epilogue -- point it at the amax of the next layer's input state and give
- * that state FP8LIN_AMAX_PRECOMPUTED to cast y in one pass. */
+ * that state FP8LIN_AMAX_PRECOMPUTED to cast y in one pass.
+ * w == NULL skips W's cast and uses w8, w8t and sw as an earlier call left
+ * them: the weight cached across calls while it is unchanged, e.g. over the
+ * micro-batches of one optimizer step (the few-token case, where W's cast
+ * dominates the step).  The result is the one a fresh cast would give as long
+ * as sw's scale has not moved since: always for dynamic scaling, and until
+ * the next fp8lin_scale of sw for delayed scaling.  EINVAL if sw is delayed
+ * and still needs its first (amax-init) cast. */
 fp8lin_status fp8lin_forward(const void* x, const void* w, int64_t M, int64_t K, int64_t N,
                              fp8lin_scaling_state* sx, fp8lin_scaling_state* sw,
                              void* y, float* y_amax, uint8_t* x8, uint8_t* x8t, uint8_t* w8,

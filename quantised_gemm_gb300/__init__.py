@@ -214,10 +214,12 @@ def gemm(a8: torch.Tensor, b8: torch.Tensor, fmt_a: int, fmt_b: int, inv_a: torc
 
 def forward(x, w, sx: ScalingState, sw: ScalingState, y, x8, x8t, w8, w8t, ws: Workspace,
             stream=None, y_amax: torch.Tensor | None = None):
+    """y = x W^T in fp8.  w=None reuses w8 / w8t / sw from an earlier call
+    (an unchanged weight); y_amax (fp32[1], optional) receives max |y|."""
     M, K = x.shape
-    N = w.shape[0]
+    N = w8.shape[0] if w is None else w.shape[0]
     for t, n in ((x, "x"), (w, "w"), (y, "y")):
-        if not t.is_contiguous():
+        if t is not None and not t.is_contiguous():
             raise ValueError("%s must be contiguous" % n)
     pw, nb = _ws(ws)
     cx, cw = sx.c_struct(), sw.c_struct()

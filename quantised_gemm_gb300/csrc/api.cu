@@ -583,7 +583,10 @@ fp8lin_status fp8lin_forward(const void* x, const void* w, int64_t M, int64_t K,
   if (sx->fmt != FP8LIN_E4M3 || sw->fmt != FP8LIN_E4M3) return FP8LIN_EUNSUPPORTED;
   if (!ws_ok(ws) || ws_bytes < kWsFixedBytes) return FP8LIN_EINVAL;
   if (M * K > 0 && !dev_ptrs_ok({x, x8, x8t})) return FP8LIN_EINVAL;
-  if (N * K > 0 && !dev_ptrs_ok({w, w8, w8t})) return FP8LIN_EINVAL;
+  if (N * K > 0 && !dev_ptrs_ok({w8, w8t})) return FP8LIN_EINVAL;
+  if (w != nullptr && N * K > 0 && !dev_ptrs_ok({w})) return FP8LIN_EINVAL;
+  // w == NULL reuses w8 / w8t / sw from an earlier call: there must have been one.
+  if (w == nullptr && sw->kind == FP8LIN_DELAYED && sw->needs_init) return FP8LIN_EINVAL;
   if (M * N > 0 && !dev_ptrs_ok({y})) return FP8LIN_EINVAL;
   if (y_amax != nullptr && (reinterpret_cast<uintptr_t>(y_amax) & 3u) != 0) return FP8LIN_EINVAL;
   DeviceInfo dev;
@@ -594,11 +597,13 @@ fp8lin_status fp8lin_forward(const void* x, const void* w, int64_t M, int64_t K,
   else
     s = delayed_cast(x, M, K, K, sx, x8, x8t, ws, dev, stream);
   if (s != FP8LIN_OK) return s;
-  if (sw->kind == FP8LIN_DYNAMIC)
-    s = cast_dynamic_scaled(w, N, K, K, sw, w8, w8t, ws, dev, stream, true);
-  else
-    s = delayed_cast(w, N, K, K, sw, w8, w8t, ws, dev, stream);
-  if (s != FP8LIN_OK) return s;
+  if (w != nullptr) {
+    if (sw->kind == FP8LIN_DYNAMIC)
+      s = cast_dynamic_scaled(w, N, K, K, sw, w8, w8t, ws, dev, stream, true);
+    else
+      s = delayed_cast(w, N, K, K, sw, w8, w8t, ws, dev, stream);
+    if (s != FP8LIN_OK) return s;
+  }
   // y = x8 . W8^T : A = x8 [M, K], B = W8 [N, K]
   return do_gemm(x8, w8, M, N, K, K, K, FP8LIN_E4M3, FP8LIN_E4M3, sx->inv_scale, sw->inv_scale, y,
                  N, y_amax, ws, ws_bytes, dev, stream);

@@ -21,7 +21,8 @@ class Fp8Linear:
     """One Linear y = x W^T with x [M, K], W [N, K], fp8 tensorwise scaling."""
 
     def __init__(self, M: int, K: int, N: int, *, scaling: str = "dynamic", history_len: int = 16,
-                 amax_algo: int = AMAX_AUTO, eps: float = 1e-12, device="cuda"):
+                 amax_algo: int = AMAX_AUTO, eps: float = 1e-12, cache_weight: bool = False,
+                 device="cuda"):
         kind = {"dynamic": DYNAMIC, "delayed": DELAYED}[scaling]
         self.M, self.K, self.N = M, K, N
         u8 = dict(dtype=torch.uint8, device=device)
@@ -41,10 +42,20 @@ class Fp8Linear:
         # Where the GEMM epilogues deliver max |y| and max |dX| (set by link_linears()).
         self.y_amax_to = None
         self.dx_amax_to = None
+        # cache_weight: cast W only when it changed since the last cast (its
+        # storage or its in-place version counter), e.g. once for all the
+        # micro-batches of an optimizer step.
+        self.cache_weight = cache_weight
+        self._w_key = None
 
     def forward(self, x: torch.Tensor, w: torch.Tensor, stream=None) -> torch.Tensor:
-        return forward(x, w, self.sx, self.sw, self.y, self.x8, self.x8t, self.w8, self.w8t,
-                       self.ws, stream, y_amax=self.y_amax_to)
+        key = ((id(w), w.data_ptr(), w._version, tuple(w.shape), w.device)
+               if self.cache_weight else None)
+        reuse = key is not None and key == self._w_key
+        forward(x, None if reuse else w, self.sx, self.sw, self.y, self.x8, self.x8t, self.w8,
+                self.w8t, self.ws, stream, y_amax=self.y_amax_to)
+        self._w_key = key
+        return self.y
 
     def backward(self, dy: torch.Tensor, need_dx: bool = True, need_dw: bool = True, stream=None):
         return backward(dy, self.x8t, self.w8t, self.sx, self.sw, self.sdy, self.dy8, self.dy8t,
@@ -53,10 +64,13 @@ class Fp8Linear:
 
     def sync_scales(self, stream=None):
         """Delayed scaling: push this step's amaxes into the histories and
-        recompute the scales (a no-op for dynamic scaling)."""
+        recompute the scales (a no-op for dynamic scaling).  A new delayed
+        weight scale makes a cached W8 stale: the next forward casts again."""
         for st in (self.sx, self.sw, self.sdy):
             if st.kind == DELAYED:
                 scale(st, stream)
+        if self.sw.kind == DELAYED:
+            self._w_key = None
 
     copy_lanes = 1   # copy streams per direction; with more, each tensor moves in row slices
 

@@ -108,6 +108,13 @@ def test_forward_backward_argument_errors(lib):
     assert fwd(128, 128, 128, _state(0, kind=1, H=4, algo=L.AMAX_PRECOMPUTED), sw) == \
         L.EUNSUPPORTED
     assert fwd(128, 128, 128, sx, sw, ctypes.c_void_p(0x10001)) == L.EINVAL   # misaligned y_amax
+    # a cached weight (w == NULL) still needs w8 / w8t, and a first delayed cast
+    assert lib.fp8lin_forward(p, None, 128, 128, 128, ctypes.byref(sx), ctypes.byref(sw), p, None,
+                              p, p, None, p, ws, nb, None) == L.EINVAL
+    swd = _state(0, kind=1, H=4)
+    swd.needs_init = 1
+    assert lib.fp8lin_forward(p, None, 128, 128, 128, ctypes.byref(sx), ctypes.byref(swd), p, None,
+                              p, p, p, p, ws, nb, None) == L.EINVAL
     assert lib.fp8lin_forward(p, p, 128, 128, 128, ctypes.byref(sx), ctypes.byref(sw), p, None, p,
                               p, p, p, None, nb, None) == L.EINVAL    # no workspace
     bwd = lambda d, dxa=None, dwa=None, dx=p, dw=p: lib.fp8lin_backward(

@@ -283,3 +283,53 @@ def test_linked_linears_match_unlinked(M):
     for i, (u, v) in enumerate(zip(o1, o2)):
         assert np.array_equal(u, v), i
     assert s1 == s2
+
+
+def test_cached_weight_dynamic_matches_recast():
+    """cache_weight: micro-batches with the same W skip W's cast (two
+    launches per forward instead of three) and give the bits of a fresh
+    cast; an in-place update of W makes the next forward cast again."""
+    M, K, N = 16, 4096, 4096
+    lc = q.Fp8Linear(M, K, N, cache_weight=True)
+    lu = q.Fp8Linear(M, K, N)
+    _, w, _ = si.linear_inputs(M, K, N, w_init="uniform64", seed=31)
+    wd = to_dev_bf16(w)
+    for step in range(4):
+        x, _, dy = si.linear_inputs(M, K, N, w_init="uniform64", seed=31, step=step)
+        if step == 2:
+            wd.mul_(2.0)                       # an optimizer step, in place
+        n0 = q.launch_count()
+        lc.forward(to_dev_bf16(x), wd)
+        launches = q.launch_count() - n0
+        assert launches == (3 if step in (0, 2) else 2), (step, launches)
+        lc.backward(to_dev_bf16(dy))
+        lu.forward(to_dev_bf16(x), wd)
+        lu.backward(to_dev_bf16(dy))
+        torch.cuda.synchronize()
+        for a, b, what in ((lc.y, lu.y, "y"), (lc.dx, lu.dx, "dX"), (lc.dw, lu.dw, "dW")):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16)), (step, what)
+
+
+def test_cached_weight_delayed_micro_batches():
+    """Delayed scaling with cache_weight: W is cast once per optimizer step
+    (sync_scales moves W's scale and drops the cache) and every micro-batch
+    gives the bits of the uncached Linear."""
+    M, K, N = 256, 768, 1024
+    lc = q.Fp8Linear(M, K, N, scaling="delayed", history_len=4, cache_weight=True)
+    lu = q.Fp8Linear(M, K, N, scaling="delayed", history_len=4)
+    _, w, _ = si.linear_inputs(M, K, N, w_init="uniform64", seed=37)
+    wd = to_dev_bf16(w)
+    for step in range(3):
+        for micro in range(3):
+            x, _, dy = si.linear_inputs(M, K, N, w_init="uniform64", seed=37,
+                                        step=3 * step + micro)
+            for lin in (lc, lu):
+                lin.forward(to_dev_bf16(x), wd)
+                lin.backward(to_dev_bf16(dy))
+            torch.cuda.synchronize()
+            for a, b, what in ((lc.y, lu.y, "y"), (lc.dx, lu.dx, "dX"), (lc.dw, lu.dw, "dW")):
+                assert torch.equal(a.view(torch.int16), b.view(torch.int16)), (step, micro, what)
+        lc.sync_scales()
+        lu.sync_scales()
+        torch.cuda.synchronize()
+        assert dev_f32_bits(lc.sw.scale) == dev_f32_bits(lu.sw.scale)
