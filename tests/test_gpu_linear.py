@@ -333,3 +333,35 @@ def test_cached_weight_delayed_micro_batches():
         lu.sync_scales()
         torch.cuda.synchronize()
         assert dev_f32_bits(lc.sw.scale) == dev_f32_bits(lu.sw.scale)
+
+
+def test_linear_degenerate_sizes_and_zero_tensors():
+    """M = 0 (no tokens): dW is all zeros and x's amax is 0 with scale F/eps.
+    All-zero x and dY: every code is +0, y, dX, dW are zeros, and the scales
+    are F/eps exactly as the oracle derives them."""
+    K, N = 256, 384
+    lin = q.Fp8Linear(0, K, N)
+    _, w, _ = si.linear_inputs(16, K, N, w_init="uniform64", seed=41)
+    lin.dw.fill_(1.0)
+    lin.forward(torch.empty((0, K), dtype=torch.bfloat16, device="cuda"), to_dev_bf16(w))
+    lin.backward(torch.empty((0, N), dtype=torch.bfloat16, device="cuda"))
+    q.check(lin.ws)
+    assert torch.count_nonzero(lin.dw.float()).item() == 0
+    s0, inv0 = oracle.scale_dynamic(0.0, oracle.E4M3)
+    assert lin.sx.amax.item() == 0.0 and dev_f32_bits(lin.sx.scale) == f32_bits(s0)
+    assert dev_f32_bits(lin.sx.inv_scale) == f32_bits(inv0)
+
+    M = 64
+    lin = q.Fp8Linear(M, K, N)
+    x = np.zeros((M, K), dtype=np.uint16)
+    dy = np.zeros((M, N), dtype=np.uint16)
+    lin.forward(to_dev_bf16(x), to_dev_bf16(w))
+    lin.backward(to_dev_bf16(dy))
+    q.check(lin.ws)
+    for t in (lin.x8, lin.x8t, lin.dy8, lin.dy8t):
+        assert torch.count_nonzero(t).item() == 0
+    for t in (lin.y, lin.dx, lin.dw):
+        assert torch.count_nonzero(t.float()).item() == 0
+    s2, _ = oracle.scale_dynamic(0.0, oracle.E5M2)
+    assert dev_f32_bits(lin.sx.scale) == f32_bits(s0)
+    assert dev_f32_bits(lin.sdy.scale) == f32_bits(s2)
