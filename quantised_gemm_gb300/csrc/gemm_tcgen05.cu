@@ -1046,16 +1046,18 @@ namespace {
 // The kernel and tile shape for a Linear GEMM of M rows and N columns:
 // swap-AB (D^T = B . A^T, the weight-side operand fills the 128-row MMA and
 // the few rows of A become N = 16 / 32 / 64) for M <= 64; one-CTA 128-row
-// tiles up to M = 128; CTA pairs with 256-row tiles above.  BN = 256 unless
-// 128 pads the N edge clearly less (e.g. N = 1600).
+// tiles up to M = 128; CTA pairs with 256-row tiles above.  BN = 256 except
+// for N <= 128: a 128-wide tile costs about 1.7x more per FLOP (each CTA
+// reads the same A block per K step for half the columns), which outweighs
+// the padding it saves everywhere else -- e.g. the N = 1600 products of a
+// 1600-wide model run 1.5-1.8x faster on 256-wide tiles, padding included.
 enum class Variant { kSwap16, kSwap32, kSwap64, kOne128, kOne256, kPair128, kPair256 };
 
 Variant choose_variant(int64_t M, int64_t N) {
   if (M <= 16) return Variant::kSwap16;
   if (M <= 32) return Variant::kSwap32;
   if (M <= 64) return Variant::kSwap64;
-  const int64_t pad256 = (N + 255) / 256 * 256, pad128 = (N + 127) / 128 * 128;
-  const bool narrow = pad256 * 100 > pad128 * 105;
+  const bool narrow = N <= 128;
   if (M > kBM) return narrow ? Variant::kPair128 : Variant::kPair256;
   return narrow ? Variant::kOne128 : Variant::kOne256;
 }

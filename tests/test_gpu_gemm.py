@@ -34,7 +34,9 @@ CASES = [
     (128, 256, 128),        # one tile, one k-block
     (256, 512, 1024),       # several tiles
     (200, 272, 336),        # ragged M, N, K
-    (384, 1600, 1600),      # N = 1600: 128-wide tiles, K tail of 64
+    (384, 1600, 1600),      # N = 1600: 256-wide tiles padded to 1792, K tail of 64
+    (512, 128, 1024),       # N = 128: 128-wide pair tiles
+    (96, 128, 512),         # one-CTA 128-wide tiles
     (144, 4096, 16),        # K = 16 (one partial k-block)
     (16, 4096, 4096),       # few rows: swapped operands, transposed store
     (48, 208, 160),         # few rows, ragged
@@ -149,8 +151,10 @@ def test_gemm_without_split_workspace_matches(ws):
     ((16, 4096, 4096), "gemm_fp8_kernel<16, 8, 1>", "K split 4 ways"),
     ((48, 208, 160), "gemm_fp8_kernel<64, 8, 1>", "whole tiles"),
     ((128, 4096, 4096), "gemm_fp8_kernel<256, 4, 0>", "K split 8 ways"),
-    ((128, 1600, 512), "gemm_fp8_kernel<128, 6, 0>", "whole tiles"),
-    ((384, 1600, 1600), "gemm_fp8_pair_kernel<128, 8>", "whole tiles"),
+    ((128, 1600, 512), "gemm_fp8_kernel<256, 4, 0>", "whole tiles"),
+    ((96, 128, 512), "gemm_fp8_kernel<128, 6, 0>", "whole tiles"),
+    ((384, 1600, 1600), "gemm_fp8_pair_kernel<256, 6>", "whole tiles"),
+    ((512, 128, 1024), "gemm_fp8_pair_kernel<128, 8>", "whole tiles"),
     ((4096, 4096, 1024), "gemm_fp8_pair_kernel<256, 6>", "whole tiles"),
 ])
 def test_gemm_describe_names_the_launched_kernel(mnk, kernel, sched, ws):
@@ -190,9 +194,11 @@ def _bf16_bits(t: torch.Tensor) -> np.ndarray:
     (16, 4096, 4096),      # swapped operands, K split 4 ways, transposed stores
     (48, 208, 160),        # swapped operands, ragged
     (128, 4096, 4096),     # one-CTA tiles, K split 8 ways
-    (128, 1600, 512),      # one-CTA 128-wide tiles, ragged N edge
+    (128, 1600, 512),      # one-CTA tiles, ragged N edge
+    (96, 128, 512),        # one-CTA 128-wide tiles
     (200, 272, 336),       # CTA pairs, ragged M, N, K
-    (384, 1600, 1600),     # CTA pairs, 128-wide tiles
+    (384, 1600, 1600),     # CTA pairs, N edge inside the last 256-wide tile
+    (512, 128, 1024),      # CTA pairs, 128-wide tiles
     (2048, 2560, 256),     # CTA pairs, more than one wave
 ])
 def test_gemm_output_amax(mnk, ws):
