@@ -45,7 +45,7 @@ L2_BYTES = 129 * 1024 * 1024
 FP8_OVER_BF16 = 2.0      # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=400)
@@ -56,7 +56,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--workload", default=HEADLINE)
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 # ------------------------------------------------------------------ helpers
@@ -152,6 +152,22 @@ def dist_info():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def max_over_ranks(torch, value, world, device):
+    """The largest `value` over all ranks (one process per GPU): the whole
+    job's step time is the slowest rank's."""
+    if world <= 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flop_per_rank_step, ms_step, world):
+    """Throughput of all ranks together: every rank does the same step (the
+    replicas of a weak-scaling run), the job takes the slowest rank's time."""
+    return world * flop_per_rank_step / (ms_step * 1e-3) / 1e12
 
 
 # ------------------------------------------------------------------ native arm
@@ -405,12 +421,13 @@ def end_to_end(q, lin, x, w, dy, M, K, N, world, flop_step, steps):
         lin.step_host(hx, hw, hdy, hy, hdx, hdw)
     torch.cuda.synchronize()
     ms = time_region(lambda: lin.step_host(hx, hw, hdy, hy, hdx, hdw), n) / n
+    ms = max_over_ranks(torch, ms, world, lin.y.device)
     h2d = 2 * (M * K + N * K + M * N)
     d2h = 2 * (M * N + M * K + N * K)
     link = host_link_rates(torch, hx, lin.y.device)
     floor_ms = max(h2d / (link["h2d_gbs"] * 1e9), d2h / (link["d2h_gbs"] * 1e9),
                    (h2d + d2h) / (link["both_gbs"] * 1e9)) * 1e3
-    return {"value": round(world * flop_step / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+    return {"value": round(whole_job_tflops(flop_step, ms, world), 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3),
             "steps": n, "copy_lanes": lin.copy_lanes,
             "api": "Fp8Linear.step_host (pinned host buffers)",
@@ -511,13 +528,9 @@ def run_native(args):
         torch.distributed.barrier()
     clocks = sampler.stop()
     q.check(lin.ws)
-    ms_step = ms / args.steps
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(torch, ms / args.steps, world, dev)
     flop_step = 6.0 * M * N * K
-    value = world * flop_step / (ms_step * 1e-3) / 1e12
+    value = whole_job_tflops(flop_step, ms_step, world)
 
     gemm_ms, gemm_n = prof["gemm"]
     gemm_avg = gemm_ms / max(1, gemm_n)

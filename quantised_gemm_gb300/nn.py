@@ -113,6 +113,9 @@ class _Fp8LinearFunction(torch.autograd.Function):
         return dx, dw, None
 
 
+_SHARED_WS: dict = {}
+
+
 class Float8Linear(nn.Module):
     """Drop-in nn.Linear whose forward and backward run as FP8 (e4m3 input
     and weight, e5m2 grad_output) with tensorwise scaling."""
@@ -132,12 +135,18 @@ class Float8Linear(nn.Module):
         self.sx = _state(c.cast_config_input, E4M3, c.eps, dev)
         self.sw = _state(c.cast_config_weight, E4M3, c.eps, dev)
         self.sdy = _state(c.cast_config_grad_output, E5M2, c.eps, dev)
-        self._ws = None
 
     def _workspace(self, device) -> Workspace:
-        if self._ws is None:
-            self._ws = Workspace(device=device)
-        return self._ws
+        # One workspace per (device, stream), shared by every Float8Linear:
+        # it holds only scratch and self-cleaning counters, and calls on one
+        # stream never overlap on the GPU, so sharing is safe there.
+        dev = torch.device(device)
+        key = (dev.index if dev.index is not None else torch.cuda.current_device(),
+               torch.cuda.current_stream(dev).cuda_stream)
+        ws = _SHARED_WS.get(key)
+        if ws is None:
+            ws = _SHARED_WS[key] = Workspace(device=dev)
+        return ws
 
     @classmethod
     def from_linear(cls, lin: nn.Linear, config: Float8LinearConfig | None = None):

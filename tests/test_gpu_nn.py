@@ -93,3 +93,16 @@ def test_rejects_non_bf16():
     lin = q.Float8Linear(64, 64)
     with pytest.raises(TypeError):
         lin(torch.randn(16, 64, device="cuda"))
+
+
+def test_float8_linears_share_one_workspace_per_stream():
+    """Every Float8Linear on a stream uses the same workspace (scratch only);
+    another stream gets its own, so calls that may overlap never share one."""
+    a, b = q.Float8Linear(64, 32), q.Float8Linear(32, 16)
+    dev = torch.device("cuda")
+    assert a._workspace(dev) is b._workspace(dev)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        other = a._workspace(dev)
+        assert other is b._workspace(dev)
+    assert other is not a._workspace(dev)
