@@ -125,3 +125,14 @@ def test_forward_backward_argument_errors(lib):
     assert bwd(sd, dwa=p, dw=None) == L.EINVAL                     # dW amax without dW
     assert lib.fp8lin_scale(None, None) == L.EINVAL
     assert lib.fp8lin_scale(ctypes.byref(_state(0, kind=1, H=0)), None) == L.EINVAL
+
+
+def test_gemm_describe_argument_errors(lib):
+    import quantised_gemm_gb300._lib as L
+    buf = ctypes.create_string_buffer(64)
+    assert lib.fp8lin_gemm_describe(16, 16, 16, None, 64) == L.EINVAL
+    assert lib.fp8lin_gemm_describe(16, 16, 16, buf, 0) == L.EINVAL
+    assert lib.fp8lin_gemm_describe(-16, 16, 16, buf, 64) == L.EINVAL
+    # without a GPU the valid call reports a CUDA error and leaves an empty line
+    st = lib.fp8lin_gemm_describe(16, 16, 16, buf, 64)
+    assert st in (L.OK, L.ECUDA) and (st == L.OK or buf.value == b"")

@@ -235,3 +235,34 @@ def test_gemm_output_amax_of_empty_products(ws):
            torch.empty((0, 64), dtype=torch.bfloat16, device="cuda"), ws, amax_out=amax_out)
     torch.cuda.synchronize()
     assert amax_out.item() == 0.0
+
+
+def _random_shapes(n, seed):
+    """Seeded M, N, K (multiples of 16) spread over every kernel variant:
+    swapped operands (M <= 64), one-CTA tiles (M <= 128), CTA pairs; N below
+    and above 128; K short and long (K-split when few tiles)."""
+    g = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        M = int(16 * g.integers(1, [5, 9, 200][i % 3]))
+        N = int(16 * g.integers(1, [9, 120][i % 2]))
+        K = int(16 * g.integers(1, [20, 260][(i // 2) % 2]))
+        out.append((M, N, K))
+    return out
+
+
+@pytest.mark.parametrize("mnk", _random_shapes(24, seed=2024))
+def test_gemm_random_shapes_match_oracle(mnk, ws):
+    M, N, K = mnk
+    fa = E4M3 if (M + N) % 32 else E5M2
+    a8, sa, inva = _operand(M, K, fa, seed=M + 3 * N)
+    b8, sb, invb = _operand(N, K, E4M3, seed=K + 5 * N)
+    d = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    amax = torch.full((1,), -1.0, device="cuda")
+    q.gemm(torch.from_numpy(a8).cuda(), torch.from_numpy(b8).cuda(), fa, E4M3,
+           torch.tensor([inva], device="cuda"), torch.tensor([invb], device="cuda"), d, ws,
+           amax_out=amax)
+    q.check(ws)
+    y, s = oracle.gemm(a8, b8, fa, E4M3, sa, sb)
+    assert_within_bound(bf16_to_f64(d), y, s, "%s %s" % (mnk, q.gemm_describe(M, N, K)))
+    assert dev_f32_bits(amax) == f32_bits(oracle.amax(_bf16_bits(d)))
