@@ -74,30 +74,43 @@ class Fp8Linear:
 
     copy_lanes = 1   # copy streams per direction; with more, each tensor moves in row slices
 
-    def step_host(self, x_h, w_h, dy_h, y_h, dx_h, dw_h, stream=None):
+    def step_host(self, x_h, w_h, dy_h, y_h, dx_h, dw_h, stream=None, wait=True):
         """End-to-end step from host buffers (pinned, for asynchronous copies):
         copy x, W, dY in, forward + backward (+ delayed sync), copy y, dX, dW
         out.  The copies run on copy streams of their own (``copy_lanes`` per
-        direction, each moving a slice of rows, so several copy engines work
-        at once), ordered by events: dY's upload overlaps the forward, y's
-        download overlaps the backward, and the next step's uploads may start
-        while this step's downloads finish.  The compute runs on `stream`
-        (default: the current stream), which waits for the last download
-        before it goes on.  Device staging buffers and the copy streams are
-        created on the first call."""
+        direction; with more than one, each moves a slice of the rows -- one
+        per direction measured fastest on a 4096 x 65536 step), ordered by
+        events.  Device inputs and outputs come in two slots used in turn, so
+        a step's uploads need only the step two back to be done with its slot:
+        dY's upload overlaps the forward, y's download the backward, and the
+        next step's uploads this step's compute.
+
+        The compute runs on `stream` (default: the current stream).  With
+        wait=True it waits, at the end, for this step's downloads: the host
+        buffers hold the results.  With wait=False the next step's compute may
+        run while those downloads are still in flight (the host link then
+        sets the pace, both directions busy at once); the host buffers are
+        complete after finish_host(), and a later step overwrites them.
+        Device slots and copy streams are created on the first call."""
         main = stream if stream is not None else torch.cuda.current_stream()
         n = self.copy_lanes
-        if not hasattr(self, "_xd"):
+        if not hasattr(self, "_slots"):
             dev = self.y.device
-            self._xd = torch.empty((self.M, self.K), dtype=torch.bfloat16, device=dev)
-            self._wd = torch.empty((self.N, self.K), dtype=torch.bfloat16, device=dev)
-            self._dyd = torch.empty((self.M, self.N), dtype=torch.bfloat16, device=dev)
+            mk = lambda r, c: torch.empty((r, c), dtype=torch.bfloat16, device=dev)  # noqa: E731
+            self._slots = []
+            for k in range(2):
+                sl = {"x": mk(self.M, self.K), "w": mk(self.N, self.K), "dy": mk(self.M, self.N),
+                      "y": self.y if k == 0 else mk(self.M, self.N),
+                      "dx": self.dx if k == 0 else mk(self.M, self.K),
+                      "dw": self.dw if k == 0 else mk(self.N, self.K),
+                      "fwd_done": torch.cuda.Event(), "bwd_done": torch.cuda.Event(),
+                      "downloads": []}
+                sl["fwd_done"].record(main)
+                sl["bwd_done"].record(main)
+                self._slots.append(sl)
+            self._slot = 0
             self._up = [torch.cuda.Stream(device=dev) for _ in range(n)]
             self._down = [torch.cuda.Stream(device=dev) for _ in range(n)]
-            self._fwd_done = torch.cuda.Event()
-            self._bwd_done = torch.cuda.Event()
-            self._fwd_done.record(main)
-            self._bwd_done.record(main)
 
         def move(pairs, streams, after):
             """Copy each (dst, src) in row slices over `streams` once `after`
@@ -116,22 +129,34 @@ class Fp8Linear:
                     done.append(ev)
             return done
 
-        # the previous forward has read x and W; the previous backward dY
-        for ev in move([(self._xd, x_h), (self._wd, w_h)], self._up, self._fwd_done):
+        sl = self._slots[self._slot]
+        self._slot ^= 1
+        # this slot's inputs are free once the step two back has consumed them
+        xw_in = move([(sl["x"], x_h), (sl["w"], w_h)], self._up, sl["fwd_done"])
+        dy_in = move([(sl["dy"], dy_h)], self._up, sl["bwd_done"])
+        for ev in sl["downloads"] + xw_in:        # its outputs once downloaded
             main.wait_event(ev)
-        dy_in = move([(self._dyd, dy_h)], self._up, self._bwd_done)
-        self.forward(self._xd, self._wd, main)
-        self._fwd_done.record(main)
-        y_out = move([(y_h, self.y)], self._down, self._fwd_done)
+        self.y, self.dx, self.dw = sl["y"], sl["dx"], sl["dw"]
+        self.forward(sl["x"], sl["w"], main)
+        sl["fwd_done"].record(main)
+        y_out = move([(y_h, sl["y"])], self._down, sl["fwd_done"])
         for ev in dy_in:
             main.wait_event(ev)
-        self.backward(self._dyd, stream=main)
+        self.backward(sl["dy"], stream=main)
         self.sync_scales(main)
-        self._bwd_done.record(main)
-        out = move([(dx_h, self.dx), (dw_h, self.dw)], self._down, self._bwd_done)
-        for ev in y_out + out:
-            main.wait_event(ev)                # host results complete; y, dX, dW free again
+        sl["bwd_done"].record(main)
+        sl["downloads"] = y_out + move([(dx_h, sl["dx"]), (dw_h, sl["dw"])], self._down,
+                                       sl["bwd_done"])
+        if wait:
+            self.finish_host(main)
         return y_h, dx_h, dw_h
+
+    def finish_host(self, stream=None):
+        """Make `stream` wait until every download of step_host is complete."""
+        main = stream if stream is not None else torch.cuda.current_stream()
+        for sl in getattr(self, "_slots", []):
+            for ev in sl["downloads"]:
+                main.wait_event(ev)
 
     def step(self, x, w, dy, stream=None):
         """One forward + backward (+ delayed sync)."""

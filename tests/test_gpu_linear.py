@@ -365,3 +365,30 @@ def test_linear_degenerate_sizes_and_zero_tensors():
     s2, _ = oracle.scale_dynamic(0.0, oracle.E5M2)
     assert dev_f32_bits(lin.sx.scale) == f32_bits(s0)
     assert dev_f32_bits(lin.sdy.scale) == f32_bits(s2)
+
+
+def test_step_host_pipelined_matches_device_path():
+    """step_host(wait=False) over alternating device slots: four steps run
+    back to back, each downloading into its own host buffers; after
+    finish_host every step's y, dX, dW equal the device path's bits."""
+    M, K, N = 560, 768, 1024
+    dev_lin = q.Fp8Linear(M, K, N)
+    host_lin = q.Fp8Linear(M, K, N)
+    pin = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
+    steps, outs, ins = 4, [], []
+    for step in range(steps):
+        x, w, dy = si.linear_inputs(M, K, N, w_init="uniform64", seed=5, step=step)
+        ins.append((x, w, dy))
+        hy = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+        hdx = torch.empty((M, K), dtype=torch.bfloat16).pin_memory()
+        hdw = torch.empty((N, K), dtype=torch.bfloat16).pin_memory()
+        outs.append((hy, hdx, hdw))
+        host_lin.step_host(pin(x), pin(w), pin(dy), hy, hdx, hdw, wait=False)
+    host_lin.finish_host()
+    torch.cuda.current_stream().synchronize()
+    for step, ((x, w, dy), (hy, hdx, hdw)) in enumerate(zip(ins, outs)):
+        dev_lin.step(to_dev_bf16(x), to_dev_bf16(w), to_dev_bf16(dy))
+        torch.cuda.synchronize()
+        assert torch.equal(hy.view(torch.int16), dev_lin.y.cpu().view(torch.int16)), step
+        assert torch.equal(hdx.view(torch.int16), dev_lin.dx.cpu().view(torch.int16)), step
+        assert torch.equal(hdw.view(torch.int16), dev_lin.dw.cpu().view(torch.int16)), step
