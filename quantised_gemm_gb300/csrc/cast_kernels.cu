@@ -47,6 +47,26 @@ __device__ __forceinline__ uint32_t vec_absmax(uint32_t acc, const uint4& v) {
   return acc;
 }
 
+// The same maximum with the low and the high bf16 of each 32-bit word kept
+// apart (bits & 0x7FFF, bits & 0x7FFF0000): each step is an AND and a native
+// 32-bit max.  It issues twice as many instructions as vec_absmax, which
+// costs the streaming kernels, but its steps are short: the kernels whose
+// amax is a latency chain (data already on chip) run faster with it.
+struct AbsMax {
+  uint32_t lo = 0, hi = 0;
+  __device__ __forceinline__ void add(const uint4& v) {
+    lo = max(lo, max(max(v.x & 0x7FFFu, v.y & 0x7FFFu), max(v.z & 0x7FFFu, v.w & 0x7FFFu)));
+    hi = max(hi, max(max(v.x & 0x7FFF0000u, v.y & 0x7FFF0000u),
+                     max(v.z & 0x7FFF0000u, v.w & 0x7FFF0000u)));
+  }
+  __device__ __forceinline__ void merge(const AbsMax& o) {
+    lo = max(lo, o.lo);
+    hi = max(hi, o.hi);
+  }
+  // As vec_absmax's packed pair: the maximum in the low 16 bits.
+  __device__ __forceinline__ uint32_t packed() const { return max(lo, hi >> 16); }
+};
+
 // Block-wide max of per-thread 2x16-bit magnitudes; result (as fp32 bits)
 // valid in thread 0.
 __device__ __forceinline__ uint32_t block_absmax_bits(uint32_t acc) {
@@ -330,12 +350,21 @@ __device__ __forceinline__ void group_sync(int group) {
   asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(kThreads) : "memory");
 }
 
+// Offset of byte `col` (0..127) of row `row` in a 128 x 128-byte fp8 tile
+// laid out as the 128-byte TMA swizzle expects: 16-byte chunk c of row r is
+// stored at chunk c ^ (r & 7).
+__device__ __forceinline__ int sw128(int row, int col) {
+  return row * 128 + ((((col >> 4) ^ (row & 7))) << 4) + (col & 15);
+}
+
 template <int kFmt, bool kTrans>
 __global__ void __launch_bounds__(kSpThreads, 1)
-    cast_single_pass_kernel(const __grid_constant__ CUtensorMap tmX, const SinglePassParams p) {
+    cast_single_pass_kernel(const __grid_constant__ CUtensorMap tmX,
+                            const __grid_constant__ CUtensorMap tmQ,
+                            const __grid_constant__ CUtensorMap tmQT, const SinglePassParams p) {
   extern __shared__ __align__(1024) uint8_t tiles_raw[];
   uint8_t* tiles = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(tiles_raw) + 127) & ~static_cast<uintptr_t>(127));
+      (reinterpret_cast<uintptr_t>(tiles_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   __shared__ __align__(8) uint64_t loaded;
   __shared__ uint32_t s_amax_bits;
   __shared__ uint32_t s_red[kSpThreads / 32];
@@ -369,17 +398,21 @@ __global__ void __launch_bounds__(kSpThreads, 1)
       return;
     }
   }
-  uint32_t acc = 0;
+  // Two independent accumulators of the short-step kind: the tile is on chip,
+  // so this loop is a latency chain, not a bandwidth stream.
+  AbsMax a0, a1;
   for (int k = group; k < mine; k += kSpGroups) {
     const uint8_t* buf = tiles + k * (kTile * kTile * 2);
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int vi = tid + kThreads * u;
-      acc = vec_absmax(acc, *reinterpret_cast<const uint4*>(buf + (vi >> 4) * (kTile * 2) +
-                                                          (vi & 15) * 16));
+      (u & 1 ? a1 : a0).add(*reinterpret_cast<const uint4*>(buf + (vi >> 4) * (kTile * 2) +
+                                                             (vi & 15) * 16));
     }
   }
   {
+    a0.merge(a1);
+    const uint32_t acc = a0.packed();
     uint32_t m = max(acc & 0xFFFFu, acc >> 16);
     m = __reduce_max_sync(0xFFFFFFFFu, m);
     if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = m;
@@ -389,8 +422,7 @@ __global__ void __launch_bounds__(kSpThreads, 1)
     uint32_t m = 0;
     for (int w = 0; w < kSpThreads / 32; ++w) m = max(m, s_red[w]);
     atomicMax(p.ws_amax, m << 16);
-    __threadfence();
-    atomicAdd(p.ws_barrier, 1u);
+    red_release_add(p.ws_barrier, 1u);  // the max above is visible to whoever sees this
     const uint64_t t0 = global_timer_ns();
     while (ld_acquire_u32(p.ws_barrier) < gridDim.x) {
       if (global_timer_ns() - t0 > kWaitLimitNs) {
@@ -399,18 +431,18 @@ __global__ void __launch_bounds__(kSpThreads, 1)
         break;
       }
     }
-    if (!s_abort) {
-      s_amax_bits = ld_acquire_u32(p.ws_amax);
-      if (atomicAdd(p.ws_exits, 1u) == gridDim.x - 1) {  // everyone has read the amax
-        atomicExch(p.ws_barrier, 0u);
-        atomicExch(p.ws_exits, 0u);
-        atomicExch(p.ws_amax, 0u);
-      }
-    }
+    if (!s_abort) s_amax_bits = ld_acquire_u32(p.ws_amax);
   }
   __syncthreads();
   if (s_abort) return;
   griddep_launch_dependents();
+  // Off the critical path: count this CTA out (it has read the amax); the
+  // last one clears the three words for the next launch.
+  if (threadIdx.x == 0 && atomicAdd(p.ws_exits, 1u) == gridDim.x - 1) {
+    atomicExch(p.ws_barrier, 0u);
+    atomicExch(p.ws_exits, 0u);
+    atomicExch(p.ws_amax, 0u);
+  }
 
   const float amax = __uint_as_float(s_amax_bits);
   const float s = scale_from_amax(amax, p.eps, fp8_max<kFmt>());
@@ -419,6 +451,12 @@ __global__ void __launch_bounds__(kSpThreads, 1)
     *p.scale_out = s;
     *p.inv_out = __fdiv_rn(1.0f, s);
   }
+  // Phase 2, per tile: cast from shared memory into registers, then stage the
+  // fp8 tile (first 16 KB of the tile's own 32 KB buffer, free once read)
+  // and its transpose (second 16 KB) in the 128-byte TMA swizzle, and write
+  // both with TMA bulk stores, which clip ragged edges.  One thread of each
+  // group issues its group's stores and waits for them before the CTA ends.
+  const bool issuer = tid == 0;
   for (int k = group; k < mine; k += kSpGroups) {
     const int64_t t = blockIdx.x + static_cast<int64_t>(k) * gridDim.x;
     uint8_t* buf = tiles + k * (kTile * kTile * 2);
@@ -430,24 +468,54 @@ __global__ void __launch_bounds__(kSpThreads, 1)
       const uint4 v = *reinterpret_cast<const uint4*>(buf + (vi >> 4) * (kTile * 2) +
                                                       (vi & 15) * 16);
       q[u] = cast8<kFmt>(v, s);
-      const int64_t row = r0 + (vi >> 4), col = c0 + (vi & 15) * 8;
-      if (p.out != nullptr && row < p.rows && col < p.cols)
-        *reinterpret_cast<uint2*>(p.out + row * p.cols + col) = q[u];
+    }
+    group_sync(group);  // the group has read the whole bf16 tile
+    uint8_t* sqt = buf;                       // fp8 tile [128 rows][128 bytes]
+    uint8_t* stt = buf + kTile * kTile;       // its transpose
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int vi = tid + kThreads * u;
+      *reinterpret_cast<uint2*>(sqt + sw128(vi >> 4, (vi & 15) * 8)) = q[u];
     }
     if (kTrans) {
-      // The bf16 tile is no longer needed: reuse its buffer for the fp8 tile.
       group_sync(group);
-      uint32_t* sq = reinterpret_cast<uint32_t*>(buf);
+      // Each thread moves a 16-row x 4-column block: 16 words down a column
+      // group of the tile, 4x4 byte transposes, four 16-byte rows of the
+      // transpose.
+      const int lane = tid & 31, warp = tid >> 5;
+      const int jg = (warp & 1) * 16 + (lane >> 1);  // 4-column group 0..31
+      const int ig = (warp >> 1) * 2 + (lane & 1);   // 16-row group 0..7
+      uint32_t w[16];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int vi = tid + kThreads * u;
-        sq[(vi >> 4) * kSqWords + (vi & 15) * 2] = q[u].x;
-        sq[(vi >> 4) * kSqWords + (vi & 15) * 2 + 1] = q[u].y;
+      for (int kk = 0; kk < 16; ++kk)
+        w[kk] = *reinterpret_cast<const uint32_t*>(sqt + sw128(ig * 16 + kk, jg * 4));
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const uint32_t t0 = __byte_perm(w[4 * g + 0], w[4 * g + 1], 0x5140);
+        const uint32_t t1 = __byte_perm(w[4 * g + 2], w[4 * g + 3], 0x5140);
+        const uint32_t t2 = __byte_perm(w[4 * g + 0], w[4 * g + 1], 0x7362);
+        const uint32_t t3 = __byte_perm(w[4 * g + 2], w[4 * g + 3], 0x7362);
+        w[4 * g + 0] = __byte_perm(t0, t1, 0x5410);
+        w[4 * g + 1] = __byte_perm(t0, t1, 0x7632);
+        w[4 * g + 2] = __byte_perm(t2, t3, 0x5410);
+        w[4 * g + 3] = __byte_perm(t2, t3, 0x7632);
       }
-      group_sync(group);
-      store_transposed_tile(sq, p.out_t, p.rows, p.cols, r0, c0, tid);
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj)
+        *reinterpret_cast<uint4*>(stt + sw128(jg * 4 + jj, ig * 16)) =
+            make_uint4(w[jj], w[4 + jj], w[8 + jj], w[12 + jj]);
+    }
+    fence_proxy_async_shared();
+    group_sync(group);
+    if (issuer) {
+      if (p.out != nullptr)
+        tma_store_2d(&tmQ, sqt, static_cast<int32_t>(c0), static_cast<int32_t>(r0));
+      if (kTrans)
+        tma_store_2d(&tmQT, stt, static_cast<int32_t>(r0), static_cast<int32_t>(c0));
+      bulk_commit_group();
     }
   }
+  if (issuer) bulk_wait_group<0>();  // stores done before the shared memory goes away
 }
 
 // ------------------------------------------------------------------ cluster single pass
@@ -525,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1) cast_cluster_kernel(const Cluster
   const int64_t ntiles = ((p.rows + kTR - 1) / kTR) * ntc;
   griddep_wait();
   uint4 v[kClusterTilesPerCta][8];
-  uint32_t acc = 0;
+  AbsMax a0, a1;
 #pragma unroll
   for (int k = 0; k < kClusterTilesPerCta; ++k) {
     const int64_t t = rank + static_cast<int64_t>(k) * nctas;
@@ -537,10 +605,11 @@ __global__ void __launch_bounds__(kThreads, 1) cast_cluster_kernel(const Cluster
       v[k][u] = (t < ntiles && row < p.rows && col < p.cols)
                     ? ld_stream_v4(p.x + row * p.ld + col)
                     : make_uint4(0, 0, 0, 0);
-      acc = vec_absmax(acc, v[k][u]);
+      (u & 1 ? a1 : a0).add(v[k][u]);
     }
   }
-  const uint32_t bits = block_absmax_bits(acc);
+  a0.merge(a1);
+  const uint32_t bits = block_absmax_bits(a0.packed());
   if (threadIdx.x == 0) s_max = bits;
   // A lone CTA (launched without a cluster) keeps to CTA-scope barriers.
   if (nctas > 1)
@@ -724,7 +793,7 @@ cudaError_t launch_cast(const CastArgs& a, const DeviceInfo& dev, cudaStream_t s
 
 namespace {
 constexpr size_t kSinglePassSmem =
-    static_cast<size_t>(kSinglePassTilesPerCta) * kTile * kTile * 2 + 128;  // + alignment slack
+    static_cast<size_t>(kSinglePassTilesPerCta) * kTile * kTile * 2 + 1024;  // + alignment slack
 
 // Opt the kernel into its shared memory and count its resident CTAs per SM,
 // once per device (the answers do not change; the calls cost host time).
@@ -833,7 +902,7 @@ cudaError_t launch_cast_single_pass(const SinglePassArgs& a, const DeviceInfo& d
   const bool trans = a.out_t != nullptr;
   int per_sm = 0;
   cudaError_t e;
-  void (*fn)(const CUtensorMap, const SinglePassParams);
+  void (*fn)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const SinglePassParams);
   if (a.fmt == 0) {
     e = trans ? single_pass_prepare<0, true>(&per_sm) : single_pass_prepare<0, false>(&per_sm);
     fn = trans ? cast_single_pass_kernel<0, true> : cast_single_pass_kernel<0, false>;
@@ -853,15 +922,34 @@ cudaError_t launch_cast_single_pass(const SinglePassArgs& a, const DeviceInfo& d
   // Spread the tiles over as many SMs as possible (fewer tiles per CTA).
   grid = ntiles < max_grid ? ntiles : max_grid;
   if (grid < 1) grid = 1;
-  CUtensorMap tm;
+  CUtensorMap tm, tq, tqt;
   if (!make_map_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, static_cast<uint64_t>(a.cols),
                    static_cast<uint64_t>(a.rows), static_cast<uint64_t>(a.ld) * 2, kTile, kTile,
                    CU_TENSOR_MAP_SWIZZLE_NONE)) {
     return map_failed("single-pass input map");
   }
+  // fp8 outputs: q [rows, cols] and q^T [cols, rows], dense, 128 x 128 boxes
+  // (maps of absent outputs are never used; they describe a valid dummy).
+  const void* qbase = a.out != nullptr ? static_cast<const void*>(a.out) : a.out_t;
+  if (!make_map_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, qbase,
+                   static_cast<uint64_t>(a.out != nullptr ? a.cols : a.rows),
+                   static_cast<uint64_t>(a.out != nullptr ? a.rows : a.cols),
+                   static_cast<uint64_t>(a.out != nullptr ? a.cols : a.rows), kTile, kTile,
+                   CU_TENSOR_MAP_SWIZZLE_128B)) {
+    return map_failed("single-pass output map");
+  }
+  if (trans) {
+    if (!make_map_2d(&tqt, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.out_t, static_cast<uint64_t>(a.rows),
+                     static_cast<uint64_t>(a.cols), static_cast<uint64_t>(a.rows), kTile, kTile,
+                     CU_TENSOR_MAP_SWIZZLE_128B)) {
+      return map_failed("single-pass transposed output map");
+    }
+  } else {
+    tqt = tq;
+  }
   set_error_site("single-pass cooperative launch");
   return launch_kernel(fn, dim3(static_cast<unsigned>(grid)), dim3(kSpThreads), kSinglePassSmem,
-                       stream, 1, true, tm, p);
+                       stream, 1, true, tm, tq, tqt, p);
 }
 
 }  // namespace fp8lin
