@@ -80,7 +80,7 @@ def load_traffic(kernel: str):
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    srcs = {"gemm": "gemm_tcgen05.cu", "cast": "cast_kernels.cu"}
+    srcs = {"gemm": "gemm_kernels.cuh", "cast": "cast_kernels.cuh"}  # device code only
     with open(os.path.join(ROOT, "quantised_gemm_gb300", "csrc", srcs[kernel]), "rb") as f:
         sha = hashlib.sha256(f.read()).hexdigest()[:16]
     with open(path) as f:
