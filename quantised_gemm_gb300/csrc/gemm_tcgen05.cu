@@ -72,40 +72,64 @@ bool make_map_out(CUtensorMap* map, const void* base, int64_t rows, int64_t cols
   return r == CUDA_SUCCESS;
 }
 
-// Number of K slices each tile runs as when `tiles` tiles of rows_per_tile x
-// bn are scheduled on `slots` persistent units (CTAs or pairs) with `num_kb`
-// K blocks each, given `split_bytes` of workspace for fp32 partials (1 = whole
-// tiles round-robin).  The K loop is split only when the tiles do not fill one
-// wave and the K loop is long: S = slots / tiles slices, reduced by the slices
-// together.  Splitting the partial last wave of a multi-wave grid (stream-K
-// style) was measured slower on the Linear's shapes than leaving it partial:
-// the extra epilogues and partial traffic cost more than the idle tail.
-int split_ways(int tiles, int slots, int num_kb, int rows_per_tile, int bn, size_t split_bytes) {
-  if (split_bytes == 0 || slots < 2 || tiles >= slots || num_kb < 16) return 1;
+// How the `tiles` tiles of rows_per_tile x bn, with `num_kb` K blocks each,
+// are dealt to `slots` persistent units (CTAs or pairs), given `split_bytes`
+// of workspace for fp32 partials: tiles [0, t_full) run whole, round-robin;
+// each tile after them runs as `ways` K slices that the slices reduce
+// together (see epilogue_unit).
+//   Few tiles (fewer than slots) with a K loop of at least 16 blocks: every
+//   tile is split, ways = slots / tiles, so the work runs on all slots.
+//   Several waves with a long K loop (at least kTailSplitMinKb blocks) and a
+//   last wave at most half full: the whole waves run whole and only the r
+//   tiles of the last wave are split, ways = slots / r, so the last round
+//   takes a fraction of a tile instead of a whole one (e.g. the dW product
+//   of a 65536-token step: 256 tiles on 76 pairs, r = 28, ways = 2).  With a
+//   short K loop the partials' traffic and the extra reductions cost more
+//   than the idle tail, as measured on 4096 x 4096 x 4096 products.
+struct SplitPlan {
+  int t_full, ways;
+};
+
+constexpr int kTailSplitMinKb = 96;
+
+SplitPlan plan_split(int tiles, int slots, int num_kb, int rows_per_tile, int bn,
+                     size_t split_bytes) {
+  const SplitPlan whole = {tiles, 1};
+  if (split_bytes == 0 || slots < 2 || tiles < 1) return whole;
+  int r, t_full;
+  if (tiles < slots) {
+    if (num_kb < 16) return whole;
+    r = tiles;
+    t_full = 0;
+  } else {
+    r = tiles % slots;
+    if (r == 0 || 2 * r > slots || num_kb < kTailSplitMinKb) return whole;
+    t_full = tiles - r;
+  }
   const size_t groups = static_cast<size_t>(rows_per_tile) / 32 * (bn >= 64 ? 2 : 1);
   const size_t tile_bytes = static_cast<size_t>(rows_per_tile) * bn * sizeof(float);
-  int s = slots / tiles;
+  int s = slots / r;
   if (s > kMaxSplit) s = kMaxSplit;
   if (s > num_kb) s = num_kb;
-  if (s < 2) return 1;
+  if (s < 2) return whole;
   const int per = (num_kb + s - 1) / s;
   s = (num_kb + per - 1) / per;  // no empty slice
-  if (s < 2) return 1;
-  const size_t need_tickets = 2 * static_cast<size_t>(tiles) * groups;
-  if (static_cast<size_t>(tiles) * s * tile_bytes > split_bytes || need_tickets > kWsTickets)
-    return 1;
-  return s;
+  if (s < 2) return whole;
+  const size_t need_tickets = 2 * static_cast<size_t>(r) * groups;
+  if (static_cast<size_t>(r) * s * tile_bytes > split_bytes || need_tickets > kWsTickets)
+    return whole;
+  return {t_full, s};
 }
 
 void plan_schedule(GemmParams& p, int tiles, int slots, int num_kb, int rows_per_tile, int bn,
                    const GemmArgs& g) {
   const bool can_split = g.ws_split != nullptr && g.ws_tickets != nullptr;
-  const int s =
-      split_ways(tiles, slots, num_kb, rows_per_tile, bn, can_split ? g.ws_split_bytes : 0);
-  p.t_full = s > 1 ? 0 : tiles;
-  p.s_tail = s;
-  p.partials = s > 1 ? g.ws_split : nullptr;
-  p.tickets = s > 1 ? g.ws_tickets : nullptr;
+  const SplitPlan sp =
+      plan_split(tiles, slots, num_kb, rows_per_tile, bn, can_split ? g.ws_split_bytes : 0);
+  p.t_full = sp.t_full;
+  p.s_tail = sp.ways;
+  p.partials = sp.ways > 1 ? g.ws_split : nullptr;
+  p.tickets = sp.ways > 1 ? g.ws_tickets : nullptr;
 }
 
 // One-time per-device set-up of a kernel's shared-memory limit (and, for the
@@ -330,12 +354,16 @@ cudaError_t describe_gemm(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev
   const int64_t tiles64 = ((tm + rows - 1) / rows) * ((tn + bn - 1) / bn);
   const int tiles = tiles64 > (1 << 30) ? (1 << 30) : static_cast<int>(tiles64);
   const int num_kb = static_cast<int>((K + kBK - 1) / kBK);
-  const int ways =
-      split_ways(tiles, slots, num_kb, rows, bn, gemm_split_workspace_bytes(dev.num_sms));
-  const int units = ways > 1 ? tiles * ways : tiles;
+  const SplitPlan sp =
+      plan_split(tiles, slots, num_kb, rows, bn, gemm_split_workspace_bytes(dev.num_sms));
+  const int units = sp.t_full + (tiles - sp.t_full) * sp.ways;
   const int used = units < slots ? units : slots;
-  char sched[32] = "whole tiles";
-  if (ways > 1) std::snprintf(sched, sizeof(sched), "K split %d ways", ways);
+  char sched[64] = "whole tiles";
+  if (sp.ways > 1 && sp.t_full == 0)
+    std::snprintf(sched, sizeof(sched), "K split %d ways", sp.ways);
+  else if (sp.ways > 1)
+    std::snprintf(sched, sizeof(sched), "last %d tiles K split %d ways", tiles - sp.t_full,
+                  sp.ways);
   std::snprintf(buf, len, "%s: %s%dx%d tiles, %d tiles on %d of %d %s, %s", name,
                 is_swap(v) ? "swap-AB (D^T = B.A^T), " : "", rows, bn, tiles, used, slots,
                 rows == 2 * kBM ? "CTA pairs" : "CTAs", sched);

@@ -155,6 +155,8 @@ def test_gemm_without_split_workspace_matches(ws):
     ((96, 128, 512), "gemm_fp8_kernel<128, 6, 0>", "whole tiles"),
     ((384, 1600, 1600), "gemm_fp8_pair_kernel<256, 6>", "whole tiles"),
     ((512, 128, 1024), "gemm_fp8_pair_kernel<128, 8>", "whole tiles"),
+    ((4096, 4096, 65536), "gemm_fp8_pair_kernel<256, 6>", "last 28 tiles K split 2 ways"),
+    ((4096, 4096, 4096), "gemm_fp8_pair_kernel<256, 6>", "whole tiles"),
     ((4096, 4096, 1024), "gemm_fp8_pair_kernel<256, 6>", "whole tiles"),
 ])
 def test_gemm_describe_names_the_launched_kernel(mnk, kernel, sched, ws):
@@ -265,4 +267,25 @@ def test_gemm_random_shapes_match_oracle(mnk, ws):
     q.check(ws)
     y, s = oracle.gemm(a8, b8, fa, E4M3, sa, sb)
     assert_within_bound(bf16_to_f64(d), y, s, "%s %s" % (mnk, q.gemm_describe(M, N, K)))
+    assert dev_f32_bits(amax) == f32_bits(oracle.amax(_bf16_bits(d)))
+
+
+def test_gemm_split_tail_of_several_waves_matches_oracle(ws):
+    """A long K loop over several waves: the tiles of the last, partly filled
+    wave run as K slices (80 pair tiles on 76 pairs: the last 4 split 8
+    ways); the result meets the bound and its amax is exact."""
+    M, N, K = 512, 10240, 12288
+    assert q.gemm_describe(M, N, K).endswith("last 4 tiles K split 8 ways"), \
+        q.gemm_describe(M, N, K)
+    a8, sa, inva = _operand(M, K, E5M2, seed=91)
+    b8, sb, invb = _operand(N, K, E4M3, seed=92)
+    d = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    amax = torch.full((1,), -1.0, device="cuda")
+    a, b = torch.from_numpy(a8).cuda(), torch.from_numpy(b8).cuda()
+    ia, ib = torch.tensor([inva], device="cuda"), torch.tensor([invb], device="cuda")
+    for _ in range(2):          # the second call checks that the tickets cleaned up
+        q.gemm(a, b, E5M2, E4M3, ia, ib, d, ws, amax_out=amax)
+        q.check(ws)
+    y, s = oracle.gemm(a8, b8, E5M2, E4M3, sa, sb)
+    assert_within_bound(bf16_to_f64(d), y, s, "tail split")
     assert dev_f32_bits(amax) == f32_bits(oracle.amax(_bf16_bits(d)))
