@@ -139,21 +139,25 @@ constexpr size_t kSinglePassSmem =
 template <int kFmt, bool kTrans>
 cudaError_t single_pass_prepare(int* ctas_per_sm) {
   static std::mutex mu;
-  static int ready_device = -1;
-  static int per_sm = 0;
+  static int per_sm[64] = {};  // 0: not prepared yet on that device
   int d = 0;
   cudaError_t e = cudaGetDevice(&d);
   if (e != cudaSuccess) return e;
+  if (d < 0 || d >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
-  if (ready_device != d) {
+  if (per_sm[d] == 0) {
     auto k = cast_single_pass_kernel<kFmt, kTrans>;
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSinglePassSmem));
     if (e != cudaSuccess) return e;
-    per_sm = resident_ctas(k, kSpThreads, kSinglePassSmem);
-    ready_device = d;
+    const int n = resident_ctas(k, kSpThreads, kSinglePassSmem);
+    if (n < 1) {
+      *ctas_per_sm = 0;  // cannot run here; not cached, the caller falls back
+      return cudaSuccess;
+    }
+    per_sm[d] = n;
   }
-  *ctas_per_sm = per_sm;
+  *ctas_per_sm = per_sm[d];
   return cudaSuccess;
 }
 }  // namespace

@@ -133,15 +133,22 @@ void plan_schedule(GemmParams& p, int tiles, int slots, int num_kb, int rows_per
 }
 
 // One-time per-device set-up of a kernel's shared-memory limit (and, for the
-// pair kernel, the number of co-resident clusters of 2 it gets).
+// pair kernel, the number of co-resident clusters of 2 it gets), kept per
+// device and guarded, so concurrent first calls from several host threads or
+// alternating devices are safe.
+constexpr int kMaxDevices = 64;
+
 template <int BN, int STAGES, bool kTransStore>
 cudaError_t one_cta_setup(const DeviceInfo& dev) {
-  static int configured_device = -1;
-  if (configured_device == dev.device) return cudaSuccess;
+  static std::mutex mu;
+  static bool done[kMaxDevices] = {};
+  if (dev.device < 0 || dev.device >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev.device]) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(gemm_fp8_kernel<BN, STAGES, kTransStore>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(Cfg<BN, STAGES>::kSmemBytes));
-  if (e == cudaSuccess) configured_device = dev.device;
+  if (e == cudaSuccess) done[dev.device] = true;
   return e;
 }
 
@@ -149,9 +156,11 @@ template <int BN, int STAGES>
 cudaError_t pair_setup(const DeviceInfo& dev, int* slots) {
   using C = PairCfg<BN, STAGES>;
   auto kernel = gemm_fp8_pair_kernel<BN, STAGES>;
-  static int configured_device = -1;
-  static int max_pairs = 0;
-  if (configured_device != dev.device) {
+  static std::mutex mu;
+  static int max_pairs[kMaxDevices] = {};
+  if (dev.device < 0 || dev.device >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (max_pairs[dev.device] == 0) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(C::kSmemBytes));
     if (e != cudaSuccess) return e;
@@ -171,10 +180,9 @@ cudaError_t pair_setup(const DeviceInfo& dev, int* slots) {
       cudaGetLastError();
       n = dev.num_sms / 2;
     }
-    max_pairs = n;
-    configured_device = dev.device;
+    max_pairs[dev.device] = n;
   }
-  *slots = max_pairs;
+  *slots = max_pairs[dev.device];
   return cudaSuccess;
 }
 
