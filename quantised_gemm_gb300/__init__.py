@@ -48,8 +48,13 @@ def library():
     return _lib.load()
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream=None) -> int:
     if stream is None:
+        if _raw_stream is not None:   # the current stream's handle, without a Stream object
+            return _raw_stream(torch.cuda.current_device())
         stream = torch.cuda.current_stream()
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 

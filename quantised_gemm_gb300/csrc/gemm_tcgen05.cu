@@ -39,37 +39,75 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// Every 2-D tiled map of the library goes through here.  Encoding is a pure
+// function of its arguments, and a training loop encodes the same few maps
+// over and over (its buffers do not move), so each host thread keeps the
+// last kMapCache encodings and reuses one whose arguments all match.
+struct MapKey {
+  const void* base;
+  uint64_t inner, rows, stride;
+  uint32_t box_inner, box_rows;
+  int dtype, swizzle, promo;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && inner == o.inner && rows == o.rows && stride == o.stride &&
+           box_inner == o.box_inner && box_rows == o.box_rows && dtype == o.dtype &&
+           swizzle == o.swizzle && promo == o.promo;
+  }
+};
+
+constexpr int kMapCache = 64;
+struct MapCache {
+  MapKey key[kMapCache];
+  CUtensorMap map[kMapCache];
+  int used = 0, next = 0;
+};
+thread_local MapCache g_map_cache;
+
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
+               uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,
+               CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promo) {
+  const MapKey k = {base, inner, rows, row_stride_bytes, box_inner, box_rows,
+                    static_cast<int>(dtype), static_cast<int>(swizzle), static_cast<int>(promo)};
+  MapCache& c = g_map_cache;
+  for (int i = 0; i < c.used; ++i) {
+    if (c.key[i] == k) {
+      *map = c.map[i];
+      return true;
+    }
+  }
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_stride_bytes)};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  g_last_encode_result = r;
+  if (r != CUDA_SUCCESS) return false;
+  const int slot = c.used < kMapCache ? c.used++ : c.next;
+  if (slot == c.next) c.next = (c.next + 1) % kMapCache;
+  c.key[slot] = k;
+  c.map[slot] = *map;
+  return true;
+}
+
 // 2-D map over an 8-bit [rows, k] matrix (row stride ld bytes), box
 // [box_rows, 128 bytes], 128-byte swizzle, zero fill outside the matrix.
 bool make_map_k_major(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t k, int64_t ld,
                       int box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  g_last_encode_result = r;
-  return r == CUDA_SUCCESS;
+  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, static_cast<uint64_t>(k),
+                   static_cast<uint64_t>(rows), static_cast<uint64_t>(ld), kBK,
+                   static_cast<uint32_t>(box_rows), CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
 // 2-D map over the bf16 output [rows, cols] (row stride ldd elements), box
 // 32 x 32, 64-byte swizzle, for the epilogue's TMA stores.
 bool make_map_out(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ldd) {
-  EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldd) * 2};
-  cuuint32_t box[2] = {32, 32};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  g_last_encode_result = r;
-  return r == CUDA_SUCCESS;
+  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, static_cast<uint64_t>(cols),
+                   static_cast<uint64_t>(rows), static_cast<uint64_t>(ldd) * 2, 32, 32,
+                   CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
 }
 
 // How the `tiles` tiles of rows_per_tile x bn, with `num_kb` K blocks each,
@@ -243,17 +281,8 @@ cudaError_t map_failed(const char* what) {
 bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
                  uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,
                  CUtensorMapSwizzle swizzle) {
-  EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_stride_bytes)};
-  cuuint32_t box[2] = {box_inner, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  g_last_encode_result = r;
-  return r == CUDA_SUCCESS;
+  return encode_2d(map, dtype, base, inner, rows, row_stride_bytes, box_inner, box_rows, swizzle,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
 size_t gemm_split_workspace_bytes(int num_sms) {
