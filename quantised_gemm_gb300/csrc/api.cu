@@ -216,6 +216,7 @@ fp8lin_status cast_dynamic_scaled(const void* x, int64_t rows, int64_t cols, int
   c.out = out;
   c.out_t = out_t;
   c.amax_rec = nullptr;
+  c.err = ws_error(ws);
   return do_cast(c, dev, stream);
 }
 
@@ -255,6 +256,7 @@ fp8lin_status delayed_cast(const void* x, int64_t rows, int64_t cols, int64_t ld
   c.amax_rec = reinterpret_cast<uint32_t*>(st->amax);
   c.rec_acc = ws_u32(ws, kWsAtomicAccOffset);
   c.rec_ticket = ws_u32(ws, kWsAtomicTicketOffset);
+  c.err = ws_error(ws);
   return do_cast(c, dev, stream);
 }
 

@@ -100,6 +100,69 @@ cudaError_t launch_scale(const float* amax, float* scale, float* inv, float* rin
                        head, history_len, delayed ? 1 : 0, F, eps);
 }
 
+namespace {
+
+template <int kFmt, bool kTrans>
+cudaError_t stream_prepare(int device) {
+  static std::mutex mu;
+  static bool done[64] = {};
+  if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[device]) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(cast_stream_kernel<kFmt, kTrans>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kStreamSmem));
+  if (e == cudaSuccess) done[device] = true;
+  return e;
+}
+
+// The TMA streaming cast: one persistent CTA per SM over the tiles.
+cudaError_t launch_cast_stream(const CastParams& p, const CastArgs& a, const DeviceInfo& dev,
+                               cudaStream_t stream) {
+  const bool trans = a.out_t != nullptr;
+  CUtensorMap tx, tq, tqt;
+  if (!make_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, static_cast<uint64_t>(a.cols),
+                   static_cast<uint64_t>(a.rows), static_cast<uint64_t>(a.ld) * 2, kTile, kTile,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+    return map_failed("streaming cast input map");
+  // q [rows, cols] and q^T [cols, rows]; the map of an absent output is a
+  // valid copy of the other and is never used.
+  const bool has_q = a.out != nullptr;
+  if (!make_map_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, has_q ? static_cast<const void*>(a.out)
+                                                             : a.out_t,
+                   static_cast<uint64_t>(has_q ? a.cols : a.rows),
+                   static_cast<uint64_t>(has_q ? a.rows : a.cols),
+                   static_cast<uint64_t>(has_q ? a.cols : a.rows), kTile, kTile,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+    return map_failed("streaming cast output map");
+  if (trans) {
+    if (!make_map_2d(&tqt, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.out_t, static_cast<uint64_t>(a.rows),
+                     static_cast<uint64_t>(a.cols), static_cast<uint64_t>(a.rows), kTile, kTile,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+      return map_failed("streaming cast transposed output map");
+  } else {
+    tqt = tq;
+  }
+  const int64_t ntiles = ((a.rows + kTile - 1) / kTile) * ((a.cols + kTile - 1) / kTile);
+  const unsigned grid =
+      static_cast<unsigned>(ntiles < dev.num_sms ? ntiles : static_cast<int64_t>(dev.num_sms));
+  void (*fn)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CastParams);
+  cudaError_t e;
+  if (a.fmt == 0) {
+    e = trans ? stream_prepare<0, true>(dev.device) : stream_prepare<0, false>(dev.device);
+    fn = trans ? cast_stream_kernel<0, true> : cast_stream_kernel<0, false>;
+  } else {
+    e = trans ? stream_prepare<1, true>(dev.device) : stream_prepare<1, false>(dev.device);
+    fn = trans ? cast_stream_kernel<1, true> : cast_stream_kernel<1, false>;
+  }
+  if (e != cudaSuccess) return e;
+  set_error_site("streaming cast launch");
+  return launch_kernel(fn, dim3(grid), dim3(kStreamThreads), kStreamSmem, stream, 1, false, tx,
+                       tq, tqt, p);
+}
+
+}  // namespace
+
 cudaError_t launch_cast(const CastArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
   CastParams p;
   p.x = a.x;
@@ -117,6 +180,10 @@ cudaError_t launch_cast(const CastArgs& a, const DeviceInfo& dev, cudaStream_t s
   p.amax_rec = a.amax_rec;
   p.rec_acc = a.rec_acc;
   p.rec_ticket = a.rec_ticket;
+  p.err = a.err;
+  // With a workspace error word (forward, backward, cast_dynamic) the TMA
+  // streaming kernel runs; the bare fp8lin_cast keeps the per-thread kernel.
+  if (a.err != nullptr) return launch_cast_stream(p, a, dev, stream);
   const int64_t ntiles = ((a.rows + kTile - 1) / kTile) * ((a.cols + kTile - 1) / kTile);
   int64_t grid = static_cast<int64_t>(dev.num_sms) * 4;
   if (ntiles < grid) grid = ntiles;

@@ -252,6 +252,7 @@ struct CastParams {
   uint32_t* amax_rec;
   uint32_t* rec_acc;     // non-null: ticketed recording through the workspace
   uint32_t* rec_ticket;
+  int* err;              // workspace error word (streaming kernel; may be null)
 };
 
 template <int kFmt, bool kTrans>
@@ -313,6 +314,225 @@ __global__ void __launch_bounds__(kThreads, 4) cast_kernel(const CastParams p) {
   }
 }
 
+// ------------------------------------------------------------------ streaming cast (TMA)
+//
+// The same cast (+ transpose, optional amax record) as cast_kernel, with the
+// data moved by TMA: one persistent CTA per SM, a producer lane that loads
+// 128 x 128 bf16 tiles into a kStreamStages-deep ring, and eight consumer
+// warps that cast a tile from shared memory, stage the fp8 tile and its
+// transpose in the 128-byte TMA swizzle (double-buffered across tiles) and
+// write both with TMA bulk stores.  No thread issues a global load or store
+// of its own.
+constexpr int kStreamStages = 3;
+constexpr int kStreamConsumers = 256;
+constexpr int kStreamThreads = 32 + kStreamConsumers;
+constexpr int kTileBytesBf16 = kTile * kTile * 2;
+constexpr size_t kStreamSmem = 1024 + static_cast<size_t>(kStreamStages) * kTileBytesBf16 +
+                               2 * static_cast<size_t>(kTileBytesBf16) + 256;
+
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"r"(kStreamConsumers) : "memory");
+}
+
+// Barrier of the consumer warps that also returns, to every one of them, the
+// OR of `bad` over all of them: one decision for the whole group.
+__device__ __forceinline__ bool consumer_sync_or(bool bad) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.or.pred po, 1, %2, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"(bad ? 1u : 0u), "r"(kStreamConsumers)
+      : "memory");
+  return r != 0;
+}
+
+// Offset of byte `col` (0..127) of row `row` in a 128 x 128-byte fp8 tile
+// laid out as the 128-byte TMA swizzle expects: 16-byte chunk c of row r is
+// stored at chunk c ^ (r & 7).
+__device__ __forceinline__ int sw128(int row, int col) {
+  return row * 128 + ((((col >> 4) ^ (row & 7))) << 4) + (col & 15);
+}
+
+// Cast 8 vectors per thread (this thread's share of a 128 x 128 bf16 tile in
+// shared memory, 256 threads) into the swizzled fp8 tile `sqt` and, with
+// kTrans, its transpose `stt`.  `sync` separates the writes of `sqt` from
+// the reads of it for the transpose.
+template <int kTrans, typename Sync>
+__device__ __forceinline__ void stage_tile_fp8(const uint2 (&q)[8], uint8_t* sqt, uint8_t* stt,
+                                               int tid, Sync sync) {
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int vi = tid + 256 * u;
+    *reinterpret_cast<uint2*>(sqt + sw128(vi >> 4, (vi & 15) * 8)) = q[u];
+  }
+  if (kTrans) {
+    sync();
+    // Each thread moves a 16-row x 4-column block: 16 words down a column
+    // group of the tile, 4x4 byte transposes, four 16-byte rows of the
+    // transpose.
+    const int lane = tid & 31, warp = tid >> 5;
+    const int jg = (warp & 1) * 16 + (lane >> 1);  // 4-column group 0..31
+    const int ig = (warp >> 1) * 2 + (lane & 1);   // 16-row group 0..7
+    uint32_t w[16];
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk)
+      w[kk] = *reinterpret_cast<const uint32_t*>(sqt + sw128(ig * 16 + kk, jg * 4));
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const uint32_t t0 = __byte_perm(w[4 * g + 0], w[4 * g + 1], 0x5140);
+      const uint32_t t1 = __byte_perm(w[4 * g + 2], w[4 * g + 3], 0x5140);
+      const uint32_t t2 = __byte_perm(w[4 * g + 0], w[4 * g + 1], 0x7362);
+      const uint32_t t3 = __byte_perm(w[4 * g + 2], w[4 * g + 3], 0x7362);
+      w[4 * g + 0] = __byte_perm(t0, t1, 0x5410);
+      w[4 * g + 1] = __byte_perm(t0, t1, 0x7632);
+      w[4 * g + 2] = __byte_perm(t2, t3, 0x5410);
+      w[4 * g + 3] = __byte_perm(t2, t3, 0x7632);
+    }
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj)
+      *reinterpret_cast<uint4*>(stt + sw128(jg * 4 + jj, ig * 16)) =
+          make_uint4(w[jj], w[4 + jj], w[8 + jj], w[12 + jj]);
+  }
+}
+
+template <int kFmt, bool kTrans>
+__global__ void __launch_bounds__(kStreamThreads, 1)
+    cast_stream_kernel(const __grid_constant__ CUtensorMap tmX,
+                       const __grid_constant__ CUtensorMap tmQ,
+                       const __grid_constant__ CUtensorMap tmQT, const CastParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* in = base;                                      // kStreamStages bf16 tiles
+  uint8_t* outb = base + kStreamStages * kTileBytesBf16;   // 2 x (fp8 tile | transpose)
+  uint64_t* full = reinterpret_cast<uint64_t*>(outb + 2 * kTileBytesBf16);
+  uint64_t* empty = full + kStreamStages;
+  __shared__ int s_abort;
+  __shared__ uint32_t s_red[kStreamConsumers / 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t ntc = (p.cols + kTile - 1) / kTile;
+  const int64_t ntiles = ((p.rows + kTile - 1) / kTile) * ntc;
+  const int64_t mine = blockIdx.x < ntiles ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < kStreamStages; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], 1);
+    }
+    s_abort = 0;
+    fence_barrier_init();
+    tma_prefetch_map(&tmX);
+    if (p.out != nullptr) tma_prefetch_map(&tmQ);
+    if (kTrans) tma_prefetch_map(&tmQT);
+  }
+  __syncthreads();
+  griddep_wait();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t fills[kStreamStages] = {};
+      bool ok = true;
+      for (int64_t i = 0; i < mine; ++i) {
+        const int st = static_cast<int>(i % kStreamStages);
+        const uint32_t ph = static_cast<uint32_t>((i / kStreamStages) & 1);
+        if (!mbar_wait_bounded(&empty[st], ph ^ 1u, &s_abort)) {
+          ok = false;
+          break;
+        }
+        const int64_t t = blockIdx.x + i * gridDim.x;
+        mbar_arrive_expect_tx(&full[st], kTileBytesBf16);
+        tma_load_2d(in + st * kTileBytesBf16, &tmX, &full[st],
+                    static_cast<int32_t>((t % ntc) * kTile), static_cast<int32_t>((t / ntc) * kTile));
+        ++fills[st];
+      }
+      if (!ok) {
+        if (p.err != nullptr) atomicCAS(p.err, 0, kErrCastWait);
+        s_abort = 1;
+      }
+      if (!ok || s_abort) {
+        // Let this lane's copies in flight land before the CTA exits.
+        volatile int never = 0;
+        for (int st = 0; st < kStreamStages; ++st)
+          if (fills[st] > 0) mbar_wait_bounded(&full[st], (fills[st] - 1) & 1u, &never);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int ctid = threadIdx.x - 32;
+  const bool issuer = ctid == 0;
+  float s;
+  if (p.derive_scale) {
+    s = scale_from_amax(*p.amax_in, p.eps, fp8_max<kFmt>());
+    if (blockIdx.x == 0 && issuer) {
+      *p.scale_out = s;
+      *p.inv_out = __fdiv_rn(1.0f, s);
+    }
+  } else {
+    s = *p.scale_in;
+  }
+  uint32_t acc = 0;
+  for (int64_t i = 0; i < mine; ++i) {
+    const int st = static_cast<int>(i % kStreamStages);
+    const uint32_t ph = static_cast<uint32_t>((i / kStreamStages) & 1);
+    const int o = static_cast<int>(i & 1);
+    const int64_t t = blockIdx.x + i * gridDim.x;
+    const int64_t r0 = (t / ntc) * kTile, c0 = (t % ntc) * kTile;
+    const bool ready = mbar_wait_bounded(&full[st], ph, &s_abort);
+    // One decision for all consumers, whatever each one's wait returned.
+    if (consumer_sync_or(!ready)) {
+      if (issuer && p.err != nullptr) atomicCAS(p.err, 0, kErrCastWait);
+      s_abort = 1;  // the producer stops refilling and drains its copies
+      break;
+    }
+    if (issuer && i >= 2) bulk_wait_group_read<1>();  // output buffer o has been read
+    uint2 q[8];
+    const uint8_t* buf = in + st * kTileBytesBf16;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int vi = ctid + 256 * u;
+      const uint4 v = *reinterpret_cast<const uint4*>(buf + (vi >> 4) * (kTile * 2) +
+                                                      (vi & 15) * 16);
+      if (p.amax_rec != nullptr) acc = vec_absmax(acc, v);
+      q[u] = cast8<kFmt>(v, s);
+    }
+    consumer_sync();  // the stage is read; output buffer o is free
+    if (issuer) mbar_arrive(&empty[st]);
+    uint8_t* sqt = outb + o * kTileBytesBf16;
+    stage_tile_fp8<kTrans>(q, sqt, sqt + kTile * kTile, ctid, consumer_sync);
+    fence_proxy_async_shared();
+    consumer_sync();
+    if (issuer) {
+      if (p.out != nullptr)
+        tma_store_2d(&tmQ, sqt, static_cast<int32_t>(c0), static_cast<int32_t>(r0));
+      if (kTrans)
+        tma_store_2d(&tmQT, sqt + kTile * kTile, static_cast<int32_t>(r0),
+                     static_cast<int32_t>(c0));
+      bulk_commit_group();
+    }
+  }
+  griddep_launch_dependents();
+  if (issuer) bulk_wait_group<0>();  // stores done before the shared memory goes away
+  if (p.amax_rec != nullptr) {
+    uint32_t m = max(acc & 0xFFFFu, acc >> 16);
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if (lane == 0) s_red[ctid >> 5] = m;
+    consumer_sync();
+    if (issuer) {
+      for (int w = 1; w < kStreamConsumers / 32; ++w) m = max(m, s_red[w]);
+      if (p.rec_ticket != nullptr)
+        ticketed_max(m << 16, p.rec_acc, p.rec_ticket, p.amax_rec, gridDim.x);
+      else
+        atomicMax(p.amax_rec, m << 16);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ single pass
 
 struct SinglePassParams {
@@ -350,13 +570,6 @@ constexpr int kSpThreads = kSpGroups * kThreads;
 
 __device__ __forceinline__ void group_sync(int group) {
   asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(kThreads) : "memory");
-}
-
-// Offset of byte `col` (0..127) of row `row` in a 128 x 128-byte fp8 tile
-// laid out as the 128-byte TMA swizzle expects: 16-byte chunk c of row r is
-// stored at chunk c ^ (r & 7).
-__device__ __forceinline__ int sw128(int row, int col) {
-  return row * 128 + ((((col >> 4) ^ (row & 7))) << 4) + (col & 15);
 }
 
 template <int kFmt, bool kTrans>
@@ -474,39 +687,7 @@ __global__ void __launch_bounds__(kSpThreads, 1)
     group_sync(group);  // the group has read the whole bf16 tile
     uint8_t* sqt = buf;                       // fp8 tile [128 rows][128 bytes]
     uint8_t* stt = buf + kTile * kTile;       // its transpose
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int vi = tid + kThreads * u;
-      *reinterpret_cast<uint2*>(sqt + sw128(vi >> 4, (vi & 15) * 8)) = q[u];
-    }
-    if (kTrans) {
-      group_sync(group);
-      // Each thread moves a 16-row x 4-column block: 16 words down a column
-      // group of the tile, 4x4 byte transposes, four 16-byte rows of the
-      // transpose.
-      const int lane = tid & 31, warp = tid >> 5;
-      const int jg = (warp & 1) * 16 + (lane >> 1);  // 4-column group 0..31
-      const int ig = (warp >> 1) * 2 + (lane & 1);   // 16-row group 0..7
-      uint32_t w[16];
-#pragma unroll
-      for (int kk = 0; kk < 16; ++kk)
-        w[kk] = *reinterpret_cast<const uint32_t*>(sqt + sw128(ig * 16 + kk, jg * 4));
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const uint32_t t0 = __byte_perm(w[4 * g + 0], w[4 * g + 1], 0x5140);
-        const uint32_t t1 = __byte_perm(w[4 * g + 2], w[4 * g + 3], 0x5140);
-        const uint32_t t2 = __byte_perm(w[4 * g + 0], w[4 * g + 1], 0x7362);
-        const uint32_t t3 = __byte_perm(w[4 * g + 2], w[4 * g + 3], 0x7362);
-        w[4 * g + 0] = __byte_perm(t0, t1, 0x5410);
-        w[4 * g + 1] = __byte_perm(t0, t1, 0x7632);
-        w[4 * g + 2] = __byte_perm(t2, t3, 0x5410);
-        w[4 * g + 3] = __byte_perm(t2, t3, 0x7632);
-      }
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj)
-        *reinterpret_cast<uint4*>(stt + sw128(jg * 4 + jj, ig * 16)) =
-            make_uint4(w[jj], w[4 + jj], w[8 + jj], w[12 + jj]);
-    }
+    stage_tile_fp8<kTrans>(q, sqt, stt, tid, [&] { group_sync(group); });
     fence_proxy_async_shared();
     group_sync(group);
     if (issuer) {

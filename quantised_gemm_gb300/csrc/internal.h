@@ -33,6 +33,7 @@ enum DeviceError : int {
   kErrGemmMmaWait = 2,
   kErrGemmEpilogueWait = 3,
   kErrGridBarrier = 4,
+  kErrCastWait = 5,          // a streaming cast's load ring wait ran out
 };
 
 // Name the operation a launcher failed in (reported by
@@ -134,6 +135,7 @@ struct CastArgs {
   uint32_t* amax_rec;
   uint32_t* rec_acc = nullptr;     // non-null: record through the self-cleaning
   uint32_t* rec_ticket = nullptr;  // workspace words instead of a pre-zeroed amax_rec
+  int* err = nullptr;              // workspace error word: use the TMA streaming kernel
 };
 cudaError_t launch_cast(const CastArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 

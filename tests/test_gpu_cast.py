@@ -276,3 +276,20 @@ def test_small_tensor_single_pass_kernel_choice(shape, kernel, ws):
     if not names:
         pytest.skip("the profiler recorded no kernels (no CUPTI activity on this host)")
     assert len(names) == 1 and kernel in names[0], names
+
+
+@pytest.mark.parametrize("algo", [q.AMAX_ATOMIC, q.AMAX_REDUCTION])
+@pytest.mark.parametrize("shape", [(1040, 1552), (4096, 4096), (272, 144)])
+def test_cast_dynamic_transpose_only(algo, shape, ws):
+    """A dynamic cast that asks only for the transposed copy (no q): the
+    streaming kernel stages q on chip for the transpose and stores q^T alone."""
+    x = _tensor(shape, seed=61)
+    a = oracle.amax(x)
+    s, inv = oracle.scale_dynamic(a, E5M2)
+    _, qtr, _ = oracle.cast(x, s, E5M2, transpose=True)
+    st = q.ScalingState(E5M2, q.DYNAMIC, amax_algo=algo)
+    out_t = torch.full(shape[::-1], 0xAA, dtype=torch.uint8, device="cuda")
+    q.cast_dynamic(to_dev_bf16(x), st, None, out_t, ws)
+    q.check(ws)
+    assert dev_f32_bits(st.scale) == f32_bits(s)
+    assert np.array_equal(out_t.cpu().numpy(), qtr)
