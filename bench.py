@@ -265,6 +265,65 @@ def linear_sweep_entry(q, torch, dev, name, steps, warmup, flush, use_graph=True
             "cuda_graph": use_graph}
 
 
+def library_gemm_entry(q, torch, dev, M, N, K, fmt_a, rounds=3, iters=10):
+    """The FP8 GEMM of this library against cuBLASLt's (torch._scaled_mm,
+    tensorwise scales) on the same operands: D[M,N] = A[M,K] B[N,K]^T, bf16
+    out.  Both read operands larger than L2.  The two alternate ABBA over
+    `rounds` rounds so clock drift under the power cap favours neither; the
+    medians are reported, with the largest |difference| of the two outputs
+    (the accumulation order may differ)."""
+    import statistics
+    fp8 = {0: torch.float8_e4m3fn, 1: torch.float8_e5m2}
+    g = torch.Generator(device=dev).manual_seed(7)
+    a = (torch.randn(M, K, device=dev, generator=g) * 4).to(fp8[fmt_a])
+    b = (torch.randn(N, K, device=dev, generator=g) * 4).to(torch.float8_e4m3fn)
+    one = torch.ones((), device=dev)
+    inv = torch.ones(1, device=dev)
+    d = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    ws = q.Workspace()
+
+    def lib():
+        return torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+
+    def ours():
+        q.gemm(a.view(torch.uint8), b.view(torch.uint8), fmt_a, 0, inv, inv, d, ws)
+
+    try:
+        ref = lib()
+    except Exception as e:  # a torch build without FP8 matmul for this GPU
+        return {"shape": [M, N, K], "unavailable": repr(e)[:200]}
+    ours()
+    torch.cuda.synchronize()
+    q.check(ws)
+    diff = (ref.float() - d.float()).abs().max().item()
+    del ref
+    s = torch.cuda.current_stream()
+
+    def timed(fn):
+        fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(iters):
+            fn()
+        e1.record(s)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / iters
+
+    tl, to = [], []
+    for _ in range(rounds):
+        tl.append(timed(lib))
+        to.append(timed(ours))
+        to.append(timed(ours))
+        tl.append(timed(lib))
+    fl = 2.0 * M * N * K
+    ml, mo = statistics.median(tl), statistics.median(to)
+    return {"shape": [M, N, K], "a": "e4m3" if fmt_a == 0 else "e5m2", "b": "e4m3",
+            "cublaslt_ms": round(ml, 4), "cublaslt_tflops": round(fl / (ml * 1e-3) / 1e12, 1),
+            "ours_ms": round(mo, 4), "ours_tflops": round(fl / (mo * 1e-3) / 1e12, 1),
+            "ours_over_cublaslt": round(ml / mo, 3), "max_abs_diff": diff,
+            "ours_kernel": q.gemm_describe(M, N, K)}
+
+
 def chain_sweep_entry(q, torch, dev, name, steps, warmup, flush, rounds=3):
     """Two Linears of a workload's shape in a chain (the second consumes the
     first's y, the first's grad_output is the second's dX), fwd+bwd of both,
@@ -610,7 +669,7 @@ def run_native(args):
     if not args.no_sweep:
         flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
         flush = lambda: flush_buf.zero_()  # noqa: E731
-        sweep = {"linears": [], "chains": None, "cast": None}
+        sweep = {"linears": [], "chains": None, "cast": None, "gemm_vs_cublaslt": None}
         for name in ("linear4096_m16", "linear4096_m256", "linear4096_m4096",
                      "gpt1.5b_linears_m12288", "llama3_8b_ffn_m8192"):
             small = si.WORKLOADS[name]["shapes"][0][0] <= 4096
@@ -626,6 +685,11 @@ def run_native(args):
         del flush_buf
         torch.cuda.empty_cache()
         sweep["cast"] = cast_sweep(q, torch, dev, peaks, args.full_sweep)
+        # the three products of the 65536-token step: y, dX (e5m2 A), dW (long K)
+        sweep["gemm_vs_cublaslt"] = [library_gemm_entry(q, torch, dev, 65536, 4096, 4096, 0),
+                                     library_gemm_entry(q, torch, dev, 65536, 4096, 4096, 1),
+                                     library_gemm_entry(q, torch, dev, 4096, 4096, 65536, 1)]
+        torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

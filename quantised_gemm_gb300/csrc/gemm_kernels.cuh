@@ -145,16 +145,17 @@ __device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, uint32_t (&r)[kC
 // TMA.  The box's rows are 64 bytes with 16-byte chunks swizzled as the
 // 64-byte TMA swizzle expects (chunk ^= (row >> 1) & 3), which also keeps the
 // warp's shared-memory writes free of bank conflicts.
+template <bool kTrack>
 __device__ __forceinline__ void store_chunk_tma(const uint32_t (&r)[32], float alpha, uint8_t* box,
                                                 const CUtensorMap* tmD, int row0, int col0,
-                                                int lane, bool track, float& vmax) {
+                                                int lane, float& vmax) {
   uint32_t w[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
-    const float v0 = __fmul_rn(__uint_as_float(r[2 * j]), alpha);
-    const float v1 = __fmul_rn(__uint_as_float(r[2 * j + 1]), alpha);
+    float v0, v1;
+    mul2_rn(r[2 * j], r[2 * j + 1], alpha, v0, v1);
     w[j] = cvt_bf16x2(v0, v1);
-    if (track) vmax = fmaxf(vmax, fmaxf(fabsf(v0), fabsf(v1)));
+    if constexpr (kTrack) vmax = fmaxf(vmax, fmaxf(fabsf(v0), fabsf(v1)));
   }
   if (lane == 0) bulk_wait_group_read<kBoxesPerWarp - 1>();  // this box's last store has read it
   __syncwarp();
@@ -187,8 +188,11 @@ __device__ __forceinline__ void emit_chunk(const uint32_t (&r)[kChunk], float al
   const bool track = p.amax_out != nullptr;
   if constexpr (!kTransStore) {
     static_assert(kChunk == 32, "TMA-store epilogue works on 32-column chunks");
-    store_chunk_tma(r, alpha, boxes + (chunk_no % kBoxesPerWarp) * kBoxBytes, tmD, row0, col0,
-                    lane, track, vmax);
+    uint8_t* box = boxes + (chunk_no % kBoxesPerWarp) * kBoxBytes;
+    if (track)  // warp-uniform; the untracked chunk carries no max at all
+      store_chunk_tma<true>(r, alpha, box, tmD, row0, col0, lane, vmax);
+    else
+      store_chunk_tma<false>(r, alpha, box, tmD, row0, col0, lane, vmax);
     ++chunk_no;
   } else {
     // kernel element (row, col) is output element (col, row)
@@ -627,6 +631,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 //   empty[s]     one per CTA; the MMA commit arrives on both (multicast);
 //   acc_full[a]  one per CTA; the MMA commit arrives on both (multicast);
 //   acc_empty[a] lives in the even CTA; all 8 epilogue warps arrive on it.
+// Every wait is a CTA-scope acquire, although peers arrive on full[] and
+// acc_empty[]: what a wait orders is carried by other means.  TMA data is
+// visible once the barrier's transaction count completes; MMA completion is
+// what the tcgen05.commit arrive signals; and TMEM reuse is ordered by the
+// tcgen05.fence before/after-thread-sync pair around the epilogue's release
+// arrive.  A cluster-scope acquire would add a memory fence to each wait.
 
 template <int BN, int STAGES>
 struct PairCfg {
@@ -705,7 +715,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int n = 0; ok && unit_at(pair, num_pairs, n, p, num_tiles, num_kb, u); ++n) {
         const int m_blk = u.tile / num_n, n_blk = u.tile % num_n;
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
-          if (!mbar_wait_cluster_bounded(&empty[stage], phase ^ 1u, abort_flag)) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
@@ -734,14 +744,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool issued = false;
       Unit u;
       for (int n = 0; ok && unit_at(pair, num_pairs, n, p, num_tiles, num_kb, u); ++n) {
-        if (!mbar_wait_cluster_bounded(&acc_empty[acc], acc_phase ^ 1u, abort_flag)) {
+        if (!mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
-          if (!mbar_wait_cluster_bounded(&full[stage], phase, abort_flag)) {
+          if (!mbar_wait_bounded(&full[stage], phase, abort_flag)) {
             ok = false;
             break;
           }
@@ -793,7 +803,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int n = 0; unit_at(pair, num_pairs, n, p, num_tiles, num_kb, u); ++n) {
       const int m_blk = u.tile / num_n, n_blk = u.tile % num_n;
       const bool ready = __all_sync(
-          0xFFFFFFFFu, mbar_wait_cluster_bounded(&acc_full[acc], acc_phase, abort_flag));
+          0xFFFFFFFFu, mbar_wait_bounded(&acc_full[acc], acc_phase, abort_flag));
       if (!ready) {
         if (lane == 0) record_error(p.err, abort_flag, kErrGemmEpilogueWait);
         break;

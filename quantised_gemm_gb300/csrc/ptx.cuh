@@ -74,6 +74,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
+// try_wait that may suspend the thread for up to `hint_ns` while the phase
+// is incomplete; the thread resumes as soon as the phase completes.
+__device__ __forceinline__ bool mbar_try_wait_for(uint64_t* bar, uint32_t parity,
+                                                  uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
+// Suspension asked for on each retry of a bounded wait.  Without it a retry
+// returns after a short system-defined time, and warps that wait a whole
+// GEMM tile (the epilogue) or a whole stage (the TMA producer) keep re-reading
+// the abort flag and the global timer: issue slots and power taken from the
+// warps that feed the tensor cores.
+constexpr uint32_t kSuspendHintNs = 50000;
+
 // Wait until the phase with parity `parity` of `bar` has completed.  Gives
 // up (returns false) after kWaitLimitNs, or as soon as *abort becomes
 // nonzero once the first try failed.
@@ -82,7 +104,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_for(bar, parity, kSuspendHintNs)) return true;
     if (*abort) return false;
     if (global_timer_ns() - t0 > kWaitLimitNs) return false;
   }
@@ -290,30 +312,6 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_saddr) {
                : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-// Bounded wait with cluster-scope acquire (barriers that a peer CTA arrives on).
-__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity,
-                                                          volatile int* abort) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if (*abort) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
-  }
-}
-
 // TMA load into this CTA's shared memory whose completion is counted on an
 // mbarrier that may live in the peer CTA of the pair (cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map,
@@ -381,6 +379,19 @@ __device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// Two round-to-nearest fp32 products in one packed instruction (each lane of
+// the pair rounds exactly as mul.rn.f32 does); returns the raw bits of the
+// products of (a0, a1) with (b, b).
+__device__ __forceinline__ void mul2_rn(uint32_t a0, uint32_t a1, float b, float& p0, float& p1) {
+  asm("{\n\t.reg .b64 a, s, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\t"
+      "mov.b64 s, {%4, %4};\n\t"
+      "mul.rn.f32x2 d, a, s;\n\t"
+      "mov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(p0), "=f"(p1)
+      : "r"(a0), "r"(a1), "f"(b));
 }
 
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t w) { return __uint_as_float(w << 16); }
