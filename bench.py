@@ -73,16 +73,25 @@ def load_peaks():
             "source": "fallback"}
 
 
+def device_code_sha(kernel: str) -> str:
+    """sha256[:16] of a kernel's device code: its own header and the PTX
+    helpers it inlines (the host-side launchers live in other files)."""
+    import hashlib
+    csrc = os.path.join(ROOT, "quantised_gemm_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in ({"gemm": "gemm_kernels.cuh", "cast": "cast_kernels.cuh"}[kernel], "ptx.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def load_traffic(kernel: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
     the current source of the kernel (else None)."""
-    import hashlib
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    srcs = {"gemm": "gemm_kernels.cuh", "cast": "cast_kernels.cuh"}  # device code only
-    with open(os.path.join(ROOT, "quantised_gemm_gb300", "csrc", srcs[kernel]), "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    sha = device_code_sha(kernel)
     with open(path) as f:
         for line in f:
             line = line.strip()
