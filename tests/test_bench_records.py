@@ -1,0 +1,50 @@
+"""bench.py's DRAM-traffic records, on CPU: a record counts only for the device
+code it was captured on, and its per-launch figure is the captured one scaled
+to the benchmark's launch."""
+import json
+import os
+import shutil
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _records():
+    with open(os.path.join(ROOT, "profiles", "dram_traffic.txt")) as f:
+        return [json.loads(line) for line in f if line.strip().startswith("{")]
+
+
+def test_records_are_internally_consistent():
+    recs = _records()
+    assert {r["kernel"] for r in recs} == {"gemm", "cast"}
+    for r in recs:
+        assert r["bytes_per_launch"] == pytest.approx(r["captured_bytes"] * r["scale"], rel=1e-3)
+        assert len(r["src_sha"]) == 16
+
+
+def test_record_applies_only_to_its_device_code(monkeypatch):
+    for kernel in ("gemm", "cast"):
+        rec = bench.load_traffic(kernel)
+        if rec is not None:  # a fresh record: keyed on exactly this code
+            assert rec["src_sha"] == bench.device_code_sha(kernel)
+        monkeypatch.setattr(bench, "device_code_sha", lambda k: "0" * 16)
+        assert bench.load_traffic(kernel) is None
+        monkeypatch.undo()
+
+
+def test_hash_covers_the_inlined_ptx_helpers(tmp_path, monkeypatch):
+    csrc = os.path.join(tmp_path, "quantised_gemm_gb300", "csrc")
+    os.makedirs(csrc)
+    for name in ("gemm_kernels.cuh", "cast_kernels.cuh", "ptx.cuh"):
+        shutil.copy(os.path.join(ROOT, "quantised_gemm_gb300", "csrc", name), csrc)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    before = {k: bench.device_code_sha(k) for k in ("gemm", "cast")}
+    assert before["gemm"] != before["cast"]
+    with open(os.path.join(csrc, "ptx.cuh"), "a") as f:
+        f.write("\n// edited\n")
+    after = {k: bench.device_code_sha(k) for k in ("gemm", "cast")}
+    assert all(after[k] != before[k] for k in before)
