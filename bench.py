@@ -733,9 +733,29 @@ def run_native(args):
 
 # ------------------------------------------------------------------ reference arm
 
+REF_BUDGET_S = 60.0
+
+
+def ref_sample_tokens(t16: float, t128: float, n_steps: int,
+                      budget_s: float = REF_BUDGET_S) -> int:
+    """Tokens per reference step: the largest multiple of 16 up to 128 for
+    which n_steps steps fit in budget_s, at least 16.  A step costs
+    a + b * tokens: the weight's amax and casts are the fixed part, so the
+    line through the probe times of 16 and 128 tokens gives the cost."""
+    b = max(0.0, (t128 - t16) / 112.0)
+    a = max(0.0, t16 - 16.0 * b)
+    for ms in range(128, 15, -16):
+        if (a + b * ms) * n_steps <= budget_s:
+            return ms
+    return 16
+
+
 def run_reference(args):
     """The oracle on host cores, same metric / unit / config, each step a
-    bounded sample of the workload (the first tokens of the Linear)."""
+    bounded sample of the workload (the first Ms tokens of the Linear).  It
+    runs exactly `warmup` untimed and `steps` timed steps; Ms (a multiple of
+    16, at most 128) is chosen from two untimed probe steps so that the whole
+    run takes about REF_BUDGET_S seconds where that is possible."""
     world, rank, _ = dist_info()
     if rank != 0:
         return
@@ -744,29 +764,39 @@ def run_reference(args):
     oracle.build()
     wl = si.WORKLOADS[args.workload]
     M, K, N = wl["shapes"][0]
-    Ms = 128
     w = si.weight(K, N, w_init=wl["w_init"], w_std=wl.get("w_std", 0.02))
-    x = si.normal_bf16((Ms, K), 1.0, 0, si.STREAM_X)
-    dy = si.normal_bf16((Ms, N), 1e-3, 0, si.STREAM_DY)
 
-    def step():
+    def sample(ms):
+        return (si.normal_bf16((ms, K), 1.0, 0, si.STREAM_X),
+                si.normal_bf16((ms, N), 1e-3, 0, si.STREAM_DY))
+
+    def step(x, dy):
         sx = oracle.scale_dynamic(oracle.amax(x), oracle.E4M3)[0]
         sw = oracle.scale_dynamic(oracle.amax(w), oracle.E4M3)[0]
         sd = oracle.scale_dynamic(oracle.amax(dy), oracle.E5M2)[0]
         oracle.linear_fwd_bwd(x, w, dy, sx, sw, sd)
 
-    for _ in range(max(1, min(args.warmup, 3))):
-        step()
-    steps = max(1, min(args.steps, 10))
+    steps, warmup = max(1, args.steps), max(0, args.warmup)
+    probe = {}
+    for ms in (16, 128):
+        x, dy = sample(ms)
+        t0 = time.perf_counter()
+        step(x, dy)
+        probe[ms] = time.perf_counter() - t0
+    Ms = ref_sample_tokens(probe[16], probe[128], steps + warmup)
+    if Ms != 128:
+        x, dy = sample(Ms)
+    for _ in range(warmup):
+        step(x, dy)
     t0 = time.perf_counter()
     for _ in range(steps):
-        step()
+        step(x, dy)
     dt = (time.perf_counter() - t0) / steps
     value = 6.0 * Ms * N * K / dt / 1e12
     sample = ("oracle fwd+bwd of the %dx%d Linear on the first %d of %d tokens per step" %
               (K, N, Ms, M))
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
-            "n_gpus": world, "steps": steps, "warmup": max(1, min(args.warmup, 3)),
+            "n_gpus": world, "steps": steps, "warmup": warmup,
             "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": "%s: Linear 4096->4096, M=%d tokens (sampled %d)" %

@@ -48,3 +48,13 @@ def test_hash_covers_the_inlined_ptx_helpers(tmp_path, monkeypatch):
         f.write("\n// edited\n")
     after = {k: bench.device_code_sha(k) for k in ("gemm", "cast")}
     assert all(after[k] != before[k] for k in before)
+
+
+def test_reference_sample_fits_the_budget():
+    # fixed 0.4 s (the weight's casts) + 1 ms per token
+    t = lambda ms: 0.4 + 0.001 * ms  # noqa: E731
+    assert bench.ref_sample_tokens(t(16), t(128), 10) == 128
+    assert bench.ref_sample_tokens(t(16), t(128), 100, budget_s=60.0) == 128  # 52.8 s
+    ms = bench.ref_sample_tokens(t(16), t(128), 120, budget_s=60.0)
+    assert ms == 96 and t(ms) * 120 <= 60.0 < t(ms + 16) * 120
+    assert bench.ref_sample_tokens(t(16), t(128), 410, budget_s=60.0) == 16  # fixed part alone overruns
