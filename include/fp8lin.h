@@ -262,6 +262,16 @@ fp8lin_status fp8lin_gemm(const uint8_t* a, const uint8_t* b, int64_t M, int64_t
  * without a usable device. */
 fp8lin_status fp8lin_gemm_describe(int64_t M, int64_t N, int64_t K, char* buf, size_t buf_len);
 
+/* The line fp8lin_gemm_describe writes, for a device of num_sms SMs that
+ * holds one GEMM CTA per SM (num_sms / 2 CTA pairs), as the kernels are
+ * sized for: the same kernel choice and the same K-split rules, computed on
+ * the host without touching a device (planning, and tests on a machine
+ * without a GPU).  On a GB300 (152 SMs) it matches fp8lin_gemm_describe.
+ * Returns FP8LIN_EINVAL for negative sizes, num_sms < 2 or a NULL / empty
+ * buffer. */
+fp8lin_status fp8lin_gemm_describe_for(int64_t M, int64_t N, int64_t K, int32_t num_sms,
+                                       char* buf, size_t buf_len);
+
 /* Forward of the Linear: amax/scale/cast of x ([M, K], e4m3, state sx) and
  * W ([N, K], e4m3, state sw), then y = x8 . W8^T * inv_x * inv_w (bf16
  * [M, N]).  Writes the fp8 copies x8 [M, K], x8t [K, M], w8 [N, K],

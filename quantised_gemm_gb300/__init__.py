@@ -35,7 +35,7 @@ __all__ = [
     "AMAX_PRECOMPUTED", "DYNAMIC",
     "DELAYED",
     "Fp8linError", "ScalingState", "Workspace", "amax", "amax_noalloc", "scale", "cast", "cast_dynamic", "gemm",
-    "gemm_describe",
+    "gemm_describe", "gemm_describe_for",
     "forward", "backward", "check", "workspace_bytes", "single_pass_max_elems", "launch_count",
     "profile_enable", "profile_collect", "Fp8Linear", "link_linears", "library", "Float8Linear",
     "Float8LinearConfig", "CastConfig", "convert_to_float8_training",
@@ -90,6 +90,15 @@ def gemm_describe(M: int, N: int, K: int) -> str:
     on the current device."""
     buf = ctypes.create_string_buffer(256)
     _lib.check(library().fp8lin_gemm_describe(M, N, K, buf, len(buf)), "fp8lin_gemm_describe")
+    return buf.value.decode()
+
+
+def gemm_describe_for(M: int, N: int, K: int, num_sms: int) -> str:
+    """gemm_describe() for a device of num_sms SMs holding one GEMM CTA per
+    SM, computed on the host: no GPU needed."""
+    buf = ctypes.create_string_buffer(256)
+    _lib.check(library().fp8lin_gemm_describe_for(M, N, K, num_sms, buf, len(buf)),
+               "fp8lin_gemm_describe_for")
     return buf.value.decode()
 
 

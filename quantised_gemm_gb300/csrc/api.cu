@@ -559,6 +559,14 @@ fp8lin_status fp8lin_gemm_describe(int64_t M, int64_t N, int64_t K, char* buf, s
   return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);
 }
 
+fp8lin_status fp8lin_gemm_describe_for(int64_t M, int64_t N, int64_t K, int32_t num_sms,
+                                       char* buf, size_t buf_len) {
+  if (M < 0 || N < 0 || K < 0 || num_sms < 2 || buf == nullptr || buf_len == 0)
+    return FP8LIN_EINVAL;
+  describe_plan(M, N, K, num_sms, num_sms / 2, buf, buf_len);
+  return FP8LIN_OK;
+}
+
 static fp8lin_status check_linear_sizes(int64_t M, int64_t K, int64_t N) {
   if (M < 0 || K < 0 || N < 0) return FP8LIN_EINVAL;
   if (M % 16 != 0 || K % 16 != 0 || N % 16 != 0) return FP8LIN_EUNSUPPORTED;

@@ -362,12 +362,11 @@ cudaError_t launch_gemm(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t s
   }
 }
 
-cudaError_t describe_gemm(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev, char* buf,
-                          size_t len) {
+void describe_plan(int64_t M, int64_t N, int64_t K, int num_sms, int pair_slots, char* buf,
+                   size_t len) {
   const Variant v = choose_variant(M, N);
   const char* name = "";
-  int rows = kBM, bn = 256, slots = dev.num_sms;
-  cudaError_t e = cudaSuccess;
+  int rows = kBM, bn = 256, slots = num_sms;
   switch (v) {
     case Variant::kSwap16: name = "gemm_fp8_kernel<16, 8, 1>"; bn = 16; break;
     case Variant::kSwap32: name = "gemm_fp8_kernel<32, 8, 1>"; bn = 32; break;
@@ -378,21 +377,20 @@ cudaError_t describe_gemm(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev
       name = "gemm_fp8_pair_kernel<128, 8>";
       bn = 128;
       rows = 2 * kBM;
-      e = pair_setup<128, 8>(dev, &slots);
+      slots = pair_slots;
       break;
     case Variant::kPair256:
       name = "gemm_fp8_pair_kernel<256, 6>";
       rows = 2 * kBM;
-      e = pair_setup<256, 6>(dev, &slots);
+      slots = pair_slots;
       break;
   }
-  if (e != cudaSuccess) return e;
   const int64_t tm = is_swap(v) ? N : M, tn = is_swap(v) ? M : N;  // as the kernel sees it
   const int64_t tiles64 = ((tm + rows - 1) / rows) * ((tn + bn - 1) / bn);
   const int tiles = tiles64 > (1 << 30) ? (1 << 30) : static_cast<int>(tiles64);
   const int num_kb = static_cast<int>((K + kBK - 1) / kBK);
   const SplitPlan sp =
-      plan_split(tiles, slots, num_kb, rows, bn, gemm_split_workspace_bytes(dev.num_sms));
+      plan_split(tiles, slots, num_kb, rows, bn, gemm_split_workspace_bytes(num_sms));
   const int units = sp.t_full + (tiles - sp.t_full) * sp.ways;
   const int used = units < slots ? units : slots;
   char sched[64] = "whole tiles";
@@ -404,6 +402,20 @@ cudaError_t describe_gemm(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev
   std::snprintf(buf, len, "%s: %s%dx%d tiles, %d tiles on %d of %d %s, %s", name,
                 is_swap(v) ? "swap-AB (D^T = B.A^T), " : "", rows, bn, tiles, used, slots,
                 rows == 2 * kBM ? "CTA pairs" : "CTAs", sched);
+}
+
+cudaError_t describe_gemm(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev, char* buf,
+                          size_t len) {
+  // The pair kernel's slots are the clusters of 2 the device holds at once.
+  int pair_slots = dev.num_sms / 2;
+  cudaError_t e = cudaSuccess;
+  switch (choose_variant(M, N)) {
+    case Variant::kPair128: e = pair_setup<128, 8>(dev, &pair_slots); break;
+    case Variant::kPair256: e = pair_setup<256, 6>(dev, &pair_slots); break;
+    default: break;
+  }
+  if (e != cudaSuccess) return e;
+  describe_plan(M, N, K, dev.num_sms, pair_slots, buf, len);
   return cudaSuccess;
 }
 

@@ -200,6 +200,10 @@ cudaError_t launch_gemm(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t s
 // an M x N x K GEMM (given a workspace of fp8lin_workspace_bytes).
 cudaError_t describe_gemm(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev, char* buf,
                           size_t len);
+// The same line for a device of num_sms SMs holding pair_slots clusters of
+// the pair kernel at once; pure host logic, no CUDA call.
+void describe_plan(int64_t M, int64_t N, int64_t K, int num_sms, int pair_slots, char* buf,
+                   size_t len);
 
 // Workspace bytes the tail K split can use at most on a device with num_sms SMs.
 size_t gemm_split_workspace_bytes(int num_sms);
