@@ -19,6 +19,7 @@ def _built():
     from quantised_gemm_gb300 import build as qb
     qb.build()
 
+
 LINE = re.compile(
     r"^(?P<kernel>[a-z0-9_]+<[0-9, ]+>): (?P<swap>swap-AB \(D\^T = B\.A\^T\), )?"
     r"(?P<rows>\d+)x(?P<bn>\d+) tiles, (?P<tiles>\d+) tiles on (?P<used>\d+) of (?P<slots>\d+) "
