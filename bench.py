@@ -9,13 +9,17 @@ dW = dY^T x).  The workload is the largest row of the single-linear table of
 (pytorch/torchtitan PR 778), with inputs that exceed L2 (x and dY are
 512 MiB each), so no L2 flush is needed between steps.
 
-Prints ONE JSON line: value = TFLOP/s of the whole job (6 M N K per step),
-plus the GEMM kernel's roofline (tensor pipe vs measured peak), the cast
-kernel's HBM roofline, an end-to-end figure through the host-buffer API,
-the oracle timed on the host cores, SM clocks sampled during the timed
-region, and a sweep of the other workloads (M = 16 / 256 / 4096, GPT-1.5B
-block Linears with delayed scaling, Llama-3-8B FFN Linears, cast-only
-bandwidth).
+Prints ONE compact JSON line: value = TFLOP/s of the whole job (6 M N K per
+step, timed without instrumentation), the GEMM kernel's roofline (tensor pipe
+vs the measured peak), the cast kernel's HBM roofline, the amax + cast stage
+against its algorithmic bytes, an end-to-end figure through the host-buffer
+API, the oracle timed on the host cores, SM clocks sampled during the timed
+region, and one entry per other workload (M = 16 / 256 / 4096, GPT-1.5B block
+Linears with delayed scaling, Llama-3-8B FFN Linears, cast-only bandwidth),
+each with its fraction of the roofline that bounds it.  Per-kernel times come
+from a separate profiled pass (an event pair around every launch) run right
+after the timed region.  ``--detail PATH`` also writes every figure behind
+the line to PATH.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
   python -m torch.distributed.run --nproc-per-node N bench.py --gpus N ...
@@ -43,6 +47,7 @@ METRIC = "FP8 Linear fwd+bwd µs & TFLOP/s (vs FP8 peak); amax+cast GB/s vs HBM"
 HEADLINE = "linear4096_m65536"
 L2_BYTES = 129 * 1024 * 1024
 FP8_OVER_BF16 = 2.0      # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
+BURST_LIMIT_S = 2.0      # timed regions shorter than this are held to the burst peak
 
 
 def parse(argv=None):
@@ -52,10 +57,10 @@ def parse(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-sweep", action="store_true")
-    ap.add_argument("--full-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--detail", default=None, help="write every figure behind the line here")
     return ap.parse_args(argv)
 
 
@@ -71,6 +76,17 @@ def load_peaks():
                 "source": "measured"}
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
             "source": "fallback"}
+
+
+def fp8_peak(peaks, region_s):
+    """Dense fp8 peak for a timed region of region_s seconds: the burst figure
+    for short regions, the sustained one (power cap) for long ones; nominal
+    fp8 / bf16 ratio applied to the measured bf16 figure."""
+    burst = region_s < BURST_LIMIT_S
+    bf = peaks["bf16_tflops"] if burst else peaks["bf16_tflops_sustained"]
+    basis = "%s bf16 %s %.1f x %.0f" % (peaks["source"], "burst" if burst else "sustained", bf,
+                                        FP8_OVER_BF16)
+    return bf * FP8_OVER_BF16, basis
 
 
 def device_code_sha(kernel: str) -> str:
@@ -112,7 +128,6 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.t0 = self.t1 = None
 
     def start(self):
         try:
@@ -122,9 +137,6 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
-
-    def mark(self, which):
-        setattr(self, which, time.time())
 
     def stop(self):
         if self.proc is None:
@@ -177,6 +189,15 @@ def whole_job_tflops(flop_per_rank_step, ms_step, world):
     """Throughput of all ranks together: every rank does the same step (the
     replicas of a weak-scaling run), the job takes the slowest rank's time."""
     return world * flop_per_rank_step / (ms_step * 1e-3) / 1e12
+
+
+def step_bytes(M, K, N, cast_w=True):
+    """Algorithmic HBM bytes of one fwd+bwd: every cast reads its bf16 tensor
+    once and writes two fp8 copies (2 + 1 + 1 B per element); each GEMM reads
+    its two fp8 operands once and writes its bf16 output."""
+    casts = 4 * (M * K + M * N + (N * K if cast_w else 0))
+    gemms = (M * K + N * K + 2 * M * N) + (M * N + N * K + 2 * M * K) + (M * N + M * K + 2 * N * K)
+    return casts + gemms
 
 
 # ------------------------------------------------------------------ native arm
@@ -233,15 +254,40 @@ def graphed(torch, fn):
     return g.replay
 
 
-def linear_sweep_entry(q, torch, dev, name, steps, warmup, flush, use_graph=True,
+def profiled(q, torch, step, n, flush=None):
+    """Per-kernel device times of n un-graphed steps (an event pair around
+    every launch).  Returns (per-kind ms per step, GEMM ms per step in launch
+    order within a step, launches per step)."""
+    torch.cuda.synchronize()
+    q.profile_enable(True)
+    for _ in range(n):
+        if flush is not None:
+            flush()
+        step()
+    torch.cuda.synchronize()
+    recs = q.profile_launches()
+    q.profile_enable(False)
+    kinds = {}
+    for k, ms in recs:
+        kinds[k] = kinds.get(k, 0.0) + ms / n
+    gemms = [ms for k, ms in recs if k == "gemm"]
+    per = len(gemms) // n if n else 0
+    gemm_each = [sum(gemms[i + j * per] for j in range(n)) / n for i in range(per)]
+    return kinds, gemm_each, len(recs) // max(1, n)
+
+
+def linear_sweep_entry(q, torch, dev, name, steps, warmup, flush, peak_fp8, peaks,
                        cache_weight=False):
-    """fwd+bwd time of every Linear of a workload (sum over its Linears).
-    cache_weight: W is cast once and reused by every step, as over the
-    micro-batches of one optimizer step (not the full step of the headline)."""
+    """fwd+bwd time of every Linear of a workload (sum over its Linears),
+    graph-replayed, with its fraction of the roofline: the tensor peak for
+    the GEMMs (per GEMM kernel, from a profiled pass), HBM for the whole step
+    on its algorithmic bytes.  cache_weight: W is cast once and reused by
+    every step, as over the micro-batches of one optimizer step."""
     import synth_inputs as si
     wl = si.WORKLOADS[name]
     delayed = wl.get("delayed", False)
-    total_ms, total_flop = 0.0, 0.0
+    total_ms = flop = gemm_ms = nbytes = 0.0
+    kinds = {}
     for idx, (M, K, N) in enumerate(wl["shapes"]):
         x, w, dy = make_inputs(name, idx)
         xd, wd, dyd = to_dev(x, dev), to_dev(w, dev), to_dev(dy, dev)
@@ -257,21 +303,33 @@ def linear_sweep_entry(q, torch, dev, name, steps, warmup, flush, use_graph=True
 
         for _ in range(warmup):
             step()
-        fn = graphed(torch, step) if use_graph else step
+        fn = graphed(torch, step)
         torch.cuda.synchronize()
-        ms = time_region(fn, steps, flush)
+        ms = time_region(fn, steps, flush) / steps
+        kk, gemm_each, _ = profiled(q, torch, step, 5, flush)
         q.check(lin.ws)
-        total_ms += ms / steps
-        total_flop += 6.0 * M * N * K
+        total_ms += ms
+        flop += 6.0 * M * N * K
+        gemm_ms += sum(gemm_each)
+        nbytes += step_bytes(M, K, N, cast_w=not cache_weight)
+        for k, v in kk.items():
+            kinds[k] = kinds.get(k, 0.0) + v
         del lin, xd, wd, dyd
         torch.cuda.empty_cache()
-    return {"workload": name + (" (W cast once, reused: micro-batches of one optimizer step)"
-                                if cache_weight else ""),
-            "us_per_fwd_bwd": round(total_ms * 1e3, 2),
-            "tflops": round(total_flop / (total_ms * 1e-3) / 1e12, 1),
+    tf = flop / (total_ms * 1e-3) / 1e12
+    gemm_tf = flop / (gemm_ms * 1e-3) / 1e12
+    hbm = nbytes / (total_ms * 1e-3) / 1e9
+    return {"workload": name + (" (W cast once, reused)" if cache_weight else ""),
+            "us": round(total_ms * 1e3, 2), "tf": round(tf, 1),
+            "frac": round(tf / peak_fp8, 3),
+            "gemm_us": round(gemm_ms * 1e3, 2), "gemm_tf": round(gemm_tf, 1),
+            "gemm": round(gemm_tf / peak_fp8, 3),
+            "bytes": int(nbytes), "hbm_gbs": round(hbm, 1),
+            "hbm": round(hbm / peaks["hbm_gbs"], 3),
+            "kernel_us": {k: round(v * 1e3, 2) for k, v in kinds.items()},
             "scaling": "delayed" if delayed else "dynamic",
             "l2": "flushed between steps" if flush else "inputs larger than L2",
-            "cuda_graph": use_graph}
+            "cuda_graph": True}
 
 
 def library_gemm_entry(q, torch, dev, M, N, K, fmt_a, rounds=3, iters=10):
@@ -281,7 +339,6 @@ def library_gemm_entry(q, torch, dev, M, N, K, fmt_a, rounds=3, iters=10):
     `rounds` rounds so clock drift under the power cap favours neither; the
     medians are reported, with the largest |difference| of the two outputs
     (the accumulation order may differ)."""
-    import statistics
     fp8 = {0: torch.float8_e4m3fn, 1: torch.float8_e5m2}
     g = torch.Generator(device=dev).manual_seed(7)
     a = (torch.randn(M, K, device=dev, generator=g) * 4).to(fp8[fmt_a])
@@ -339,9 +396,7 @@ def chain_sweep_entry(q, torch, dev, name, steps, warmup, flush, rounds=3):
     with the amax of y and dX taken in the GEMM epilogues (link_linears: those
     two casts read their tensor once) and with separate amax passes.  The two
     variants alternate over `rounds` rounds (median reported), so clock drift
-    under the power cap does not favour either; a profiled pass of each gives
-    its time per kernel kind."""
-    import statistics
+    under the power cap does not favour either."""
     import synth_inputs as si
     M, K, N = si.WORKLOADS[name]["shapes"][0]
     assert K == N, "a chain of square Linears"
@@ -362,15 +417,10 @@ def chain_sweep_entry(q, torch, dev, name, steps, warmup, flush, rounds=3):
 
         for _ in range(warmup):
             step()
-        q.profile_enable(True)
-        for _ in range(2):
-            step()
-        prof = q.profile_collect()
-        q.profile_enable(False)
+        kk, _, _ = profiled(q, torch, step, 2)
         variants["fused_amax" if linked else "separate_amax"] = {
-            "step": step, "graph": graphed(torch, step), "lins": (l1, l2), "ms": [],
-            "kernel_us_per_step": {k: round(v[0] * 1e3 / 2, 1) for k, v in prof.items()
-                                   if v[1] > 0}}
+            "graph": graphed(torch, step), "lins": (l1, l2), "ms": [],
+            "kernel_us_per_step": {k: round(v * 1e3, 1) for k, v in kk.items()}}
     torch.cuda.synchronize()
     for _ in range(rounds):
         for v in variants.values():
@@ -391,35 +441,46 @@ def chain_sweep_entry(q, torch, dev, name, steps, warmup, flush, rounds=3):
     return res
 
 
-def cast_sweep(q, torch, dev, peaks, full):
-    """amax + scale + cast (+T) of [R, 4096] / [4096, R] tensors: GB/s of the
-    algorithmic bytes (2 B read + 1 B per fp8 copy) and fraction of HBM."""
-    import synth_inputs as si
-    sizes = [1 << 20, 1 << 22, 1 << 24, 1 << 26, 1 << 28, 1 << 30] if full else \
-        [1 << 20, 1 << 24, 1 << 28]
-    fmts = [q.E4M3, q.E5M2] if full else [q.E4M3]
-    shapes = ["rows", "cols"] if full else ["rows"]
+CAST_ALGOS = ("atomic", "reduction", "single_pass", "delayed")
+
+
+def cast_sweep(q, torch, dev, peaks):
+    """amax + scale + cast (+T) of [R, 4096] / [4096, R] bf16 N(0,1) tensors,
+    R * 4096 = 2^20 ... 2^30, e4m3 and e5m2, with and without the transposed
+    copy, for each amax algorithm: two-pass ATOMIC and REDUCTION, the
+    single pass where the tensor fits on chip, and delayed scaling's cast
+    (stored scale, amax recorded in the same pass: one read).  GB/s of the
+    algorithmic bytes (2 B read + 1 B per fp8 copy), so a second read by a
+    two-pass amax counts as time.  Inputs are drawn on the device (seeded):
+    this is a measurement, the parity of these casts is in the tests."""
+    sizes = [1 << 20, 1 << 22, 1 << 24, 1 << 26, 1 << 28, 1 << 30]
     ws = q.Workspace(device=dev)
     flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    gen = torch.Generator(device=dev)
     out = []
     for n in sizes:
-        for shp in shapes:
+        for shp in ("rows", "cols"):
             R = n // 4096
             rows, cols = (R, 4096) if shp == "rows" else (4096, R)
-            x = si.normal_bf16((rows, cols), 1.0, 0, 1)
-            xd = to_dev(x, dev)
-            del x
+            gen.manual_seed(n + (shp == "cols"))
+            xd = torch.randn((rows, cols), device=dev, generator=gen).to(torch.bfloat16)
             o = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
             ot = torch.empty((cols, rows), dtype=torch.uint8, device=dev)
-            for fmt in fmts:
+            for fmt in (q.E4M3, q.E5M2):
                 for trans in (True, False):
-                    for algo in (q.AMAX_ATOMIC, q.AMAX_REDUCTION, q.AMAX_SINGLE_PASS):
-                        if algo == q.AMAX_SINGLE_PASS and n > q.single_pass_max_elems():
+                    for algo in CAST_ALGOS:
+                        if algo == "single_pass" and n > q.single_pass_max_elems():
                             continue
-                        if algo == q.AMAX_REDUCTION and not full:
-                            continue
-                        st = q.ScalingState(fmt, q.DYNAMIC, amax_algo=algo, device=dev)
-                        call = lambda: q.cast_dynamic(xd, st, o, ot if trans else None, ws)  # noqa
+                        if algo == "delayed":
+                            st = q.ScalingState(fmt, q.DELAYED, history_len=16, device=dev)
+                            call = lambda st=st: q.cast_delayed(  # noqa: E731
+                                xd, st, o, ot if trans else None, ws)
+                        else:
+                            a = {"atomic": q.AMAX_ATOMIC, "reduction": q.AMAX_REDUCTION,
+                                 "single_pass": q.AMAX_SINGLE_PASS}[algo]
+                            st = q.ScalingState(fmt, q.DYNAMIC, amax_algo=a, device=dev)
+                            call = lambda st=st: q.cast_dynamic(  # noqa: E731
+                                xd, st, o, ot if trans else None, ws)
                         for _ in range(3):
                             call()
                         fn = graphed(torch, call)
@@ -430,15 +491,29 @@ def cast_sweep(q, torch, dev, peaks, full):
                         q.check(ws)
                         alg_bytes = n * (2 + 1 + (1 if trans else 0))
                         gbs = alg_bytes / (ms * 1e-3) / 1e9
-                        out.append({"elems": n, "shape": [rows, cols], "cuda_graph": True,
+                        out.append({"elems": n, "shape": [rows, cols],
                                     "fmt": "e4m3" if fmt == q.E4M3 else "e5m2",
-                                    "transpose": trans,
-                                    "amax": {0: "atomic", 1: "reduction", 2: "single_pass"}[algo],
+                                    "transpose": trans, "amax": algo,
                                     "us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
                                     "frac_hbm": round(gbs / peaks["hbm_gbs"], 3)})
             del xd, o, ot
             torch.cuda.empty_cache()
+    del flush_buf
+    torch.cuda.empty_cache()
     return out
+
+
+def cast_sweep_summary(rows):
+    """Per size: [median, min] fraction of HBM over the 8 format x shape x
+    transpose cases, per amax algorithm (None where it does not apply)."""
+    res = {}
+    for n in sorted({r["elems"] for r in rows}):
+        ent = []
+        for algo in CAST_ALGOS:
+            f = [r["frac_hbm"] for r in rows if r["elems"] == n and r["amax"] == algo]
+            ent.append([round(statistics.median(f), 3), round(min(f), 3)] if f else None)
+        res["2^%d" % (n.bit_length() - 1)] = ent
+    return res
 
 
 def cpu_baseline_sample(name, budget_s=12.0):
@@ -466,8 +541,8 @@ def cpu_baseline_sample(name, budget_s=12.0):
         if spent > budget_s or Ms >= M or dt > budget_s / 3:
             break
         Ms *= 2
-    desc = ("oracle fwd+bwd (C casts + numpy fp64 GEMMs) of the %dx%d Linear on the first %d "
-            "of %d tokens, %.2f s" % (K, N, Ms, M, elapsed))
+    desc = ("oracle fwd+bwd (C casts, numpy fp64 GEMMs), %dx%d Linear, first %d of %d tokens, "
+            "%.2f s" % (K, N, Ms, M, elapsed))
     return flop / elapsed / 1e12, desc, oracle.num_threads()
 
 
@@ -482,9 +557,6 @@ def end_to_end(q, lin, x, w, dy, M, K, N, world, flop_step, steps):
     hdx = torch.empty((M, K), dtype=torch.bfloat16).pin_memory()
     hdw = torch.empty((N, K), dtype=torch.bfloat16).pin_memory()
     n = max(3, min(20, steps // 10))
-    lanes = os.environ.get("FP8LIN_COPY_LANES")
-    if lanes:
-        lin.copy_lanes = int(lanes)
     for _ in range(2):
         lin.step_host(hx, hw, hdy, hy, hdx, hdw)
     torch.cuda.synchronize()
@@ -512,7 +584,6 @@ def end_to_end(q, lin, x, w, dy, M, K, N, world, flop_step, steps):
     return {"value": round(whole_job_tflops(flop_step, ms, world), 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3),
             "steps": n, "blocks_ms_per_step": [round(b, 3) for b in blocks],
-            "copy_lanes": lin.copy_lanes,
             "api": "Fp8Linear.step_host(wait=False) + finish_host (pinned host buffers)",
             "host_link": link, "copy_floor_ms": round(floor_ms, 3),
             "frac_of_copy_floor": round(floor_ms / ms, 3)}
@@ -564,6 +635,10 @@ def host_link_rates(torch, host, dev):
             "bytes": nbytes}
 
 
+SHORT = {"linear4096_m16": "m16", "linear4096_m256": "m256", "linear4096_m4096": "m4096",
+         "gpt1.5b_linears_m12288": "gpt1.5b_delayed", "llama3_8b_ffn_m8192": "llama3_ffn"}
+
+
 def run_native(args):
     import torch
     import quantised_gemm_gb300 as q
@@ -592,6 +667,7 @@ def run_native(args):
     torch.cuda.synchronize()
     q.check(lin.ws)
 
+    # ---- timed region: plain launches, no instrumentation
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
@@ -599,14 +675,9 @@ def run_native(args):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     launches0 = q.launch_count()
-    q.profile_enable(True)
-    sampler.mark("t0")
     ms = time_region(step, args.steps)
-    sampler.mark("t1")
-    torch.cuda.synchronize()
-    prof = q.profile_collect()
-    q.profile_enable(False)
     launches = q.launch_count() - launches0
+    torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
@@ -614,24 +685,25 @@ def run_native(args):
     ms_step = max_over_ranks(torch, ms / args.steps, world, dev)
     flop_step = 6.0 * M * N * K
     value = whole_job_tflops(flop_step, ms_step, world)
+    region_s = ms_step * args.steps * 1e-3
+    peak, basis = fp8_peak(peaks, region_s)
 
-    gemm_ms, gemm_n = prof["gemm"]
-    gemm_avg = gemm_ms / max(1, gemm_n)
+    # ---- per-kernel split: a profiled pass of the same steps, right after
+    n_prof = max(3, min(args.steps, 40))
+    kinds, gemm_each, per_step = profiled(q, torch, step, n_prof)
+    q.check(lin.ws)
     gemm_flop = 2.0 * M * N * K          # each of the three GEMMs of this square Linear
+    gemm_avg = sum(gemm_each) / len(gemm_each)
     achieved = gemm_flop / (gemm_avg * 1e-3) / 1e12
-    peak = peaks["bf16_tflops_sustained"] * FP8_OVER_BF16
     tr = load_traffic("gemm")
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1),
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 3),
                 "traffic": tr["bytes_per_launch"] if tr else None,
-                "kernel": q.gemm_describe(M, N, K).split(":")[0] +
-                          " (tcgen05, e4m3/e5m2 x e4m3 -> bf16)",
-                "schedule": {"y = x8.W8^T": q.gemm_describe(M, N, K),
-                             "dX = dY8.W8t^T": q.gemm_describe(M, K, N),
-                             "dW = dY8t.x8t^T": q.gemm_describe(N, K, M)},
-                "launch_us": round(gemm_avg * 1e3, 1),
-                "peak_basis": "%s bf16 sustained %.1f TFLOP/s x %.0f (nominal fp8/bf16)" % (
-                    peaks["source"], peaks["bf16_tflops_sustained"], FP8_OVER_BF16)}
+                "kernel": q.gemm_describe(M, N, K).split(":")[0],
+                "peak_basis": basis + " (of measured)" if peaks["source"] == "measured" else
+                basis + " (of fallback)",
+                "kernel_time": "mean of %d launches, profiled pass of %d steps after the timed "
+                               "region" % (len(gemm_each) * n_prof, n_prof)}
     # Casts of the step: x [M,K], W [N,K], dY [M,N], each 2 B read + 1 B + 1 B
     # (transposed) written per element.  Tensors that fit on chip run as the
     # single-pass kernel (kind "cast_fused", amax included); the others as
@@ -639,33 +711,33 @@ def run_native(args):
     cap = q.single_pass_max_elems()
     two_pass = [n for n in (M * K, N * K, M * N) if n > cap]
     one_pass = [n for n in (M * K, N * K, M * N) if n <= cap]
-    cast_ms = prof["cast"][0] / args.steps
-    fused_ms = prof["cast_fused"][0] / args.steps
-    amax_ms = prof["amax"][0] / args.steps
+    cast_ms, fused_ms = kinds.get("cast", 0.0), kinds.get("cast_fused", 0.0)
+    amax_ms, scale_ms = kinds.get("amax", 0.0), kinds.get("scale", 0.0)
     if two_pass and cast_ms > 0:
         kernel_bytes = 4.0 * sum(two_pass)
         cast_gbs = kernel_bytes / (cast_ms * 1e-3) / 1e9
-        cast_kernel = "cast_stream_kernel (+transpose, TMA ring), two-pass casts"
+        cast_kernel = "cast_stream_kernel"
     else:
         kernel_bytes = 4.0 * sum(one_pass)
         cast_gbs = kernel_bytes / (max(fused_ms, 1e-9) * 1e-3) / 1e9
-        cast_kernel = "cast_single_pass_kernel (+transpose)"
+        cast_kernel = "cast_single_pass_kernel"
     trc = load_traffic("cast")
     cast_roofline = {"bound": "hbm", "achieved": round(cast_gbs, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(cast_gbs / peaks["hbm_gbs"], 3),
-                     "traffic": trc["bytes_per_launch"] if trc else None,
-                     "kernel": cast_kernel, "bytes_per_step": round(kernel_bytes)}
+                     "traffic": trc["bytes_per_launch"] if trc else None, "kernel": cast_kernel}
     # The whole amax + scale + cast stage against its algorithmic bytes (one
-    # read, one write per fp8 copy): a second read by two-pass amax counts as
-    # time, not as bytes.
+    # read, one write per fp8 copy); a second read by two-pass amax counts as
+    # time.  Two-pass dynamic scaling moves 6 B per element for 4 algorithmic
+    # ones, so its ceiling is 2/3 of HBM.
     stage_bytes = 4.0 * (M * K + N * K + M * N)
-    stage_ms = cast_ms + fused_ms + amax_ms + prof["scale"][0] / args.steps
-    amax_cast_stage = {"bound": "hbm", "unit": "GB/s", "peak": peaks["hbm_gbs"],
-                       "achieved": round(stage_bytes / (stage_ms * 1e-3) / 1e9, 1),
-                       "frac": round(stage_bytes / (stage_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3),
-                       "us_per_step": round(stage_ms * 1e3, 1),
-                       "algorithmic_bytes_per_step": round(stage_bytes)}
-    kernel_ms = {k: round(v[0] / args.steps, 4) for k, v in prof.items()}
+    stage_ms = cast_ms + fused_ms + amax_ms + scale_ms
+    stage_frac = stage_bytes / (stage_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]
+    stage = {"us": round(stage_ms * 1e3, 1), "frac": round(stage_frac, 3),
+             "of_two_pass_ceiling": round(stage_frac / (4.0 / 6.0), 3)}
+    kernel_us = {"gemm_y": round(gemm_each[0] * 1e3, 1), "gemm_dx": round(gemm_each[1] * 1e3, 1),
+                 "gemm_dw": round(gemm_each[2] * 1e3, 1), "cast": round(cast_ms * 1e3, 1),
+                 "cast_fused": round(fused_ms * 1e3, 1), "amax": round(amax_ms * 1e3, 1),
+                 "scale": round(scale_ms * 1e3, 1)}
 
     e2e = None
     if not args.no_e2e:
@@ -674,30 +746,49 @@ def run_native(args):
     del lin, xd, wd, dyd
     torch.cuda.empty_cache()
 
-    sweep = None
+    detail = {"headline_kernels_ms_per_step": kinds, "headline_gemm_ms": gemm_each,
+              "launches_per_step": per_step}
+    configs, cast_sum, vs_lt, chains = None, None, None, None
     if not args.no_sweep:
         flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
         flush = lambda: flush_buf.zero_()  # noqa: E731
-        sweep = {"linears": [], "chains": None, "cast": None, "gemm_vs_cublaslt": None}
+        entries = []
         for name in ("linear4096_m16", "linear4096_m256", "linear4096_m4096",
                      "gpt1.5b_linears_m12288", "llama3_8b_ffn_m8192"):
             small = si.WORKLOADS[name]["shapes"][0][0] <= 4096
-            sweep["linears"].append(linear_sweep_entry(
+            entries.append((SHORT[name], linear_sweep_entry(
                 q, torch, dev, name, steps=50 if small else 20, warmup=5,
-                flush=flush if small else None))
+                flush=flush if small else None, peak_fp8=peak, peaks=peaks)))
         for name in ("linear4096_m16", "linear4096_m256"):
-            sweep["linears"].append(linear_sweep_entry(
-                q, torch, dev, name, steps=50, warmup=5, flush=flush, cache_weight=True))
-        sweep["chains"] = [
-            chain_sweep_entry(q, torch, dev, "linear4096_m4096", steps=50, warmup=5, flush=flush),
-            chain_sweep_entry(q, torch, dev, "linear4096_m65536", steps=10, warmup=3, flush=None)]
+            entries.append((SHORT[name] + "_cachedW", linear_sweep_entry(
+                q, torch, dev, name, steps=50, warmup=5, flush=flush, peak_fp8=peak,
+                peaks=peaks, cache_weight=True)))
+        detail["linears"] = dict(entries)
+        configs = {}
+        for key, e in entries:
+            c = {"us": e["us"], "tf": e["tf"]}
+            if key.startswith(("m16", "m256")):
+                c["hbm"] = e["hbm"]           # HBM-bound: the step against its bytes
+            else:
+                c["gemm"] = e["gemm"]         # tensor-bound: GEMM kernels vs fp8 peak
+                c["frac"] = e["frac"]
+            configs[key] = c
+        chains = [chain_sweep_entry(q, torch, dev, "linear4096_m4096", steps=50, warmup=5,
+                                    flush=flush),
+                  chain_sweep_entry(q, torch, dev, "linear4096_m65536", steps=10, warmup=3,
+                                    flush=None)]
+        detail["chains"] = chains
         del flush_buf
         torch.cuda.empty_cache()
-        sweep["cast"] = cast_sweep(q, torch, dev, peaks, args.full_sweep)
+        rows = cast_sweep(q, torch, dev, peaks)
+        detail["cast_sweep"] = rows
+        cast_sum = cast_sweep_summary(rows)
         # the three products of the 65536-token step: y, dX (e5m2 A), dW (long K)
-        sweep["gemm_vs_cublaslt"] = [library_gemm_entry(q, torch, dev, 65536, 4096, 4096, 0),
-                                     library_gemm_entry(q, torch, dev, 65536, 4096, 4096, 1),
-                                     library_gemm_entry(q, torch, dev, 4096, 4096, 65536, 1)]
+        lt = [library_gemm_entry(q, torch, dev, 65536, 4096, 4096, 0),
+              library_gemm_entry(q, torch, dev, 65536, 4096, 4096, 1),
+              library_gemm_entry(q, torch, dev, 4096, 4096, 65536, 1)]
+        detail["gemm_vs_cublaslt"] = lt
+        vs_lt = [e.get("ours_over_cublaslt") for e in lt]
         torch.cuda.empty_cache()
 
     cpu = None
@@ -707,26 +798,36 @@ def run_native(args):
                "sample": desc}
 
     if rank == 0:
+        e2e_line = None
+        if e2e is not None:
+            e2e_line = {k: e2e[k] for k in ("value", "unit", "h2d_bytes_per_step",
+                                            "d2h_bytes_per_step", "ms_per_step",
+                                            "frac_of_copy_floor")}
+            e2e_line["api"] = "Fp8Linear.step_host"
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": max(3, args.warmup),
             "ms_per_step": round(ms_step, 4), "us_per_fwd_bwd": round(ms_step * 1e3, 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8",
             "data": "synthetic",
-            "config": {"workload": "%s: Linear 4096->4096, M=%d tokens, dynamic tensorwise "
-                                   "scaling, x~N(0,1)+0.1%% N(0,50) outliers, W~U(+-1/64), "
-                                   "dY~N(0,1e-3)" % (args.workload, M),
-                       "M": M, "K": K, "N": N, "l2": "inputs larger than L2 (x, dY 512 MiB)",
-                       "parallelism": "replicas" if world > 1 else "single GPU"},
-            "roofline": roofline, "cast_roofline": cast_roofline,
-            "amax_cast_stage": amax_cast_stage,
-            "kernel_ms_per_step": kernel_ms,
-            "cpu_baseline": cpu,
-            "e2e": e2e,
-            "gpu_launches": int(launches), "clocks": clocks, "peaks": peaks,
-            "sweep": sweep,
+            "config": {"workload": "%s: Linear 4096->4096, M=%d, dynamic tensorwise" %
+                                   (args.workload, M),
+                       "l2": "inputs > L2", "parallelism": "replicas" if world > 1 else "1 GPU"},
+            "roofline": roofline, "cast_roofline": cast_roofline, "amax_cast_stage": stage,
+            "kernel_us": kernel_us, "cpu_baseline": cpu, "e2e": e2e_line,
+            "gpu_launches": int(launches), "clocks": clocks,
+            "configs": configs,
+            "cast_sweep": ({"cols": "per size [median,min] frac HBM over fmt x shape x T: "
+                                    "atomic, reduction, single_pass, delayed", **cast_sum}
+                           if cast_sum else None),
+            "vs_cublaslt_y_dx_dw": vs_lt,
+            "chain_fused_amax_saved_us": [c["saved_us"] for c in chains] if chains else None,
         }
-        print(json.dumps(line), flush=True)
+        print(json.dumps(line, separators=(",", ":"), ensure_ascii=False), flush=True)
+        if args.detail:
+            detail.update({"line": line, "e2e": e2e, "peaks": peaks})
+            with open(args.detail, "w") as f:
+                json.dump(detail, f, indent=1)
     if world > 1:
         torch.distributed.destroy_process_group()
 

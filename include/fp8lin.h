@@ -54,6 +54,12 @@
  *     wherever a transposed copy (or a GEMM operand) has them as its row
  *     length.  In practice: M, K, N multiples of 16.
  *   - Inputs are NaN-free by contract; NaN propagation is not specified.
+ *   - Per-device set-up (kernel shared-memory attributes, occupancy counts,
+ *     the device address of fp8lin_amax_noalloc's static array) is done by
+ *     the first call on each device and kept for the life of the process,
+ *     for that device's primary context.  cudaDeviceReset() ends that
+ *     context and with it the set-up: do not call the library on a device
+ *     after resetting it in the same process.
  */
 #ifndef FP8LIN_H
 #define FP8LIN_H
@@ -238,6 +244,19 @@ fp8lin_status fp8lin_cast_dynamic(const void* x, int64_t rows, int64_t cols, int
                                   const fp8lin_scaling_state* st, uint8_t* out,
                                   uint8_t* out_t, void* ws, cudaStream_t stream);
 
+/* Delayed scaling's cast of one tensor, as fp8lin_forward / fp8lin_backward
+ * run it: cast with the stored *st->scale into out (+ out_t) and record the
+ * tensor's amax into *st->amax in the same pass -- one read of the tensor.
+ * If st->needs_init is set, the scale is first taken from the tensor's own
+ * amax (enable_amax_init), without touching the ring, and needs_init is
+ * cleared.  st->kind must be FP8LIN_DELAYED; the ring update is
+ * fp8lin_scale's, after backward.  Source: "[float8] FP8 GPT 1.5B Delayed
+ * Scaling 2x Slower than BF16" (pytorch/ao issue 1297), repro script
+ * (ScalingType.DELAYED, enable_amax_init). */
+fp8lin_status fp8lin_cast_delayed(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                  fp8lin_scaling_state* st, uint8_t* out, uint8_t* out_t,
+                                  void* ws, cudaStream_t stream);
+
 /* FP8 GEMM (rows a4-a6): d[m, n] = bf16( (sum_k A[m, k] * B[n, k]) *
  * fl32(inv_a * inv_b) ), accumulated in fp32 on the tensor cores.
  * a: fp8 [M, K] row stride lda bytes; b: fp8 [N, K] row stride ldb bytes
@@ -326,6 +345,12 @@ enum {
 };
 void fp8lin_profile_enable(int on);
 fp8lin_status fp8lin_profile_collect(double* ms, int64_t* count);
+
+/* The same record launch by launch, in launch order: synchronises the
+ * events, writes the milliseconds and the FP8LIN_PROF_* kind of the first
+ * min(recorded, capacity) launches into ms[] / kind[] (host arrays), clears
+ * the record and returns how many it wrote; a negative value is -status. */
+int64_t fp8lin_profile_launches(double* ms, int32_t* kind, int64_t capacity);
 
 #ifdef __cplusplus
 }

@@ -34,10 +34,10 @@ __all__ = [
     "E4M3", "E5M2", "AMAX_ATOMIC", "AMAX_REDUCTION", "AMAX_SINGLE_PASS", "AMAX_AUTO",
     "AMAX_PRECOMPUTED", "DYNAMIC",
     "DELAYED",
-    "Fp8linError", "ScalingState", "Workspace", "amax", "amax_noalloc", "scale", "cast", "cast_dynamic", "gemm",
+    "Fp8linError", "ScalingState", "Workspace", "amax", "amax_noalloc", "scale", "cast", "cast_dynamic", "cast_delayed", "gemm",
     "gemm_describe", "gemm_describe_for",
     "forward", "backward", "check", "workspace_bytes", "single_pass_max_elems", "launch_count",
-    "profile_enable", "profile_collect", "Fp8Linear", "link_linears", "library", "Float8Linear",
+    "profile_enable", "profile_collect", "profile_launches", "Fp8Linear", "link_linears", "library", "Float8Linear",
     "Float8LinearConfig", "CastConfig", "convert_to_float8_training",
     "sync_float8_amax_and_scale_history",
 ]
@@ -204,6 +204,19 @@ def cast_dynamic(x: torch.Tensor, state: ScalingState, out: torch.Tensor | None,
     _lib.check(st, "fp8lin_cast_dynamic")
 
 
+def cast_delayed(x: torch.Tensor, state: ScalingState, out: torch.Tensor | None,
+                 out_t: torch.Tensor | None, ws: Workspace, stream=None):
+    """Delayed scaling's cast: the stored scale, the amax recorded in the same
+    pass (amax init first if the state still needs it)."""
+    px, rows, cols, ld = _bf16_2d(x, "x")
+    c = state.c_struct()
+    st = library().fp8lin_cast_delayed(px, rows, cols, ld, ctypes.byref(c),
+                                       _dev(out, "out", torch.uint8),
+                                       _dev(out_t, "out_t", torch.uint8), ws.ptr, _stream(stream))
+    state._pull()
+    _lib.check(st, "fp8lin_cast_delayed")
+
+
 def gemm(a8: torch.Tensor, b8: torch.Tensor, fmt_a: int, fmt_b: int, inv_a: torch.Tensor,
          inv_b: torch.Tensor, out: torch.Tensor, ws: Workspace, stream=None,
          amax_out: torch.Tensor | None = None):
@@ -287,6 +300,17 @@ def profile_collect() -> dict:
     cnt = (ctypes.c_int64 * len(PROF_KINDS))()
     _lib.check(library().fp8lin_profile_collect(ms, cnt), "fp8lin_profile_collect")
     return {k: (ms[i], cnt[i]) for i, k in enumerate(PROF_KINDS)}
+
+
+def profile_launches(capacity: int = 8192) -> list:
+    """[(kind, milliseconds), ...] of every launch since profile_enable(True),
+    in launch order."""
+    ms = (ctypes.c_double * capacity)()
+    kind = (ctypes.c_int32 * capacity)()
+    n = int(library().fp8lin_profile_launches(ms, kind, capacity))
+    if n < 0:
+        _lib.check(-n, "fp8lin_profile_launches")
+    return [(PROF_KINDS[kind[i]], ms[i]) for i in range(n)]
 
 
 from .linear import Fp8Linear, link_linears  # noqa: E402

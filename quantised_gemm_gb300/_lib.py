@@ -72,6 +72,7 @@ _SIGNATURES = {
     "fp8lin_scale": (ctypes.c_int, [_ST, _P]),
     "fp8lin_cast": (ctypes.c_int, [_P, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P]),
     "fp8lin_cast_dynamic": (ctypes.c_int, [_P, _I64, _I64, _I64, _ST, _P, _P, _P, _P]),
+    "fp8lin_cast_delayed": (ctypes.c_int, [_P, _I64, _I64, _I64, _ST, _P, _P, _P, _P]),
     "fp8lin_gemm": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I64, _I64, _I32, _I32, _P, _P,
                                    _P, _I64, _P, _P, _SZ, _P]),
     "fp8lin_gemm_describe": (ctypes.c_int, [_I64, _I64, _I64, ctypes.c_char_p, _SZ]),
@@ -84,6 +85,7 @@ _SIGNATURES = {
     "fp8lin_launch_count": (ctypes.c_uint64, []),
     "fp8lin_profile_enable": (None, [ctypes.c_int]),
     "fp8lin_profile_collect": (ctypes.c_int, [_P, _P]),
+    "fp8lin_profile_launches": (_I64, [_P, _P, _I64]),
 }
 
 

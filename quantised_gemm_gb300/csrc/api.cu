@@ -516,6 +516,25 @@ fp8lin_status fp8lin_cast_dynamic(const void* x, int64_t rows, int64_t cols, int
   return cast_dynamic_scaled(x, rows, cols, ld, st, out, out_t, ws, dev, stream, false);
 }
 
+fp8lin_status fp8lin_cast_delayed(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                  fp8lin_scaling_state* st, uint8_t* out, uint8_t* out_t,
+                                  void* ws, cudaStream_t stream) {
+  fp8lin_status s = check_bf16(x, rows, cols, ld);
+  if (s != FP8LIN_OK) return s;
+  if ((s = check_state(st, false)) != FP8LIN_OK) return s;
+  if (st->kind != FP8LIN_DELAYED) return FP8LIN_EINVAL;
+  if (!ws_ok(ws)) return FP8LIN_EINVAL;
+  if (out == nullptr && out_t == nullptr) return FP8LIN_EINVAL;
+  if (out != nullptr && !aligned16(out)) return FP8LIN_EINVAL;
+  if (out_t != nullptr) {
+    if (!aligned16(out_t)) return FP8LIN_EINVAL;
+    if (rows % 16 != 0) return FP8LIN_EUNSUPPORTED;
+  }
+  DeviceInfo dev;
+  if ((s = get_dev(&dev)) != FP8LIN_OK) return s;
+  return delayed_cast(x, rows, cols, ld, st, out, out_t, ws, dev, stream);
+}
+
 fp8lin_status fp8lin_gemm(const uint8_t* a, const uint8_t* b, int64_t M, int64_t N, int64_t K,
                           int64_t lda, int64_t ldb, int32_t fmt_a, int32_t fmt_b,
                           const float* inv_a, const float* inv_b, void* d, int64_t ldd,
@@ -668,6 +687,22 @@ uint64_t fp8lin_launch_count(void) { return g_launches.load(std::memory_order_re
 void fp8lin_profile_enable(int on) {
   g_prof_on = on != 0;
   if (g_prof_on) g_prof_used = 0;
+}
+
+int64_t fp8lin_profile_launches(double* ms, int32_t* kind, int64_t capacity) {
+  if (ms == nullptr || kind == nullptr || capacity < 0) return -static_cast<int64_t>(FP8LIN_EINVAL);
+  const int64_t n = g_prof_used < capacity ? g_prof_used : capacity;
+  for (int64_t i = 0; i < n; ++i) {
+    cudaError_t e = cudaEventSynchronize(g_prof[i].stop);
+    if (e != cudaSuccess) return -static_cast<int64_t>(cuda_fail(e));
+    float t = 0.0f;
+    e = cudaEventElapsedTime(&t, g_prof[i].start, g_prof[i].stop);
+    if (e != cudaSuccess) return -static_cast<int64_t>(cuda_fail(e));
+    ms[i] = t;
+    kind[i] = g_prof[i].kind;
+  }
+  g_prof_used = 0;
+  return n;
 }
 
 fp8lin_status fp8lin_profile_collect(double* ms, int64_t* count) {

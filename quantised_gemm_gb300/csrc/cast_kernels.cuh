@@ -453,12 +453,14 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         if (p.err != nullptr) atomicCAS(p.err, 0, kErrCastWait);
         s_abort = 1;
       }
-      if (!ok || s_abort) {
-        // Let this lane's copies in flight land before the CTA exits.
-        volatile int never = 0;
-        for (int st = 0; st < kStreamStages; ++st)
-          if (fills[st] > 0) mbar_wait_bounded(&full[st], (fills[st] - 1) & 1u, &never);
-      }
+      // Stay until every copy this lane issued has landed, whatever the
+      // consumers do: the CTA (and its shared memory) lives as long as this
+      // lane does, so no copy can land in a CTA that has left.  Only the last
+      // phase of each stage can still be open; without a failure the
+      // consumers have waited for all of them already, or are about to.
+      volatile int never = 0;
+      for (int st = 0; st < kStreamStages; ++st)
+        if (fills[st] > 0) mbar_wait_bounded(&full[st], (fills[st] - 1) & 1u, &never);
     }
     return;
   }

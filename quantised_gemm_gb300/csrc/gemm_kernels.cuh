@@ -669,6 +669,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* drain = acc_empty + 2;       // [1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // Written by the peer CTA just before the closing cluster barrier: whether
+  // it gave up anywhere, and (odd CTA -> even CTA) how many loads its
+  // producer issued into each stage.
+  volatile uint32_t* peer_abort = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);
+  volatile uint32_t* peer_fills = peer_abort + 1;       // [STAGES]
+  volatile uint32_t* own_fills = peer_fills + STAGES;   // [STAGES] this CTA's producer's
+  static_assert(sizeof(uint64_t) * (2 * STAGES + 5) + sizeof(uint32_t) * (3 + 2 * STAGES) <= 256,
+                "barrier block");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();      // 0: issues the MMAs
@@ -689,6 +697,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
+    *peer_abort = 0;
+    for (int s = 0; s < STAGES; ++s) peer_fills[s] = own_fills[s] = 0;
     fence_barrier_init();
     tma_prefetch_map(&tmA);
     tma_prefetch_map(&tmB);
@@ -708,6 +718,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producers (both CTAs)
     if (lane == 0) {
+      uint32_t fills[STAGES];  // loads issued into each stage
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) fills[s] = 0;
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -725,6 +738,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                            m_blk * 2 * kBM + static_cast<int>(rank) * kBM);
           tma_load_2d_pair(sB + stage * C::kBBytes, &tmB, full_even, kb * kBK,
                            n_blk * BN + static_cast<int>(rank) * (BN / 2));
+#pragma unroll
+          for (int s = 0; s < STAGES; ++s)
+            if (s == stage) ++fills[s];
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -732,6 +748,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
       if (!ok) record_error(p.err, abort_flag, kErrGemmProducerWait);
+      // The even CTA's full[] barriers count the odd CTA's loads too: only
+      // the even CTA can tell that they have landed (see the end).
+      if (rank == 1) {
+        const uint32_t even_fills = map_to_cta(smem_addr(const_cast<uint32_t*>(peer_fills)), 0);
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s) st_shared_cluster_u32(even_fills + 4u * s, fills[s]);
+      } else {
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s) own_fills[s] = fills[s];
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
@@ -831,8 +857,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 
   __syncwarp();
+  __syncthreads();  // every role of this CTA is done: its abort flag is final
+  if (threadIdx.x == 0)
+    st_shared_cluster_u32(map_to_cta(smem_addr(const_cast<uint32_t*>(peer_abort)), rank ^ 1u),
+                          *abort_flag != 0 ? 1u : 0u);
   tc_fence_before_sync();
   cluster_sync_all();  // no CTA leaves while its peer may still read its shared memory
+  // Both CTAs take the same decision from the two flags.  Without a failure
+  // every load has been consumed by an MMA, so it has landed.  After one, a
+  // producer may have stopped with loads in flight, and the two producers
+  // may have stopped one phase apart on a stage (each waits for the same MMA
+  // commits, so neither gets further ahead).  The even CTA, whose full[]
+  // barriers count both CTAs' bytes, balances each stage's last phase -- it
+  // arms a phase only the odd CTA loaded into, and completes the bytes of one
+  // the odd CTA never loaded -- then waits (bounded) for that phase; every
+  // earlier phase of a stage has completed already.  The second cluster
+  // barrier keeps the odd CTA until then.
+  if (*abort_flag != 0 || *peer_abort != 0) {
+    if (rank == 0 && threadIdx.x == 0) {
+      volatile int never = 0;
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) {
+        const uint32_t fe = own_fills[s], fo = peer_fills[s];
+        if (fo > fe) mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+        if (fe > fo) mbar_complete_tx(&full[s], C::kStageBytes);
+        const uint32_t last = fe > fo ? fe : fo;
+        if (last > 0) mbar_wait_bounded(&full[s], (last - 1) & 1u, &never);
+      }
+    }
+    cluster_sync_all();
+  }
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc_pair(tmem_base, C::kTmemCols);

@@ -307,6 +307,19 @@ __device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_saddr
   return v;
 }
 
+// 32-bit store into shared memory of a CTA of the cluster (address from
+// map_to_cta); a later cluster barrier makes it visible there.
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_saddr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_saddr), "r"(v) : "memory");
+}
+
+// Count `bytes` as transferred on this CTA's mbarrier without any copy: the
+// share of a phase whose copy was never issued.
+__device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_saddr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_saddr)
                : "memory");

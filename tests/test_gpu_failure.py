@@ -36,9 +36,15 @@ def _operand(rows, k, fmt, seed):
     return q8, s, inv
 
 
-def test_split_gemm_wait_runs_out_and_the_workspace_recovers():
-    M, N, K = 16, 4096, 4096
-    assert q.gemm_describe(M, N, K).endswith("K split 4 ways")
+@pytest.mark.parametrize("M", [16, 256])
+def test_split_gemm_wait_runs_out_and_the_workspace_recovers(M):
+    """M = 16: the one-CTA kernel; M = 256: the CTA-pair kernel, whose
+    closing path then has both CTAs exchange their failure state and the even
+    CTA confirm every stage's last load before either CTA leaves."""
+    N, K = 4096, 4096
+    desc = q.gemm_describe(M, N, K)
+    assert desc.endswith("K split 4 ways"), desc
+    assert ("pair" in desc) == (M > 128), desc
     a8, sa, inva = _operand(M, K, oracle.E4M3, seed=71)
     b8, sb, invb = _operand(N, K, oracle.E4M3, seed=72)
     a, b = torch.from_numpy(a8).cuda(), torch.from_numpy(b8).cuda()

@@ -54,3 +54,38 @@ def test_noalloc_amax_matches_workspace_amax_twice():
         assert got.view(torch.int32).item() == ref.view(torch.int32).item()
         expect = np.max(np.abs(si.bf16_bits_to_f32(host)))
         assert got.item() == float(expect)
+
+
+def _noalloc_raw(x_ptr, rows, cols, ld):
+    lib = q.library()
+    out = torch.full((1,), -1.0, device="cuda")
+    st = lib.fp8lin_amax_noalloc(ctypes.c_void_p(x_ptr), rows, cols, ld,
+                                 ctypes.c_void_p(out.data_ptr()),
+                                 ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0, lib.fp8lin_status_string(st)
+    return out
+
+
+def test_noalloc_amax_empty_tensor_is_zero():
+    """rows == 0 or cols == 0: the amax of an empty tensor is exactly +0.0
+    (the call writes it; the -1 placed there beforehand must go)."""
+    x = torch.empty((0, 4096), dtype=torch.bfloat16, device="cuda")
+    for rows, cols in ((0, 4096), (64, 0)):
+        got = _noalloc_raw(x.data_ptr(), rows, cols, 4096)
+        torch.cuda.synchronize()
+        assert got.view(torch.int32).item() == 0
+
+
+def test_noalloc_amax_ignores_row_padding():
+    """A strided view (row stride ld > cols): the padding columns hold values
+    far above the tensor's own maximum and must not reach the amax."""
+    rows, cols, ld = 1040, 784, 1024
+    host = si.normal_bf16((rows, cols), 1.0, 43, 1)
+    full = np.full((rows, ld), 0x7F00, dtype=np.uint16)      # bf16 1.7e38 in the padding
+    full[:, :cols] = host
+    x = to_dev_bf16(full)
+    got = _noalloc_raw(x.data_ptr(), rows, cols, ld)
+    ref = _reference_amax(x[:, :cols], q.Workspace())
+    torch.cuda.synchronize()
+    assert got.view(torch.int32).item() == ref.view(torch.int32).item()
+    assert got.item() == float(np.max(np.abs(si.bf16_bits_to_f32(host))))
