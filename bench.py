@@ -24,8 +24,10 @@ the line to PATH.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
   python -m torch.distributed.run --nproc-per-node N bench.py --gpus N ...
 
-With N > 1 every rank runs an independent replica on its own GPU (the path
-has no exchange step); value is the sum over ranks, time the max over ranks.
+With N > 1 the Linear is split over the tokens: every rank runs M tokens on
+its own GPU with the whole job's tensorwise scales (one all-reduce(max) of
+the amax of x and of dY per step, quantised_gemm_gb300.sharded); value is the
+sum over ranks, time the max over ranks.
 """
 from __future__ import annotations
 
@@ -546,9 +548,10 @@ def cpu_baseline_sample(name, budget_s=12.0):
     return flop / elapsed / 1e12, desc, oracle.num_threads()
 
 
-def end_to_end(q, lin, x, w, dy, M, K, N, world, flop_step, steps):
-    """The same step through the host-buffer API (Fp8Linear.step_host):
-    pinned host inputs copied in and y, dX, dW copied out every step."""
+def end_to_end(q, lin, x, w, dy, M, K, N, world, flop_step):
+    """The same step through the C ABI's host-buffer entry point
+    (fp8lin_step_host, called by Fp8Linear.step_host): pinned host inputs
+    copied in and y, dX, dW copied out every step."""
     import torch
     hx = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
     hw = torch.from_numpy(w.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -556,7 +559,11 @@ def end_to_end(q, lin, x, w, dy, M, K, N, world, flop_step, steps):
     hy = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
     hdx = torch.empty((M, K), dtype=torch.bfloat16).pin_memory()
     hdw = torch.empty((N, K), dtype=torch.bfloat16).pin_memory()
-    n = max(3, min(20, steps // 10))
+    # Blocks of 12 steps whatever --steps says: the two device slots make the
+    # copies of one step overlap the compute of the next, a pipeline that
+    # needs several steps to reach its steady state (blocks of 3 measured
+    # 7.64 ms per step where blocks of 20 measured 6.65 ms on the same box).
+    n = 12
     for _ in range(2):
         lin.step_host(hx, hw, hdy, hy, hdx, hdw)
     torch.cuda.synchronize()
@@ -584,7 +591,8 @@ def end_to_end(q, lin, x, w, dy, M, K, N, world, flop_step, steps):
     return {"value": round(whole_job_tflops(flop_step, ms, world), 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3),
             "steps": n, "blocks_ms_per_step": [round(b, 3) for b in blocks],
-            "api": "Fp8Linear.step_host(wait=False) + finish_host (pinned host buffers)",
+            "api": "fp8lin_step_host via Fp8Linear.step_host(wait=False) + finish_host "
+                   "(pinned host buffers, two device slots)",
             "host_link": link, "copy_floor_ms": round(floor_ms, 3),
             "frac_of_copy_floor": round(floor_ms / ms, 3)}
 
@@ -656,11 +664,21 @@ def run_native(args):
 
     x, w, dy = make_inputs(args.workload, 0)
     xd, wd, dyd = to_dev(x, dev), to_dev(w, dev), to_dev(dy, dev)
-    lin = q.Fp8Linear(M, K, N, device=dev)
+    if world > 1:
+        # M-sharded over the ranks (weak scaling: M tokens per rank) with one
+        # tensorwise scale for the whole job: the amaxes of x and dY are
+        # all-reduced (max) before their casts.  dW stays per rank: its sum
+        # is the data-parallel gradient reduction, outside the Linear.
+        from quantised_gemm_gb300.sharded import ShardedFp8Linear
+        sharded = ShardedFp8Linear(M, K, N, reduce_dw=False, device=dev)
+        lin = sharded.lin
+        layer = sharded
+    else:
+        lin = layer = q.Fp8Linear(M, K, N, device=dev)
 
     def step():
-        lin.forward(xd, wd)
-        lin.backward(dyd)
+        layer.forward(xd, wd)
+        layer.backward(dyd)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -741,7 +759,7 @@ def run_native(args):
 
     e2e = None
     if not args.no_e2e:
-        e2e = end_to_end(q, lin, x, w, dy, M, K, N, world, flop_step, args.steps)
+        e2e = end_to_end(q, lin, x, w, dy, M, K, N, world, flop_step)
     del x, w, dy
     del lin, xd, wd, dyd
     torch.cuda.empty_cache()
@@ -803,7 +821,7 @@ def run_native(args):
             e2e_line = {k: e2e[k] for k in ("value", "unit", "h2d_bytes_per_step",
                                             "d2h_bytes_per_step", "ms_per_step",
                                             "frac_of_copy_floor")}
-            e2e_line["api"] = "Fp8Linear.step_host"
+            e2e_line["api"] = "fp8lin_step_host"
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": max(3, args.warmup),
@@ -812,7 +830,9 @@ def run_native(args):
             "data": "synthetic",
             "config": {"workload": "%s: Linear 4096->4096, M=%d, dynamic tensorwise" %
                                    (args.workload, M),
-                       "l2": "inputs > L2", "parallelism": "replicas" if world > 1 else "1 GPU"},
+                       "l2": "inputs > L2",
+                       "parallelism": "dp%d, M-sharded, global amax" % world if world > 1
+                       else "1 GPU"},
             "roofline": roofline, "cast_roofline": cast_roofline, "amax_cast_stage": stage,
             "kernel_us": kernel_us, "cpu_baseline": cpu, "e2e": e2e_line,
             "gpu_launches": int(launches), "clocks": clocks,

@@ -328,6 +328,62 @@ fp8lin_status fp8lin_backward(const void* dy, int64_t M, int64_t K, int64_t N,
                               void* dx, void* dw, float* dx_amax, float* dw_amax, void* ws,
                               size_t ws_bytes, cudaStream_t stream);
 
+/* ---- one step from host buffers --------------------------------------- */
+
+/* Caller-owned device side of one slot of fp8lin_step_host.  x, w, dy receive
+ * the step's inputs (bf16 [M, K], [N, K], [M, N]); y, dx, dw hold its outputs
+ * (bf16 [M, N], [M, K], [N, K]) until they are copied out; x8 ... dy8t and
+ * ws are as for fp8lin_forward / fp8lin_backward.  ev[0..4] are caller-created
+ * events (cudaEventCreateWithFlags(..., cudaEventDisableTiming)) that order
+ * this slot's copies against its compute; the library only records and waits
+ * on them.  Two slots used in turn let one step's copies run while the other
+ * slot's step computes: their bf16 buffers and events must be distinct, their
+ * fp8 buffers and workspace may be shared (all compute runs on one stream). */
+typedef struct fp8lin_step_slot {
+  void* x;
+  void* w;
+  void* dy;
+  void* y;
+  void* dx;
+  void* dw;
+  uint8_t* x8;
+  uint8_t* x8t;
+  uint8_t* w8;
+  uint8_t* w8t;
+  uint8_t* dy8;
+  uint8_t* dy8t;
+  void* ws;
+  size_t ws_bytes;
+  cudaEvent_t ev[5];
+} fp8lin_step_slot;
+
+/* One training step of the Linear from host memory: copies x_h, w_h, dy_h
+ * (host bf16, dense, pinned for the copies to be asynchronous) into the
+ * slot, runs fp8lin_forward and fp8lin_backward on `compute` (and, for each
+ * delayed state, the fp8lin_scale of sync_float8_amax_and_scale_history
+ * after backward, as in the repro script of "[float8] FP8 GPT 1.5B Delayed
+ * Scaling 2x Slower than BF16", pytorch/ao issue 1297), and copies y, dX, dW
+ * back into y_h, dx_h, dw_h.  Uploads run on `h2d`, downloads on `d2h`
+ * (one cudaMemcpyAsync per tensor), ordered by the slot's events:
+ *   - the uploads of x, W wait until this slot's previous forward has read
+ *     them, the upload of dY until its previous backward has;
+ *   - the forward waits for x, W and for this slot's previous downloads;
+ *     the backward waits for dY; y's download follows the forward (it
+ *     overlaps the backward), dX's and dW's the backward.
+ * With wait != 0, `compute` then waits for this step's downloads: the host
+ * buffers hold the results once `compute` has reached this point.  With
+ * wait == 0 the next step's compute may run while the downloads are in
+ * flight; make `compute` wait on slot->ev[4] (downloads done) before reading
+ * the host outputs.  Every argument is checked before anything is enqueued.
+ * The library allocates nothing; the host buffers and the slot are the
+ * caller's. */
+fp8lin_status fp8lin_step_host(const void* x_h, const void* w_h, const void* dy_h, void* y_h,
+                               void* dx_h, void* dw_h, int64_t M, int64_t K, int64_t N,
+                               fp8lin_scaling_state* sx, fp8lin_scaling_state* sw,
+                               fp8lin_scaling_state* sdy, const fp8lin_step_slot* slot,
+                               cudaStream_t compute, cudaStream_t h2d, cudaStream_t d2h,
+                               int wait);
+
 /* ---- measurement hooks ------------------------------------------------ */
 
 /* Count of kernels this library has launched in the process. */

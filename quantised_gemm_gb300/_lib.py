@@ -41,6 +41,15 @@ class ScalingStateC(ctypes.Structure):
     ]
 
 
+class StepSlotC(ctypes.Structure):
+    """Mirror of struct fp8lin_step_slot."""
+    _fields_ = [(n, ctypes.c_void_p) for n in ("x", "w", "dy", "y", "dx", "dw", "x8", "x8t", "w8",
+                                               "w8t", "dy8", "dy8t", "ws")] + [
+        ("ws_bytes", ctypes.c_size_t),
+        ("ev", ctypes.c_void_p * 5),
+    ]
+
+
 class Fp8linError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
@@ -82,6 +91,8 @@ _SIGNATURES = {
                                       _P, _P, _SZ, _P]),
     "fp8lin_backward": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _ST, _ST, _ST, _P, _P,
                                        _P, _P, _P, _P, _P, _SZ, _P]),
+    "fp8lin_step_host": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _ST, _ST, _ST,
+                                        ctypes.POINTER(StepSlotC), _P, _P, _P, ctypes.c_int]),
     "fp8lin_launch_count": (ctypes.c_uint64, []),
     "fp8lin_profile_enable": (None, [ctypes.c_int]),
     "fp8lin_profile_collect": (ctypes.c_int, [_P, _P]),

@@ -315,6 +315,14 @@ bool ws_ok(const void* ws) {
   return ws != nullptr && (reinterpret_cast<uintptr_t>(ws) & 255u) == 0;
 }
 
+fp8lin_status run_scale(const fp8lin_scaling_state* st, cudaStream_t stream) {
+  const bool delayed = st->kind == FP8LIN_DELAYED;
+  ProfScope ps(FP8LIN_PROF_SCALE, stream);
+  cudaError_t e = launch_scale(st->amax, st->scale, st->inv_scale, st->amax_history, st->head,
+                               delayed ? st->history_len : 1, delayed, st->fmt, st->eps, stream);
+  return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);
+}
+
 }  // namespace
 
 void set_error_site(const char* site) { g_error_site = site; }
@@ -453,11 +461,7 @@ fp8lin_status fp8lin_amax_noalloc(const void* x, int64_t rows, int64_t cols, int
 fp8lin_status fp8lin_scale(const fp8lin_scaling_state* st, cudaStream_t stream) {
   fp8lin_status s = check_state(st, true);
   if (s != FP8LIN_OK) return s;
-  const bool delayed = st->kind == FP8LIN_DELAYED;
-  ProfScope ps(FP8LIN_PROF_SCALE, stream);
-  cudaError_t e = launch_scale(st->amax, st->scale, st->inv_scale, st->amax_history, st->head,
-                               delayed ? st->history_len : 1, delayed, st->fmt, st->eps, stream);
-  return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);
+  return run_scale(st, stream);
 }
 
 fp8lin_status fp8lin_cast(const void* x, int64_t rows, int64_t cols, int64_t ld, int32_t fmt,
@@ -601,10 +605,15 @@ static bool dev_ptrs_ok(std::initializer_list<const void*> ps) {
   return true;
 }
 
-fp8lin_status fp8lin_forward(const void* x, const void* w, int64_t M, int64_t K, int64_t N,
-                             fp8lin_scaling_state* sx, fp8lin_scaling_state* sw, void* y,
-                             float* y_amax, uint8_t* x8, uint8_t* x8t, uint8_t* w8, uint8_t* w8t,
-                             void* ws, size_t ws_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+fp8lin_status check_forward(const void* x, const void* w, int64_t M, int64_t K, int64_t N,
+                            const fp8lin_scaling_state* sx, const fp8lin_scaling_state* sw,
+                            const void* y, const float* y_amax, const uint8_t* x8,
+                            const uint8_t* x8t, const uint8_t* w8, const uint8_t* w8t,
+                            const void* ws, size_t ws_bytes) {
   fp8lin_status s = check_linear_sizes(M, K, N);
   if (s != FP8LIN_OK) return s;
   if ((s = check_state(sx, true)) != FP8LIN_OK) return s;
@@ -618,9 +627,14 @@ fp8lin_status fp8lin_forward(const void* x, const void* w, int64_t M, int64_t K,
   if (w == nullptr && sw->kind == FP8LIN_DELAYED && sw->needs_init) return FP8LIN_EINVAL;
   if (M * N > 0 && !dev_ptrs_ok({y})) return FP8LIN_EINVAL;
   if (y_amax != nullptr && (reinterpret_cast<uintptr_t>(y_amax) & 3u) != 0) return FP8LIN_EINVAL;
-  DeviceInfo dev;
-  if ((s = get_dev(&dev)) != FP8LIN_OK) return s;
+  return FP8LIN_OK;
+}
 
+fp8lin_status run_forward(const void* x, const void* w, int64_t M, int64_t K, int64_t N,
+                          fp8lin_scaling_state* sx, fp8lin_scaling_state* sw, void* y,
+                          float* y_amax, uint8_t* x8, uint8_t* x8t, uint8_t* w8, uint8_t* w8t,
+                          void* ws, size_t ws_bytes, const DeviceInfo& dev, cudaStream_t stream) {
+  fp8lin_status s;
   if (sx->kind == FP8LIN_DYNAMIC)
     s = cast_dynamic_scaled(x, M, K, K, sx, x8, x8t, ws, dev, stream, true);
   else
@@ -638,12 +652,12 @@ fp8lin_status fp8lin_forward(const void* x, const void* w, int64_t M, int64_t K,
                  N, y_amax, ws, ws_bytes, dev, stream);
 }
 
-fp8lin_status fp8lin_backward(const void* dy, int64_t M, int64_t K, int64_t N,
-                              const uint8_t* x8t, const uint8_t* w8t,
-                              const fp8lin_scaling_state* sx, const fp8lin_scaling_state* sw,
-                              fp8lin_scaling_state* sdy, uint8_t* dy8, uint8_t* dy8t, void* dx,
-                              void* dw, float* dx_amax, float* dw_amax, void* ws, size_t ws_bytes,
-                              cudaStream_t stream) {
+fp8lin_status check_backward(const void* dy, int64_t M, int64_t K, int64_t N, const uint8_t* x8t,
+                             const uint8_t* w8t, const fp8lin_scaling_state* sx,
+                             const fp8lin_scaling_state* sw, const fp8lin_scaling_state* sdy,
+                             const uint8_t* dy8, const uint8_t* dy8t, const void* dx,
+                             const void* dw, const float* dx_amax, const float* dw_amax,
+                             const void* ws, size_t ws_bytes) {
   fp8lin_status s = check_linear_sizes(M, K, N);
   if (s != FP8LIN_OK) return s;
   if ((s = check_state(sx, false)) != FP8LIN_OK) return s;
@@ -659,9 +673,16 @@ fp8lin_status fp8lin_backward(const void* dy, int64_t M, int64_t K, int64_t N,
   if ((dx_amax != nullptr && (dx == nullptr || (reinterpret_cast<uintptr_t>(dx_amax) & 3u))) ||
       (dw_amax != nullptr && (dw == nullptr || (reinterpret_cast<uintptr_t>(dw_amax) & 3u))))
     return FP8LIN_EINVAL;
-  DeviceInfo dev;
-  if ((s = get_dev(&dev)) != FP8LIN_OK) return s;
+  return FP8LIN_OK;
+}
 
+fp8lin_status run_backward(const void* dy, int64_t M, int64_t K, int64_t N, const uint8_t* x8t,
+                           const uint8_t* w8t, const fp8lin_scaling_state* sx,
+                           const fp8lin_scaling_state* sw, fp8lin_scaling_state* sdy,
+                           uint8_t* dy8, uint8_t* dy8t, void* dx, void* dw, float* dx_amax,
+                           float* dw_amax, void* ws, size_t ws_bytes, const DeviceInfo& dev,
+                           cudaStream_t stream) {
+  fp8lin_status s;
   if (sdy->kind == FP8LIN_DYNAMIC)
     s = cast_dynamic_scaled(dy, M, N, N, sdy, dy8, dy8t, ws, dev, stream, true);
   else
@@ -679,6 +700,110 @@ fp8lin_status fp8lin_backward(const void* dy, int64_t M, int64_t K, int64_t N,
                 dw, K, dw_amax, ws, ws_bytes, dev, stream);
     if (s != FP8LIN_OK) return s;
   }
+  return FP8LIN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fp8lin_status fp8lin_forward(const void* x, const void* w, int64_t M, int64_t K, int64_t N,
+                             fp8lin_scaling_state* sx, fp8lin_scaling_state* sw, void* y,
+                             float* y_amax, uint8_t* x8, uint8_t* x8t, uint8_t* w8, uint8_t* w8t,
+                             void* ws, size_t ws_bytes, cudaStream_t stream) {
+  fp8lin_status s =
+      check_forward(x, w, M, K, N, sx, sw, y, y_amax, x8, x8t, w8, w8t, ws, ws_bytes);
+  if (s != FP8LIN_OK) return s;
+  DeviceInfo dev;
+  if ((s = get_dev(&dev)) != FP8LIN_OK) return s;
+  return run_forward(x, w, M, K, N, sx, sw, y, y_amax, x8, x8t, w8, w8t, ws, ws_bytes, dev,
+                     stream);
+}
+
+fp8lin_status fp8lin_backward(const void* dy, int64_t M, int64_t K, int64_t N,
+                              const uint8_t* x8t, const uint8_t* w8t,
+                              const fp8lin_scaling_state* sx, const fp8lin_scaling_state* sw,
+                              fp8lin_scaling_state* sdy, uint8_t* dy8, uint8_t* dy8t, void* dx,
+                              void* dw, float* dx_amax, float* dw_amax, void* ws, size_t ws_bytes,
+                              cudaStream_t stream) {
+  fp8lin_status s = check_backward(dy, M, K, N, x8t, w8t, sx, sw, sdy, dy8, dy8t, dx, dw, dx_amax,
+                                   dw_amax, ws, ws_bytes);
+  if (s != FP8LIN_OK) return s;
+  DeviceInfo dev;
+  if ((s = get_dev(&dev)) != FP8LIN_OK) return s;
+  return run_backward(dy, M, K, N, x8t, w8t, sx, sw, sdy, dy8, dy8t, dx, dw, dx_amax, dw_amax, ws,
+                      ws_bytes, dev, stream);
+}
+
+fp8lin_status fp8lin_step_host(const void* x_h, const void* w_h, const void* dy_h, void* y_h,
+                               void* dx_h, void* dw_h, int64_t M, int64_t K, int64_t N,
+                               fp8lin_scaling_state* sx, fp8lin_scaling_state* sw,
+                               fp8lin_scaling_state* sdy, const fp8lin_step_slot* slot,
+                               cudaStream_t compute, cudaStream_t h2d, cudaStream_t d2h,
+                               int wait) {
+  if (slot == nullptr) return FP8LIN_EINVAL;
+  const fp8lin_step_slot& d = *slot;
+  fp8lin_status s = check_forward(d.x, d.w, M, K, N, sx, sw, d.y, nullptr, d.x8, d.x8t, d.w8,
+                                  d.w8t, d.ws, d.ws_bytes);
+  if (s != FP8LIN_OK) return s;
+  if ((s = check_backward(d.dy, M, K, N, d.x8t, d.w8t, sx, sw, sdy, d.dy8, d.dy8t, d.dx, d.dw,
+                          nullptr, nullptr, d.ws, d.ws_bytes)) != FP8LIN_OK)
+    return s;
+  if (M * K > 0 && (x_h == nullptr || dx_h == nullptr || d.dx == nullptr)) return FP8LIN_EINVAL;
+  if (N * K > 0 && (w_h == nullptr || dw_h == nullptr || d.w == nullptr || d.dw == nullptr))
+    return FP8LIN_EINVAL;
+  if (M * N > 0 && (dy_h == nullptr || y_h == nullptr)) return FP8LIN_EINVAL;
+  for (cudaEvent_t e : d.ev)
+    if (e == nullptr) return FP8LIN_EINVAL;
+  DeviceInfo dev;
+  if ((s = get_dev(&dev)) != FP8LIN_OK) return s;
+
+  enum { kXwIn = 0, kDyIn = 1, kFwdDone = 2, kBwdDone = 3, kOutDone = 4 };
+  const size_t bx = static_cast<size_t>(M) * K * 2, bw = static_cast<size_t>(N) * K * 2,
+               by = static_cast<size_t>(M) * N * 2;
+  cudaError_t e;
+  // Uploads: x and W once this slot's previous forward has read them; dY once
+  // its previous backward has.
+  if ((e = cudaStreamWaitEvent(h2d, d.ev[kFwdDone], 0)) != cudaSuccess) return cuda_fail(e);
+  if (bx > 0 && (e = cudaMemcpyAsync(d.x, x_h, bx, cudaMemcpyHostToDevice, h2d)) != cudaSuccess)
+    return cuda_fail(e);
+  if (bw > 0 && (e = cudaMemcpyAsync(d.w, w_h, bw, cudaMemcpyHostToDevice, h2d)) != cudaSuccess)
+    return cuda_fail(e);
+  if ((e = cudaEventRecord(d.ev[kXwIn], h2d)) != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaStreamWaitEvent(h2d, d.ev[kBwdDone], 0)) != cudaSuccess) return cuda_fail(e);
+  if (by > 0 && (e = cudaMemcpyAsync(d.dy, dy_h, by, cudaMemcpyHostToDevice, h2d)) != cudaSuccess)
+    return cuda_fail(e);
+  if ((e = cudaEventRecord(d.ev[kDyIn], h2d)) != cudaSuccess) return cuda_fail(e);
+  // Forward once x and W are in and this slot's outputs have gone out.
+  if ((e = cudaStreamWaitEvent(compute, d.ev[kXwIn], 0)) != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaStreamWaitEvent(compute, d.ev[kOutDone], 0)) != cudaSuccess) return cuda_fail(e);
+  s = run_forward(d.x, d.w, M, K, N, sx, sw, d.y, nullptr, d.x8, d.x8t, d.w8, d.w8t, d.ws,
+                  d.ws_bytes, dev, compute);
+  if (s != FP8LIN_OK) return s;
+  if ((e = cudaEventRecord(d.ev[kFwdDone], compute)) != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaStreamWaitEvent(d2h, d.ev[kFwdDone], 0)) != cudaSuccess) return cuda_fail(e);
+  if (by > 0 && (e = cudaMemcpyAsync(y_h, d.y, by, cudaMemcpyDeviceToHost, d2h)) != cudaSuccess)
+    return cuda_fail(e);
+  // Backward once dY is in, then the delayed states' history sync.
+  if ((e = cudaStreamWaitEvent(compute, d.ev[kDyIn], 0)) != cudaSuccess) return cuda_fail(e);
+  s = run_backward(d.dy, M, K, N, d.x8t, d.w8t, sx, sw, sdy, d.dy8, d.dy8t, d.dx, d.dw, nullptr,
+                   nullptr, d.ws, d.ws_bytes, dev, compute);
+  if (s != FP8LIN_OK) return s;
+  for (const fp8lin_scaling_state* st : {static_cast<const fp8lin_scaling_state*>(sx),
+                                         static_cast<const fp8lin_scaling_state*>(sw),
+                                         static_cast<const fp8lin_scaling_state*>(sdy)}) {
+    if (st->kind != FP8LIN_DELAYED) continue;
+    if ((s = run_scale(st, compute)) != FP8LIN_OK) return s;
+  }
+  if ((e = cudaEventRecord(d.ev[kBwdDone], compute)) != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaStreamWaitEvent(d2h, d.ev[kBwdDone], 0)) != cudaSuccess) return cuda_fail(e);
+  if (bx > 0 && (e = cudaMemcpyAsync(dx_h, d.dx, bx, cudaMemcpyDeviceToHost, d2h)) != cudaSuccess)
+    return cuda_fail(e);
+  if (bw > 0 && (e = cudaMemcpyAsync(dw_h, d.dw, bw, cudaMemcpyDeviceToHost, d2h)) != cudaSuccess)
+    return cuda_fail(e);
+  if ((e = cudaEventRecord(d.ev[kOutDone], d2h)) != cudaSuccess) return cuda_fail(e);
+  if (wait && (e = cudaStreamWaitEvent(compute, d.ev[kOutDone], 0)) != cudaSuccess)
+    return cuda_fail(e);
   return FP8LIN_OK;
 }
 

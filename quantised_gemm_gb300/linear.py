@@ -11,10 +11,13 @@ once, through PyTorch; the library itself allocates nothing.
 """
 from __future__ import annotations
 
+import ctypes
+
 import torch
 
+from . import _lib
 from . import (AMAX_AUTO, AMAX_PRECOMPUTED, DELAYED, DYNAMIC, E4M3, E5M2, ScalingState,
-               Workspace, backward, forward, scale)
+               Workspace, _stream, backward, forward, scale)
 
 
 class Fp8Linear:
@@ -72,91 +75,78 @@ class Fp8Linear:
         if self.sw.kind == DELAYED:
             self._w_key = None
 
-    copy_lanes = 1   # copy streams per direction; with more, each tensor moves in row slices
+    def _step_slots(self):
+        """Two device slots for step_host, created on first use: the bf16
+        inputs and outputs and five events each (the fp8 copies and the
+        workspace are shared: all compute runs on one stream)."""
+        if getattr(self, "_slots", None) is not None:
+            return self._slots
+        dev = self.y.device
+        cur = torch.cuda.current_stream(dev)
+        mk = lambda r, c: torch.empty((r, c), dtype=torch.bfloat16, device=dev)  # noqa: E731
+        slots = []
+        for k in range(2):
+            bufs = {"x": mk(self.M, self.K), "w": mk(self.N, self.K), "dy": mk(self.M, self.N),
+                    "y": self.y if k == 0 else mk(self.M, self.N),
+                    "dx": self.dx if k == 0 else mk(self.M, self.K),
+                    "dw": self.dw if k == 0 else mk(self.N, self.K)}
+            evs = [torch.cuda.Event() for _ in range(5)]
+            for ev in evs:
+                ev.record(cur)                  # creates the event (torch creates it lazily)
+            c = _lib.StepSlotC()
+            for name, t in bufs.items():
+                setattr(c, name, t.data_ptr())
+            for name in ("x8", "x8t", "w8", "w8t", "dy8", "dy8t"):
+                setattr(c, name, getattr(self, name).data_ptr())
+            c.ws, c.ws_bytes = self.ws.ptr, self.ws.nbytes
+            for i, ev in enumerate(evs):
+                c.ev[i] = ev.cuda_event
+            slots.append((bufs, evs, c))
+        self._slots = slots
+        self._slot = 0
+        self._h2d = torch.cuda.Stream(device=dev)
+        self._d2h = torch.cuda.Stream(device=dev)
+        return slots
 
     def step_host(self, x_h, w_h, dy_h, y_h, dx_h, dw_h, stream=None, wait=True):
-        """End-to-end step from host buffers (pinned, for asynchronous copies):
-        copy x, W, dY in, forward + backward (+ delayed sync), copy y, dX, dW
-        out.  The copies run on copy streams of their own (``copy_lanes`` per
-        direction; with more than one, each moves a slice of the rows -- one
-        per direction measured fastest on a 4096 x 65536 step), ordered by
-        events.  Device inputs and outputs come in two slots used in turn, so
-        a step's uploads need only the step two back to be done with its slot:
-        dY's upload overlaps the forward, y's download the backward, and the
-        next step's uploads this step's compute.
-
-        The compute runs on `stream` (default: the current stream).  With
-        wait=True it waits, at the end, for this step's downloads: the host
-        buffers hold the results.  With wait=False the next step's compute may
-        run while those downloads are still in flight (the host link then
-        sets the pace, both directions busy at once); the host buffers are
-        complete after finish_host(), and a later step overwrites them.
-        Device slots and copy streams are created on the first call."""
-        main = stream if stream is not None else torch.cuda.current_stream()
-        n = self.copy_lanes
-        if not hasattr(self, "_slots"):
-            dev = self.y.device
-            mk = lambda r, c: torch.empty((r, c), dtype=torch.bfloat16, device=dev)  # noqa: E731
-            self._slots = []
-            for k in range(2):
-                sl = {"x": mk(self.M, self.K), "w": mk(self.N, self.K), "dy": mk(self.M, self.N),
-                      "y": self.y if k == 0 else mk(self.M, self.N),
-                      "dx": self.dx if k == 0 else mk(self.M, self.K),
-                      "dw": self.dw if k == 0 else mk(self.N, self.K),
-                      "fwd_done": torch.cuda.Event(), "bwd_done": torch.cuda.Event(),
-                      "downloads": []}
-                sl["fwd_done"].record(main)
-                sl["bwd_done"].record(main)
-                self._slots.append(sl)
-            self._slot = 0
-            self._up = [torch.cuda.Stream(device=dev) for _ in range(n)]
-            self._down = [torch.cuda.Stream(device=dev) for _ in range(n)]
-
-        def move(pairs, streams, after):
-            """Copy each (dst, src) in row slices over `streams` once `after`
-            has fired; returns the events marking each stream's end."""
-            done = []
-            for i, st in enumerate(streams):
-                st.wait_event(after)
-                with torch.cuda.stream(st):
-                    for dst, src in pairs:
-                        rows = dst.shape[0]
-                        lo, hi = rows * i // len(streams), rows * (i + 1) // len(streams)
-                        if hi > lo:
-                            dst[lo:hi].copy_(src[lo:hi], non_blocking=True)
-                    ev = torch.cuda.Event()
-                    ev.record(st)
-                    done.append(ev)
-            return done
-
-        sl = self._slots[self._slot]
+        """End-to-end step from host buffers through fp8lin_step_host: copy x,
+        W, dY in, forward + backward (+ the delayed scales' sync), copy y, dX,
+        dW out.  Host tensors: bf16, contiguous, pinned for the copies to be
+        asynchronous.  Uploads and downloads run on two copy streams of this
+        Linear, ordered against the compute by the slot's events; the two
+        device slots are used in turn, so a step's copies overlap the other
+        slot's compute.  The compute runs on `stream` (default: the current
+        stream).  With wait=True that stream then waits for this step's
+        downloads; with wait=False the next step may start while they are in
+        flight -- finish_host() makes the stream wait for all of them."""
+        for t, n, shape in ((x_h, "x_h", (self.M, self.K)), (w_h, "w_h", (self.N, self.K)),
+                            (dy_h, "dy_h", (self.M, self.N)), (y_h, "y_h", (self.M, self.N)),
+                            (dx_h, "dx_h", (self.M, self.K)), (dw_h, "dw_h", (self.N, self.K))):
+            if t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or \
+                    tuple(t.shape) != shape:
+                raise ValueError("%s must be a contiguous host bf16 tensor of shape %s" %
+                                 (n, shape))
+        slots = self._step_slots()
+        bufs, evs, c = slots[self._slot]
         self._slot ^= 1
-        # this slot's inputs are free once the step two back has consumed them
-        xw_in = move([(sl["x"], x_h), (sl["w"], w_h)], self._up, sl["fwd_done"])
-        dy_in = move([(sl["dy"], dy_h)], self._up, sl["bwd_done"])
-        for ev in sl["downloads"] + xw_in:        # its outputs once downloaded
-            main.wait_event(ev)
-        self.y, self.dx, self.dw = sl["y"], sl["dx"], sl["dw"]
-        self.forward(sl["x"], sl["w"], main)
-        sl["fwd_done"].record(main)
-        y_out = move([(y_h, sl["y"])], self._down, sl["fwd_done"])
-        for ev in dy_in:
-            main.wait_event(ev)
-        self.backward(sl["dy"], stream=main)
-        self.sync_scales(main)
-        sl["bwd_done"].record(main)
-        sl["downloads"] = y_out + move([(dx_h, sl["dx"]), (dw_h, sl["dw"])], self._down,
-                                       sl["bwd_done"])
-        if wait:
-            self.finish_host(main)
+        cx, cw, cd = self.sx.c_struct(), self.sw.c_struct(), self.sdy.c_struct()
+        st = _lib.load().fp8lin_step_host(
+            x_h.data_ptr(), w_h.data_ptr(), dy_h.data_ptr(), y_h.data_ptr(), dx_h.data_ptr(),
+            dw_h.data_ptr(), self.M, self.K, self.N, ctypes.byref(cx), ctypes.byref(cw),
+            ctypes.byref(cd), ctypes.byref(c), _stream(stream), self._h2d.cuda_stream,
+            self._d2h.cuda_stream, 1 if wait else 0)
+        for state in (self.sx, self.sw, self.sdy):
+            state._pull()
+        _lib.check(st, "fp8lin_step_host")
+        self.y, self.dx, self.dw = bufs["y"], bufs["dx"], bufs["dw"]
+        self._w_key = None      # W was cast from the slot's copy
         return y_h, dx_h, dw_h
 
     def finish_host(self, stream=None):
         """Make `stream` wait until every download of step_host is complete."""
         main = stream if stream is not None else torch.cuda.current_stream()
-        for sl in getattr(self, "_slots", []):
-            for ev in sl["downloads"]:
-                main.wait_event(ev)
+        for _, evs, _ in getattr(self, "_slots", None) or []:
+            main.wait_event(evs[4])
 
     def step(self, x, w, dy, stream=None):
         """One forward + backward (+ delayed sync)."""

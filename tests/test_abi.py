@@ -136,3 +136,38 @@ def test_gemm_describe_argument_errors(lib):
     # without a GPU the valid call reports a CUDA error and leaves an empty line
     st = lib.fp8lin_gemm_describe(16, 16, 16, buf, 64)
     assert st in (L.OK, L.ECUDA) and (st == L.OK or buf.value == b"")
+
+
+def test_cast_delayed_step_host_and_profile_argument_errors(lib):
+    import quantised_gemm_gb300._lib as L
+    p = ctypes.c_void_p(0x10000)
+    ws = ctypes.c_void_p(0x20000)
+    nb = lib.fp8lin_workspace_bytes(128, 128, 128)
+    # the delayed cast wants a delayed state, a workspace and an output
+    dyn, dly = _state(0), _state(0, kind=1, H=4)
+    assert lib.fp8lin_cast_delayed(p, 128, 128, 128, ctypes.byref(dyn), p, p, ws, None) == L.EINVAL
+    assert lib.fp8lin_cast_delayed(p, 128, 128, 128, ctypes.byref(dly), p, p, None, None) == \
+        L.EINVAL
+    assert lib.fp8lin_cast_delayed(p, 128, 128, 128, ctypes.byref(dly), None, None, ws, None) == \
+        L.EINVAL
+    assert lib.fp8lin_cast_delayed(p, 120, 128, 128, ctypes.byref(dly), p, p, ws, None) == \
+        L.EUNSUPPORTED                                              # transposed copy: rows % 16
+    # the host step checks its slot, sizes, states and events before anything else
+    sx, sw, sd = _state(0), _state(0), _state(1)
+    slot = L.StepSlotC()
+    for name in ("x", "w", "dy", "y", "dx", "dw", "x8", "x8t", "w8", "w8t", "dy8", "dy8t"):
+        setattr(slot, name, 0x10000)
+    slot.ws, slot.ws_bytes = 0x20000, nb
+    step = lambda M, s, sdy=sd: lib.fp8lin_step_host(
+        p, p, p, p, p, p, M, 128, 128, ctypes.byref(sx), ctypes.byref(sw), ctypes.byref(sdy),
+        s, None, None, None, 1)
+    assert step(128, None) == L.EINVAL                             # no slot
+    assert step(128, ctypes.byref(slot)) == L.EINVAL               # events missing
+    for i in range(5):
+        slot.ev[i] = 0x60000 + 64 * i                              # never used: checks fail first
+    assert step(100, ctypes.byref(slot)) == L.EUNSUPPORTED         # M % 16
+    assert step(128, ctypes.byref(slot), sdy=_state(0)) == L.EUNSUPPORTED   # grad_output e5m2
+    slot.dx = 0
+    assert step(128, ctypes.byref(slot)) == L.EINVAL               # the step needs dX's buffer
+    # the launch-ordered profile record wants both arrays
+    assert lib.fp8lin_profile_launches(None, None, 4) == -L.EINVAL

@@ -96,15 +96,15 @@ def test_bad_arguments_raise_without_launch():
     assert q.launch_count() == before
 
 
-@pytest.mark.parametrize("lanes", [1, 3])
-def test_step_host_matches_device_path(lanes):
-    """The host-buffer API (overlapped uploads / downloads on copy streams,
-    one stream per direction or row slices over three) returns the same
-    bits as the device path, over consecutive steps."""
-    M, K, N = 560, 768, 1024                      # 560 rows: slices of 186/187/187
-    dev_lin = q.Fp8Linear(M, K, N)
-    host_lin = q.Fp8Linear(M, K, N)
-    host_lin.copy_lanes = lanes
+@pytest.mark.parametrize("scaling", ["dynamic", "delayed"])
+def test_step_host_matches_device_path(scaling):
+    """The host-buffer step (fp8lin_step_host: uploads and downloads on copy
+    streams, ordered by the slot's events, two slots used in turn) returns
+    the bits of the device path, over consecutive steps; with delayed
+    scaling the history sync runs inside the step as well."""
+    M, K, N = 560, 768, 1024
+    dev_lin = q.Fp8Linear(M, K, N, scaling=scaling, history_len=4)
+    host_lin = q.Fp8Linear(M, K, N, scaling=scaling, history_len=4)
     hy = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
     hdx = torch.empty((M, K), dtype=torch.bfloat16).pin_memory()
     hdw = torch.empty((N, K), dtype=torch.bfloat16).pin_memory()
@@ -118,6 +118,27 @@ def test_step_host_matches_device_path(lanes):
         assert torch.equal(hy.view(torch.int16), dev_lin.y.cpu().view(torch.int16)), step
         assert torch.equal(hdx.view(torch.int16), dev_lin.dx.cpu().view(torch.int16)), step
         assert torch.equal(hdw.view(torch.int16), dev_lin.dw.cpu().view(torch.int16)), step
+        for a, b in ((host_lin.sx, dev_lin.sx), (host_lin.sw, dev_lin.sw),
+                     (host_lin.sdy, dev_lin.sdy)):
+            assert dev_f32_bits(a.scale) == dev_f32_bits(b.scale), step
+
+
+def test_step_host_rejects_bad_arguments_without_launch():
+    lin = q.Fp8Linear(128, 256, 192)
+    good = dict(x_h=torch.empty((128, 256), dtype=torch.bfloat16),
+                w_h=torch.empty((192, 256), dtype=torch.bfloat16),
+                dy_h=torch.empty((128, 192), dtype=torch.bfloat16),
+                y_h=torch.empty((128, 192), dtype=torch.bfloat16),
+                dx_h=torch.empty((128, 256), dtype=torch.bfloat16),
+                dw_h=torch.empty((192, 256), dtype=torch.bfloat16))
+    before = q.launch_count()
+    bad = dict(good, x_h=torch.empty((128, 256), dtype=torch.bfloat16, device="cuda"))
+    with pytest.raises(ValueError):
+        lin.step_host(**bad)
+    lin.sdy.fmt = E4M3                    # wrong format for the grad_output role
+    with pytest.raises(q.Fp8linError):
+        lin.step_host(**good)
+    assert q.launch_count() == before
 
 
 def _bits(t: torch.Tensor) -> np.ndarray:
