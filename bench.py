@@ -272,7 +272,9 @@ def profiled(q, torch, step, n, flush=None):
     kinds = {}
     for k, ms in recs:
         kinds[k] = kinds.get(k, 0.0) + ms / n
-    gemms = [ms for k, ms in recs if k == "gemm"]
+    # the products of a step, in order: GEMM launches, and the few-token
+    # launches that fuse a product with its casts
+    gemms = [ms for k, ms in recs if k in ("gemm", "small_m")]
     per = len(gemms) // n if n else 0
     gemm_each = [sum(gemms[i + j * per] for j in range(n)) / n for i in range(per)]
     return kinds, gemm_each, len(recs) // max(1, n)
@@ -731,31 +733,34 @@ def run_native(args):
     one_pass = [n for n in (M * K, N * K, M * N) if n <= cap]
     cast_ms, fused_ms = kinds.get("cast", 0.0), kinds.get("cast_fused", 0.0)
     amax_ms, scale_ms = kinds.get("amax", 0.0), kinds.get("scale", 0.0)
+    cast_roofline = None
     if two_pass and cast_ms > 0:
-        kernel_bytes = 4.0 * sum(two_pass)
-        cast_gbs = kernel_bytes / (cast_ms * 1e-3) / 1e9
-        cast_kernel = "cast_stream_kernel"
-    else:
-        kernel_bytes = 4.0 * sum(one_pass)
-        cast_gbs = kernel_bytes / (max(fused_ms, 1e-9) * 1e-3) / 1e9
-        cast_kernel = "cast_single_pass_kernel"
-    trc = load_traffic("cast")
-    cast_roofline = {"bound": "hbm", "achieved": round(cast_gbs, 1), "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": round(cast_gbs / peaks["hbm_gbs"], 3),
-                     "traffic": trc["bytes_per_launch"] if trc else None, "kernel": cast_kernel}
+        kernel_bytes, kernel_ms, cast_kernel = 4.0 * sum(two_pass), cast_ms, "cast_stream_kernel"
+    elif fused_ms > 0:
+        kernel_bytes, kernel_ms, cast_kernel = 4.0 * sum(one_pass), fused_ms, "cast_single_pass_kernel"
+    else:                     # (a few-token step runs its casts inside the products)
+        kernel_ms = 0.0
+    if kernel_ms > 0:
+        cast_gbs = kernel_bytes / (kernel_ms * 1e-3) / 1e9
+        trc = load_traffic("cast")
+        cast_roofline = {"bound": "hbm", "achieved": round(cast_gbs, 1), "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(cast_gbs / peaks["hbm_gbs"], 3),
+                         "traffic": trc["bytes_per_launch"] if trc else None,
+                         "kernel": cast_kernel}
     # The whole amax + scale + cast stage against its algorithmic bytes (one
     # read, one write per fp8 copy); a second read by two-pass amax counts as
     # time.  Two-pass dynamic scaling moves 6 B per element for 4 algorithmic
     # ones, so its ceiling is 2/3 of HBM.
     stage_bytes = 4.0 * (M * K + N * K + M * N)
     stage_ms = cast_ms + fused_ms + amax_ms + scale_ms
-    stage_frac = stage_bytes / (stage_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]
-    stage = {"us": round(stage_ms * 1e3, 1), "frac": round(stage_frac, 3),
-             "of_two_pass_ceiling": round(stage_frac / (4.0 / 6.0), 3)}
-    kernel_us = {"gemm_y": round(gemm_each[0] * 1e3, 1), "gemm_dx": round(gemm_each[1] * 1e3, 1),
-                 "gemm_dw": round(gemm_each[2] * 1e3, 1), "cast": round(cast_ms * 1e3, 1),
-                 "cast_fused": round(fused_ms * 1e3, 1), "amax": round(amax_ms * 1e3, 1),
-                 "scale": round(scale_ms * 1e3, 1)}
+    stage = None
+    if stage_ms > 0:          # (a few-token step runs its casts inside the products)
+        stage_frac = stage_bytes / (stage_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]
+        stage = {"us": round(stage_ms * 1e3, 1), "frac": round(stage_frac, 3),
+                 "of_two_pass_ceiling": round(stage_frac / (4.0 / 6.0), 3)}
+    kernel_us = {k: round(v * 1e3, 1) for k, v in zip(("y", "dx", "dw"), gemm_each)}
+    kernel_us.update({"cast": round(cast_ms * 1e3, 1), "cast_fused": round(fused_ms * 1e3, 1),
+                      "amax": round(amax_ms * 1e3, 1), "scale": round(scale_ms * 1e3, 1)})
 
     e2e = None
     if not args.no_e2e:

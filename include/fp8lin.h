@@ -397,7 +397,9 @@ uint64_t fp8lin_launch_count(void);
  * thread-safe; not for use under CUDA graph capture. */
 enum {
   FP8LIN_PROF_AMAX = 0, FP8LIN_PROF_SCALE = 1, FP8LIN_PROF_CAST = 2,
-  FP8LIN_PROF_CAST_FUSED = 3, FP8LIN_PROF_GEMM = 4, FP8LIN_PROF_KINDS = 5
+  FP8LIN_PROF_CAST_FUSED = 3, FP8LIN_PROF_GEMM = 4,
+  FP8LIN_PROF_SMALL_M = 5,   /* a few-token product fused with its casts */
+  FP8LIN_PROF_KINDS = 6
 };
 void fp8lin_profile_enable(int on);
 fp8lin_status fp8lin_profile_collect(double* ms, int64_t* count);

@@ -21,7 +21,7 @@ AMAX_ATOMIC, AMAX_REDUCTION, AMAX_SINGLE_PASS, AMAX_AUTO, AMAX_PRECOMPUTED = 0, 
 # fp8lin_scaling
 DYNAMIC, DELAYED = 0, 1
 # profile kinds
-PROF_KINDS = ("amax", "scale", "cast", "cast_fused", "gemm")
+PROF_KINDS = ("amax", "scale", "cast", "cast_fused", "gemm", "small_m")
 
 
 class ScalingStateC(ctypes.Structure):

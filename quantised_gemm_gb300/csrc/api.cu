@@ -386,7 +386,7 @@ const char* fp8lin_last_error_detail(void) {
   return g_last_cuda_error == 0 ? "" : g_error_detail;
 }
 
-int fp8lin_version(void) { return 100; }
+int fp8lin_version(void) { return 101; }
 
 size_t fp8lin_workspace_bytes(int64_t M, int64_t K, int64_t N) {
   (void)M;
@@ -630,10 +630,93 @@ fp8lin_status check_forward(const void* x, const void* w, int64_t M, int64_t K, 
   return FP8LIN_OK;
 }
 
+// Few-token products run as one fused launch each (small_m.cu) when the
+// token side has dynamic scaling; FP8LIN_SMALL_M=0 turns this off.
+bool small_m_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("FP8LIN_SMALL_M");
+    return !(v != nullptr && v[0] == '0');
+  }();
+  return on;
+}
+
+bool few_token_state(const fp8lin_scaling_state* st, int64_t M) {
+  return small_m_enabled() && M >= 1 && M <= kSmallMaxRows && st->kind == FP8LIN_DYNAMIC &&
+         (st->amax_algo == FP8LIN_AMAX_AUTO || st->amax_algo == FP8LIN_AMAX_SINGLE_PASS ||
+          st->amax_algo == FP8LIN_AMAX_PRECOMPUTED);
+}
+
+size_t split_bytes(size_t ws_bytes) {
+  return ws_bytes > kWsSplitOffset ? ws_bytes - kWsSplitOffset : 0;
+}
+
+// The fused few-token product D = B8 . A8^T (token side B cast in the launch).
+SmallMArgs small_m_args(const fp8lin_scaling_state* sb, const void* b, int64_t M, uint8_t* b8,
+                        uint8_t* b8t, void* d, int64_t ldd, float* d_amax, void* ws,
+                        size_t ws_bytes) {
+  SmallMArgs a = {};
+  a.MB = M;
+  a.b = static_cast<const uint16_t*>(b);
+  a.eps = sb->eps;
+  a.fmt_b = sb->fmt;
+  a.b_amax_in = sb->amax_algo == FP8LIN_AMAX_PRECOMPUTED ? sb->amax : nullptr;
+  a.b_amax = sb->amax;
+  a.b_scale = sb->scale;
+  a.b_inv = sb->inv_scale;
+  a.b8 = b8;
+  a.b8t = b8t;
+  a.d = d;
+  a.ldd = ldd;
+  a.d_amax = reinterpret_cast<uint32_t*>(d_amax);
+  a.ws_amax_acc = ws_u32(ws, kWsGemmAmaxAccOffset);
+  a.ws_amax_ticket = ws_u32(ws, kWsGemmAmaxTicketOffset);
+  a.ws_partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kWsSplitOffset);
+  a.ws_partial_bytes = split_bytes(ws_bytes);
+  a.ws_tickets = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + kWsTicketOffset);
+  a.ws_barrier = ws_u32(ws, kWsBarrierOffset);
+  a.ws_exits = ws_u32(ws, kWsExitsOffset);
+  a.ws_amax = ws_u32(ws, kWsAmaxOffset);
+  a.ws_b_amax = ws_u32(ws, kWsSmallBAmaxOffset);
+  a.ws_error = ws_error(ws);
+  return a;
+}
+
+fp8lin_status run_small_m(const SmallMArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
+  ProfScope ps(FP8LIN_PROF_SMALL_M, stream);
+  cudaError_t e = launch_small_m(a, dev, stream);
+  return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);
+}
+
 fp8lin_status run_forward(const void* x, const void* w, int64_t M, int64_t K, int64_t N,
                           fp8lin_scaling_state* sx, fp8lin_scaling_state* sw, void* y,
                           float* y_amax, uint8_t* x8, uint8_t* x8t, uint8_t* w8, uint8_t* w8t,
                           void* ws, size_t ws_bytes, const DeviceInfo& dev, cudaStream_t stream) {
+  // A few tokens: x's cast, W's cast (unless W8 is reused) and y in one launch.
+  if (K > 0 && N > 0 && few_token_state(sx, M)) {
+    const bool cast_w = w != nullptr;
+    const bool w_ok = !cast_w || (sw->kind == FP8LIN_DYNAMIC &&
+                                  (sw->amax_algo == FP8LIN_AMAX_AUTO ||
+                                   sw->amax_algo == FP8LIN_AMAX_SINGLE_PASS));
+    if (w_ok && small_m_fits(dev, cast_w, 0, M, N, K, split_bytes(ws_bytes))) {
+      SmallMArgs a = small_m_args(sx, x, M, x8, x8t, y, N, y_amax, ws, ws_bytes);
+      a.cast_a = cast_w;
+      a.NA = N;
+      a.KA = K;
+      a.ldb = K;
+      if (cast_w) {
+        a.a = w;
+        a.a8 = w8;
+        a.a8t = w8t;
+        a.a_amax = sw->amax;
+        a.a_scale = sw->scale;
+        a.a_inv = sw->inv_scale;
+      } else {
+        a.a = w8;
+        a.a_inv_in = sw->inv_scale;
+      }
+      return run_small_m(a, dev, stream);
+    }
+  }
   fp8lin_status s;
   if (sx->kind == FP8LIN_DYNAMIC)
     s = cast_dynamic_scaled(x, M, K, K, sx, x8, x8t, ws, dev, stream, true);
@@ -683,12 +766,26 @@ fp8lin_status run_backward(const void* dy, int64_t M, int64_t K, int64_t N, cons
                            float* dw_amax, void* ws, size_t ws_bytes, const DeviceInfo& dev,
                            cudaStream_t stream) {
   fp8lin_status s;
-  if (sdy->kind == FP8LIN_DYNAMIC)
+  bool dx_done = false;
+  if (dx != nullptr && K > 0 && N > 0 && few_token_state(sdy, M) &&
+      small_m_fits(dev, false, FP8LIN_E5M2, M, K, N, split_bytes(ws_bytes))) {
+    // A few tokens: dY's cast and dX = dY8 . W8 (A = W8^T [K, N]) in one launch.
+    SmallMArgs a = small_m_args(sdy, dy, M, dy8, dy8t, dx, K, dx_amax, ws, ws_bytes);
+    a.cast_a = false;
+    a.NA = K;
+    a.KA = N;
+    a.ldb = N;
+    a.a = w8t;
+    a.a_inv_in = sw->inv_scale;
+    if ((s = run_small_m(a, dev, stream)) != FP8LIN_OK) return s;
+    dx_done = true;
+  } else if (sdy->kind == FP8LIN_DYNAMIC) {
     s = cast_dynamic_scaled(dy, M, N, N, sdy, dy8, dy8t, ws, dev, stream, true);
-  else
+  } else {
     s = delayed_cast(dy, M, N, N, sdy, dy8, dy8t, ws, dev, stream);
-  if (s != FP8LIN_OK) return s;
-  if (dx != nullptr) {
+  }
+  if (!dx_done && s != FP8LIN_OK) return s;
+  if (dx != nullptr && !dx_done) {
     // dX = dY8 . W8 : A = dY8 [M, N], B = W8^T [K, N], contract over N
     s = do_gemm(dy8, w8t, M, K, N, N, N, FP8LIN_E5M2, FP8LIN_E4M3, sdy->inv_scale, sw->inv_scale,
                 dx, K, dx_amax, ws, ws_bytes, dev, stream);

@@ -18,6 +18,7 @@ constexpr size_t kWsAtomicAccOffset = 192;     // uint32: ticketed amax accumula
 constexpr size_t kWsAtomicTicketOffset = 196;  // uint32: ticketed amax arrivals
 constexpr size_t kWsGemmAmaxAccOffset = 200;     // uint32: GEMM output amax accumulator
 constexpr size_t kWsGemmAmaxTicketOffset = 204;  // uint32: GEMM epilogue warps arrived
+constexpr size_t kWsSmallBAmaxOffset = 208;      // uint32: few-token product, token-side amax
 constexpr size_t kWsScratchBegin = 64;    // [64, 256): self-cleaning counters
 constexpr size_t kWsPartialOffset = 256;  // uint32[kMaxPartials]: REDUCTION partial maxima
 constexpr int kMaxPartials = 4096;
@@ -174,6 +175,55 @@ bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, 
 // Record a failed tensor-map encoding (with its CUresult) as the error site;
 // returns cudaErrorInvalidValue.
 cudaError_t map_failed(const char* what);
+
+// ---- few-token products fused with their casts (small_m.cu)
+//
+// D [MB, NA] = B8 [MB, KA] . A8 [NA, KA]^T * inv_b * inv_a in one launch, for
+// MB <= kSmallMaxRows tokens: B (bf16) is cast with a dynamic tensorwise
+// scale in the same launch (its amax computed, or given by b_amax_in), and
+// with cast_a the bf16 A (the weight) too (cooperative launch: its amax is a
+// grid-wide reduction).  Writes B's fp8 copies and state, A's with cast_a,
+// and D (+ its amax).
+constexpr int kSmallMaxRows = 32;
+struct SmallMArgs {
+  bool cast_a;
+  int fmt_b;
+  int64_t MB, NA, KA;
+  const void* a;            // cast_a: bf16 A [NA, KA]; else fp8 A8 [NA, KA] (dense)
+  uint8_t* a8;              // cast_a: fp8 outputs A8 [NA, KA] and A8^T [KA, NA]
+  uint8_t* a8t;
+  float* a_amax;            // cast_a: A's state outputs
+  float* a_scale;
+  float* a_inv;
+  const float* a_inv_in;    // !cast_a: A's inverse scale
+  const uint16_t* b;        // bf16 B [MB, KA], row stride ldb
+  int64_t ldb;
+  float eps;
+  const float* b_amax_in;   // nullptr: computed in the launch
+  float* b_amax;
+  float* b_scale;
+  float* b_inv;
+  uint8_t* b8;              // fp8 B [MB, KA] and B^T [KA, MB]
+  uint8_t* b8t;
+  void* d;                  // bf16 D [MB, NA], row stride ldd
+  int64_t ldd;
+  uint32_t* d_amax;
+  uint32_t* ws_amax_acc;
+  uint32_t* ws_amax_ticket;
+  float* ws_partials;
+  size_t ws_partial_bytes;
+  int* ws_tickets;
+  uint32_t* ws_barrier;
+  uint32_t* ws_exits;
+  uint32_t* ws_amax;
+  uint32_t* ws_b_amax;
+  int* ws_error;
+};
+// Whether launch_small_m takes these sizes on this device with this much
+// workspace for partials.
+bool small_m_fits(const DeviceInfo& dev, bool cast_a, int fmt_b, int64_t MB, int64_t NA,
+                  int64_t KA, size_t partial_bytes);
+cudaError_t launch_small_m(const SmallMArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 
 // ---- GEMM (gemm_tcgen05.cu)
 

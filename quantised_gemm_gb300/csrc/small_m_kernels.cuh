@@ -1,0 +1,535 @@
+// small_m_kernels.cuh -- device code of the few-token Linear products: a
+// GEMM with few rows (M <= 32 tokens) against a large weight, fused with the
+// casts around it, in ONE launch per product.
+//
+//   D [M, NA] = (B8 [M, KA] . A8 [NA, KA]^T) * inv_b * inv_a      (bf16)
+//
+// A is the weight side (W8 for y, W8^T for dX), B the few-token side (x for
+// y, dY for dX).  With few tokens the products are short of work and long on
+// fixed costs: the step of a 16-token 4096 x 4096 Linear ran as six kernels
+// whose boundaries cost more than their bytes.  Here one kernel
+//   1. loads its A tiles (128 x 128) by TMA -- bf16 W when kCastA (the weight
+//      is cast in the same launch), else the fp8 copy; the CTA owning each
+//      128-column slice of B folds that slice's amax into a workspace word
+//      (unless the amax is given);
+//   2. kCastA: folds the amax of its W tiles, each as it lands, into the
+//      grid's; then every CTA passes a bounded grid barrier (cooperative
+//      launch: all CTAs are resident) that makes both amaxes complete -- for
+//      !kCastA the barrier counts only the slices of B;
+//   3. per tile: casts the W tile (kCastA) into the 128-byte-swizzled K-major
+//      layout the tensor cores read, stores W8 (TMA) and W8^T (16-byte
+//      stores); casts B's slice of the tile's K range into the same layout
+//      beside it, and its group's thread issues the tile's tcgen05 MMAs
+//      (M = 128 rows of A, N = kMN tokens, K = 128) into the tile's own
+//      TMEM columns at once.  Tiles are numbered band-major (128 rows of A,
+//      then K), so the few consecutive tiles of a CTA fall in one or two
+//      bands;
+//   4. sums the accumulators of its tiles of each band in tile order, writes
+//      that fp32 partial of D^T to the workspace and adds its tile count to
+//      the band's ticket; the CTA that
+//      completes a band (all its K tiles counted) sums the band's partials in
+//      K order (deterministic), scales by alpha = fl32(inv_a * inv_b) and
+//      stores bf16 D, plus the amax of D when asked for.
+// B's fp8 copy and its transpose (x8 / x8^T, dY8 / dY8^T) are written by
+// the CTAs that own B's K slices.
+//
+// Numerics are those of the separate kernels: amax of the bf16 bit patterns,
+// scale = __fdiv_rn(F, max(amax, eps)), q = cvt.rn.satfinite(x * scale), fp32
+// accumulation on the tensor cores; only the order in which the fp32 partial
+// sums of D are added differs from the split-K GEMM's.
+#pragma once
+
+#include "cast_kernels.cuh"
+
+namespace fp8lin {
+namespace {
+
+constexpr int kSmThreads = 512;                        // two 256-thread tile groups
+constexpr int kSmMmaK = 32;                            // K of one kind::f8f6f4 MMA
+constexpr int kSmTilesPerCta = 7;
+constexpr int kSmTileBytes = kTile * kTile * 2;        // one bf16 tile; fp8 uses the first half
+constexpr int kSmBSliceOffset = kTile * kTile;         // B's slice sits in the second half
+constexpr size_t kSmSmem = static_cast<size_t>(kSmTilesPerCta) * kSmTileBytes + 1024;
+
+struct SmallParams {
+  int NA, KA, MB;               // D^T [NA, MB] = A [NA, KA] . B [MB, KA]^T
+  const uint16_t* b;            // bf16 B [MB, KA], row stride ldb elements
+  int64_t ldb;
+  float eps;
+  const float* b_amax_in;       // amax of B given by its producer (nullptr: computed here)
+  float* b_amax;                // B's state: amax, scale, inverse (written by CTA 0)
+  float* b_scale;
+  float* b_inv;
+  uint8_t* b8;                  // fp8 B [MB, KA] and B^T [KA, MB]
+  uint8_t* b8t;
+  uint8_t* a8t;                 // kCastA: fp8 A^T [KA, NA] (the W8 copy goes out by TMA)
+  float* a_amax;                // kCastA: A's state outputs
+  float* a_scale;
+  float* a_inv;
+  const float* a_inv_in;        // !kCastA: A's inverse scale
+  uint16_t* d;                  // bf16 D [MB, NA], row stride ldd elements
+  int64_t ldd;
+  uint32_t* d_amax;             // max |D| as fp32 bits (nullptr: not wanted)
+  uint32_t* d_amax_acc;         // self-cleaning workspace words of that maximum
+  uint32_t* d_amax_ticket;
+  float* partials;              // fp32 partials, [first tile of the CTA in the band][kMN][128]
+  int* tickets;                 // per 128-row band of A (zero between launches)
+  uint32_t* ws_barrier;         // grid barrier words (zero between launches)
+  uint32_t* ws_exits;
+  uint32_t* ws_amax;            // amax of A (kCastA)
+  uint32_t* ws_b_amax;          // amax of B (unless given)
+  int* err;
+};
+
+__device__ __forceinline__ void sm_group_sync(int group) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(256) : "memory");
+}
+
+// Max over the 512 threads of a 16-bit magnitude pattern; result in s_out
+// (as fp32 bits) after the call, visible to every thread.
+__device__ __forceinline__ void sm_block_max(uint32_t m16, uint32_t* s_red, uint32_t* s_out) {
+  m16 = __reduce_max_sync(0xFFFFFFFFu, m16);
+  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = m16;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    uint32_t m = threadIdx.x < kSmThreads / 32 ? s_red[threadIdx.x] : 0u;
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if (threadIdx.x == 0) *s_out = m << 16;
+  }
+  __syncthreads();
+}
+
+template <int kMN>
+__device__ __forceinline__ void sm_tmem_load(uint32_t taddr, uint32_t (&r)[kMN]) {
+  if constexpr (kMN == 32)
+    tmem_load_32cols(taddr, r);
+  else
+    tmem_load_16cols(taddr, r);
+  tmem_load_wait();
+}
+
+template <bool kCastA, int kFmtB, int kMN>
+__global__ void __launch_bounds__(kSmThreads, 1)
+    small_m_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA8,
+                   const SmallParams p) {
+  static_assert(kMN == 16 || kMN == 32, "tokens per MMA");
+  constexpr int kTmemCols = kSmTilesPerCta * kMN <= 128 ? 128 : 256;
+  constexpr int kBVec = kMN * 16 / 256;  // B slice vectors per thread of a group, per tile
+  constexpr int kGroupTiles = (kSmTilesPerCta + 1) / 2;
+  constexpr uint32_t kIdesc = make_idesc_f8(0u, static_cast<uint32_t>(kFmtB), 128u, kMN);
+  extern __shared__ __align__(1024) uint8_t sm_raw[];
+  uint8_t* tiles = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  __shared__ __align__(8) uint64_t loaded[kSmTilesPerCta];
+  __shared__ __align__(8) uint64_t mma_done[2];
+  __shared__ uint32_t s_tmem;
+  __shared__ uint32_t s_red[kSmThreads / 32];
+  __shared__ uint32_t s_b_bits, s_a_bits, s_d_bits;
+  __shared__ int s_abort;
+  __shared__ int s_nbands;
+  __shared__ int s_bands[kSmTilesPerCta];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int group = tid >> 8, gtid = tid & 255;
+  const int nbands = (p.NA + kTile - 1) / kTile, nks = (p.KA + kTile - 1) / kTile;
+  const int ntiles = nbands * nks;
+  const int G = static_cast<int>(gridDim.x);
+  const int per = ntiles / G, extra = ntiles % G;
+  const int t0 = static_cast<int>(blockIdx.x) * per + min(static_cast<int>(blockIdx.x), extra);
+  const int mine = per + (static_cast<int>(blockIdx.x) < extra ? 1 : 0);  // <= kSmTilesPerCta
+  const int band0 = t0 / nks;  // tile t: band t / nks, K slice t % nks
+  const bool b_given = p.b_amax_in != nullptr;
+
+  if (tid == 0) {
+    s_abort = 0;
+    for (int k = 0; k < kSmTilesPerCta; ++k) mbar_init(&loaded[k], 1);
+    mbar_init(&mma_done[0], 1);
+    mbar_init(&mma_done[1], 1);
+    fence_barrier_init();
+    if (kCastA) tma_prefetch_map(&tmA);
+    tma_prefetch_map(&tmA8);
+  }
+  if (warp == 0) {
+    tmem_alloc(&s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = s_tmem;
+  griddep_wait();  // B, A and the states are ready; D and the outputs are free
+
+  // ---- phase 1: A tiles in flight (one barrier each); this thread's B
+  // vectors for its group's tiles in one batch; the amax of B's slices
+  if (tid == 0) {
+    constexpr uint32_t kTileIn = kCastA ? kTile * kTile * 2 : kTile * kTile;
+    for (int k = 0; k < mine; ++k) {
+      const int t = t0 + k;
+      mbar_arrive_expect_tx(&loaded[k], kTileIn);
+      tma_load_2d(tiles + k * kSmTileBytes, kCastA ? &tmA : &tmA8, &loaded[k], (t % nks) * kTile,
+                  (t / nks) * kTile);
+    }
+  }
+  uint4 bv[kGroupTiles][kBVec];
+#pragma unroll
+  for (int kq = 0; kq < kGroupTiles; ++kq) {
+    const int k = group + 2 * kq;
+    const int c0 = ((t0 + k) % nks) * kTile;
+#pragma unroll
+    for (int u = 0; u < kBVec; ++u) {
+      const int i = gtid + 256 * u, m = i >> 4, j = c0 + (i & 15) * 8;
+      bv[kq][u] = (k < mine && m < p.MB && j < p.KA)
+                      ? ld_stream_v4(p.b + static_cast<int64_t>(m) * p.ldb + j)
+                      : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  int my_slices = 0;  // B slices this CTA owns: blockIdx.x, blockIdx.x + G, ...
+  if (!b_given) {
+    AbsMax am;
+    for (int c = blockIdx.x; c < nks; c += G, ++my_slices) {
+      for (int i = tid; i < p.MB * 16; i += kSmThreads) {
+        const int m = i >> 4, j = c * kTile + (i & 15) * 8;
+        if (j < p.KA) am.add(ld_stream_v4(p.b + static_cast<int64_t>(m) * p.ldb + j));
+      }
+    }
+    if (my_slices > 0) {  // CTA-uniform
+      const uint32_t pk = am.packed();
+      sm_block_max(max(pk & 0xFFFFu, pk >> 16), s_red, &s_b_bits);
+      if (tid == 0) atomicMax(p.ws_b_amax, s_b_bits);
+    }
+  } else if (tid == 0) {
+    s_b_bits = __float_as_uint(*p.b_amax_in);
+  }
+
+  bool ok = true;
+  if constexpr (kCastA) {
+    // The amax of each W tile as soon as it lands.
+    volatile int never = 0;
+    AbsMax a0, a1;
+    for (int k = group; k < mine; k += 2) {
+      if (!mbar_wait_bounded(&loaded[k], 0, &never)) {
+        ok = false;
+        break;
+      }
+      const uint8_t* buf = tiles + k * kSmTileBytes;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int vi = gtid + 256 * u;
+        (u & 1 ? a1 : a0).add(*reinterpret_cast<const uint4*>(buf + (vi >> 4) * (kTile * 2) +
+                                                               (vi & 15) * 16));
+      }
+    }
+    a0.merge(a1);
+    const uint32_t pk = a0.packed();
+    ok = __syncthreads_and(ok ? 1 : 0) != 0;
+    if (ok) sm_block_max(max(pk & 0xFFFFu, pk >> 16), s_red, &s_a_bits);
+  }
+  if (!ok && tid == 0) atomicCAS(p.err, 0, kErrCastWait);
+
+  // ---- the grid barrier: A's amax (kCastA) and B's slices complete
+  const bool need_barrier = kCastA || !b_given;  // grid-uniform
+  if (ok && need_barrier) {
+    if (tid == 0) {
+      if (kCastA) atomicMax(p.ws_amax, s_a_bits);
+      // kCastA: every CTA arrives once; else each slice of B arrives once.
+      const uint32_t arrive = kCastA ? 1u : static_cast<uint32_t>(my_slices);
+      const uint32_t target = kCastA ? gridDim.x : static_cast<uint32_t>(nks);
+      if (arrive > 0) red_release_add(p.ws_barrier, arrive);
+      const uint64_t start = global_timer_ns();
+      while (ld_acquire_u32(p.ws_barrier) < target) {
+        if (global_timer_ns() - start > kWaitLimitNs) {
+          atomicCAS(p.err, 0, kErrGridBarrier);
+          s_abort = 1;
+          break;
+        }
+      }
+      if (!s_abort) {
+        if (kCastA) s_a_bits = ld_acquire_u32(p.ws_amax);
+        if (!b_given) s_b_bits = ld_acquire_u32(p.ws_b_amax);
+      }
+    }
+    __syncthreads();
+    ok = s_abort == 0;
+    // Count this CTA out; the last one clears the words for the next launch.
+    if (ok && tid == 0 && atomicAdd(p.ws_exits, 1u) == gridDim.x - 1) {
+      atomicExch(p.ws_barrier, 0u);
+      atomicExch(p.ws_exits, 0u);
+      atomicExch(p.ws_amax, 0u);
+      atomicExch(p.ws_b_amax, 0u);
+    }
+  } else {
+    __syncthreads();
+  }
+
+  const float amax_b = __uint_as_float(s_b_bits);
+  const float s_b = scale_from_amax(amax_b, p.eps, fp8_max<kFmtB>());
+  const float inv_b = __fdiv_rn(1.0f, s_b);
+  float s_a = 1.0f, inv_a;
+  if constexpr (kCastA) {
+    s_a = scale_from_amax(__uint_as_float(s_a_bits), p.eps, fp8_max<0>());
+    inv_a = __fdiv_rn(1.0f, s_a);
+  } else {
+    inv_a = *p.a_inv_in;
+  }
+  if (ok && blockIdx.x == 0 && tid == 0) {
+    *p.b_amax = amax_b;
+    *p.b_scale = s_b;
+    *p.b_inv = inv_b;
+    if constexpr (kCastA) {
+      *p.a_amax = __uint_as_float(s_a_bits);
+      *p.a_scale = s_a;
+      *p.a_inv = inv_a;
+    }
+  }
+
+  // ---- phase 2: per tile, the casts into the MMA layout, then its MMAs
+  bool issued = false;
+  if (ok) {
+    volatile int never = 0;
+#pragma unroll
+    for (int kq = 0; kq < kGroupTiles; ++kq) {
+      const int k = group + 2 * kq;
+      if (k >= mine) break;
+      const int t = t0 + k, c0 = (t % nks) * kTile, r0 = (t / nks) * kTile;
+      uint8_t* buf = tiles + k * kSmTileBytes;
+      uint8_t* bsl = buf + kSmBSliceOffset;
+      if constexpr (kCastA) {
+        uint2 q[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int vi = gtid + 256 * u;
+          q[u] = cast8<0>(*reinterpret_cast<const uint4*>(buf + (vi >> 4) * (kTile * 2) +
+                                                          (vi & 15) * 16),
+                          s_a);
+        }
+        sm_group_sync(group);  // the group has read the bf16 tile: the buffer is free
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int vi = gtid + 256 * u;
+          *reinterpret_cast<uint2*>(buf + sw128(vi >> 4, (vi & 15) * 8)) = q[u];
+        }
+      } else {
+        mbar_wait_bounded(&loaded[k], 0, &never);  // the fp8 tile has landed (bounded)
+      }
+      // B's slice of this tile's K range, [kMN rows][128 bytes], same swizzle.
+#pragma unroll
+      for (int u = 0; u < kBVec; ++u) {
+        const int i = gtid + 256 * u;
+        *reinterpret_cast<uint2*>(bsl + sw128(i >> 4, (i & 15) * 8)) = cast8<kFmtB>(bv[kq][u], s_b);
+      }
+      fence_proxy_async_shared();
+      sm_group_sync(group);
+      if (gtid == 0) {
+        const bool landed = kCastA || mbar_try_wait(&loaded[k], 0);
+        if (landed) {
+          tc_fence_after_sync();
+          const uint64_t a_desc = smem_desc_k_sw128(smem_addr(buf));
+          const uint64_t b_desc = smem_desc_k_sw128(smem_addr(bsl));
+#pragma unroll
+          for (int kk = 0; kk < kTile / kSmMmaK; ++kk)  // K offset kk * 32 bytes (encoded >> 4)
+            mma_f8f6f4(tmem + static_cast<uint32_t>(k * kMN),
+                       a_desc + static_cast<uint64_t>(kk * (kSmMmaK >> 4)),
+                       b_desc + static_cast<uint64_t>(kk * (kSmMmaK >> 4)), kIdesc,
+                       kk > 0 ? 1u : 0u);
+          issued = true;
+        } else {
+          atomicCAS(p.err, 0, kErrCastWait);
+          s_abort = 1;
+        }
+      }
+      if constexpr (kCastA) {
+        // W8^T: each thread a 16-row x 4-column block of the tile, four
+        // 16-byte rows of the transpose, straight to global memory.
+        const int lw = gtid & 31, gw = gtid >> 5;
+        const int jg = (gw & 1) * 16 + (lw >> 1);  // 4-column group 0..31
+        const int ig = (gw >> 1) * 2 + (lw & 1);   // 16-row group 0..7
+        if (r0 + ig * 16 < p.NA) {
+          uint32_t w[16];
+#pragma unroll
+          for (int kk = 0; kk < 16; ++kk)
+            w[kk] = *reinterpret_cast<const uint32_t*>(buf + sw128(ig * 16 + kk, jg * 4));
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const uint32_t x0 = __byte_perm(w[4 * g + 0], w[4 * g + 1], 0x5140);
+            const uint32_t x1 = __byte_perm(w[4 * g + 2], w[4 * g + 3], 0x5140);
+            const uint32_t x2 = __byte_perm(w[4 * g + 0], w[4 * g + 1], 0x7362);
+            const uint32_t x3 = __byte_perm(w[4 * g + 2], w[4 * g + 3], 0x7362);
+            w[4 * g + 0] = __byte_perm(x0, x1, 0x5410);
+            w[4 * g + 1] = __byte_perm(x0, x1, 0x7632);
+            w[4 * g + 2] = __byte_perm(x2, x3, 0x5410);
+            w[4 * g + 3] = __byte_perm(x2, x3, 0x7632);
+          }
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int col = c0 + jg * 4 + jj;
+            if (col < p.KA)
+              *reinterpret_cast<uint4*>(p.a8t + static_cast<int64_t>(col) * p.NA + r0 + ig * 16) =
+                  make_uint4(w[jj], w[4 + jj], w[8 + jj], w[12 + jj]);
+          }
+        }
+        if (gtid == 0) {
+          tma_store_2d(&tmA8, buf, c0, r0);  // W8 tile (clipped at the edges)
+          bulk_commit_group();
+        }
+      }
+    }
+  }
+  if (gtid == 0) {
+    if (issued)
+      mma_commit(&mma_done[group]);  // arrives once this thread's MMAs are complete
+    else
+      mbar_arrive(&mma_done[group]);
+  }
+  // ---- B's fp8 copies (for the later kernels): the CTA of each K slice
+  // writes it (q [MB, KA], q^T [KA, MB]), while its MMAs run
+  if (ok) {
+    for (int c = blockIdx.x; c < nks; c += G) {
+      for (int i = tid; i < kMN * 16; i += kSmThreads) {
+        const int m = i >> 4, j = (c * kTile) + (i & 15) * 8;
+        if (m < p.MB && j < p.KA) {
+          const uint4 v = ld_stream_v4(p.b + static_cast<int64_t>(m) * p.ldb + j);
+          const uint2 q = cast8<kFmtB>(v, s_b);
+          *reinterpret_cast<uint2*>(p.b8 + static_cast<int64_t>(m) * p.KA + j) = q;
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            p.b8t[static_cast<int64_t>(j + e) * p.MB + m] =
+                static_cast<uint8_t>(((e < 4 ? q.x : q.y) >> (8 * (e & 3))) & 0xFFu);
+        }
+      }
+    }
+  }
+
+  griddep_launch_dependents();
+  {
+    volatile int never = 0;
+    bool done = mbar_wait_bounded(&mma_done[0], 0, &never);
+    done = mbar_wait_bounded(&mma_done[1], 0, &never) && done;
+    if (!done && tid == 0) atomicCAS(p.err, 0, kErrGemmMmaWait);
+    ok = __syncthreads_and(ok && done && s_abort == 0 ? 1 : 0) != 0;
+  }
+  tc_fence_after_sync();
+
+  // ---- phase 3: one partial per band of this CTA (its tiles summed in tile
+  // order), tickets, the last one reduces
+  const int nacc = mine > 0 ? (t0 + mine - 1) / nks - band0 + 1 : 0;
+  if (ok) {
+    const int quarter = warp & 3;
+    for (int a = warp >> 2; a < nacc; a += kSmThreads / 128) {
+      const int band = band0 + a;
+      const int lo = max(t0, band * nks), hi = min(t0 + mine, (band + 1) * nks);
+      float acc[kMN];
+#pragma unroll
+      for (int m = 0; m < kMN; ++m) acc[m] = 0.0f;
+      for (int t = lo; t < hi; ++t) {
+        uint32_t r[kMN];
+        sm_tmem_load<kMN>(tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
+                              static_cast<uint32_t>((t - t0) * kMN),
+                          r);
+#pragma unroll
+        for (int m = 0; m < kMN; ++m) acc[m] += __uint_as_float(r[m]);
+      }
+      float* dst = p.partials + static_cast<size_t>(lo) * kMN * kTile + quarter * 32 + lane;
+#pragma unroll
+      for (int m = 0; m < kMN; ++m)
+        if (m < p.MB) __stcg(dst + m * kTile, acc[m]);
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (tid == 0) {
+    s_nbands = 0;
+    if (ok) {
+      // The CTA's partials (ordered before this thread by the barrier) are
+      // visible GPU-wide before its ticket counts them.
+      __threadfence();
+      for (int a = 0; a < nacc; ++a) {
+        const int band = band0 + a;
+        const int lo = max(t0, band * nks), hi = min(t0 + mine, (band + 1) * nks);
+        if (atomicAdd(&p.tickets[band], hi - lo) + (hi - lo) == nks) {
+          p.tickets[band] = 0;  // every K tile has arrived: clear for the next launch
+          s_bands[s_nbands++] = band;
+        }
+      }
+      __threadfence();
+    }
+  }
+  __syncthreads();
+  const float alpha = __fmul_rn(inv_a, inv_b);
+  float vmax = 0.0f;
+  const int nb = s_nbands;
+  for (int bi = 0; bi < nb; ++bi) {
+    const int band = s_bands[bi];
+    // The band's partials: one per CTA holding some of its K tiles, at that
+    // CTA's first tile in the band, in K order.  The CTA holding the band's
+    // first tile (CTAs below `extra` hold per + 1 tiles) is one division
+    // away; the next slots are the starts of the CTAs after it.
+    const int b0 = band * nks, t_end = (band + 1) * nks;
+    const int slot_cta0 =
+        b0 < extra * (per + 1) ? b0 / (per + 1) : extra + (b0 - extra * (per + 1)) / per;
+    for (int i = tid; i < p.MB * (kTile / 4); i += kSmThreads) {
+      const int m = i / (kTile / 4), nq = (i - m * (kTile / 4)) * 4;
+      const int n = band * kTile + nq;
+      if (n >= p.NA) continue;
+      float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      // Slot j of the band: its first tile, then the starts of the next CTAs.
+      for (int j0 = 0;; j0 += 8) {
+        float4 v[8];
+        bool any = false;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int cta = slot_cta0 + j0 + j;
+          const int ts = (j0 + j == 0) ? band * nks : cta * per + min(cta, extra);
+          const bool in = (j0 + j == 0) || ts < t_end;
+          any |= in;
+          v[j] = in ? __ldcg(reinterpret_cast<const float4*>(
+                          p.partials + static_cast<size_t>(ts) * kMN * kTile + m * kTile + nq))
+                    : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {  // in K order; absent slots add exact zeros
+          acc.x += v[j].x;
+          acc.y += v[j].y;
+          acc.z += v[j].z;
+          acc.w += v[j].w;
+        }
+        const int next = slot_cta0 + j0 + 8;
+        if (!any || next * per + min(next, extra) >= t_end) break;
+      }
+      const float v0 = __fmul_rn(acc.x, alpha), v1 = __fmul_rn(acc.y, alpha);
+      const float v2 = __fmul_rn(acc.z, alpha), v3 = __fmul_rn(acc.w, alpha);
+      *reinterpret_cast<uint2*>(p.d + static_cast<int64_t>(m) * p.ldd + n) =
+          make_uint2(cvt_bf16x2(v0, v1), cvt_bf16x2(v2, v3));
+      vmax = fmaxf(vmax, fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3))));
+    }
+  }
+  if (p.d_amax != nullptr && nb > 0) {
+    // Rounding to bf16 is monotone: the bf16 of the largest |v| is the amax
+    // of the stored D.  Every reduced band counts once on the ticket.
+    sm_block_max(cvt_bf16x2(vmax, 0.0f) & 0xFFFFu, s_red, &s_d_bits);
+    if (tid == 0) {
+      atomicMax(p.d_amax_acc, s_d_bits);
+      __threadfence();
+      if (atomicAdd(p.d_amax_ticket, static_cast<uint32_t>(nb)) + nb ==
+          static_cast<uint32_t>(nbands)) {
+        __threadfence();
+        *p.d_amax = atomicExch(p.d_amax_acc, 0u);
+        atomicExch(p.d_amax_ticket, 0u);
+      }
+    }
+  }
+  if (kCastA && gtid == 0) bulk_wait_group<0>();  // W8 stores done before the smem goes away
+  if (!ok && tid == 0) {
+    // Copies in flight land before the shared memory goes away (bounded).
+    volatile int never = 0;
+    for (int k = 0; k < mine; ++k) mbar_wait_bounded(&loaded[k], 0, &never);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+}  // namespace fp8lin

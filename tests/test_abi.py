@@ -45,7 +45,7 @@ def test_status_strings(lib):
     for code in range(5):
         assert lib.fp8lin_status_string(code).startswith(b"FP8LIN_")
     assert b"unknown" in lib.fp8lin_status_string(99)
-    assert lib.fp8lin_version() == 100
+    assert lib.fp8lin_version() == 101
     assert lib.fp8lin_workspace_bytes(65536, 4096, 4096) >= 256
 
 

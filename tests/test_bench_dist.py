@@ -1,5 +1,6 @@
-"""The multi-rank side of bench.py, on CPU.  With one process per GPU the
-benchmark runs replicas: the ranks share no data, only a barrier and the
+"""The multi-rank side of bench.py, on CPU.  With one process per GPU each
+rank runs its own M tokens (the Linear's exchange, one amax per tensor, is
+covered by test_sharded_dist.py); the timing shares a barrier and the
 slowest rank's step time.  Two gloo ranks check that they agree on that
 time, and that the whole-job throughput counts every rank's work.  A
 non-zero rank of the reference arm must leave at once, without work."""

@@ -44,6 +44,59 @@ def test_linear_dynamic_full_compare(mkn, algo):
     _check_full(lin, x, w, dy, sx, sw, sd)
 
 
+@pytest.mark.parametrize("mkn", [(16, 272, 208), (32, 784, 1040), (16, 16, 16), (32, 4096, 4096),
+                                 (16, 2048, 6144)])
+@pytest.mark.parametrize("given_amax", [False, True])
+def test_few_token_fused_path(mkn, given_amax):
+    """M <= 32 tokens with dynamic scaling: x's cast, W's cast and y in one
+    launch, dY's cast and dX in another (then dW).  Every fp8 byte and scalar
+    exact, the GEMMs within the bound, over ragged bands and K tails; with
+    given_amax the token-side amaxes come from the caller (PRECOMPUTED), as a
+    producing GEMM's epilogue would deliver them."""
+    M, K, N = mkn
+    x, w, dy = si.linear_inputs(M, K, N, w_init="uniform64", outlier_frac=1e-2, seed=M + K + N)
+    lin = q.Fp8Linear(M, K, N)
+    if given_amax:
+        lin.sx.amax_algo = lin.sdy.amax_algo = q.AMAX_PRECOMPUTED
+        lin.sx.amax.fill_(oracle.amax(x))
+        lin.sdy.amax.fill_(oracle.amax(dy))
+    n0 = q.launch_count()
+    lin.forward(to_dev_bf16(x), to_dev_bf16(w))
+    lin.backward(to_dev_bf16(dy))
+    assert q.launch_count() - n0 == 3              # fused forward, fused dY + dX, dW
+    q.check(lin.ws)
+    sx, ix = oracle.scale_dynamic(oracle.amax(x), E4M3)
+    sw, iw = oracle.scale_dynamic(oracle.amax(w), E4M3)
+    sd, idy = oracle.scale_dynamic(oracle.amax(dy), E5M2)
+    for st, s, inv, src in ((lin.sx, sx, ix, x), (lin.sw, sw, iw, w), (lin.sdy, sd, idy, dy)):
+        assert dev_f32_bits(st.amax) == f32_bits(oracle.amax(src))
+        assert dev_f32_bits(st.scale) == f32_bits(s)
+        assert dev_f32_bits(st.inv_scale) == f32_bits(inv)
+    _check_full(lin, x, w, dy, sx, sw, sd)
+
+
+def test_few_token_fused_output_amaxes_and_repeat():
+    """The fused few-token products deliver max |y| and max |dX| from their
+    reduction, and a second call on the same workspace gives the same bits
+    (the band tickets and amax words clean themselves)."""
+    M, K, N = 16, 784, 1040
+    lin = q.Fp8Linear(M, K, N)
+    x, w, dy = si.linear_inputs(M, K, N, w_init="uniform64", seed=61)
+    ya, dxa = (torch.full((1,), -1.0, device="cuda") for _ in range(2))
+    outs = []
+    for _ in range(2):
+        q.forward(to_dev_bf16(x), to_dev_bf16(w), lin.sx, lin.sw, lin.y, lin.x8, lin.x8t, lin.w8,
+                  lin.w8t, lin.ws, y_amax=ya)
+        q.backward(to_dev_bf16(dy), lin.x8t, lin.w8t, lin.sx, lin.sw, lin.sdy, lin.dy8, lin.dy8t,
+                   lin.dx, lin.dw, lin.ws, dx_amax=dxa)
+        q.check(lin.ws)
+        assert dev_f32_bits(ya) == f32_bits(oracle.amax(_bits(lin.y)))
+        assert dev_f32_bits(dxa) == f32_bits(oracle.amax(_bits(lin.dx)))
+        outs.append([_bits(t) for t in (lin.y, lin.dx, lin.dw)])
+    for a, b in zip(*outs):
+        assert np.array_equal(a, b)
+
+
 def test_linear_delayed_small_full_compare():
     """Delayed scaling with a stale scale can saturate; compare everything."""
     M, K, N = 144, 272, 208
@@ -196,11 +249,14 @@ def test_linked_linears_match_unlinked(M):
     assert s1 == s2
 
 
-def test_cached_weight_dynamic_matches_recast():
-    """cache_weight: micro-batches with the same W skip W's cast (two
-    launches per forward instead of three) and give the bits of a fresh
-    cast; an in-place update of W makes the next forward cast again."""
-    M, K, N = 16, 4096, 4096
+@pytest.mark.parametrize("M", [16, 48])
+def test_cached_weight_dynamic_matches_recast(M):
+    """cache_weight: micro-batches with the same W skip W's cast and give the
+    bits of a fresh cast; an in-place update of W makes the next forward cast
+    again.  At 48 tokens the forward is two launches instead of three; at 16
+    tokens it is one fused launch either way, and the skipped cast shows in
+    W's state, which a cached forward leaves untouched."""
+    K, N = 4096, 4096
     lc = q.Fp8Linear(M, K, N, cache_weight=True)
     lu = q.Fp8Linear(M, K, N)
     _, w, _ = si.linear_inputs(M, K, N, w_init="uniform64", seed=31)
@@ -209,10 +265,17 @@ def test_cached_weight_dynamic_matches_recast():
         x, _, dy = si.linear_inputs(M, K, N, w_init="uniform64", seed=31, step=step)
         if step == 2:
             wd.mul_(2.0)                       # an optimizer step, in place
+        lc.sw.amax.fill_(-1.0)                 # only a cast of W writes it
         n0 = q.launch_count()
         lc.forward(to_dev_bf16(x), wd)
         launches = q.launch_count() - n0
-        assert launches == (3 if step in (0, 2) else 2), (step, launches)
+        cast_w = step in (0, 2)
+        if M > 32:
+            assert launches == (3 if cast_w else 2), (step, launches)
+        else:
+            assert launches == 1, (step, launches)
+        torch.cuda.synchronize()
+        assert (lc.sw.amax.item() > 0) == cast_w, step
         lc.backward(to_dev_bf16(dy))
         lu.forward(to_dev_bf16(x), wd)
         lu.backward(to_dev_bf16(dy))
