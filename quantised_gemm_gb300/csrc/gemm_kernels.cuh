@@ -55,8 +55,9 @@ constexpr int kBK = 128;           // bytes (= 8-bit elements) of K per stage
 constexpr int kMmaK = 32;          // K of one kind::f8f6f4 MMA
 constexpr int kGemmThreads = 320;  // 10 warps: producer, MMA, 8 epilogue
 constexpr int kEpiWarps = 8;       // two per TMEM lane quarter, each on half the columns
-constexpr int kBoxBytes = 32 * 32 * 2;              // one 32x32 bf16 epilogue box
-constexpr int kBoxesPerWarp = 2;                     // staging boxes per epilogue warp
+constexpr int kBoxCols = 64;                          // epilogue box: 32 rows x 64 bf16 columns
+constexpr int kBoxBytes = 32 * kBoxCols * 2;          // (128-byte rows: whole L2 lines)
+constexpr int kBoxesPerWarp = 1;                      // staging boxes per epilogue warp
 constexpr int kEpiStagingBytes = kEpiWarps * kBoxesPerWarp * kBoxBytes;
 
 // Epilogue warps split the BN columns of a tile in two halves when each half
@@ -140,29 +141,38 @@ __device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, uint32_t (&r)[kC
   tmem_load_wait();
 }
 
-// Scale one 32-row x 32-column accumulator chunk (this lane's row in r[]),
-// convert to bf16, stage it in `box` and store it at (row0, col0) of D with
-// TMA.  The box's rows are 64 bytes with 16-byte chunks swizzled as the
-// 64-byte TMA swizzle expects (chunk ^= (row >> 1) & 3), which also keeps the
-// warp's shared-memory writes free of bank conflicts.
+// Scale two 32-row x 32-column accumulator chunks (this lane's row in ra[]
+// and rb[], columns col0..col0+63), convert to bf16, stage them in `box` and
+// store the 32 x 64 box at (row0, col0) of D with TMA.  The box's rows are
+// 128 bytes -- whole L2 lines of D -- with 16-byte chunks swizzled as the
+// 128-byte TMA swizzle expects (chunk ^= row & 7), which also keeps the
+// warp's shared-memory writes free of bank conflicts.  Columns beyond D are
+// clipped by the store.
 template <bool kTrack>
-__device__ __forceinline__ void store_chunk_tma(const uint32_t (&r)[32], float alpha, uint8_t* box,
-                                                const CUtensorMap* tmD, int row0, int col0,
-                                                int lane, float& vmax) {
-  uint32_t w[16];
+__device__ __forceinline__ void store_pair_tma(const uint32_t (&ra)[32], const uint32_t (&rb)[32],
+                                               float alpha, uint8_t* box, const CUtensorMap* tmD,
+                                               int row0, int col0, int lane, float& vmax) {
+  uint32_t w[32];
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     float v0, v1;
-    mul2_rn(r[2 * j], r[2 * j + 1], alpha, v0, v1);
+    mul2_rn(ra[2 * j], ra[2 * j + 1], alpha, v0, v1);
     w[j] = cvt_bf16x2(v0, v1);
+    if constexpr (kTrack) vmax = fmaxf(vmax, fmaxf(fabsf(v0), fabsf(v1)));
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    float v0, v1;
+    mul2_rn(rb[2 * j], rb[2 * j + 1], alpha, v0, v1);
+    w[16 + j] = cvt_bf16x2(v0, v1);
     if constexpr (kTrack) vmax = fmaxf(vmax, fmaxf(fabsf(v0), fabsf(v1)));
   }
   if (lane == 0) bulk_wait_group_read<kBoxesPerWarp - 1>();  // this box's last store has read it
   __syncwarp();
-  uint8_t* rowp = box + lane * 64;
-  const int sw = (lane >> 1) & 3;
+  uint8_t* rowp = box + lane * 128;
+  const int sw = lane & 7;
 #pragma unroll
-  for (int q = 0; q < 4; ++q)
+  for (int q = 0; q < 8; ++q)
     *reinterpret_cast<uint4*>(rowp + ((q ^ sw) << 4)) =
         make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
   fence_proxy_async_shared();
@@ -173,7 +183,34 @@ __device__ __forceinline__ void store_chunk_tma(const uint32_t (&r)[32], float a
   }
 }
 
-// Final bf16 output of one chunk of raw fp32 accumulators (this lane's row).
+// One 32-column chunk of a K-split tile's reduced sums (this lane's row),
+// scaled, rounded to bf16 and stored straight from registers: 16-byte
+// stores, 16 columns at a time inside D (N is a multiple of 16).
+template <bool kTrack>
+__device__ __forceinline__ void store_chunk_direct(const float (&acc)[32], float alpha,
+                                                   const GemmParams& p, int row, int col0,
+                                                   float& vmax) {
+  if (row >= p.M) return;
+  uint16_t* dst = p.d + static_cast<int64_t>(row) * p.ldd + col0;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    if (col0 + 16 * h >= p.N) break;
+    uint32_t w[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float v0 = __fmul_rn(acc[16 * h + 2 * j], alpha);
+      const float v1 = __fmul_rn(acc[16 * h + 2 * j + 1], alpha);
+      w[j] = cvt_bf16x2(v0, v1);
+      if constexpr (kTrack) vmax = fmaxf(vmax, fmaxf(fabsf(v0), fabsf(v1)));
+    }
+    *reinterpret_cast<uint4*>(dst + 16 * h) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(dst + 16 * h + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+
+// Final bf16 output of raw fp32 accumulators (this lane's row): two
+// consecutive 32-column chunks ra, rb at col0 (TMA store of a 32 x 64 box),
+// or, with kTransStore, one chunk ra of kChunk columns stored transposed.
 // When D's amax is wanted (p.amax_out, warp-uniform), vmax collects the
 // largest |v| of the fp32 values before their rounding to bf16: rounding to
 // nearest even is monotone and odd, so max |bf16(v)| = bf16(max |v|), and one
@@ -181,19 +218,19 @@ __device__ __forceinline__ void store_chunk_tma(const uint32_t (&r)[32], float a
 // outside D come from zero-filled operand rows or columns, hence are zero and
 // cannot raise it.
 template <int kChunk, bool kTransStore>
-__device__ __forceinline__ void emit_chunk(const uint32_t (&r)[kChunk], float alpha,
-                                           const GemmParams& p, const CUtensorMap* tmD,
-                                           uint8_t* boxes, uint32_t& chunk_no, int row0, int col0,
-                                           int lane, float& vmax) {
+__device__ __forceinline__ void emit(const uint32_t (&ra)[kChunk], const uint32_t (&rb)[kChunk],
+                                     float alpha, const GemmParams& p, const CUtensorMap* tmD,
+                                     uint8_t* boxes, uint32_t& box_no, int row0, int col0, int lane,
+                                     float& vmax) {
   const bool track = p.amax_out != nullptr;
   if constexpr (!kTransStore) {
-    static_assert(kChunk == 32, "TMA-store epilogue works on 32-column chunks");
-    uint8_t* box = boxes + (chunk_no % kBoxesPerWarp) * kBoxBytes;
-    if (track)  // warp-uniform; the untracked chunk carries no max at all
-      store_chunk_tma<true>(r, alpha, box, tmD, row0, col0, lane, vmax);
+    static_assert(kChunk == 32, "TMA-store epilogue works on pairs of 32-column chunks");
+    uint8_t* box = boxes + (box_no % kBoxesPerWarp) * kBoxBytes;
+    if (track)  // warp-uniform; the untracked store carries no max at all
+      store_pair_tma<true>(ra, rb, alpha, box, tmD, row0, col0, lane, vmax);
     else
-      store_chunk_tma<false>(r, alpha, box, tmD, row0, col0, lane, vmax);
-    ++chunk_no;
+      store_pair_tma<false>(ra, rb, alpha, box, tmD, row0, col0, lane, vmax);
+    ++box_no;
   } else {
     // kernel element (row, col) is output element (col, row)
     const int row = row0 + lane;
@@ -201,7 +238,7 @@ __device__ __forceinline__ void emit_chunk(const uint32_t (&r)[kChunk], float al
 #pragma unroll
       for (int j = 0; j < kChunk; ++j) {
         if (col0 + j < p.N) {
-          const float v = __fmul_rn(__uint_as_float(r[j]), alpha);
+          const float v = __fmul_rn(__uint_as_float(ra[j]), alpha);
           const uint32_t b = cvt_bf16x2(v, 0.0f) & 0xFFFFu;
           p.d[static_cast<int64_t>(col0 + j) * p.ldd + row] = static_cast<uint16_t>(b);
           if (track) vmax = fmaxf(vmax, fabsf(v));
@@ -259,7 +296,7 @@ template <int kCols, bool kTransStore, typename Release>
 __device__ __forceinline__ void epilogue_unit(const GemmParams& p, const Unit& u, int G,
                                               int group, int row0, int col_base, uint32_t t_row,
                                               float alpha, const CUtensorMap* tmD, uint8_t* boxes,
-                                              uint32_t& chunk_no, int lane,
+                                              uint32_t& box_no, int lane,
                                               volatile int* abort_flag, float& vmax,
                                               Release release) {
   constexpr int kChunk = (kCols % 32 == 0) ? 32 : 16;
@@ -268,8 +305,9 @@ __device__ __forceinline__ void epilogue_unit(const GemmParams& p, const Unit& u
   while (nch < kCols / kChunk && col_base + nch * kChunk < p.N) ++nch;
   if (u.role == kWhole) {
     if (active && nch > 0) {
-      // Two chunks per iteration: the TMEM load of the second is in flight
-      // while the first is converted and stored.
+      // Two chunks per iteration, loaded from TMEM together.  The TMA store
+      // takes them as one 32 x 64 box; a chunk past the last one inside D
+      // (nch odd) is not loaded, and its half of the box is clipped.
       uint32_t ra[kChunk], rb[kChunk];
 #pragma unroll 1
       for (int c = 0; c < nch; c += 2) {
@@ -282,14 +320,21 @@ __device__ __forceinline__ void epilogue_unit(const GemmParams& p, const Unit& u
             tmem_load_16cols(t_row + (c + 1) * kChunk, rb);
           }
           tmem_load_wait();
-          emit_chunk<kChunk, kTransStore>(ra, alpha, p, tmD, boxes, chunk_no, row0,
-                                          col_base + c * kChunk, lane, vmax);
-          emit_chunk<kChunk, kTransStore>(rb, alpha, p, tmD, boxes, chunk_no, row0,
-                                          col_base + (c + 1) * kChunk, lane, vmax);
+          if constexpr (kTransStore) {
+            emit<kChunk, true>(ra, ra, alpha, p, tmD, boxes, box_no, row0, col_base + c * kChunk,
+                               lane, vmax);
+            emit<kChunk, true>(rb, rb, alpha, p, tmD, boxes, box_no, row0,
+                               col_base + (c + 1) * kChunk, lane, vmax);
+          } else {
+            emit<kChunk, false>(ra, rb, alpha, p, tmD, boxes, box_no, row0, col_base + c * kChunk,
+                                lane, vmax);
+          }
         } else {
           tmem_load_chunk<kChunk>(t_row + c * kChunk, ra);
-          emit_chunk<kChunk, kTransStore>(ra, alpha, p, tmD, boxes, chunk_no, row0,
-                                          col_base + c * kChunk, lane, vmax);
+#pragma unroll
+          for (int j = 0; j < kChunk; ++j) rb[j] = 0u;
+          emit<kChunk, kTransStore>(ra, rb, alpha, p, tmD, boxes, box_no, row0,
+                                    col_base + c * kChunk, lane, vmax);
         }
       }
     }
@@ -351,6 +396,7 @@ __device__ __forceinline__ void epilogue_unit(const GemmParams& p, const Unit& u
   const int share = (nch + u.nsplit - 1) / u.nsplit;
   const int c_lo = u.split * share;
   const int c_hi = min(nch, c_lo + share);
+  const bool track = p.amax_out != nullptr;  // warp-uniform
 #pragma unroll 1
   for (int c = c_lo; c < c_hi; ++c) {
     float acc[kChunk];
@@ -362,11 +408,17 @@ __device__ __forceinline__ void epilogue_unit(const GemmParams& p, const Unit& u
                            region_floats;
       add_partial<kChunk>(region, c, acc, lane);
     }
-    uint32_t r[kChunk];
+    if constexpr (kTransStore) {
+      uint32_t r[kChunk];
 #pragma unroll
-    for (int j = 0; j < kChunk; ++j) r[j] = __float_as_uint(acc[j]);
-    emit_chunk<kChunk, kTransStore>(r, alpha, p, tmD, boxes, chunk_no, row0,
-                                    col_base + c * kChunk, lane, vmax);
+      for (int j = 0; j < kChunk; ++j) r[j] = __float_as_uint(acc[j]);
+      emit<kChunk, true>(r, r, alpha, p, tmD, boxes, box_no, row0, col_base + c * kChunk, lane,
+                         vmax);
+    } else if (track) {
+      store_chunk_direct<true>(acc, alpha, p, row0 + lane, col_base + c * kChunk, vmax);
+    } else {
+      store_chunk_direct<false>(acc, alpha, p, row0 + lane, col_base + c * kChunk, vmax);
+    }
   }
   __syncwarp();
   if (lane == 0) {
@@ -571,7 +623,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const bool has_cols = half < E::kHalves;
     const float alpha = __fmul_rn(*p.inv_a, *p.inv_b);
     uint8_t* boxes = sEpi + (warp - 2) * kBoxesPerWarp * kBoxBytes;
-    uint32_t chunk_no = 0;
+    uint32_t box_no = 0;
     float vmax = 0.0f;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -598,7 +650,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         epilogue_unit<E::kCols, kTransStore>(p, u, 4 * E::kHalves, half * 4 + quarter,
                                              m_blk * kBM + quarter * 32,
                                              n_blk * BN + half * E::kCols, t_row, alpha, &tmD,
-                                             boxes, chunk_no, lane, abort_flag, vmax, release);
+                                             boxes, box_no, lane, abort_flag, vmax, release);
       else
         release();
       if (++acc == 2) {
@@ -821,7 +873,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const float alpha = __fmul_rn(*p.inv_a, *p.inv_b);
     const uint32_t acc_empty_even0 = map_to_cta(smem_addr(&acc_empty[0]), 0);
     uint8_t* boxes = sEpi + (warp - 2) * kBoxesPerWarp * kBoxBytes;
-    uint32_t chunk_no = 0;
+    uint32_t box_no = 0;
     float vmax = 0.0f;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -841,7 +893,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t release_addr = acc_empty_even0 + static_cast<uint32_t>(acc * 8);
       epilogue_unit<E::kCols, false>(p, u, 8 * E::kHalves, half * 8 + row_group,
                                      m_blk * 2 * kBM + row_group * 32, n_blk * BN + half * E::kCols,
-                                     t_row, alpha, &tmD, boxes, chunk_no, lane, abort_flag, vmax,
+                                     t_row, alpha, &tmD, boxes, box_no, lane, abort_flag, vmax,
                                      [&] {
                                        tc_fence_before_sync();
                                        __syncwarp();

@@ -103,11 +103,12 @@ bool make_map_k_major(CUtensorMap* map, const uint8_t* base, int64_t rows, int64
 }
 
 // 2-D map over the bf16 output [rows, cols] (row stride ldd elements), box
-// 32 x 32, 64-byte swizzle, for the epilogue's TMA stores.
+// 32 rows x 64 columns (128-byte rows), 128-byte swizzle, for the
+// epilogue's TMA stores.
 bool make_map_out(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ldd) {
   return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, static_cast<uint64_t>(cols),
-                   static_cast<uint64_t>(rows), static_cast<uint64_t>(ldd) * 2, 32, 32,
-                   CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+                   static_cast<uint64_t>(rows), static_cast<uint64_t>(ldd) * 2, kBoxCols, 32,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
 }
 
 // How the `tiles` tiles of rows_per_tile x bn, with `num_kb` K blocks each,
