@@ -258,7 +258,11 @@ fp8lin_status fp8lin_cast_delayed(const void* x, int64_t rows, int64_t cols, int
                                   void* ws, cudaStream_t stream);
 
 /* FP8 GEMM (rows a4-a6): d[m, n] = bf16( (sum_k A[m, k] * B[n, k]) *
- * fl32(inv_a * inv_b) ), accumulated in fp32 on the tensor cores.
+ * fl32(inv_a * inv_b) ), accumulated in fp32 on the tensor cores -- the form
+ * every product of the FP8Linear of "Why swapping nn.Linear with FP8Linear
+ * brings throughput decrease for 7B LLAMA2-like model?" (pytorch/ao issue
+ * 1199) takes once the transposed fp8 copies exist: y = x8 . W8^T,
+ * dX = dY8 . (W8^T)^T, dW = dY8^T . (x8^T)^T.
  * a: fp8 [M, K] row stride lda bytes; b: fp8 [N, K] row stride ldb bytes
  * (both with the contraction index fastest); fmt_a, fmt_b: fp8lin_fmt;
  * inv_a, inv_b: device fp32[1]; d: bf16 [M, N] row stride ldd elements.
@@ -291,9 +295,12 @@ fp8lin_status fp8lin_gemm_describe(int64_t M, int64_t N, int64_t K, char* buf, s
 fp8lin_status fp8lin_gemm_describe_for(int64_t M, int64_t N, int64_t K, int32_t num_sms,
                                        char* buf, size_t buf_len);
 
-/* Forward of the Linear: amax/scale/cast of x ([M, K], e4m3, state sx) and
- * W ([N, K], e4m3, state sw), then y = x8 . W8^T * inv_x * inv_w (bf16
- * [M, N]).  Writes the fp8 copies x8 [M, K], x8t [K, M], w8 [N, K],
+/* Forward of the Linear -- the forward half of the "forward+backward" of one
+ * Linear timed in "Integrate float8nocompile, an experimental feature for
+ * high performance" (torchtitan PR 778), "Benchmarking single linear layer
+ * forward+backward performance"; the FP8Linear of pytorch/ao issue 1199:
+ * amax/scale/cast of x ([M, K], e4m3, state sx) and W ([N, K], e4m3, state
+ * sw), then y = x8 . W8^T * inv_x * inv_w (bf16 [M, N]).  Writes the fp8 copies x8 [M, K], x8t [K, M], w8 [N, K],
  * w8t [K, N]; x8t and w8t are what fp8lin_backward needs.  Dynamic states
  * take their scale from this call's amax; delayed states cast with their
  * stored scale and record this call's amax (and do the amax init first when
@@ -307,20 +314,31 @@ fp8lin_status fp8lin_gemm_describe_for(int64_t M, int64_t N, int64_t K, int32_t 
  * dominates the step).  The result is the one a fresh cast would give as long
  * as sw's scale has not moved since: always for dynamic scaling, and until
  * the next fp8lin_scale of sw for delayed scaling.  EINVAL if sw is delayed
- * and still needs its first (amax-init) cast. */
+ * and still needs its first (amax-init) cast.
+ * A few tokens (M <= 32) with dynamic scaling of x (amax_algo AUTO,
+ * SINGLE_PASS or PRECOMPUTED) and, when W is cast, of W (AUTO or
+ * SINGLE_PASS): x's cast, W's cast and y run as one fused launch (same
+ * results: casts and scales bit for bit, y within the GEMM's bound; only the
+ * order in which y's fp32 partial sums are added differs).
+ * FP8LIN_SMALL_M=0 in the environment turns this off. */
 fp8lin_status fp8lin_forward(const void* x, const void* w, int64_t M, int64_t K, int64_t N,
                              fp8lin_scaling_state* sx, fp8lin_scaling_state* sw,
                              void* y, float* y_amax, uint8_t* x8, uint8_t* x8t, uint8_t* w8,
                              uint8_t* w8t, void* ws, size_t ws_bytes, cudaStream_t stream);
 
-/* Backward of the Linear: amax/scale/cast of dY ([M, N], e5m2, state sdy)
+/* Backward of the Linear -- the backward half of the single-linear
+ * "forward+backward" of torchtitan PR 778; the FP8Linear's backward of
+ * pytorch/ao issue 1199: amax/scale/cast of dY ([M, N], e5m2, state sdy)
  * into dy8 [M, N] and dy8t [N, M], then
  *   dX = dY8 . W8 * inv_dy * inv_w     (bf16 [M, K], skipped if dx == NULL)
  *   dW = dY8^T . x8 * inv_dy * inv_x   (bf16 [N, K], skipped if dw == NULL)
  * from the x8t / w8t written by fp8lin_forward and the inv_scale of sx, sw.
  * dx_amax, dw_amax: NULL, or device fp32[1] receiving max |dX| / max |dW|
  * from the GEMM epilogues (each needs its GEMM: dx / dw not NULL); dx_amax
- * can feed the previous layer's grad_output state as PRECOMPUTED. */
+ * can feed the previous layer's grad_output state as PRECOMPUTED.
+ * A few tokens (M <= 32) with dynamic scaling of dY (AUTO, SINGLE_PASS or
+ * PRECOMPUTED) and dx not NULL: dY's cast and dX run as one fused launch
+ * (as in fp8lin_forward); dW follows as its own GEMM. */
 fp8lin_status fp8lin_backward(const void* dy, int64_t M, int64_t K, int64_t N,
                               const uint8_t* x8t, const uint8_t* w8t,
                               const fp8lin_scaling_state* sx, const fp8lin_scaling_state* sw,
