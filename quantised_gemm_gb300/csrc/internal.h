@@ -46,15 +46,18 @@ void set_error_site(const char* site);
 bool pdl_enabled();
 
 // Launch `kernel` on `stream` with cudaLaunchKernelEx: programmatic
-// dependent launch when enabled (not for cooperative grids), a cluster of
-// `cluster_x` CTAs when > 1, and a cooperative launch when `cooperative`.
+// dependent launch when enabled, a cluster of `cluster_x` CTAs when > 1, and
+// a cooperative launch when `cooperative`.  A cooperative grid launched
+// early waits in griddepcontrol.wait, before its grid barrier, until the
+// grid ahead of it has finished and freed its SMs; it lets the next grid
+// launch only after its barrier, when all of its own CTAs are resident.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                           cudaStream_t stream, int cluster_x, bool cooperative, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[3];
   unsigned n = 0;
-  if (pdl_enabled() && !cooperative) {  // a cooperative grid is launched whole
+  if (pdl_enabled()) {
     attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[n].val.programmaticStreamSerializationAllowed = 1;
     ++n;
