@@ -103,9 +103,9 @@ def device_code_sha(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def load_traffic(kernel: str):
+def load_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current source of the kernel (else None)."""
+    the current source of the kernel for this workload (else None)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
@@ -115,7 +115,8 @@ def load_traffic(kernel: str):
             line = line.strip()
             if line.startswith("{"):
                 rec = json.loads(line)
-                if rec.get("kernel") == kernel and rec.get("src_sha") == sha:
+                if (rec.get("kernel") == kernel and rec.get("src_sha") == sha
+                        and rec.get("workload") == workload):
                     return rec
     return None
 
@@ -645,6 +646,25 @@ def host_link_rates(torch, host, dev):
             "bytes": nbytes}
 
 
+def few_token_roofline(M, K, N, product_ms, peaks):
+    """HBM roofline of the slower few-token product of a step (M <= 32).
+    Algorithmic bytes of each launch: the forward reads x and W (2 B) and
+    writes x8, x8^T, W8, W8^T (1 B each) and y (2 B); the backward reads dY
+    (2 B) and W8^T (1 B), writes dY8, dY8^T (1 B) and dX (2 B), and with dW
+    fused (two products per step) also reads x8^T (1 B) and writes dW (2 B)."""
+    fwd = 4.0 * N * K + 4.0 * M * K + 2.0 * M * N
+    with_dw = len(product_ms) == 2
+    bwd = 1.0 * N * K + 4.0 * M * N + 2.0 * M * K + (2.0 * N * K + 1.0 * M * K if with_dw else 0)
+    names = ["small_m_kernel<cast W> (x, W casts; y)",
+             "small_m_kernel<dW> (dY cast; dX, dW)" if with_dw else "small_m_kernel (dY cast; dX)"]
+    i = 0 if product_ms[0] >= product_ms[1] else 1
+    gbs = (fwd, bwd)[i] / (product_ms[i] * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(gbs / peaks["hbm_gbs"], 3), "traffic": None, "kernel": names[i],
+            "peak_basis": "measured HBM copy (of measured)" if peaks["source"] == "measured"
+            else "HBM copy (of fallback)"}
+
+
 SHORT = {"linear4096_m16": "m16", "linear4096_m256": "m256", "linear4096_m4096": "m4096",
          "gpt1.5b_linears_m12288": "gpt1.5b_delayed", "llama3_8b_ffn_m8192": "llama3_ffn"}
 
@@ -712,18 +732,25 @@ def run_native(args):
     n_prof = max(3, min(args.steps, 40))
     kinds, gemm_each, per_step = profiled(q, torch, step, n_prof)
     q.check(lin.ws)
-    gemm_flop = 2.0 * M * N * K          # each of the three GEMMs of this square Linear
-    gemm_avg = sum(gemm_each) / len(gemm_each)
-    achieved = gemm_flop / (gemm_avg * 1e-3) / 1e12
-    tr = load_traffic("gemm")
-    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1),
-                "unit": "TFLOP/s", "frac": round(achieved / peak, 3),
-                "traffic": tr["bytes_per_launch"] if tr else None,
-                "kernel": q.gemm_describe(M, N, K).split(":")[0],
-                "peak_basis": basis + " (of measured)" if peaks["source"] == "measured" else
-                basis + " (of fallback)",
-                "kernel_time": "mean of %d launches, profiled pass of %d steps after the timed "
-                               "region" % (len(gemm_each) * n_prof, n_prof)}
+    if kinds.get("small_m", 0.0) > 0:
+        # A few tokens: the products are fused with their casts and bound by
+        # their bytes; the slower of the two against HBM.
+        roofline = few_token_roofline(M, K, N, gemm_each, peaks)
+        roofline["kernel_time"] = ("mean of %d launches, profiled pass of %d steps after the "
+                                   "timed region" % (n_prof, n_prof))
+    else:
+        gemm_flop = 2.0 * M * N * K          # each of the three GEMMs of this square Linear
+        gemm_avg = sum(gemm_each) / len(gemm_each)
+        achieved = gemm_flop / (gemm_avg * 1e-3) / 1e12
+        tr = load_traffic("gemm", args.workload)
+        roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1),
+                    "unit": "TFLOP/s", "frac": round(achieved / peak, 3),
+                    "traffic": tr["bytes_per_launch"] if tr else None,
+                    "kernel": q.gemm_describe(M, N, K).split(":")[0],
+                    "peak_basis": basis + " (of measured)" if peaks["source"] == "measured" else
+                    basis + " (of fallback)",
+                    "kernel_time": "mean of %d launches, profiled pass of %d steps after the "
+                                   "timed region" % (len(gemm_each) * n_prof, n_prof)}
     # Casts of the step: x [M,K], W [N,K], dY [M,N], each 2 B read + 1 B + 1 B
     # (transposed) written per element.  Tensors that fit on chip run as the
     # single-pass kernel (kind "cast_fused", amax included); the others as
@@ -742,7 +769,7 @@ def run_native(args):
         kernel_ms = 0.0
     if kernel_ms > 0:
         cast_gbs = kernel_bytes / (kernel_ms * 1e-3) / 1e9
-        trc = load_traffic("cast")
+        trc = load_traffic("cast", args.workload)
         cast_roofline = {"bound": "hbm", "achieved": round(cast_gbs, 1), "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": round(cast_gbs / peaks["hbm_gbs"], 3),
                          "traffic": trc["bytes_per_launch"] if trc else None,

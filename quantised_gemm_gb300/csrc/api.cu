@@ -640,6 +640,15 @@ bool small_m_enabled() {
   return on;
 }
 
+// The backward's few-token product also computes dW unless FP8LIN_SMALL_M_DW=0.
+bool small_m_dw_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("FP8LIN_SMALL_M_DW");
+    return !(v != nullptr && v[0] == '0');
+  }();
+  return on;
+}
+
 bool few_token_state(const fp8lin_scaling_state* st, int64_t M) {
   return small_m_enabled() && M >= 1 && M <= kSmallMaxRows && st->kind == FP8LIN_DYNAMIC &&
          (st->amax_algo == FP8LIN_AMAX_AUTO || st->amax_algo == FP8LIN_AMAX_SINGLE_PASS ||
@@ -766,10 +775,11 @@ fp8lin_status run_backward(const void* dy, int64_t M, int64_t K, int64_t N, cons
                            float* dw_amax, void* ws, size_t ws_bytes, const DeviceInfo& dev,
                            cudaStream_t stream) {
   fp8lin_status s;
-  bool dx_done = false;
+  bool dx_done = false, dw_done = false;
   if (dx != nullptr && K > 0 && N > 0 && few_token_state(sdy, M) &&
       small_m_fits(dev, false, FP8LIN_E5M2, M, K, N, split_bytes(ws_bytes))) {
-    // A few tokens: dY's cast and dX = dY8 . W8 (A = W8^T [K, N]) in one launch.
+    // A few tokens: dY's cast and dX = dY8 . W8 (A = W8^T [K, N]) in one launch,
+    // and dW = dY8^T . x8 in the same launch when its amax is not wanted.
     SmallMArgs a = small_m_args(sdy, dy, M, dy8, dy8t, dx, K, dx_amax, ws, ws_bytes);
     a.cast_a = false;
     a.NA = K;
@@ -777,6 +787,14 @@ fp8lin_status run_backward(const void* dy, int64_t M, int64_t K, int64_t N, cons
     a.ldb = N;
     a.a = w8t;
     a.a_inv_in = sw->inv_scale;
+    if (dw != nullptr && dw_amax == nullptr && small_m_dw_enabled() &&
+        small_m_fits(dev, false, FP8LIN_E5M2, M, K, N, split_bytes(ws_bytes), true)) {
+      a.fuse_dw = true;
+      a.x8t = x8t;
+      a.x_inv = sx->inv_scale;
+      a.dw = dw;
+      dw_done = true;
+    }
     if ((s = run_small_m(a, dev, stream)) != FP8LIN_OK) return s;
     dx_done = true;
   } else if (sdy->kind == FP8LIN_DYNAMIC) {
@@ -791,7 +809,7 @@ fp8lin_status run_backward(const void* dy, int64_t M, int64_t K, int64_t N, cons
                 dx, K, dx_amax, ws, ws_bytes, dev, stream);
     if (s != FP8LIN_OK) return s;
   }
-  if (dw != nullptr) {
+  if (dw != nullptr && !dw_done) {
     // dW = dY8^T . x8 : A = dY8^T [N, M], B = x8^T [K, M], contract over M
     s = do_gemm(dy8t, x8t, N, K, M, M, M, FP8LIN_E5M2, FP8LIN_E4M3, sdy->inv_scale, sx->inv_scale,
                 dw, K, dw_amax, ws, ws_bytes, dev, stream);

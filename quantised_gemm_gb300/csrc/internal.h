@@ -221,11 +221,15 @@ struct SmallMArgs {
   uint32_t* ws_amax;
   uint32_t* ws_b_amax;
   int* ws_error;
+  bool fuse_dw;             // the backward also computes dW [KA, NA] = dY8^T . x8
+  const uint8_t* x8t;       // fuse_dw: fp8 x^T [NA, MB]
+  const float* x_inv;       // fuse_dw: x's inverse scale
+  void* dw;                 // fuse_dw: bf16 dW [KA, NA], dense
 };
 // Whether launch_small_m takes these sizes on this device with this much
-// workspace for partials.
+// workspace for partials (fuse_dw: with the weight gradient in the launch).
 bool small_m_fits(const DeviceInfo& dev, bool cast_a, int fmt_b, int64_t MB, int64_t NA,
-                  int64_t KA, size_t partial_bytes);
+                  int64_t KA, size_t partial_bytes, bool fuse_dw = false);
 cudaError_t launch_small_m(const SmallMArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 
 // ---- GEMM (gemm_tcgen05.cu)

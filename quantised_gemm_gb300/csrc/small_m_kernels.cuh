@@ -33,6 +33,18 @@
 // B's fp8 copy and its transpose (x8 / x8^T, dY8 / dY8^T) are written by
 // the CTAs that own B's K slices.
 //
+// kDW (the backward): the same launch also computes the weight gradient
+//   dW [KA, NA] = (dY8^T . x8) * inv_dy * inv_x          (bf16)
+// with K = MB tokens, once the MMAs of dX are done.  dW has as many 128 x 128
+// tiles as dX's product, row-band-major, and each CTA takes the same tile
+// numbers t0 .. t0 + mine - 1, split between the two groups.  Per tile the
+// group writes dY8^T's 128 rows (dY re-cast from bf16 with the scale just
+// found: the same bytes the slice owners store) and x8^T's 128 rows (the
+// forward's transposed x8) into 128-byte-swizzled K-major operands, zero
+// beyond the tokens; one MMA of K = 32 puts the tile into the group's 128
+// TMEM columns; each of the group's 8 warps stores its 32 x 64 block as one
+// TMA box.  The next tile's operand loads are in flight meanwhile.
+//
 // Numerics are those of the separate kernels: amax of the bf16 bit patterns,
 // scale = __fdiv_rn(F, max(amax, eps)), q = cvt.rn.satfinite(x * scale), fp32
 // accumulation on the tensor cores; only the order in which the fp32 partial
@@ -50,6 +62,12 @@ constexpr int kSmTilesPerCta = 7;
 constexpr int kSmTileBytes = kTile * kTile * 2;        // one bf16 tile; fp8 uses the first half
 constexpr int kSmBSliceOffset = kTile * kTile;         // B's slice sits in the second half
 constexpr size_t kSmSmem = static_cast<size_t>(kSmTilesPerCta) * kSmTileBytes + 1024;
+
+constexpr int kSmDwTmemCol = 256;                      // kDW: dW accumulators, 128 columns per group
+constexpr int kSmDwStageOffset = 4 * kTile * kTile;    // kDW: operands (2 x 2 x 16 KB), then boxes
+constexpr int kSmDwBoxBytes = 32 * 64 * 2;             // one 32-row x 64-column bf16 box
+static_assert(kSmDwStageOffset + 16 * 2 * kSmDwBoxBytes <= kSmTilesPerCta * kSmTileBytes,
+              "dW operands and staging boxes fit in the tile slots");
 
 struct SmallParams {
   int NA, KA, MB;               // D^T [NA, MB] = A [NA, KA] . B [MB, KA]^T
@@ -79,10 +97,26 @@ struct SmallParams {
   uint32_t* ws_amax;            // amax of A (kCastA)
   uint32_t* ws_b_amax;          // amax of B (unless given)
   int* err;
+  const uint8_t* x8t;           // kDW: fp8 x^T [NA, MB] (e4m3, from the forward)
+  const float* x_inv;           // kDW: x's inverse scale
 };
 
 __device__ __forceinline__ void sm_group_sync(int group) {
   asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(256) : "memory");
+}
+
+// AND of `pred` over the 256 threads of `group` (also a barrier of the group).
+__device__ __forceinline__ bool sm_group_and(int group, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %2, 0;\n\t"
+      "bar.red.and.pred p, %1, 256, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(1 + group), "r"(pred ? 1u : 0u)
+      : "memory");
+  return r != 0;
 }
 
 // Max over the 512 threads of a 16-bit magnitude pattern; result in s_out
@@ -108,12 +142,142 @@ __device__ __forceinline__ void sm_tmem_load(uint32_t taddr, uint32_t (&r)[kMN])
   tmem_load_wait();
 }
 
-template <bool kCastA, int kFmtB, int kMN>
+// kDW: the global operand bytes of one dW tile for this thread of its group
+// -- dY vectors of the tile's 128 rows of dW (kMN / 16 per thread) and one
+// 16-byte piece of x8^T's 128 rows.
+template <int kMN>
+struct DwLoads {
+  uint4 y[kMN / 16];
+  uint4 x;
+};
+
+template <int kMN>
+__device__ __forceinline__ void dw_load(const SmallParams& p, int t, int nbands, int gtid,
+                                        DwLoads<kMN>& l) {
+  const int n0 = (t / nbands) * kTile, k0 = (t % nbands) * kTile;
+#pragma unroll
+  for (int u = 0; u < kMN / 16; ++u) {
+    const int i = gtid + 256 * u, m = i >> 4, n = n0 + (i & 15) * 8;
+    l.y[u] = n < p.KA ? ld_stream_v4(p.b + static_cast<int64_t>(m) * p.ldb + n)
+                      : make_uint4(0u, 0u, 0u, 0u);
+  }
+  // x8^T rows are kMN bytes: one 16-byte piece per thread (16 tokens: the first 128 threads).
+  const int row = kMN == 16 ? gtid : gtid >> 1, piece = kMN == 16 ? 0 : gtid & 1;
+  const int k = k0 + row;
+  l.x = (row < kTile && k < p.NA)
+            ? *reinterpret_cast<const uint4*>(p.x8t + static_cast<int64_t>(k) * kMN + 16 * piece)
+            : make_uint4(0u, 0u, 0u, 0u);
+}
+
+// kDW: the group's dW tiles (its share of t0 .. t0 + mine - 1), after the
+// MMAs of dX are done: operands into the group's two 16 KB buffers, one MMA
+// (K = 32, the tokens zero-padded), the group's 8 warps each take a 32-row x
+// 64-column block out of TMEM and store it as one TMA box (two boxes per
+// warp, used in turn).  `l` holds the group's first tile's loads on entry.
+// Returns false (group-uniform) when the wait for an MMA ran out.
+template <int kFmtB, int kMN>
+__device__ __forceinline__ bool dw_tiles(const SmallParams& p, const CUtensorMap* tmDW,
+                                         uint8_t* tiles, uint32_t tmem, uint64_t* done, int t0,
+                                         int mine, int nbands, float s_dy, float alpha,
+                                         DwLoads<kMN>& l) {
+  constexpr uint32_t kIdesc = make_idesc_f8(static_cast<uint32_t>(kFmtB), 0u, 128u, 128u);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int group = tid >> 8, gtid = tid & 255;
+  uint8_t* opA = tiles + group * (2 * kTile * kTile);  // dY8^T rows, 128 B each (swizzled)
+  uint8_t* opB = opA + kTile * kTile;                   // x8^T rows
+  const uint32_t d_tmem = tmem + static_cast<uint32_t>(kSmDwTmemCol + 128 * group);
+  if constexpr (kMN == 16) {  // tokens 16..31 of every row stay zero
+    uint8_t* buf = gtid < kTile ? opA : opB;
+    *reinterpret_cast<uint4*>(buf + sw128(gtid & (kTile - 1), 16)) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  const int quarter = warp & 3, half = (warp >> 2) & 1;
+  bool prev_stored = false, ok = true;
+  uint32_t phase = 0;
+  int band = -1;
+  for (int k = group, kq = 0; k < mine; k += 2, ++kq) {
+    const int t = t0 + k, nb = t / nbands;
+    if (nb != band) {  // dY8^T of this band of dW rows: byte m of row n (8 rows per vector)
+      band = nb;
+#pragma unroll
+      for (int u = 0; u < kMN / 16; ++u) {
+        const int i = gtid + 256 * u, m = i >> 4, j = i & 15;
+        const uint2 q = cast8<kFmtB>(l.y[u], s_dy);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int r = (e + j) & 7;  // rotated: the warp's rows fall in different chunks
+          opA[sw128(8 * j + r, m)] = static_cast<uint8_t>(((r < 4 ? q.x : q.y) >> (8 * (r & 3))));
+        }
+      }
+    }
+    if (kMN == 32 || gtid < kTile) {
+      const int row = kMN == 16 ? gtid : gtid >> 1, piece = kMN == 16 ? 0 : gtid & 1;
+      *reinterpret_cast<uint4*>(opB + sw128(row, 16 * piece)) = l.x;
+    }
+    if (k + 2 < mine) dw_load<kMN>(p, t + 2, nbands, gtid, l);  // lands during this tile
+    fence_proxy_async_shared();
+    sm_group_sync(group);
+    if (gtid == 0) {
+      tc_fence_after_sync();
+      mma_f8f6f4(d_tmem, smem_desc_k_sw128(smem_addr(opA)), smem_desc_k_sw128(smem_addr(opB)),
+                 kIdesc, 0u);
+      mma_commit(&done[group]);
+    }
+    volatile int never = 0;
+    const bool landed = mbar_wait_bounded(&done[group], phase, &never);
+    phase ^= 1u;
+    if (!sm_group_and(group, landed)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after_sync();
+    uint32_t ra[32], rb[32];
+    const uint32_t taddr = d_tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
+                           static_cast<uint32_t>(half * 64);
+    tmem_load_32cols(taddr, ra);
+    tmem_load_32cols(taddr + 32, rb);
+    tmem_load_wait();
+    tc_fence_before_sync();  // the reads are done before the group's next MMA
+    uint32_t w[32];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      float v0, v1;
+      mul2_rn(ra[2 * j], ra[2 * j + 1], alpha, v0, v1);
+      w[j] = cvt_bf16x2(v0, v1);
+      mul2_rn(rb[2 * j], rb[2 * j + 1], alpha, v0, v1);
+      w[16 + j] = cvt_bf16x2(v0, v1);
+    }
+    uint8_t* box = tiles + kSmDwStageOffset + (warp * 2 + (kq & 1)) * kSmDwBoxBytes;
+    if (lane == 0) {  // the box's last store has read it
+      if (prev_stored)
+        bulk_wait_group_read<1>();
+      else
+        bulk_wait_group_read<0>();
+    }
+    __syncwarp();
+    uint8_t* rowp = box + lane * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      *reinterpret_cast<uint4*>(rowp + ((c ^ (lane & 7)) << 4)) =
+          make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+    fence_proxy_async_shared();
+    __syncwarp();
+    const int row0 = nb * kTile + quarter * 32, col0 = (t % nbands) * kTile + half * 64;
+    prev_stored = row0 < p.KA && col0 < p.NA;  // boxes are clipped at dW's edges
+    if (lane == 0 && prev_stored) {
+      tma_store_2d(tmDW, box, col0, row0);
+      bulk_commit_group();
+    }
+  }
+  return ok;
+}
+
+template <bool kCastA, int kFmtB, int kMN, bool kDW>
 __global__ void __launch_bounds__(kSmThreads, 1)
     small_m_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA8,
-                   const SmallParams p) {
+                   const __grid_constant__ CUtensorMap tmDW, const SmallParams p) {
   static_assert(kMN == 16 || kMN == 32, "tokens per MMA");
-  constexpr int kTmemCols = kSmTilesPerCta * kMN <= 128 ? 128 : 256;
+  static_assert(!(kDW && kCastA), "dW is fused into the backward product only");
+  constexpr int kTmemCols = kDW ? 512 : (kSmTilesPerCta * kMN <= 128 ? 128 : 256);
   constexpr int kBVec = kMN * 16 / 256;  // B slice vectors per thread of a group, per tile
   constexpr int kGroupTiles = (kSmTilesPerCta + 1) / 2;
   constexpr uint32_t kIdesc = make_idesc_f8(0u, static_cast<uint32_t>(kFmtB), 128u, kMN);
@@ -122,6 +286,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
       (reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   __shared__ __align__(8) uint64_t loaded[kSmTilesPerCta];
   __shared__ __align__(8) uint64_t mma_done[2];
+  __shared__ __align__(8) uint64_t dw_done[2];
   __shared__ uint32_t s_tmem;
   __shared__ uint32_t s_red[kSmThreads / 32];
   __shared__ uint32_t s_b_bits, s_a_bits, s_d_bits;
@@ -145,6 +310,11 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     for (int k = 0; k < kSmTilesPerCta; ++k) mbar_init(&loaded[k], 1);
     mbar_init(&mma_done[0], 1);
     mbar_init(&mma_done[1], 1);
+    if (kDW) {
+      mbar_init(&dw_done[0], 1);
+      mbar_init(&dw_done[1], 1);
+      tma_prefetch_map(&tmDW);
+    }
     fence_barrier_init();
     if (kCastA) tma_prefetch_map(&tmA);
     tma_prefetch_map(&tmA8);
@@ -399,6 +569,9 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     }
   }
 
+  DwLoads<kMN> dwl;
+  if (kDW && ok && group < mine) dw_load<kMN>(p, t0 + group, nbands, gtid, dwl);
+
   griddep_launch_dependents();
   {
     volatile int never = 0;
@@ -454,6 +627,15 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     }
   }
   __syncthreads();
+  if constexpr (kDW) {
+    // dW (the tile slots are free: the MMAs that read them are done)
+    if (ok) {
+      const float alpha_dw = __fmul_rn(inv_b, *p.x_inv);
+      const bool dw_ok = dw_tiles<kFmtB, kMN>(p, &tmDW, tiles, tmem, dw_done, t0, mine, nbands,
+                                              s_b, alpha_dw, dwl);
+      if (!dw_ok && gtid == 0) atomicCAS(p.err, 0, kErrGemmMmaWait);
+    }
+  }
   const float alpha = __fmul_rn(inv_a, inv_b);
   float vmax = 0.0f;
   const int nb = s_nbands;
@@ -518,6 +700,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     }
   }
   if (kCastA && gtid == 0) bulk_wait_group<0>();  // W8 stores done before the smem goes away
+  if (kDW && lane == 0) bulk_wait_group<0>();     // and dW's boxes
   if (!ok && tid == 0) {
     // Copies in flight land before the shared memory goes away (bounded).
     volatile int never = 0;

@@ -1,6 +1,6 @@
 """bench.py's DRAM-traffic records, on CPU: a record counts only for the device
-code it was captured on, and its per-launch figure is the captured one scaled
-to the benchmark's launch."""
+code and the workload it was captured on, and its per-launch figure is the
+captured one scaled to the benchmark's launch."""
 import json
 import os
 import shutil
@@ -28,12 +28,32 @@ def test_records_are_internally_consistent():
 
 def test_record_applies_only_to_its_device_code(monkeypatch):
     for kernel in ("gemm", "cast"):
-        rec = bench.load_traffic(kernel)
+        rec = bench.load_traffic(kernel, bench.HEADLINE)
         if rec is not None:  # a fresh record: keyed on exactly this code
             assert rec["src_sha"] == bench.device_code_sha(kernel)
         monkeypatch.setattr(bench, "device_code_sha", lambda k: "0" * 16)
-        assert bench.load_traffic(kernel) is None
+        assert bench.load_traffic(kernel, bench.HEADLINE) is None
         monkeypatch.undo()
+
+
+def test_record_applies_only_to_its_workload():
+    assert {r["workload"] for r in _records()} == {bench.HEADLINE}
+    for kernel in ("gemm", "cast"):
+        assert bench.load_traffic(kernel, "linear4096_m16") is None
+
+
+def test_few_token_roofline_bytes():
+    peaks = {"hbm_gbs": 1000.0, "source": "measured"}
+    M, K, N = 16, 4096, 4096
+    # forward: x, W read (2 B), x8, x8^T, W8, W8^T written (1 B each), y (2 B)
+    fwd = 2 * M * K + 2 * N * K + 2 * M * K + 2 * N * K + 2 * M * N
+    # backward with dW: dY (2 B), W8^T, x8^T read; dY8, dY8^T, dX (2 B), dW (2 B) written
+    bwd = 2 * M * N + N * K + M * K + 2 * M * N + 2 * M * K + 2 * N * K
+    r = bench.few_token_roofline(M, K, N, [0.02, 0.01], peaks)
+    assert r["achieved"] == pytest.approx(fwd / 0.02e-3 / 1e9, rel=1e-3) and "cast W" in r["kernel"]
+    r = bench.few_token_roofline(M, K, N, [0.01, 0.02], peaks)
+    assert r["achieved"] == pytest.approx(bwd / 0.02e-3 / 1e9, rel=1e-3) and "dW" in r["kernel"]
+    assert r["bound"] == "hbm" and r["frac"] == pytest.approx(r["achieved"] / 1000.0, abs=1e-3)
 
 
 def test_hash_covers_the_inlined_ptx_helpers(tmp_path, monkeypatch):
