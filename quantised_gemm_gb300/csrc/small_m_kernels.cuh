@@ -105,6 +105,25 @@ __device__ __forceinline__ void sm_group_sync(int group) {
   asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(256) : "memory");
 }
 
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Atomic add with release semantics at GPU scope (this thread's earlier
+// writes, and those ordered before it by a CTA barrier, are visible to a
+// thread that acquires the new value); returns the old value.
+__device__ __forceinline__ int atom_add_release(int* p, int v) {
+  int old;
+  asm volatile("atom.release.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
 // AND of `pred` over the 256 threads of `group` (also a barrier of the group).
 __device__ __forceinline__ bool sm_group_and(int group, bool pred) {
   uint32_t r;
@@ -365,7 +384,6 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     if (my_slices > 0) {  // CTA-uniform
       const uint32_t pk = am.packed();
       sm_block_max(max(pk & 0xFFFFu, pk >> 16), s_red, &s_b_bits);
-      if (tid == 0) atomicMax(p.ws_b_amax, s_b_bits);
     }
   } else if (tid == 0) {
     s_b_bits = __float_as_uint(*p.b_amax_in);
@@ -401,6 +419,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
   if (ok && need_barrier) {
     if (tid == 0) {
       if (kCastA) atomicMax(p.ws_amax, s_a_bits);
+      if (!b_given && my_slices > 0) atomicMax(p.ws_b_amax, s_b_bits);
       // kCastA: every CTA arrives once; else each slice of B arrives once.
       const uint32_t arrive = kCastA ? 1u : static_cast<uint32_t>(my_slices);
       const uint32_t target = kCastA ? gridDim.x : static_cast<uint32_t>(nks);
@@ -413,23 +432,19 @@ __global__ void __launch_bounds__(kSmThreads, 1)
           break;
         }
       }
-      if (!s_abort) {
-        if (kCastA) s_a_bits = ld_acquire_u32(p.ws_amax);
-        if (!b_given) s_b_bits = ld_acquire_u32(p.ws_b_amax);
+      if (!s_abort) {  // ordered after every arrival by the acquiring poll; both in flight at once
+        const uint32_t a_bits = kCastA ? ld_relaxed_u32(p.ws_amax) : 0u;
+        const uint32_t b_bits = b_given ? 0u : ld_relaxed_u32(p.ws_b_amax);
+        if (kCastA) s_a_bits = a_bits;
+        if (!b_given) s_b_bits = b_bits;
       }
     }
     __syncthreads();
     ok = s_abort == 0;
-    // Count this CTA out; the last one clears the words for the next launch.
-    if (ok && tid == 0 && atomicAdd(p.ws_exits, 1u) == gridDim.x - 1) {
-      atomicExch(p.ws_barrier, 0u);
-      atomicExch(p.ws_exits, 0u);
-      atomicExch(p.ws_amax, 0u);
-      atomicExch(p.ws_b_amax, 0u);
-    }
   } else {
     __syncthreads();
   }
+  const bool passed = need_barrier && ok;  // counts out once its MMAs are issued
 
   const float amax_b = __uint_as_float(s_b_bits);
   const float s_b = scale_from_amax(amax_b, p.eps, fp8_max<kFmtB>());
@@ -573,6 +588,14 @@ __global__ void __launch_bounds__(kSmThreads, 1)
   if (kDW && ok && group < mine) dw_load<kMN>(p, t0 + group, nbands, gtid, dwl);
 
   griddep_launch_dependents();
+  // Count this CTA out of the grid barrier (it has read its words); the last
+  // one clears them for the next launch.  Off the path: the MMAs are running.
+  if (passed && tid == 0 && atomicAdd(p.ws_exits, 1u) == gridDim.x - 1) {
+    atomicExch(p.ws_barrier, 0u);
+    atomicExch(p.ws_exits, 0u);
+    atomicExch(p.ws_amax, 0u);
+    atomicExch(p.ws_b_amax, 0u);
+  }
   {
     volatile int never = 0;
     bool done = mbar_wait_bounded(&mma_done[0], 0, &never);
@@ -609,24 +632,17 @@ __global__ void __launch_bounds__(kSmThreads, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
-  if (tid == 0) {
-    s_nbands = 0;
-    if (ok) {
-      // The CTA's partials (ordered before this thread by the barrier) are
-      // visible GPU-wide before its ticket counts them.
-      __threadfence();
-      for (int a = 0; a < nacc; ++a) {
-        const int band = band0 + a;
-        const int lo = max(t0, band * nks), hi = min(t0 + mine, (band + 1) * nks);
-        if (atomicAdd(&p.tickets[band], hi - lo) + (hi - lo) == nks) {
-          p.tickets[band] = 0;  // every K tile has arrived: clear for the next launch
-          s_bands[s_nbands++] = band;
-        }
-      }
-      __threadfence();
-    }
+  // Tickets: one lane of the last warp per band of this CTA adds the CTA's
+  // tile count, releasing its partials (ordered before the lane by the
+  // barrier).  The old values are looked at only after dW (kDW), so the
+  // warp does not wait for them.
+  int old_ticket = 0, my_band = -1, my_count = 0;
+  if (warp == kSmThreads / 32 - 1 && ok && lane < nacc) {
+    my_band = band0 + lane;
+    const int lo = max(t0, my_band * nks), hi = min(t0 + mine, (my_band + 1) * nks);
+    my_count = hi - lo;
+    old_ticket = atom_add_release(&p.tickets[my_band], my_count);
   }
-  __syncthreads();
   if constexpr (kDW) {
     // dW (the tile slots are free: the MMAs that read them are done)
     if (ok) {
@@ -636,6 +652,17 @@ __global__ void __launch_bounds__(kSmThreads, 1)
       if (!dw_ok && gtid == 0) atomicCAS(p.err, 0, kErrGemmMmaWait);
     }
   }
+  if (warp == kSmThreads / 32 - 1) {
+    const bool completes = my_band >= 0 && old_ticket + my_count == nks;
+    if (completes) {
+      p.tickets[my_band] = 0;  // every K tile has arrived: clear for the next launch
+      fence_acq_rel_gpu();     // ...and every partial of the band is visible to this CTA
+    }
+    const uint32_t m = __ballot_sync(0xFFFFFFFFu, completes);
+    if (completes) s_bands[__popc(m & ((1u << lane) - 1u))] = my_band;
+    if (lane == 0) s_nbands = __popc(m);
+  }
+  __syncthreads();
   const float alpha = __fmul_rn(inv_a, inv_b);
   float vmax = 0.0f;
   const int nb = s_nbands;
