@@ -338,7 +338,10 @@ fp8lin_status fp8lin_forward(const void* x, const void* w, int64_t M, int64_t K,
  * can feed the previous layer's grad_output state as PRECOMPUTED.
  * A few tokens (M <= 32) with dynamic scaling of dY (AUTO, SINGLE_PASS or
  * PRECOMPUTED) and dx not NULL: dY's cast and dX run as one fused launch
- * (as in fp8lin_forward); dW follows as its own GEMM. */
+ * (as in fp8lin_forward), and dW in the same launch when dw is not NULL and
+ * dw_amax is NULL (dW equals the GEMM's value for value; an exact zero may
+ * differ in sign).  Otherwise dW follows as its own GEMM; so it does with
+ * FP8LIN_SMALL_M_DW=0 in the environment. */
 fp8lin_status fp8lin_backward(const void* dy, int64_t M, int64_t K, int64_t N,
                               const uint8_t* x8t, const uint8_t* w8t,
                               const fp8lin_scaling_state* sx, const fp8lin_scaling_state* sw,
