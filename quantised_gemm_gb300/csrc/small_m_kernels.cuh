@@ -349,8 +349,12 @@ __global__ void __launch_bounds__(kSmThreads, 1)
   griddep_wait();  // B, A and the states are ready; D and the outputs are free
 
   // ---- phase 1: A tiles in flight (one barrier each); this thread's B
-  // vectors for its group's tiles in one batch; the amax of B's slices
-  if (tid == 0) {
+  // vectors for its group's tiles in one batch; the amax of B's slices.
+  // The fp8 variant whose token side needs the grid barrier loads its tiles
+  // after the barrier instead: the barrier waits on the few bytes of B's
+  // slices, which would otherwise queue behind every CTA's tile loads.
+  const bool late_a = !kCastA && !b_given;  // grid-uniform
+  auto issue_a = [&] {
     constexpr uint32_t kTileIn = kCastA ? kTile * kTile * 2 : kTile * kTile;
     for (int k = 0; k < mine; ++k) {
       const int t = t0 + k;
@@ -358,7 +362,8 @@ __global__ void __launch_bounds__(kSmThreads, 1)
       tma_load_2d(tiles + k * kSmTileBytes, kCastA ? &tmA : &tmA8, &loaded[k], (t % nks) * kTile,
                   (t / nks) * kTile);
     }
-  }
+  };
+  if (tid == 0 && !late_a) issue_a();
   uint4 bv[kGroupTiles][kBVec];
 #pragma unroll
   for (int kq = 0; kq < kGroupTiles; ++kq) {
@@ -445,6 +450,8 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     __syncthreads();
   }
   const bool passed = need_barrier && ok;  // counts out once its MMAs are issued
+  const bool a_issued = !late_a || ok;      // CTA-uniform
+  if (late_a && ok && tid == 0) issue_a();
 
   const float amax_b = __uint_as_float(s_b_bits);
   const float s_b = scale_from_amax(amax_b, p.eps, fp8_max<kFmtB>());
@@ -728,7 +735,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
   }
   if (kCastA && gtid == 0) bulk_wait_group<0>();  // W8 stores done before the smem goes away
   if (kDW && lane == 0) bulk_wait_group<0>();     // and dW's boxes
-  if (!ok && tid == 0) {
+  if (!ok && a_issued && tid == 0) {
     // Copies in flight land before the shared memory goes away (bounded).
     volatile int never = 0;
     for (int k = 0; k < mine; ++k) mbar_wait_bounded(&loaded[k], 0, &never);
