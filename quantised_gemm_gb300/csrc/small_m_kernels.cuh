@@ -378,20 +378,29 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     }
   }
   int my_slices = 0;  // B slices this CTA owns: blockIdx.x, blockIdx.x + G, ...
-  if (!b_given) {
+  uint4 b_own = make_uint4(0u, 0u, 0u, 0u);  // this thread's vector of slice blockIdx.x, kept
+  if (!b_given) {                            // for B's fp8 copies (MB * 16 <= threads)
     AbsMax am;
     for (int c = blockIdx.x; c < nks; c += G, ++my_slices) {
       for (int i = tid; i < p.MB * 16; i += kSmThreads) {
         const int m = i >> 4, j = c * kTile + (i & 15) * 8;
-        if (j < p.KA) am.add(ld_stream_v4(p.b + static_cast<int64_t>(m) * p.ldb + j));
+        if (j < p.KA) {
+          const uint4 v = ld_stream_v4(p.b + static_cast<int64_t>(m) * p.ldb + j);
+          am.add(v);
+          if (c == static_cast<int>(blockIdx.x)) b_own = v;
+        }
       }
     }
     if (my_slices > 0) {  // CTA-uniform
       const uint32_t pk = am.packed();
       sm_block_max(max(pk & 0xFFFFu, pk >> 16), s_red, &s_b_bits);
     }
-  } else if (tid == 0) {
-    s_b_bits = __float_as_uint(*p.b_amax_in);
+  } else {
+    if (tid == 0) s_b_bits = __float_as_uint(*p.b_amax_in);
+    if (static_cast<int>(blockIdx.x) < nks && tid < p.MB * 16) {
+      const int j = static_cast<int>(blockIdx.x) * kTile + (tid & 15) * 8;
+      if (j < p.KA) b_own = ld_stream_v4(p.b + static_cast<int64_t>(tid >> 4) * p.ldb + j);
+    }
   }
 
   bool ok = true;
@@ -471,6 +480,29 @@ __global__ void __launch_bounds__(kSmThreads, 1)
       *p.a_amax = __uint_as_float(s_a_bits);
       *p.a_scale = s_a;
       *p.a_inv = inv_a;
+    }
+  }
+
+  // ---- B's fp8 copies (for the later kernels): the CTA of each K slice
+  // writes it (q [MB, KA], q^T [KA, MB]), the first slice from the registers
+  // its amax was taken from.  Before the tiles' casts: behind their stores
+  // these few bytes waited about a microsecond.
+  if (ok) {
+    for (int c = blockIdx.x; c < nks; c += G) {
+      for (int i = tid; i < kMN * 16; i += kSmThreads) {
+        const int m = i >> 4, j = (c * kTile) + (i & 15) * 8;
+        if (m < p.MB && j < p.KA) {
+          const uint4 v = c == static_cast<int>(blockIdx.x)
+                              ? b_own
+                              : ld_stream_v4(p.b + static_cast<int64_t>(m) * p.ldb + j);
+          const uint2 q = cast8<kFmtB>(v, s_b);
+          *reinterpret_cast<uint2*>(p.b8 + static_cast<int64_t>(m) * p.KA + j) = q;
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            p.b8t[static_cast<int64_t>(j + e) * p.MB + m] =
+                static_cast<uint8_t>(((e < 4 ? q.x : q.y) >> (8 * (e & 3))) & 0xFFu);
+        }
+      }
     }
   }
 
@@ -572,25 +604,6 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     else
       mbar_arrive(&mma_done[group]);
   }
-  // ---- B's fp8 copies (for the later kernels): the CTA of each K slice
-  // writes it (q [MB, KA], q^T [KA, MB]), while its MMAs run
-  if (ok) {
-    for (int c = blockIdx.x; c < nks; c += G) {
-      for (int i = tid; i < kMN * 16; i += kSmThreads) {
-        const int m = i >> 4, j = (c * kTile) + (i & 15) * 8;
-        if (m < p.MB && j < p.KA) {
-          const uint4 v = ld_stream_v4(p.b + static_cast<int64_t>(m) * p.ldb + j);
-          const uint2 q = cast8<kFmtB>(v, s_b);
-          *reinterpret_cast<uint2*>(p.b8 + static_cast<int64_t>(m) * p.KA + j) = q;
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            p.b8t[static_cast<int64_t>(j + e) * p.MB + m] =
-                static_cast<uint8_t>(((e < 4 ? q.x : q.y) >> (8 * (e & 3))) & 0xFFu);
-        }
-      }
-    }
-  }
-
   DwLoads<kMN> dwl;
   if (kDW && ok && group < mine) dw_load<kMN>(p, t0 + group, nbands, gtid, dwl);
 
