@@ -582,7 +582,7 @@ __global__ void __launch_bounds__(kSpThreads, 1)
   extern __shared__ __align__(1024) uint8_t tiles_raw[];
   uint8_t* tiles = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(tiles_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  __shared__ __align__(8) uint64_t loaded;
+  __shared__ __align__(8) uint64_t loaded[kSinglePassTilesPerCta];  // one per tile
   __shared__ uint32_t s_amax_bits;
   __shared__ uint32_t s_red[kSpThreads / 32];
   __shared__ int s_abort;
@@ -597,28 +597,27 @@ __global__ void __launch_bounds__(kSpThreads, 1)
   griddep_wait();
   if (threadIdx.x == 0) {
     s_abort = 0;
-    mbar_init(&loaded, 1);
+    for (int k = 0; k < mine; ++k) mbar_init(&loaded[k], 1);
     fence_barrier_init();
-    mbar_arrive_expect_tx(&loaded, static_cast<uint32_t>(mine) * (kTile * kTile * 2));
     for (int k = 0; k < mine; ++k) {
       const int64_t t = blockIdx.x + static_cast<int64_t>(k) * gridDim.x;
-      tma_load_2d(tiles + k * (kTile * kTile * 2), &tmX, &loaded,
+      mbar_arrive_expect_tx(&loaded[k], kTile * kTile * 2);
+      tma_load_2d(tiles + k * (kTile * kTile * 2), &tmX, &loaded[k],
                   static_cast<int32_t>((t % ntc) * kTile), static_cast<int32_t>((t / ntc) * kTile));
     }
   }
   __syncthreads();
-  {
-    volatile int never = 0;
-    if (!mbar_wait_bounded(&loaded, 0, &never)) {
-      if (threadIdx.x == 0) atomicCAS(p.ws_error, 0, kErrGridBarrier);
-      mbar_wait_bounded(&loaded, 0, &never);  // give copies in flight a second chance to land
-      return;
-    }
-  }
-  // Two independent accumulators of the short-step kind: the tile is on chip,
-  // so this loop is a latency chain, not a bandwidth stream.
+  // The amax of each tile as soon as it lands.  Two independent accumulators
+  // of the short-step kind: the tile is on chip, so this loop is a latency
+  // chain, not a bandwidth stream.
   AbsMax a0, a1;
+  bool landed = true;
   for (int k = group; k < mine; k += kSpGroups) {
+    volatile int never = 0;
+    if (!mbar_wait_bounded(&loaded[k], 0, &never)) {
+      landed = false;
+      break;
+    }
     const uint8_t* buf = tiles + k * (kTile * kTile * 2);
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
@@ -634,7 +633,14 @@ __global__ void __launch_bounds__(kSpThreads, 1)
     m = __reduce_max_sync(0xFFFFFFFFu, m);
     if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = m;
   }
-  __syncthreads();
+  if (__syncthreads_and(landed ? 1 : 0) == 0) {  // one decision for the CTA
+    if (threadIdx.x == 0) {
+      atomicCAS(p.ws_error, 0, kErrGridBarrier);
+      volatile int never = 0;  // copies in flight land before the shared memory goes away
+      for (int k = 0; k < mine; ++k) mbar_wait_bounded(&loaded[k], 0, &never);
+    }
+    return;
+  }
   if (threadIdx.x == 0) {
     uint32_t m = 0;
     for (int w = 0; w < kSpThreads / 32; ++w) m = max(m, s_red[w]);
@@ -648,18 +654,12 @@ __global__ void __launch_bounds__(kSpThreads, 1)
         break;
       }
     }
-    if (!s_abort) s_amax_bits = ld_acquire_u32(p.ws_amax);
+    // Ordered after every arrival by the acquiring poll above.
+    if (!s_abort) s_amax_bits = *reinterpret_cast<volatile uint32_t*>(p.ws_amax);
   }
   __syncthreads();
   if (s_abort) return;
   griddep_launch_dependents();
-  // Off the critical path: count this CTA out (it has read the amax); the
-  // last one clears the three words for the next launch.
-  if (threadIdx.x == 0 && atomicAdd(p.ws_exits, 1u) == gridDim.x - 1) {
-    atomicExch(p.ws_barrier, 0u);
-    atomicExch(p.ws_exits, 0u);
-    atomicExch(p.ws_amax, 0u);
-  }
 
   const float amax = __uint_as_float(s_amax_bits);
   const float s = scale_from_amax(amax, p.eps, fp8_max<kFmt>());
@@ -699,6 +699,14 @@ __global__ void __launch_bounds__(kSpThreads, 1)
         tma_store_2d(&tmQT, stt, static_cast<int32_t>(r0), static_cast<int32_t>(c0));
       bulk_commit_group();
     }
+  }
+  // Count this CTA out (it has read the amax; after its casts, so that the
+  // atomic's round trip delays no group); the last one clears the three words
+  // for the next launch.
+  if (threadIdx.x == 0 && atomicAdd(p.ws_exits, 1u) == gridDim.x - 1) {
+    atomicExch(p.ws_barrier, 0u);
+    atomicExch(p.ws_exits, 0u);
+    atomicExch(p.ws_amax, 0u);
   }
   if (issuer) bulk_wait_group<0>();  // stores done before the shared memory goes away
 }

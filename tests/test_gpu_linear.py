@@ -102,6 +102,39 @@ def test_few_token_fused_output_amaxes_and_repeat():
         assert np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("M", [16, 32])
+def test_few_token_backward_variants(M):
+    """The few-token backward with dW's amax asked for (dW then runs as its own
+    GEMM after the fused dY / dX launch), with dX skipped (no fused launch),
+    and with dW skipped: every variant's dX and dW equal the fused launch's
+    value for value, and max |dW| is the stored dW's."""
+    K, N = 784, 1040
+    x, w, dy = si.linear_inputs(M, K, N, w_init="uniform64", seed=67)
+    lin = q.Fp8Linear(M, K, N)
+    lin.forward(to_dev_bf16(x), to_dev_bf16(w))
+    dyd = to_dev_bf16(dy)
+    n0 = q.launch_count()
+    lin.backward(dyd)
+    assert q.launch_count() - n0 == 1               # dY's cast, dX and dW in one launch
+    dx_f, dw_f = lin.dx.clone(), lin.dw.clone()
+    dwa = torch.full((1,), -1.0, device="cuda")
+    q.backward(dyd, lin.x8t, lin.w8t, lin.sx, lin.sw, lin.sdy, lin.dy8, lin.dy8t, lin.dx, lin.dw,
+               lin.ws, dw_amax=dwa)
+    q.check(lin.ws)
+    assert torch.equal(lin.dx.view(torch.int16), dx_f.view(torch.int16))
+    assert torch.equal(lin.dw.float(), dw_f.float())
+    assert dev_f32_bits(dwa) == f32_bits(oracle.amax(_bits(lin.dw)))
+    lin.dx.fill_(5.0)
+    lin.dw.zero_()
+    lin.backward(dyd, need_dx=False)
+    assert torch.all(lin.dx == 5.0) and torch.equal(lin.dw.float(), dw_f.float())
+    lin.dw.fill_(5.0)
+    lin.backward(dyd, need_dw=False)
+    q.check(lin.ws)
+    assert torch.all(lin.dw == 5.0)
+    assert torch.equal(lin.dx.view(torch.int16), dx_f.view(torch.int16))
+
+
 def test_linear_delayed_small_full_compare():
     """Delayed scaling with a stale scale can saturate; compare everything."""
     M, K, N = 144, 272, 208
