@@ -324,6 +324,20 @@ __global__ void __launch_bounds__(kThreads, 4) cast_kernel(const CastParams p) {
 // write both with TMA bulk stores.  No thread issues a global load or store
 // of its own.
 constexpr int kStreamStages = 3;
+constexpr int kStreamBlockRows = 8;  // tile rows per block of the walk order
+
+// Tile t of the streaming walk as (tile row, tile column): blocks of
+// kStreamBlockRows tile rows, column by column inside a block, so that the
+// tiles in flight at once cover a few rows and columns and both outputs, q
+// and its transpose, are written in runs of several tiles.
+__device__ __forceinline__ void stream_tile(int64_t t, int64_t ntr, int64_t ntc, int64_t& tr,
+                                            int64_t& tc) {
+  const int64_t per_block = static_cast<int64_t>(kStreamBlockRows) * ntc;
+  const int64_t b = t / per_block, i = t - b * per_block;
+  const int64_t rows = min(static_cast<int64_t>(kStreamBlockRows), ntr - b * kStreamBlockRows);
+  tr = b * kStreamBlockRows + i % rows;
+  tc = i / rows;
+}
 constexpr int kStreamConsumers = 256;
 constexpr int kStreamThreads = 32 + kStreamConsumers;
 constexpr int kTileBytesBf16 = kTile * kTile * 2;
@@ -414,7 +428,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   __shared__ uint32_t s_red[kStreamConsumers / 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t ntc = (p.cols + kTile - 1) / kTile;
-  const int64_t ntiles = ((p.rows + kTile - 1) / kTile) * ntc;
+  const int64_t ntr = (p.rows + kTile - 1) / kTile;
+  const int64_t ntiles = ntr * ntc;
   const int64_t mine = blockIdx.x < ntiles ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
 
   if (threadIdx.x == 0) {
@@ -443,10 +458,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
           ok = false;
           break;
         }
-        const int64_t t = blockIdx.x + i * gridDim.x;
+        int64_t tr, tc;
+        stream_tile(blockIdx.x + i * gridDim.x, ntr, ntc, tr, tc);
         mbar_arrive_expect_tx(&full[st], kTileBytesBf16);
-        tma_load_2d(in + st * kTileBytesBf16, &tmX, &full[st],
-                    static_cast<int32_t>((t % ntc) * kTile), static_cast<int32_t>((t / ntc) * kTile));
+        tma_load_2d(in + st * kTileBytesBf16, &tmX, &full[st], static_cast<int32_t>(tc * kTile),
+                    static_cast<int32_t>(tr * kTile));
         ++fills[st];
       }
       if (!ok) {
@@ -483,8 +499,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     const int st = static_cast<int>(i % kStreamStages);
     const uint32_t ph = static_cast<uint32_t>((i / kStreamStages) & 1);
     const int o = static_cast<int>(i & 1);
-    const int64_t t = blockIdx.x + i * gridDim.x;
-    const int64_t r0 = (t / ntc) * kTile, c0 = (t % ntc) * kTile;
+    int64_t tr, tc;
+    stream_tile(blockIdx.x + i * gridDim.x, ntr, ntc, tr, tc);
+    const int64_t r0 = tr * kTile, c0 = tc * kTile;
     const bool ready = mbar_wait_bounded(&full[st], ph, &s_abort);
     // One decision for all consumers, whatever each one's wait returned.
     if (consumer_sync_or(!ready)) {
