@@ -51,7 +51,6 @@ cudaError_t run_small_m(const SmallMArgs& a, const DeviceInfo& dev, cudaStream_t
   p.b_inv = a.b_inv;
   p.b8 = a.b8;
   p.b8t = a.b8t;
-  p.a8t = a.a8t;
   p.a_amax = a.a_amax;
   p.a_scale = a.a_scale;
   p.a_inv = a.a_inv;
@@ -86,12 +85,17 @@ cudaError_t run_small_m(const SmallMArgs& a, const DeviceInfo& dev, cudaStream_t
   } else {
     ma = ma8;
   }
-  // dW [KA, NA] bf16 (kDW): 32-row x 64-column boxes, 128-byte rows, 128-byte swizzle.
-  CUtensorMap mdw = ma8;
-  if (kDW && !make_map_2d(&mdw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.dw, static_cast<uint64_t>(a.NA),
+  // The third map: dW [KA, NA] bf16 (kDW; 32-row x 64-column boxes, 128-byte
+  // rows, 128-byte swizzle) or W8^T [KA, NA] fp8 (kCastA; 128 x 128 boxes).
+  CUtensorMap mc = ma8;
+  if (kDW && !make_map_2d(&mc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.dw, static_cast<uint64_t>(a.NA),
                           static_cast<uint64_t>(a.KA), static_cast<uint64_t>(a.NA) * 2, 64, 32,
                           CU_TENSOR_MAP_SWIZZLE_128B))
     return map_failed("few-token product weight-gradient map");
+  if (kCastA && !make_map_2d(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.a8t, static_cast<uint64_t>(a.NA),
+                             static_cast<uint64_t>(a.KA), static_cast<uint64_t>(a.NA), kTile, kTile,
+                             CU_TENSOR_MAP_SWIZZLE_128B))
+    return map_failed("few-token product fp8 weight transpose map");
   const int64_t tiles = small_m_tiles(a.NA, a.KA);
   const int64_t grid = tiles < dev.num_sms ? tiles : dev.num_sms;
   set_error_site(kCastA ? "few-token fused product (weight cast) cooperative launch"
@@ -99,7 +103,7 @@ cudaError_t run_small_m(const SmallMArgs& a, const DeviceInfo& dev, cudaStream_t
                         : "few-token fused product cooperative launch");
   // Cooperative: the CTAs wait for one another (the amaxes), so all must be resident.
   return launch_kernel(small_m_kernel<kCastA, kFmtB, kMN, kDW>, dim3(static_cast<unsigned>(grid)),
-                       dim3(kSmThreads), kSmSmem, stream, 1, true, ma, ma8, mdw, p);
+                       dim3(kSmThreads), kSmSmem, stream, 1, true, ma, ma8, mc, p);
 }
 
 }  // namespace

@@ -80,7 +80,6 @@ struct SmallParams {
   float* b_inv;
   uint8_t* b8;                  // fp8 B [MB, KA] and B^T [KA, MB]
   uint8_t* b8t;
-  uint8_t* a8t;                 // kCastA: fp8 A^T [KA, NA] (the W8 copy goes out by TMA)
   float* a_amax;                // kCastA: A's state outputs
   float* a_scale;
   float* a_inv;
@@ -159,6 +158,35 @@ __device__ __forceinline__ void sm_tmem_load(uint32_t taddr, uint32_t (&r)[kMN])
   else
     tmem_load_16cols(taddr, r);
   tmem_load_wait();
+}
+
+// kCastA: the transpose of a cast 128 x 128 fp8 tile (128-byte swizzled, as
+// the tensor cores read it) into `dst` in the same layout, for one TMA store
+// of W8^T.  Each thread of the group takes a 16-row x 4-column block: four
+// 16-byte rows of the transpose.
+__device__ __forceinline__ void stage_transpose(const uint8_t* src, uint8_t* dst, int gtid) {
+  const int lw = gtid & 31, gw = gtid >> 5;
+  const int jg = (gw & 1) * 16 + (lw >> 1);  // 4-column group 0..31
+  const int ig = (gw >> 1) * 2 + (lw & 1);   // 16-row group 0..7
+  uint32_t w[16];
+#pragma unroll
+  for (int kk = 0; kk < 16; ++kk)
+    w[kk] = *reinterpret_cast<const uint32_t*>(src + sw128(ig * 16 + kk, jg * 4));
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const uint32_t x0 = __byte_perm(w[4 * g + 0], w[4 * g + 1], 0x5140);
+    const uint32_t x1 = __byte_perm(w[4 * g + 2], w[4 * g + 3], 0x5140);
+    const uint32_t x2 = __byte_perm(w[4 * g + 0], w[4 * g + 1], 0x7362);
+    const uint32_t x3 = __byte_perm(w[4 * g + 2], w[4 * g + 3], 0x7362);
+    w[4 * g + 0] = __byte_perm(x0, x1, 0x5410);
+    w[4 * g + 1] = __byte_perm(x0, x1, 0x7632);
+    w[4 * g + 2] = __byte_perm(x2, x3, 0x5410);
+    w[4 * g + 3] = __byte_perm(x2, x3, 0x7632);
+  }
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj)
+    *reinterpret_cast<uint4*>(dst + sw128(jg * 4 + jj, ig * 16)) =
+        make_uint4(w[jj], w[4 + jj], w[8 + jj], w[12 + jj]);
 }
 
 // kDW: the global operand bytes of one dW tile for this thread of its group
@@ -293,7 +321,7 @@ __device__ __forceinline__ bool dw_tiles(const SmallParams& p, const CUtensorMap
 template <bool kCastA, int kFmtB, int kMN, bool kDW>
 __global__ void __launch_bounds__(kSmThreads, 1)
     small_m_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA8,
-                   const __grid_constant__ CUtensorMap tmDW, const SmallParams p) {
+                   const __grid_constant__ CUtensorMap tmC, const SmallParams p) {
   static_assert(kMN == 16 || kMN == 32, "tokens per MMA");
   static_assert(!(kDW && kCastA), "dW is fused into the backward product only");
   constexpr int kTmemCols = kDW ? 512 : (kSmTilesPerCta * kMN <= 128 ? 128 : 256);
@@ -332,8 +360,8 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     if (kDW) {
       mbar_init(&dw_done[0], 1);
       mbar_init(&dw_done[1], 1);
-      tma_prefetch_map(&tmDW);
     }
+    if (kDW || kCastA) tma_prefetch_map(&tmC);
     fence_barrier_init();
     if (kCastA) tma_prefetch_map(&tmA);
     tma_prefetch_map(&tmA8);
@@ -562,35 +590,6 @@ __global__ void __launch_bounds__(kSmThreads, 1)
         }
       }
       if constexpr (kCastA) {
-        // W8^T: each thread a 16-row x 4-column block of the tile, four
-        // 16-byte rows of the transpose, straight to global memory.
-        const int lw = gtid & 31, gw = gtid >> 5;
-        const int jg = (gw & 1) * 16 + (lw >> 1);  // 4-column group 0..31
-        const int ig = (gw >> 1) * 2 + (lw & 1);   // 16-row group 0..7
-        if (r0 + ig * 16 < p.NA) {
-          uint32_t w[16];
-#pragma unroll
-          for (int kk = 0; kk < 16; ++kk)
-            w[kk] = *reinterpret_cast<const uint32_t*>(buf + sw128(ig * 16 + kk, jg * 4));
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const uint32_t x0 = __byte_perm(w[4 * g + 0], w[4 * g + 1], 0x5140);
-            const uint32_t x1 = __byte_perm(w[4 * g + 2], w[4 * g + 3], 0x5140);
-            const uint32_t x2 = __byte_perm(w[4 * g + 0], w[4 * g + 1], 0x7362);
-            const uint32_t x3 = __byte_perm(w[4 * g + 2], w[4 * g + 3], 0x7362);
-            w[4 * g + 0] = __byte_perm(x0, x1, 0x5410);
-            w[4 * g + 1] = __byte_perm(x0, x1, 0x7632);
-            w[4 * g + 2] = __byte_perm(x2, x3, 0x5410);
-            w[4 * g + 3] = __byte_perm(x2, x3, 0x7632);
-          }
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            const int col = c0 + jg * 4 + jj;
-            if (col < p.KA)
-              *reinterpret_cast<uint4*>(p.a8t + static_cast<int64_t>(col) * p.NA + r0 + ig * 16) =
-                  make_uint4(w[jj], w[4 + jj], w[8 + jj], w[12 + jj]);
-          }
-        }
         if (gtid == 0) {
           tma_store_2d(&tmA8, buf, c0, r0);  // W8 tile (clipped at the edges)
           bulk_commit_group();
@@ -663,11 +662,33 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     my_count = hi - lo;
     old_ticket = atom_add_release(&p.tickets[my_band], my_count);
   }
+  if constexpr (kCastA) {
+    // W8^T: each tile's transpose staged in the second half of its slot (the
+    // bf16 data and B's slice there are used up: the MMAs are done) and
+    // stored by TMA, while the tickets' atomics are in flight.  Stored from
+    // registers during the casts, these 16-byte rows took 3.7 us of them;
+    // staged before the partials, they held the partials back by 2.5 us.
+    if (ok) {
+      for (int k = group; k < mine; k += 2)
+        stage_transpose(tiles + k * kSmTileBytes, tiles + k * kSmTileBytes + kSmBSliceOffset,
+                        gtid);
+      fence_proxy_async_shared();
+      sm_group_sync(group);
+      if (gtid == 0) {
+        for (int k = group; k < mine; k += 2) {
+          const int t = t0 + k;
+          tma_store_2d(&tmC, tiles + k * kSmTileBytes + kSmBSliceOffset, (t / nks) * kTile,
+                       (t % nks) * kTile);  // W8^T [KA, NA] at (K slice, band)
+        }
+        bulk_commit_group();
+      }
+    }
+  }
   if constexpr (kDW) {
     // dW (the tile slots are free: the MMAs that read them are done)
     if (ok) {
       const float alpha_dw = __fmul_rn(inv_b, *p.x_inv);
-      const bool dw_ok = dw_tiles<kFmtB, kMN>(p, &tmDW, tiles, tmem, dw_done, t0, mine, nbands,
+      const bool dw_ok = dw_tiles<kFmtB, kMN>(p, &tmC, tiles, tmem, dw_done, t0, mine, nbands,
                                               s_b, alpha_dw, dwl);
       if (!dw_ok && gtid == 0) atomicCAS(p.err, 0, kErrGemmMmaWait);
     }
