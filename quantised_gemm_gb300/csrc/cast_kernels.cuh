@@ -27,7 +27,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kTile = 128;          // cast tile: 128 rows x 128 columns
 constexpr int kSqWords = 33;        // shared fp8 tile row pitch: 132 bytes
-constexpr int kAmaxRows = 32;       // amax tile: 32 rows x 256 columns
+constexpr int kAmaxRows = 64;       // amax tile: 64 rows x 256 columns
 constexpr int kSinglePassTilesPerCta = 7;
 
 template <int kFmt>
@@ -172,14 +172,14 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t* __restri
     const int64_t tr = t / ntc, tc = t - tr * ntc;
     const int64_t c = (tc << 5) + lane;
     if (c < cvec) {
-      uint4 v[4];
+      uint4 v[8];  // eight 16-byte loads in flight per thread
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 8; ++u) {
         const int64_t r = tr * kAmaxRows + warp + u * 8;
         v[u] = r < rows ? ld_stream_v4(x + r * ld + c * 8) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) acc = vec_absmax(acc, v[u]);
+      for (int u = 0; u < 8; ++u) acc = vec_absmax(acc, v[u]);
     }
   }
   griddep_launch_dependents();
