@@ -8,30 +8,34 @@
 // y, dY for dX).  With few tokens the products are short of work and long on
 // fixed costs: the step of a 16-token 4096 x 4096 Linear ran as six kernels
 // whose boundaries cost more than their bytes.  Here one kernel
-//   1. loads its A tiles (128 x 128) by TMA -- bf16 W when kCastA (the weight
-//      is cast in the same launch), else the fp8 copy; the CTA owning each
-//      128-column slice of B folds that slice's amax into a workspace word
-//      (unless the amax is given);
-//   2. kCastA: folds the amax of its W tiles, each as it lands, into the
-//      grid's; then every CTA passes a bounded grid barrier (cooperative
-//      launch: all CTAs are resident) that makes both amaxes complete -- for
-//      !kCastA the barrier counts only the slices of B;
+//   1. loads its A tiles (128 x 128) by TMA, each on its own mbarrier --
+//      bf16 W when kCastA (the weight is cast in the same launch), else the
+//      fp8 copy, which is loaded after the grid barrier when B's amax is
+//      taken here (ahead of the barrier, those loads held up the few bytes of
+//      B the barrier waits for); the CTA owning each 128-column slice of B
+//      takes that slice's amax (unless the amax is given) and keeps the
+//      slice in registers;
+//   2. kCastA: folds the amax of its W tiles, each as it lands; every CTA
+//      then passes a bounded grid barrier (cooperative launch: all CTAs are
+//      resident) that makes both amaxes complete -- for !kCastA the barrier
+//      counts only the slices of B -- and the slice owners write B's fp8 copy
+//      and its transpose (x8 / x8^T, dY8 / dY8^T) from those registers;
 //   3. per tile: casts the W tile (kCastA) into the 128-byte-swizzled K-major
-//      layout the tensor cores read, stores W8 (TMA) and W8^T (16-byte
-//      stores); casts B's slice of the tile's K range into the same layout
-//      beside it, and its group's thread issues the tile's tcgen05 MMAs
-//      (M = 128 rows of A, N = kMN tokens, K = 128) into the tile's own
-//      TMEM columns at once.  Tiles are numbered band-major (128 rows of A,
-//      then K), so the few consecutive tiles of a CTA fall in one or two
-//      bands;
-//   4. sums the accumulators of its tiles of each band in tile order, writes
-//      that fp32 partial of D^T to the workspace and adds its tile count to
-//      the band's ticket; the CTA that
-//      completes a band (all its K tiles counted) sums the band's partials in
-//      K order (deterministic), scales by alpha = fl32(inv_a * inv_b) and
-//      stores bf16 D, plus the amax of D when asked for.
-// B's fp8 copy and its transpose (x8 / x8^T, dY8 / dY8^T) are written by
-// the CTAs that own B's K slices.
+//      layout the tensor cores read and stores W8 by TMA; casts B's slice of
+//      the tile's K range into the same layout beside it, and its group's
+//      thread issues the tile's tcgen05 MMAs (M = 128 rows of A, N = kMN
+//      tokens, K = 128) into the tile's own TMEM columns at once.  Tiles are
+//      numbered band-major (128 rows of A, then K), so the few consecutive
+//      tiles of a CTA fall in one or two bands;
+//   4. once the MMAs are done, sums the accumulators of its tiles of each
+//      band in tile order and writes that fp32 partial of D^T to the
+//      workspace; one lane per band adds the CTA's tile count to the band's
+//      ticket with a release atomic.  While those are in flight, kCastA
+//      stages each tile's transpose in the second half of its slot and
+//      stores W8^T by TMA (kDW computes dW, below).  The CTA that completes a
+//      band (all its K tiles counted) sums the band's partials in K order
+//      (deterministic), scales by alpha = fl32(inv_a * inv_b) and stores
+//      bf16 D, plus the amax of D when asked for.
 //
 // kDW (the backward): the same launch also computes the weight gradient
 //   dW [KA, NA] = (dY8^T . x8) * inv_dy * inv_x          (bf16)
