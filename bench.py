@@ -739,18 +739,22 @@ def run_native(args):
         roofline["kernel_time"] = ("mean of %d launches, profiled pass of %d steps after the "
                                    "timed region" % (n_prof, n_prof))
     else:
-        gemm_flop = 2.0 * M * N * K          # each of the three GEMMs of this square Linear
-        gemm_avg = sum(gemm_each) / len(gemm_each)
-        achieved = gemm_flop / (gemm_avg * 1e-3) / 1e12
+        # y, dX and dW (2MNK each) over the step's GEMM launches: three, or
+        # two when the backward runs dX and dW in one grouped launch.
+        gemm_flop = 3 * 2.0 * M * N * K
+        achieved = gemm_flop / (sum(gemm_each) * 1e-3) / 1e12
+        grouped = len(gemm_each) == 2
         tr = load_traffic("gemm", args.workload)
         roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1),
                     "unit": "TFLOP/s", "frac": round(achieved / peak, 3),
                     "traffic": tr["bytes_per_launch"] if tr else None,
-                    "kernel": q.gemm_describe(M, N, K).split(":")[0],
+                    "kernel": q.gemm_describe(M, N, K).split(":")[0] +
+                              ("; dX + dW: gemm_fp8_pair2_kernel<256, 6>" if grouped else ""),
                     "peak_basis": basis + " (of measured)" if peaks["source"] == "measured" else
                     basis + " (of fallback)",
-                    "kernel_time": "mean of %d launches, profiled pass of %d steps after the "
-                                   "timed region" % (len(gemm_each) * n_prof, n_prof)}
+                    "kernel_time": "the step's GEMM flops over the summed time of its %d GEMM "
+                                   "launches, profiled pass of %d steps after the timed region"
+                                   % (len(gemm_each), n_prof)}
     # Casts of the step: x [M,K], W [N,K], dY [M,N], each 2 B read + 1 B + 1 B
     # (transposed) written per element.  Tensors that fit on chip run as the
     # single-pass kernel (kind "cast_fused", amax included); the others as
@@ -785,7 +789,8 @@ def run_native(args):
         stage_frac = stage_bytes / (stage_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]
         stage = {"us": round(stage_ms * 1e3, 1), "frac": round(stage_frac, 3),
                  "of_two_pass_ceiling": round(stage_frac / (4.0 / 6.0), 3)}
-    kernel_us = {k: round(v * 1e3, 1) for k, v in zip(("y", "dx", "dw"), gemm_each)}
+    labels = ("y", "dx", "dw") if len(gemm_each) == 3 else ("y", "dx_dw")
+    kernel_us = {k: round(v * 1e3, 1) for k, v in zip(labels, gemm_each)}
     kernel_us.update({"cast": round(cast_ms * 1e3, 1), "cast_fused": round(fused_ms * 1e3, 1),
                       "amax": round(amax_ms * 1e3, 1), "scale": round(scale_ms * 1e3, 1)})
 

@@ -295,6 +295,22 @@ fp8lin_status fp8lin_gemm_describe(int64_t M, int64_t N, int64_t K, char* buf, s
 fp8lin_status fp8lin_gemm_describe_for(int64_t M, int64_t N, int64_t K, int32_t num_sms,
                                        char* buf, size_t buf_len);
 
+/* How fp8lin_backward would run its two GEMMs (dX: Ma x Na x Ka, dW:
+ * Mb x Nb x Kb) on a device of num_sms SMs, computed on the host: "grouped"
+ * when both take 256-wide CTA-pair tiles and one launch that deals the tiles
+ * of both by their K loops is expected to take at most 0.92 of the time of
+ * two, else "separate"; then the tile counts (problem 0: the longer K loop),
+ * K blocks, the deal's parameter d, the estimated K blocks of the busiest
+ * CTA pair both ways, and "DEAL BROKEN" if the deal would not hand out every
+ * tile exactly once (a self-check of the same function the kernel deals
+ * with).  This is the plan's decision; FP8LIN_GROUP in the environment
+ * overrides it in fp8lin_backward (0: never group, 2: group whenever both
+ * qualify).  Returns FP8LIN_EINVAL for sizes < 1, num_sms < 2 or a NULL /
+ * empty buffer. */
+fp8lin_status fp8lin_gemm_group_describe_for(int64_t Ma, int64_t Na, int64_t Ka, int64_t Mb,
+                                             int64_t Nb, int64_t Kb, int32_t num_sms, char* buf,
+                                             size_t buf_len);
+
 /* Forward of the Linear -- the forward half of the "forward+backward" of one
  * Linear timed in "Integrate float8nocompile, an experimental feature for
  * high performance" (torchtitan PR 778), "Benchmarking single linear layer
@@ -341,7 +357,14 @@ fp8lin_status fp8lin_forward(const void* x, const void* w, int64_t M, int64_t K,
  * (as in fp8lin_forward), and dW in the same launch when dw is not NULL and
  * dw_amax is NULL (dW equals the GEMM's value for value; an exact zero may
  * differ in sign).  Otherwise dW follows as its own GEMM; so it does with
- * FP8LIN_SMALL_M_DW=0 in the environment. */
+ * FP8LIN_SMALL_M_DW=0 in the environment.
+ * When dX and dW both run on the 256-wide pair tiles, at most one of dx_amax
+ * and dw_amax is given, and the host plan expects one launch over both GEMMs'
+ * tiles to take at most 0.92 of the time of two (fp8lin_gemm_group_describe_for
+ * prints the decision), they run as one launch; it computes every tile whole,
+ * as the separate GEMM does where it splits no K loop.  FP8LIN_GROUP=0 in the
+ * environment never groups them, FP8LIN_GROUP=2 groups them whenever they
+ * qualify. */
 fp8lin_status fp8lin_backward(const void* dy, int64_t M, int64_t K, int64_t N,
                               const uint8_t* x8t, const uint8_t* w8t,
                               const fp8lin_scaling_state* sx, const fp8lin_scaling_state* sw,

@@ -93,6 +93,17 @@ def gemm_describe(M: int, N: int, K: int) -> str:
     return buf.value.decode()
 
 
+def gemm_group_describe_for(dx_mnk, dw_mnk, num_sms: int) -> str:
+    """How backward() would run its two GEMMs (dX and dW, each an (M, N, K)
+    as the GEMM sees it) on a device of num_sms SMs, computed on the host:
+    "grouped" (one launch dealing the tiles of both by their K loops) or
+    "separate", with the plan's figures.  No GPU needed."""
+    buf = ctypes.create_string_buffer(256)
+    _lib.check(library().fp8lin_gemm_group_describe_for(*dx_mnk, *dw_mnk, num_sms, buf, len(buf)),
+               "fp8lin_gemm_group_describe_for")
+    return buf.value.decode()
+
+
 def gemm_describe_for(M: int, N: int, K: int, num_sms: int) -> str:
     """gemm_describe() for a device of num_sms SMs holding one GEMM CTA per
     SM, computed on the host: no GPU needed."""

@@ -87,6 +87,8 @@ _SIGNATURES = {
     "fp8lin_gemm_describe": (ctypes.c_int, [_I64, _I64, _I64, ctypes.c_char_p, _SZ]),
     "fp8lin_gemm_describe_for": (ctypes.c_int,
                                  [_I64, _I64, _I64, ctypes.c_int32, ctypes.c_char_p, _SZ]),
+    "fp8lin_gemm_group_describe_for": (ctypes.c_int, [_I64, _I64, _I64, _I64, _I64, _I64,
+                                                      ctypes.c_int32, ctypes.c_char_p, _SZ]),
     "fp8lin_forward": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _ST, _ST, _P, _P, _P, _P, _P,
                                       _P, _P, _SZ, _P]),
     "fp8lin_backward": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _ST, _ST, _ST, _P, _P,

@@ -260,20 +260,10 @@ fp8lin_status delayed_cast(const void* x, int64_t rows, int64_t cols, int64_t ld
   return do_cast(c, dev, stream);
 }
 
-fp8lin_status do_gemm(const uint8_t* a, const uint8_t* b, int64_t M, int64_t N, int64_t K,
-                      int64_t lda, int64_t ldb, int32_t fa, int32_t fb, const float* inv_a,
-                      const float* inv_b, void* d, int64_t ldd, float* d_amax, void* ws,
-                      size_t ws_bytes, const DeviceInfo& dev, cudaStream_t stream) {
-  if (M == 0 || N == 0 || K == 0) {
-    // Nothing to multiply: D (if any) is zeros, and so is its amax.
-    cudaError_t e = cudaSuccess;
-    if (M > 0 && N > 0)
-      e = cudaMemset2DAsync(d, static_cast<size_t>(ldd) * 2, 0, static_cast<size_t>(N) * 2,
-                            static_cast<size_t>(M), stream);
-    if (e == cudaSuccess && d_amax != nullptr)
-      e = cudaMemsetAsync(d_amax, 0, sizeof(float), stream);
-    return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);
-  }
+GemmArgs gemm_args(const uint8_t* a, const uint8_t* b, int64_t M, int64_t N, int64_t K,
+                   int64_t lda, int64_t ldb, int32_t fa, int32_t fb, const float* inv_a,
+                   const float* inv_b, void* d, int64_t ldd, float* d_amax, void* ws,
+                   size_t ws_bytes) {
   GemmArgs g;
   g.a = a;
   g.b = b;
@@ -301,6 +291,25 @@ fp8lin_status do_gemm(const uint8_t* a, const uint8_t* b, int64_t M, int64_t N, 
     g.ws_split = nullptr;
     g.ws_split_bytes = 0;
   }
+  return g;
+}
+
+fp8lin_status do_gemm(const uint8_t* a, const uint8_t* b, int64_t M, int64_t N, int64_t K,
+                      int64_t lda, int64_t ldb, int32_t fa, int32_t fb, const float* inv_a,
+                      const float* inv_b, void* d, int64_t ldd, float* d_amax, void* ws,
+                      size_t ws_bytes, const DeviceInfo& dev, cudaStream_t stream) {
+  if (M == 0 || N == 0 || K == 0) {
+    // Nothing to multiply: D (if any) is zeros, and so is its amax.
+    cudaError_t e = cudaSuccess;
+    if (M > 0 && N > 0)
+      e = cudaMemset2DAsync(d, static_cast<size_t>(ldd) * 2, 0, static_cast<size_t>(N) * 2,
+                            static_cast<size_t>(M), stream);
+    if (e == cudaSuccess && d_amax != nullptr)
+      e = cudaMemsetAsync(d_amax, 0, sizeof(float), stream);
+    return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);
+  }
+  const GemmArgs g = gemm_args(a, b, M, N, K, lda, ldb, fa, fb, inv_a, inv_b, d, ldd, d_amax, ws,
+                               ws_bytes);
   ProfScope ps(FP8LIN_PROF_GEMM, stream);
   cudaError_t e = launch_gemm(g, dev, stream);
   return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);
@@ -590,6 +599,16 @@ fp8lin_status fp8lin_gemm_describe_for(int64_t M, int64_t N, int64_t K, int32_t 
   return FP8LIN_OK;
 }
 
+fp8lin_status fp8lin_gemm_group_describe_for(int64_t Ma, int64_t Na, int64_t Ka, int64_t Mb,
+                                             int64_t Nb, int64_t Kb, int32_t num_sms, char* buf,
+                                             size_t buf_len) {
+  if (Ma < 1 || Na < 1 || Ka < 1 || Mb < 1 || Nb < 1 || Kb < 1 || num_sms < 2 || buf == nullptr ||
+      buf_len == 0)
+    return FP8LIN_EINVAL;
+  describe_group_plan(Ma, Na, Ka, Mb, Nb, Kb, num_sms, num_sms / 2, buf, buf_len);
+  return FP8LIN_OK;
+}
+
 static fp8lin_status check_linear_sizes(int64_t M, int64_t K, int64_t N) {
   if (M < 0 || K < 0 || N < 0) return FP8LIN_EINVAL;
   if (M % 16 != 0 || K % 16 != 0 || N % 16 != 0) return FP8LIN_EUNSUPPORTED;
@@ -803,6 +822,22 @@ fp8lin_status run_backward(const void* dy, int64_t M, int64_t K, int64_t N, cons
     s = delayed_cast(dy, M, N, N, sdy, dy8, dy8t, ws, dev, stream);
   }
   if (!dx_done && s != FP8LIN_OK) return s;
+  if (dx != nullptr && !dx_done && dw != nullptr && !dw_done && M > 0 && N > 0 && K > 0) {
+    // dX and dW in one launch when the grouped plan expects it to be faster
+    const GemmArgs gx = gemm_args(dy8, w8t, M, K, N, N, N, FP8LIN_E5M2, FP8LIN_E4M3,
+                                  sdy->inv_scale, sw->inv_scale, dx, K, dx_amax, ws, ws_bytes);
+    const GemmArgs gw = gemm_args(dy8t, x8t, N, K, M, M, M, FP8LIN_E5M2, FP8LIN_E4M3,
+                                  sdy->inv_scale, sx->inv_scale, dw, K, dw_amax, ws, ws_bytes);
+    bool grouped = false;
+    cudaError_t e = plan_gemm_pair2(gx, gw, dev, &grouped);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (grouped) {
+      ProfScope ps(FP8LIN_PROF_GEMM, stream);
+      e = launch_gemm_pair2(gx, gw, dev, stream);
+      if (e != cudaSuccess) return cuda_fail(e);
+      dx_done = dw_done = true;
+    }
+  }
   if (dx != nullptr && !dx_done) {
     // dX = dY8 . W8 : A = dY8 [M, N], B = W8^T [K, N], contract over N
     s = do_gemm(dy8, w8t, M, K, N, N, N, FP8LIN_E5M2, FP8LIN_E4M3, sdy->inv_scale, sw->inv_scale,

@@ -98,6 +98,7 @@ enum Role : int {
 
 struct Unit {
   int tile, split, nsplit, kb0, kb1, role;
+  int prob;  // which GEMM of a two-GEMM launch (0 otherwise)
 };
 
 // The n-th work unit of persistent slot `slot` (a CTA, or a CTA pair) out of
@@ -107,6 +108,7 @@ __device__ __forceinline__ bool unit_at(int slot, int slots, int n, const GemmPa
                                         int num_tiles, int num_kb, Unit& u) {
   const int ui = slot + n * slots;
   if (ui >= p.t_full + (num_tiles - p.t_full) * p.s_tail) return false;
+  u.prob = 0;
   if (ui < p.t_full) {
     u.tile = ui;
     u.split = 0;
@@ -125,6 +127,57 @@ __device__ __forceinline__ bool unit_at(int slot, int slots, int n, const GemmPa
     u.role = kSlice;
   }
   return true;
+}
+
+// Two GEMMs in one launch of the pair kernel, whole tiles only.  Problem 0
+// is the one with the longer K loop (cost c0 K blocks a tile, tiles0 tiles),
+// problem 1 the other (c1, tiles1).  Problem 0's tiles are dealt round-robin:
+// pair p gets L_p = tiles0 / slots (+1 for the first tiles0 % slots pairs, the
+// heavy ones).  Each light pair then gets up to `d` of problem 1's tiles
+// first (tiles [0, E), E = min(tiles1, light pairs * d), round-robin over the
+// light pairs), and the rest of problem 1's tiles go round-robin over all
+// pairs, light pairs first.  The host picks d so that the busiest pair's
+// K blocks are fewest (d = 0 is plain round-robin).  The same function deals
+// the units on the device and checks the deal on the host.
+struct GroupSched {
+  int tiles0, tiles1, d;
+};
+
+__host__ __device__ inline bool unit_at_grouped(int p, int slots, int n, const GroupSched& gs,
+                                                int num_kb0, int num_kb1, Unit& u) {
+  const int ll = gs.tiles0 / slots, heavy = gs.tiles0 % slots, light = slots - heavy;
+  const int e = gs.tiles1 < light * gs.d ? gs.tiles1 : light * gs.d;
+  const int r = gs.tiles1 - e;
+  u.split = 0;
+  u.nsplit = 1;
+  u.kb0 = 0;
+  u.role = kWhole;
+  const int lp = ll + (p < heavy ? 1 : 0);
+  if (n < lp) {
+    u.prob = 0;
+    u.tile = p + n * slots;
+    u.kb1 = num_kb0;
+    return true;
+  }
+  int m = n - lp;
+  u.prob = 1;
+  u.kb1 = num_kb1;
+  if (p >= heavy) {
+    const int q = p - heavy;
+    const int ep = e > q ? (e - q + light - 1) / light : 0;
+    if (m < ep) {
+      u.tile = q + light * m;
+      return true;
+    }
+    m -= ep;
+  }
+  const int pos = p >= heavy ? p - heavy : light + p;
+  const int rp = r > pos ? (r - pos + slots - 1) / slots : 0;
+  if (m < rp) {
+    u.tile = e + pos + slots * m;
+    return true;
+  }
+  return false;
 }
 
 __device__ __forceinline__ void record_error(int* err, volatile int* abort_flag, int code) {
@@ -702,11 +755,14 @@ struct PairCfg {
   static_assert(kBBytes % 1024 == 0, "B tiles keep 1024-byte alignment");
 };
 
-template <int BN, int STAGES>
-__global__ void __launch_bounds__(kGemmThreads, 1)
-    gemm_fp8_pair_kernel(const __grid_constant__ CUtensorMap tmA,
-                         const __grid_constant__ CUtensorMap tmB,
-                         const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
+// The pair kernel's body; kGrouped runs two GEMMs in one launch (problem 1:
+// tmA1 / tmB1 / tmD1 / p1, dealt with problem 0's tiles by unit_at_grouped).
+template <int BN, int STAGES, bool kGrouped>
+__device__ __forceinline__ void pair_gemm_body(const CUtensorMap* tmA0, const CUtensorMap* tmB0,
+                                               const CUtensorMap* tmD0, const GemmParams& p,
+                                               const CUtensorMap* tmA1, const CUtensorMap* tmB1,
+                                               const CUtensorMap* tmD1, const GemmParams& p1,
+                                               const GroupSched& gs) {
   using C = PairCfg<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -737,6 +793,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int num_n = (p.N + BN - 1) / BN;
   const int num_tiles = ((p.M + 2 * kBM - 1) / (2 * kBM)) * num_n;
   const int num_kb = (p.K + kBK - 1) / kBK;
+  const int num_n1 = kGrouped ? (p1.N + BN - 1) / BN : num_n;
+  const int num_kb1 = kGrouped ? (p1.K + kBK - 1) / kBK : num_kb;
+  auto next_unit = [&](int n, Unit& u) -> bool {
+    if constexpr (kGrouped)
+      return unit_at_grouped(pair, num_pairs, n, gs, num_kb, num_kb1, u);
+    else
+      return unit_at(pair, num_pairs, n, p, num_tiles, num_kb, u);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -752,9 +816,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     *peer_abort = 0;
     for (int s = 0; s < STAGES; ++s) peer_fills[s] = own_fills[s] = 0;
     fence_barrier_init();
-    tma_prefetch_map(&tmA);
-    tma_prefetch_map(&tmB);
-    tma_prefetch_map(&tmD);
+    tma_prefetch_map(tmA0);
+    tma_prefetch_map(tmB0);
+    tma_prefetch_map(tmD0);
+    if (kGrouped) {
+      tma_prefetch_map(tmA1);
+      tma_prefetch_map(tmB1);
+      tma_prefetch_map(tmD1);
+    }
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, C::kTmemCols);
@@ -777,8 +846,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       Unit u;
-      for (int n = 0; ok && unit_at(pair, num_pairs, n, p, num_tiles, num_kb, u); ++n) {
-        const int m_blk = u.tile / num_n, n_blk = u.tile % num_n;
+      for (int n = 0; ok && next_unit(n, u); ++n) {
+        const bool second = kGrouped && u.prob != 0;
+        const int nn = second ? num_n1 : num_n;
+        const int m_blk = u.tile / nn, n_blk = u.tile % nn;
+        const CUtensorMap* tmA = second ? tmA1 : tmA0;
+        const CUtensorMap* tmB = second ? tmB1 : tmB0;
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
@@ -786,9 +859,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           const uint32_t full_even = map_to_cta(smem_addr(&full[stage]), 0);
           if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * C::kStageBytes);
-          tma_load_2d_pair(sA + stage * C::kABytes, &tmA, full_even, kb * kBK,
+          tma_load_2d_pair(sA + stage * C::kABytes, tmA, full_even, kb * kBK,
                            m_blk * 2 * kBM + static_cast<int>(rank) * kBM);
-          tma_load_2d_pair(sB + stage * C::kBBytes, &tmB, full_even, kb * kBK,
+          tma_load_2d_pair(sB + stage * C::kBBytes, tmB, full_even, kb * kBK,
                            n_blk * BN + static_cast<int>(rank) * (BN / 2));
 #pragma unroll
           for (int s = 0; s < STAGES; ++s)
@@ -821,7 +894,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool ok = true;
       bool issued = false;
       Unit u;
-      for (int n = 0; ok && unit_at(pair, num_pairs, n, p, num_tiles, num_kb, u); ++n) {
+      for (int n = 0; ok && next_unit(n, u); ++n) {
+        const uint32_t idesc = (kGrouped && u.prob != 0) ? p1.idesc : p.idesc;
         if (!mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
@@ -839,7 +913,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
           for (int k = 0; k < kBK / kMmaK; ++k) {
             mma_f8f6f4_pair(d_tmem, a_desc + static_cast<uint64_t>(k * (kMmaK >> 4)),
-                            b_desc + static_cast<uint64_t>(k * (kMmaK >> 4)), p.idesc,
+                            b_desc + static_cast<uint64_t>(k * (kMmaK >> 4)), idesc,
                             (kb > u.kb0 || k > 0) ? 1u : 0u);
           }
           issued = true;
@@ -870,16 +944,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     using E = EpiSplit<BN>;
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
-    const float alpha = __fmul_rn(*p.inv_a, *p.inv_b);
+    const float alpha0 = __fmul_rn(*p.inv_a, *p.inv_b);
+    const float alpha1 = kGrouped ? __fmul_rn(*p1.inv_a, *p1.inv_b) : alpha0;
     const uint32_t acc_empty_even0 = map_to_cta(smem_addr(&acc_empty[0]), 0);
     uint8_t* boxes = sEpi + (warp - 2) * kBoxesPerWarp * kBoxBytes;
     uint32_t box_no = 0;
-    float vmax = 0.0f;
+    float vmax0 = 0.0f, vmax1 = 0.0f;
     int acc = 0;
     uint32_t acc_phase = 0;
     Unit u;
-    for (int n = 0; unit_at(pair, num_pairs, n, p, num_tiles, num_kb, u); ++n) {
-      const int m_blk = u.tile / num_n, n_blk = u.tile % num_n;
+    for (int n = 0; next_unit(n, u); ++n) {
+      const bool second = kGrouped && u.prob != 0;
+      const GemmParams& pu = second ? p1 : p;
+      const int nn = second ? num_n1 : num_n;
+      const int m_blk = u.tile / nn, n_blk = u.tile % nn;
       const bool ready = __all_sync(
           0xFFFFFFFFu, mbar_wait_bounded(&acc_full[acc], acc_phase, abort_flag));
       if (!ready) {
@@ -891,9 +969,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                              static_cast<uint32_t>(acc * BN + half * E::kCols);
       const int row_group = static_cast<int>(rank) * 4 + quarter;
       const uint32_t release_addr = acc_empty_even0 + static_cast<uint32_t>(acc * 8);
-      epilogue_unit<E::kCols, false>(p, u, 8 * E::kHalves, half * 8 + row_group,
+      epilogue_unit<E::kCols, false>(pu, u, 8 * E::kHalves, half * 8 + row_group,
                                      m_blk * 2 * kBM + row_group * 32, n_blk * BN + half * E::kCols,
-                                     t_row, alpha, &tmD, boxes, box_no, lane, abort_flag, vmax,
+                                     t_row, second ? alpha1 : alpha0, second ? tmD1 : tmD0, boxes,
+                                     box_no, lane, abort_flag, second ? vmax1 : vmax0,
                                      [&] {
                                        tc_fence_before_sync();
                                        __syncwarp();
@@ -904,7 +983,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         acc_phase ^= 1u;
       }
     }
-    publish_amax(p, vmax, lane);
+    publish_amax(p, vmax0, lane);
+    if (kGrouped) publish_amax(p1, vmax1, lane);  // (at most one of the two asks for it)
     if (lane == 0) bulk_wait_group<0>();  // stores done before the staging memory goes away
   }
 
@@ -943,6 +1023,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after_sync();
     tmem_dealloc_pair(tmem_base, C::kTmemCols);
   }
+}
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_fp8_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                         const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmD,
+                         const __grid_constant__ GemmParams p) {
+  pair_gemm_body<BN, STAGES, false>(&tmA, &tmB, &tmD, p, &tmA, &tmB, &tmD, p, GroupSched{0, 0, 0});
+}
+
+// Two GEMMs of the same tile shape in one launch (see unit_at_grouped).
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_fp8_pair2_kernel(const __grid_constant__ CUtensorMap tmA0,
+                          const __grid_constant__ CUtensorMap tmB0,
+                          const __grid_constant__ CUtensorMap tmD0,
+                          const __grid_constant__ GemmParams p0,
+                          const __grid_constant__ CUtensorMap tmA1,
+                          const __grid_constant__ CUtensorMap tmB1,
+                          const __grid_constant__ CUtensorMap tmD1,
+                          const __grid_constant__ GemmParams p1,
+                          const __grid_constant__ GroupSched gs) {
+  pair_gemm_body<BN, STAGES, true>(&tmA0, &tmB0, &tmD0, p0, &tmA1, &tmB1, &tmD1, p1, gs);
 }
 
 }  // namespace

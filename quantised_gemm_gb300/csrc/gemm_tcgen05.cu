@@ -9,6 +9,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <mutex>
+#include <vector>
 
 #include "gemm_kernels.cuh"
 
@@ -270,6 +271,97 @@ cudaError_t run_pair(const uint8_t* a, int64_t lda, const uint8_t* b, int64_t ld
                        ma, mb, md, p);
 }
 
+template <int BN, int STAGES>
+cudaError_t pair2_setup(const DeviceInfo& dev) {
+  static std::mutex mu;
+  static bool done[kMaxDevices] = {};
+  if (dev.device < 0 || dev.device >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev.device]) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(gemm_fp8_pair2_kernel<BN, STAGES>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(PairCfg<BN, STAGES>::kSmemBytes));
+  if (e == cudaSuccess) done[dev.device] = true;
+  return e;
+}
+
+// Estimated time of a pair-kernel GEMM alone, in K blocks of its busiest
+// pair (a split tail tile's slices add kSplitExtraKb for their partials,
+// measured at about 4 us beyond a whole tile's epilogue).
+constexpr int kSplitExtraKb = 13;
+constexpr int kLaunchExtraKb = 9;  // a launch boundary, about 3 us
+// Grouping is chosen only when the estimate gains at least this share.  In a
+// graphed step the second of two launches overlaps its prologue with the
+// first's drain, so small estimated gains were measured as none (a 4096-token
+// Linear of 4096 x 4096, 0.976 of the separate estimate: no faster) or as a
+// loss (the 8192 x 4096 x 14336 FFN projections, 0.994: 1% slower), while
+// 0.88 and below gained 3 to 11% of the whole step.
+constexpr int kGroupMinGainPct = 8;
+
+int alone_kb(int tiles, int num_kb, int slots, size_t split_bytes) {
+  const SplitPlan sp = plan_split(tiles, slots, num_kb, 2 * kBM, 256, split_bytes);
+  if (sp.ways == 1) return (tiles + slots - 1) / slots * num_kb;
+  const int per = (num_kb + sp.ways - 1) / sp.ways;
+  return sp.t_full / slots * num_kb + per + kSplitExtraKb;
+}
+
+// K blocks of the busiest pair under unit_at_grouped's deal with this d
+// (the counts unit_at_grouped deals to each pair, in closed form).
+int grouped_kb(const GroupSched& gs, int kb0, int kb1, int slots) {
+  const int ll = gs.tiles0 / slots, heavy = gs.tiles0 % slots, light = slots - heavy;
+  const int e = gs.tiles1 < light * gs.d ? gs.tiles1 : light * gs.d;
+  const int r = gs.tiles1 - e;
+  int worst = 0;
+  for (int p = 0; p < slots; ++p) {
+    const int q = p - heavy;
+    const int ep = p >= heavy && e > q ? (e - q + light - 1) / light : 0;
+    const int pos = p >= heavy ? q : light + p;
+    const int rp = r > pos ? (r - pos + slots - 1) / slots : 0;
+    const int load = (ll + (p < heavy ? 1 : 0)) * kb0 + (ep + rp) * kb1;
+    if (load > worst) worst = load;
+  }
+  return worst;
+}
+
+// The grouped plan for two pair-kernel GEMMs (problem 0: the longer K loop):
+// the d with the least busiest pair, and whether it beats two launches.
+struct GroupPlan {
+  bool use;
+  GroupSched gs;
+  int grouped, alone;  // estimated K blocks of the busiest pair
+};
+
+GroupPlan plan_group(int tiles0, int kb0, int tiles1, int kb1, int slots, size_t split_bytes) {
+  GroupPlan g = {false, {tiles0, tiles1, 0}, 0, 0};
+  g.alone = alone_kb(tiles0, kb0, slots, split_bytes) + alone_kb(tiles1, kb1, slots, split_bytes) +
+            kLaunchExtraKb;
+  const int dmax = kb1 > 0 ? kb0 / kb1 + 2 : 0;
+  g.grouped = 1 << 30;
+  for (int d = 0; d <= dmax; ++d) {
+    const GroupSched gs = {tiles0, tiles1, d};
+    const int kb = grouped_kb(gs, kb0, kb1, slots);
+    if (kb < g.grouped) {
+      g.grouped = kb;
+      g.gs = gs;
+    }
+  }
+  g.use = static_cast<int64_t>(g.grouped) * 100 <
+          static_cast<int64_t>(g.alone) * (100 - kGroupMinGainPct);
+  return g;
+}
+
+// FP8LIN_GROUP: 0 never runs two GEMMs in one launch, 2 always when they
+// qualify, anything else when the plan expects it to be faster.
+int group_mode() {
+  static const int mode = [] {
+    const char* v = std::getenv("FP8LIN_GROUP");
+    if (v != nullptr && v[0] == '0') return 0;
+    if (v != nullptr && v[0] == '2') return 2;
+    return 1;
+  }();
+  return mode;
+}
+
 }  // namespace
 
 cudaError_t map_failed(const char* what) {
@@ -315,6 +407,30 @@ Variant choose_variant(int64_t M, int64_t N) {
 
 bool is_swap(Variant v) {
   return v == Variant::kSwap16 || v == Variant::kSwap32 || v == Variant::kSwap64;
+}
+
+}  // namespace
+
+namespace {
+
+GemmParams base_params(const GemmArgs& g) {
+  GemmParams p;
+  p.inv_a = g.inv_a;
+  p.inv_b = g.inv_b;
+  p.d = static_cast<uint16_t*>(g.d);
+  p.ldd = g.ldd;
+  p.err = g.ws_error;
+  p.K = static_cast<int>(g.K);
+  p.M = static_cast<int>(g.M);
+  p.N = static_cast<int>(g.N);
+  p.amax_out = g.d_amax;
+  p.amax_acc = g.ws_amax_acc;
+  p.amax_ticket = g.ws_amax_ticket;
+  p.t_full = 0;
+  p.s_tail = 1;
+  p.partials = nullptr;
+  p.tickets = nullptr;
+  return p;
 }
 
 }  // namespace
@@ -418,6 +534,123 @@ cudaError_t describe_gemm(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev
   if (e != cudaSuccess) return e;
   describe_plan(M, N, K, dev.num_sms, pair_slots, buf, len);
   return cudaSuccess;
+}
+
+static bool group_qualifies(const GemmArgs& g0, const GemmArgs& g1) {
+  return choose_variant(g0.M, g0.N) == Variant::kPair256 &&
+         choose_variant(g1.M, g1.N) == Variant::kPair256 &&
+         (g0.d_amax == nullptr || g1.d_amax == nullptr) && g0.K > 0 && g1.K > 0;
+}
+
+namespace {
+
+// The grouped plan for two qualifying GEMMs: problem 0 the one with the
+// longer K loop (*swap: b), its tiles and the deal.
+struct Pair2 {
+  bool use, swap;
+  int tiles0, tiles1, max_pairs;
+  GroupSched gs;
+};
+
+cudaError_t pair2_plan(const GemmArgs& ga, const GemmArgs& gb, const DeviceInfo& dev, Pair2* out) {
+  out->use = false;
+  if (group_mode() == 0 || !group_qualifies(ga, gb)) return cudaSuccess;
+  int max_pairs = 0;
+  cudaError_t e = pair_setup<256, 6>(dev, &max_pairs);
+  if (e != cudaSuccess) return e;
+  out->swap = (gb.K + kBK - 1) / kBK > (ga.K + kBK - 1) / kBK;
+  const GemmArgs& g0 = out->swap ? gb : ga;
+  const GemmArgs& g1 = out->swap ? ga : gb;
+  out->tiles0 = static_cast<int>(((g0.M + 2 * kBM - 1) / (2 * kBM)) * ((g0.N + 255) / 256));
+  out->tiles1 = static_cast<int>(((g1.M + 2 * kBM - 1) / (2 * kBM)) * ((g1.N + 255) / 256));
+  out->max_pairs = max_pairs;
+  const int kb0 = static_cast<int>((g0.K + kBK - 1) / kBK);
+  const int kb1 = static_cast<int>((g1.K + kBK - 1) / kBK);
+  const size_t split = g0.ws_split != nullptr && g0.ws_tickets != nullptr ? g0.ws_split_bytes : 0;
+  const GroupPlan plan = plan_group(out->tiles0, kb0, out->tiles1, kb1, max_pairs, split);
+  out->gs = plan.gs;
+  out->use = plan.use || group_mode() == 2;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t plan_gemm_pair2(const GemmArgs& a, const GemmArgs& b, const DeviceInfo& dev,
+                            bool* use) {
+  Pair2 pl;
+  cudaError_t e = pair2_plan(a, b, dev, &pl);
+  *use = pl.use;
+  return e;
+}
+
+cudaError_t launch_gemm_pair2(const GemmArgs& ga, const GemmArgs& gb, const DeviceInfo& dev,
+                              cudaStream_t stream) {
+  Pair2 pl;
+  cudaError_t e = pair2_plan(ga, gb, dev, &pl);
+  if (e != cudaSuccess) return e;
+  if (!pl.use) return cudaErrorInvalidValue;
+  if ((e = pair2_setup<256, 6>(dev)) != cudaSuccess) return e;
+  const GemmArgs& g0 = pl.swap ? gb : ga;
+  const GemmArgs& g1 = pl.swap ? ga : gb;
+  GemmParams p0 = base_params(g0), p1 = base_params(g1);
+  p0.t_full = pl.tiles0;
+  p1.t_full = pl.tiles1;
+  p0.idesc = make_idesc_f8(g0.fmt_a, g0.fmt_b, 2 * kBM, 256);
+  p1.idesc = make_idesc_f8(g1.fmt_a, g1.fmt_b, 2 * kBM, 256);
+  CUtensorMap ma0, mb0, md0, ma1, mb1, md1;
+  if (!make_map_k_major(&ma0, g0.a, p0.M, p0.K, g0.lda, kBM) ||
+      !make_map_k_major(&ma1, g1.a, p1.M, p1.K, g1.lda, kBM))
+    return map_failed("grouped pair GEMM operand A map");
+  if (!make_map_k_major(&mb0, g0.b, p0.N, p0.K, g0.ldb, 128) ||
+      !make_map_k_major(&mb1, g1.b, p1.N, p1.K, g1.ldb, 128))
+    return map_failed("grouped pair GEMM operand B map");
+  if (!make_map_out(&md0, p0.d, p0.M, p0.N, p0.ldd) || !make_map_out(&md1, p1.d, p1.M, p1.N, p1.ldd))
+    return map_failed("grouped pair GEMM output map");
+  set_error_site("grouped pair GEMM launch");
+  const int units = pl.tiles0 + pl.tiles1;
+  const int pairs = units < pl.max_pairs ? units : pl.max_pairs;
+  GroupSched gs = pl.gs;
+  if (pairs < pl.max_pairs) gs = {pl.tiles0, pl.tiles1, 0};  // one round: a pair per unit
+  return launch_kernel(gemm_fp8_pair2_kernel<256, 6>, dim3(2 * pairs), dim3(kGemmThreads),
+                       PairCfg<256, 6>::kSmemBytes, stream, 2, false, ma0, mb0, md0, p0, ma1, mb1,
+                       md1, p1, gs);
+}
+
+void describe_group_plan(int64_t Ma, int64_t Na, int64_t Ka, int64_t Mb, int64_t Nb, int64_t Kb,
+                         int num_sms, int pair_slots, char* buf, size_t len) {
+  if (choose_variant(Ma, Na) != Variant::kPair256 || choose_variant(Mb, Nb) != Variant::kPair256) {
+    std::snprintf(buf, len, "separate: not both on 256-wide pair tiles");
+    return;
+  }
+  const int kba = static_cast<int>((Ka + kBK - 1) / kBK), kbb = static_cast<int>((Kb + kBK - 1) / kBK);
+  const bool swap = kbb > kba;
+  const int64_t M0 = swap ? Mb : Ma, N0 = swap ? Nb : Na, M1 = swap ? Ma : Mb, N1 = swap ? Na : Nb;
+  const int kb0 = swap ? kbb : kba, kb1 = swap ? kba : kbb;
+  const int tiles0 = static_cast<int>(((M0 + 2 * kBM - 1) / (2 * kBM)) * ((N0 + 255) / 256));
+  const int tiles1 = static_cast<int>(((M1 + 2 * kBM - 1) / (2 * kBM)) * ((N1 + 255) / 256));
+  const GroupPlan plan =
+      plan_group(tiles0, kb0, tiles1, kb1, pair_slots, gemm_split_workspace_bytes(num_sms));
+  // Every unit dealt exactly once, with the pairs and the deal the launch
+  // uses (the device deals with the same function; under one round, one unit
+  // a pair).
+  const int units = tiles0 + tiles1;
+  const int pairs = units < pair_slots ? units : pair_slots;
+  const GroupSched gs = pairs < pair_slots ? GroupSched{tiles0, tiles1, 0} : plan.gs;
+  std::vector<int> seen(static_cast<size_t>(units), 0);
+  bool ok = true;
+  for (int p = 0; p < pairs; ++p) {
+    Unit u;
+    for (int n = 0; unit_at_grouped(p, pairs, n, gs, kb0, kb1, u); ++n) {
+      const int i = u.prob == 0 ? u.tile : tiles0 + u.tile;
+      if (u.tile < 0 || u.tile >= (u.prob == 0 ? tiles0 : tiles1)) ok = false;
+      else ++seen[static_cast<size_t>(i)];
+    }
+  }
+  for (int c : seen) ok = ok && c == 1;
+  std::snprintf(buf, len, "%s: %d + %d tiles (K blocks %d, %d), d = %d; busiest pair %d K blocks "
+                "grouped, %d alone%s",
+                plan.use ? "grouped" : "separate", tiles0, tiles1, kb0, kb1, plan.gs.d,
+                plan.grouped, plan.alone, ok ? "" : "; DEAL BROKEN");
 }
 
 }  // namespace fp8lin

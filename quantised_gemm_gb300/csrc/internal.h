@@ -262,6 +262,22 @@ cudaError_t describe_gemm(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev
 void describe_plan(int64_t M, int64_t N, int64_t K, int num_sms, int pair_slots, char* buf,
                    size_t len);
 
+// Two GEMMs of the pair kernel (256-wide tiles) in one launch, whole tiles
+// dealt by cost.  plan_gemm_pair2 tells whether the plan expects that to beat
+// two launches (always with FP8LIN_GROUP=2, never with FP8LIN_GROUP=0; both
+// must qualify, and at most one may ask for its output amax);
+// launch_gemm_pair2 runs them so, cudaErrorInvalidValue if the plan says no.
+cudaError_t plan_gemm_pair2(const GemmArgs& a, const GemmArgs& b, const DeviceInfo& dev,
+                            bool* use);
+cudaError_t launch_gemm_pair2(const GemmArgs& a, const GemmArgs& b, const DeviceInfo& dev,
+                              cudaStream_t stream);
+// The grouped plan for two GEMMs (M x N x K each) on a device of num_sms SMs
+// holding pair_slots clusters: grouped or separate, the deal's d, the
+// estimated K blocks of the busiest pair both ways, and a check that the deal
+// hands out every tile once.  Pure host logic.
+void describe_group_plan(int64_t Ma, int64_t Na, int64_t Ka, int64_t Mb, int64_t Nb, int64_t Kb,
+                         int num_sms, int pair_slots, char* buf, size_t len);
+
 // Workspace bytes the tail K split can use at most on a device with num_sms SMs.
 size_t gemm_split_workspace_bytes(int num_sms);
 

@@ -1,0 +1,83 @@
+"""The backward's two GEMMs (dX and dW) in one launch of the grouped pair
+kernel, against two launches of the pair kernel: FP8LIN_GROUP (read once per
+process, so each setting runs in a child process) 0 never groups, 2 always
+groups when both GEMMs run on 256-wide pair tiles.  Same fp8 bytes and scales,
+every output within the oracle's bound, one launch fewer when grouped, and dX
+and dW the same bits wherever the separate launch runs whole tiles (no K
+split: the same accumulation order).  The shapes cover one round, several
+rounds with the long tiles' pairs taking d short ones, and ragged edges."""
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+import oracle
+import synth_inputs as si
+from helpers import assert_within_bound
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SHAPES = [(4096, 2048, 1024), (2064, 1552, 784), (1040, 784, 2000), (3008, 1200, 4992)]
+
+CHILD = r"""
+import sys, numpy as np, torch
+sys.path.insert(0, sys.argv[1])
+import quantised_gemm_gb300 as q, synth_inputs as si
+out = {}
+for i, (M, K, N) in enumerate(%r):
+    x, w, dy = si.linear_inputs(M, K, N, w_init="uniform64", outlier_frac=1e-3, seed=91 + i)
+    dev = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
+    lin = q.Fp8Linear(M, K, N)
+    lin.forward(dev(x), dev(w))
+    torch.cuda.synchronize()
+    n0 = q.launch_count()
+    lin.backward(dev(dy))
+    q.check(lin.ws)
+    out["launches%%d" %% i] = np.array([q.launch_count() - n0])
+    for name in ("x8", "w8", "dy8", "dy8t"):
+        out[name + "%%d" %% i] = getattr(lin, name).cpu().numpy()
+    for name in ("y", "dx", "dw"):
+        out[name + "%%d" %% i] = getattr(lin, name).cpu().view(torch.int16).numpy()
+    for st in ("sx", "sw", "sdy"):
+        out[st + "%%d" %% i] = getattr(lin, st).scale.cpu().numpy()
+    out["desc_dx%%d" %% i] = np.array(q.gemm_describe(M, K, N))
+    out["desc_dw%%d" %% i] = np.array(q.gemm_describe(N, K, M))
+np.savez(sys.argv[2], **out)
+""" % (SHAPES,)
+
+
+def _run(tmp_path, mode):
+    path = os.path.join(tmp_path, "group%s.npz" % mode)
+    env = dict(os.environ, FP8LIN_GROUP=mode)
+    subprocess.run([sys.executable, "-c", CHILD, ROOT, path], env=env, check=True, timeout=900)
+    return dict(np.load(path))
+
+
+def bf16_to_f64_bits(bits):
+    return (bits.astype(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def test_grouped_backward_matches_separate(tmp_path):
+    sep, grp = _run(tmp_path, "0"), _run(tmp_path, "2")
+    for i, (M, K, N) in enumerate(SHAPES):
+        assert int(sep["launches%d" % i][0]) - int(grp["launches%d" % i][0]) == 1, (M, K, N)
+        x, w, dy = si.linear_inputs(M, K, N, w_init="uniform64", outlier_frac=1e-3, seed=91 + i)
+        sx = oracle.scale_dynamic(oracle.amax(x), oracle.E4M3)[0]
+        sw = oracle.scale_dynamic(oracle.amax(w), oracle.E4M3)[0]
+        sd = oracle.scale_dynamic(oracle.amax(dy), oracle.E5M2)[0]
+        ref = oracle.linear_fwd_bwd(x, w, dy, sx, sw, sd)
+        for label, r in (("separate", sep), ("grouped", grp)):
+            for name in ("x8", "w8", "dy8", "dy8t"):
+                assert np.array_equal(r[name + str(i)], ref[name]), (label, name, M, K, N)
+            for st, s in (("sx", sx), ("sw", sw), ("sdy", sd)):
+                assert np.float32(r[st + str(i)][0]) == np.float32(s), (label, st)
+            for name, sref in (("y", "sy"), ("dx", "sdx"), ("dw", "sdw")):
+                assert_within_bound(bf16_to_f64_bits(r[name + str(i)]), ref[name], ref[sref],
+                                    "%s %s %s" % (label, name, (M, K, N)))
+        assert np.array_equal(sep["y%d" % i], grp["y%d" % i])
+        for name in ("dx", "dw"):
+            if str(sep["desc_%s%d" % (name, i)]).endswith("whole tiles"):
+                assert np.array_equal(sep[name + str(i)], grp[name + str(i)]), (name, M, K, N)

@@ -117,3 +117,67 @@ def test_describe_for_rejects_bad_arguments():
     small = ctypes.create_string_buffer(8)          # truncated, still terminated
     assert lib.fp8lin_gemm_describe_for(65536, 4096, 4096, 152, small, len(small)) == 0
     assert small.value == b"gemm_fp"
+
+
+GROUP = re.compile(
+    r"^(?P<use>grouped|separate): (?P<t0>\d+) \+ (?P<t1>\d+) tiles \(K blocks (?P<kb0>\d+), "
+    r"(?P<kb1>\d+)\), d = (?P<d>\d+); busiest pair (?P<g>\d+) K blocks grouped, (?P<a>\d+) alone$")
+
+
+def _backward_group(M, K, N, sms=GB300_SMS):
+    """The plan for a Linear's backward: dX = dY8 . W8 ([M, K], K loop N) and
+    dW = dY8^T . x8 ([N, K], K loop M)."""
+    return q.gemm_group_describe_for((M, K, N), (N, K, M), sms)
+
+
+@pytest.mark.parametrize("mkn,use,tiles,kb", [
+    ((4096, 4096, 4096), "grouped", (256, 256), (32, 32)),      # 3.37 + 3.37 rounds -> 7 rounds
+    ((12288, 1600, 1600), "grouped", (49, 336), (96, 13)),     # dW's long loop first
+    ((65536, 4096, 4096), "separate", (256, 4096), (512, 32)),  # 2.4% estimated: not enough
+    ((8192, 4096, 14336), "separate", (512, 896), (112, 64)),
+    ((12288, 1600, 4800), "grouped", (133, 336), (96, 38)),
+    ((1040, 784, 512), "grouped", (8, 20), (9, 4)),            # under one round
+])
+def test_group_plan_on_gb300(mkn, use, tiles, kb):
+    desc = _backward_group(*mkn)
+    m = GROUP.match(desc)
+    assert m, desc
+    assert m["use"] == use
+    assert (int(m["t0"]), int(m["t1"])) == tiles and (int(m["kb0"]), int(m["kb1"])) == kb
+
+
+def test_group_plan_separate_when_not_both_pair256():
+    # dX of a 16-token step runs on the swapped narrow tiles
+    assert _backward_group(16, 4096, 4096).startswith("separate: not both")
+
+
+def test_group_deal_covers_every_tile_once():
+    rng = random.Random(4321)
+    shapes = [(4096, 4096, 4096), (12288, 1600, 4800), (12288, 1600, 1600), (12288, 6400, 1600),
+              (8192, 4096, 14336), (8192, 14336, 4096), (65536, 4096, 4096), (256, 4096, 4096)]
+    shapes += [(256 * rng.randint(1, 64), 256 * rng.randint(1, 32), 256 * rng.randint(1, 64))
+               for _ in range(150)]
+    shapes += [(16 * rng.randint(17, 1024), 16 * rng.randint(17, 512), 16 * rng.randint(1, 2048))
+               for _ in range(150)]
+    for M, K, N in shapes:
+        for sms in (GB300_SMS, 148, 132, 4):
+            desc = _backward_group(M, K, N, sms)
+            assert "DEAL BROKEN" not in desc, (M, K, N, sms, desc)
+            m = GROUP.match(desc)
+            if m is None:
+                assert desc.startswith("separate: not both"), desc
+                continue
+            assert int(m["kb0"]) >= int(m["kb1"]), desc              # problem 0: the longer loop
+            assert (m["use"] == "grouped") == (int(m["g"]) * 100 < int(m["a"]) * 92), desc
+            # the busiest pair does at least its share of all K blocks
+            total = int(m["t0"]) * int(m["kb0"]) + int(m["t1"]) * int(m["kb1"])
+            assert int(m["g"]) * (sms // 2) >= total, desc
+
+
+def test_group_describe_rejects_bad_arguments():
+    lib = q.library()
+    buf = ctypes.create_string_buffer(64)
+    assert lib.fp8lin_gemm_group_describe_for(0, 16, 16, 16, 16, 16, 152, buf, len(buf)) == 1
+    assert lib.fp8lin_gemm_group_describe_for(16, 16, 16, 16, 16, 16, 1, buf, len(buf)) == 1
+    assert lib.fp8lin_gemm_group_describe_for(16, 16, 16, 16, 16, 16, 152, None, 64) == 1
+    assert lib.fp8lin_gemm_group_describe_for(16, 16, 16, 16, 16, 16, 152, buf, 0) == 1
