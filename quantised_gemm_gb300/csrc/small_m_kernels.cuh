@@ -673,18 +673,17 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     // registers during the casts, these 16-byte rows took 3.7 us of them;
     // staged before the partials, they held the partials back by 2.5 us.
     if (ok) {
-      for (int k = group; k < mine; k += 2)
+      for (int k = group; k < mine; k += 2) {  // each tile's store leaves as it is staged
         stage_transpose(tiles + k * kSmTileBytes, tiles + k * kSmTileBytes + kSmBSliceOffset,
                         gtid);
-      fence_proxy_async_shared();
-      sm_group_sync(group);
-      if (gtid == 0) {
-        for (int k = group; k < mine; k += 2) {
+        fence_proxy_async_shared();
+        sm_group_sync(group);
+        if (gtid == 0) {
           const int t = t0 + k;
           tma_store_2d(&tmC, tiles + k * kSmTileBytes + kSmBSliceOffset, (t / nks) * kTile,
                        (t % nks) * kTile);  // W8^T [KA, NA] at (K slice, band)
+          bulk_commit_group();
         }
-        bulk_commit_group();
       }
     }
   }
