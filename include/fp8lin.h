@@ -206,9 +206,10 @@ fp8lin_status fp8lin_amax(const void* x, int64_t rows, int64_t cols, int64_t ld,
  * Limits: the shape rules of fp8lin_amax; a launch that would need more
  * than 4096 CTAs (a device with more than 512 SMs) returns
  * FP8LIN_EUNSUPPORTED with nothing enqueued.
- * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  All calls on a device share the one array,
+ * Each call looks up the array's device address (cudaGetSymbolAddress) with
+ * the device current, so the address stays right after a device reset; the
+ * first lookup on a device may load the library's device code, so make the
+ * first call before any stream capture.  All calls on a device share the one array,
  * which keeps the last call's contents (nothing in it needs clearing: each
  * call writes every slot it reads); calls that overlap on the GPU -- on two
  * streams, or from two host threads -- race on it and must be serialised

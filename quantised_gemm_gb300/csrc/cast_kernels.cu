@@ -50,28 +50,18 @@ cudaError_t launch_amax_final(const uint32_t* partials, int n, uint32_t* amax_bi
 // kStaticAmaxPartials words (16 KiB), resident on every GPU that loads the
 // library until the process exits.  Host code must not pass the array's name
 // to a kernel (on the host it only stands in for the symbol); the device
-// address is looked up once per device with cudaGetSymbolAddress.
+// address is looked up with cudaGetSymbolAddress on every call (no
+// allocation), so it stays right after a device reset reloads the module.
 static __device__ __align__(256) uint32_t g_static_amax_partials[kStaticAmaxPartials];
 
 namespace {
 
-// Device address of g_static_amax_partials on the current device, looked up
-// on the first call for each device.
+// Device address of g_static_amax_partials in the current context.
 cudaError_t static_partials(uint32_t** out) {
-  static std::mutex mu;
-  static uint32_t* addr[64] = {};
-  int d = 0;
-  cudaError_t e = cudaGetDevice(&d);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_static_amax_partials);
   if (e != cudaSuccess) return e;
-  if (d < 0 || d >= 64) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  if (addr[d] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_amax_partials);
-    if (e != cudaSuccess) return e;
-    addr[d] = static_cast<uint32_t*>(p);
-  }
-  *out = addr[d];
+  *out = static_cast<uint32_t*>(p);
   return cudaSuccess;
 }
 
