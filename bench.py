@@ -257,6 +257,18 @@ def graphed(torch, fn):
     return g.replay
 
 
+def gemm_roofline(M, N, K, gemm_each, peak, kernel, traffic):
+    """The step's GEMMs against the tensor peak: y, dX and dW (2MNK flops
+    each) over the summed time (ms) of the step's GEMM launches -- three, or
+    two when the backward runs dX and dW as one grouped launch."""
+    achieved = 3 * 2.0 * M * N * K / (sum(gemm_each) * 1e-3) / 1e12
+    if len(gemm_each) == 2:
+        kernel += "; dX + dW: gemm_fp8_pair2_kernel<256, 6>"
+    return {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1),
+            "unit": "TFLOP/s", "frac": round(achieved / peak, 3), "traffic": traffic,
+            "kernel": kernel}
+
+
 def profiled(q, torch, step, n, flush=None):
     """Per-kernel device times of n un-graphed steps (an event pair around
     every launch).  Returns (per-kind ms per step, GEMM ms per step in launch
@@ -739,22 +751,15 @@ def run_native(args):
         roofline["kernel_time"] = ("mean of %d launches, profiled pass of %d steps after the "
                                    "timed region" % (n_prof, n_prof))
     else:
-        # y, dX and dW (2MNK each) over the step's GEMM launches: three, or
-        # two when the backward runs dX and dW in one grouped launch.
-        gemm_flop = 3 * 2.0 * M * N * K
-        achieved = gemm_flop / (sum(gemm_each) * 1e-3) / 1e12
-        grouped = len(gemm_each) == 2
         tr = load_traffic("gemm", args.workload)
-        roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1),
-                    "unit": "TFLOP/s", "frac": round(achieved / peak, 3),
-                    "traffic": tr["bytes_per_launch"] if tr else None,
-                    "kernel": q.gemm_describe(M, N, K).split(":")[0] +
-                              ("; dX + dW: gemm_fp8_pair2_kernel<256, 6>" if grouped else ""),
-                    "peak_basis": basis + " (of measured)" if peaks["source"] == "measured" else
-                    basis + " (of fallback)",
-                    "kernel_time": "the step's GEMM flops over the summed time of its %d GEMM "
+        roofline = gemm_roofline(M, N, K, gemm_each, peak,
+                                 q.gemm_describe(M, N, K).split(":")[0],
+                                 tr["bytes_per_launch"] if tr else None)
+        roofline["peak_basis"] = (basis + " (of measured)" if peaks["source"] == "measured" else
+                                  basis + " (of fallback)")
+        roofline["kernel_time"] = ("the step's GEMM flops over the summed time of its %d GEMM "
                                    "launches, profiled pass of %d steps after the timed region"
-                                   % (len(gemm_each), n_prof)}
+                                   % (len(gemm_each), n_prof))
     # Casts of the step: x [M,K], W [N,K], dY [M,N], each 2 B read + 1 B + 1 B
     # (transposed) written per element.  Tensors that fit on chip run as the
     # single-pass kernel (kind "cast_fused", amax included); the others as

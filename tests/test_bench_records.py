@@ -78,3 +78,15 @@ def test_reference_sample_fits_the_budget():
     ms = bench.ref_sample_tokens(t(16), t(128), 120, budget_s=60.0)
     assert ms == 96 and t(ms) * 120 <= 60.0 < t(ms + 16) * 120
     assert bench.ref_sample_tokens(t(16), t(128), 410, budget_s=60.0) == 16  # fixed part alone overruns
+
+
+def test_gemm_roofline_counts_the_step_flops_once():
+    M, N, K = 4096, 4096, 4096
+    flop = 3 * 2.0 * M * N * K
+    three = bench.gemm_roofline(M, N, K, [0.05, 0.05, 0.05], 4000.0, "pair", None)
+    two = bench.gemm_roofline(M, N, K, [0.05, 0.10], 4000.0, "pair", 123)
+    assert three["achieved"] == pytest.approx(flop / 0.15e-3 / 1e12, rel=1e-3)
+    assert two["achieved"] == three["achieved"]          # same work, same summed time
+    assert "pair2" in two["kernel"] and "pair2" not in three["kernel"]
+    assert two["frac"] == pytest.approx(two["achieved"] / 4000.0, abs=1e-3)
+    assert two["traffic"] == 123 and two["bound"] == "tensor"
