@@ -263,7 +263,7 @@ def gemm_roofline(M, N, K, gemm_each, peak, kernel, traffic):
     two when the backward runs dX and dW as one grouped launch."""
     achieved = 3 * 2.0 * M * N * K / (sum(gemm_each) * 1e-3) / 1e12
     if len(gemm_each) == 2:
-        kernel += "; dX + dW: gemm_fp8_pair2_kernel<256, 6>"
+        kernel += "; dX + dW: one grouped launch (gemm_fp8_pair2_kernel)"
     return {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1),
             "unit": "TFLOP/s", "frac": round(achieved / peak, 3), "traffic": traffic,
             "kernel": kernel}

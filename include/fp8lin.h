@@ -281,7 +281,7 @@ fp8lin_status fp8lin_gemm(const uint8_t* a, const uint8_t* b, int64_t M, int64_t
  * device for an M x N x K GEMM with a workspace of fp8lin_workspace_bytes,
  * as one NUL-terminated line written into buf (caller-owned host memory of
  * buf_len bytes; truncated to fit).  The kernel name is spelled as profilers
- * list it, e.g. "gemm_fp8_pair_kernel<256, 6>".  Enqueues nothing.  Returns
+ * list it, e.g. "gemm_fp8_pair_kernel<256, 6, 4>".  Enqueues nothing.  Returns
  * FP8LIN_EINVAL for negative sizes or a NULL / empty buffer, FP8LIN_ECUDA
  * without a usable device. */
 fp8lin_status fp8lin_gemm_describe(int64_t M, int64_t N, int64_t K, char* buf, size_t buf_len);
@@ -302,7 +302,8 @@ fp8lin_status fp8lin_gemm_describe_for(int64_t M, int64_t N, int64_t K, int32_t 
  * of both by their K loops is expected to take at most 0.92 of the time of
  * two, else "separate"; then the tile counts (problem 0: the longer K loop),
  * K blocks, the deal's parameter d, the estimated K blocks of the busiest
- * CTA pair both ways, and "DEAL BROKEN" if the deal would not hand out every
+ * CTA pair both ways, the grouped launch's epilogue warps (4 or 8), and
+ * "DEAL BROKEN" if the deal would not hand out every
  * tile exactly once (a self-check of the same function the kernel deals
  * with).  This is the plan's decision; FP8LIN_GROUP in the environment
  * overrides it in fp8lin_backward (0: never group, 2: group whenever both

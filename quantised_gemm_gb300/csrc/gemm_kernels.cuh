@@ -60,11 +60,22 @@ constexpr int kBoxBytes = 32 * kBoxCols * 2;          // (128-byte rows: whole L
 constexpr int kBoxesPerWarp = 1;                      // staging boxes per epilogue warp
 constexpr int kEpiStagingBytes = kEpiWarps * kBoxesPerWarp * kBoxBytes;
 
+// The pair kernel runs EPI epilogue warps: 8 (two per TMEM lane quarter,
+// each on half the columns) where the epilogue is on the critical path --
+// tiles of few K blocks, or fewer tiles than pairs -- or 4 (one per quarter,
+// on all the columns) where a tile's epilogue hides under the next tile's
+// main loop: there the fewer warps took 0.5-3 % off the products (their
+// issue slots and their draw on the SM are the main loop's).
+template <int EPI>
+constexpr int pair_threads() {
+  return 64 + 32 * EPI;
+}
+
 // Epilogue warps split the BN columns of a tile in two halves when each half
-// still holds whole 32-column chunks.
-template <int BN>
+// still holds whole 32-column chunks (and there are two warps a quarter).
+template <int BN, int EPI = kEpiWarps>
 struct EpiSplit {
-  static constexpr int kHalves = BN >= 64 ? 2 : 1;
+  static constexpr int kHalves = EPI == 8 && BN >= 64 ? 2 : 1;
   static constexpr int kCols = BN / kHalves;
 };
 constexpr int kMaxSplit = 8;
@@ -490,13 +501,14 @@ __device__ __forceinline__ void epilogue_unit(const GemmParams& p, const Unit& u
 // publishes it to p.amax_out and clears both words for the next call.  A bf16
 // bit pattern shifted up by 16 is the fp32 bit pattern of the same value, and
 // non-negative values order like their bits.
-__device__ __forceinline__ void publish_amax(const GemmParams& p, float vmax, int lane) {
+__device__ __forceinline__ void publish_amax(const GemmParams& p, float vmax, int lane,
+                                             unsigned epi_warps = kEpiWarps) {
   if (p.amax_out == nullptr) return;
   const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, cvt_bf16x2(vmax, 0.0f) & 0xFFFFu);
   if (lane == 0) {
     atomicMax(p.amax_acc, m << 16);
     __threadfence();
-    if (atomicAdd(p.amax_ticket, 1u) == gridDim.x * static_cast<unsigned>(kEpiWarps) - 1u) {
+    if (atomicAdd(p.amax_ticket, 1u) == gridDim.x * epi_warps - 1u) {
       __threadfence();
       *p.amax_out = atomicExch(p.amax_acc, 0u);
       atomicExch(p.amax_ticket, 0u);
@@ -757,7 +769,7 @@ struct PairCfg {
 
 // The pair kernel's body; kGrouped runs two GEMMs in one launch (problem 1:
 // tmA1 / tmB1 / tmD1 / p1, dealt with problem 0's tiles by unit_at_grouped).
-template <int BN, int STAGES, bool kGrouped>
+template <int BN, int STAGES, bool kGrouped, int EPI>
 __device__ __forceinline__ void pair_gemm_body(const CUtensorMap* tmA0, const CUtensorMap* tmB0,
                                                const CUtensorMap* tmD0, const GemmParams& p,
                                                const CUtensorMap* tmA1, const CUtensorMap* tmB1,
@@ -809,7 +821,7 @@ __device__ __forceinline__ void pair_gemm_body(const CUtensorMap* tmA0, const CU
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 2 * kEpiWarps);  // every epilogue warp of both CTAs
+      mbar_init(&acc_empty[a], 2 * EPI);  // every epilogue warp of both CTAs
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -941,9 +953,9 @@ __device__ __forceinline__ void pair_gemm_body(const CUtensorMap* tmA0, const CU
     }
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
-    using E = EpiSplit<BN>;
+    using E = EpiSplit<BN, EPI>;
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int half = (warp - 2) >> 2;  // 0 for every warp when EPI == 4
     const float alpha0 = __fmul_rn(*p.inv_a, *p.inv_b);
     const float alpha1 = kGrouped ? __fmul_rn(*p1.inv_a, *p1.inv_b) : alpha0;
     const uint32_t acc_empty_even0 = map_to_cta(smem_addr(&acc_empty[0]), 0);
@@ -983,8 +995,8 @@ __device__ __forceinline__ void pair_gemm_body(const CUtensorMap* tmA0, const CU
         acc_phase ^= 1u;
       }
     }
-    publish_amax(p, vmax0, lane);
-    if (kGrouped) publish_amax(p1, vmax1, lane);  // (at most one of the two asks for it)
+    publish_amax(p, vmax0, lane, EPI);
+    if (kGrouped) publish_amax(p1, vmax1, lane, EPI);  // (at most one of the two asks for it)
     if (lane == 0) bulk_wait_group<0>();  // stores done before the staging memory goes away
   }
 
@@ -1025,18 +1037,19 @@ __device__ __forceinline__ void pair_gemm_body(const CUtensorMap* tmA0, const CU
   }
 }
 
-template <int BN, int STAGES>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+template <int BN, int STAGES, int EPI>
+__global__ void __launch_bounds__(pair_threads<EPI>(), 1)
     gemm_fp8_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmD,
                          const __grid_constant__ GemmParams p) {
-  pair_gemm_body<BN, STAGES, false>(&tmA, &tmB, &tmD, p, &tmA, &tmB, &tmD, p, GroupSched{0, 0, 0});
+  pair_gemm_body<BN, STAGES, false, EPI>(&tmA, &tmB, &tmD, p, &tmA, &tmB, &tmD, p,
+                                         GroupSched{0, 0, 0});
 }
 
 // Two GEMMs of the same tile shape in one launch (see unit_at_grouped).
-template <int BN, int STAGES>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+template <int BN, int STAGES, int EPI>
+__global__ void __launch_bounds__(pair_threads<EPI>(), 1)
     gemm_fp8_pair2_kernel(const __grid_constant__ CUtensorMap tmA0,
                           const __grid_constant__ CUtensorMap tmB0,
                           const __grid_constant__ CUtensorMap tmD0,
@@ -1046,7 +1059,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                           const __grid_constant__ CUtensorMap tmD1,
                           const __grid_constant__ GemmParams p1,
                           const __grid_constant__ GroupSched gs) {
-  pair_gemm_body<BN, STAGES, true>(&tmA0, &tmB0, &tmD0, p0, &tmA1, &tmB1, &tmD1, p1, gs);
+  pair_gemm_body<BN, STAGES, true, EPI>(&tmA0, &tmB0, &tmD0, p0, &tmA1, &tmB1, &tmD1, p1, gs);
 }
 
 }  // namespace

@@ -192,10 +192,27 @@ cudaError_t one_cta_setup(const DeviceInfo& dev) {
   return e;
 }
 
-template <int BN, int STAGES>
+// Epilogue warps of a pair-kernel launch: 4 when at least one whole round of
+// tiles runs whole and each tile's main loop has at least kLeanMinKb K
+// blocks, so that a tile's epilogue hides under the next tile's main loop;
+// else 8.  Measured on GB300: 4 warps took 0.5-3 % off products of 13 or
+// more K blocks a tile; with 8 or fewer (K = 1024: 4 % slower; K = 256:
+// 14 % slower) and under one round the epilogue is on the critical path.
+constexpr int kLeanMinKb = 12;
+
+int pair_epi(int t_full, int slots, int num_kb) {
+  return t_full >= slots && num_kb >= kLeanMinKb ? 4 : 8;
+}
+
+// The same for a grouped launch of two GEMMs of kb0 and kb1 K blocks a tile.
+int group_epi(int units, int slots, int kb0, int kb1) {
+  return pair_epi(units, slots, kb0 < kb1 ? kb0 : kb1);
+}
+
+template <int BN, int STAGES, int EPI>
 cudaError_t pair_setup(const DeviceInfo& dev, int* slots) {
   using C = PairCfg<BN, STAGES>;
-  auto kernel = gemm_fp8_pair_kernel<BN, STAGES>;
+  auto kernel = gemm_fp8_pair_kernel<BN, STAGES, EPI>;
   static std::mutex mu;
   static int max_pairs[kMaxDevices] = {};
   if (dev.device < 0 || dev.device >= kMaxDevices) return cudaErrorInvalidDevice;
@@ -211,7 +228,7 @@ cudaError_t pair_setup(const DeviceInfo& dev, int* slots) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     probe.gridDim = dim3(2 * (dev.num_sms / 2));
-    probe.blockDim = dim3(kGemmThreads);
+    probe.blockDim = dim3(pair_threads<EPI>());
     probe.dynamicSmemBytes = C::kSmemBytes;
     probe.attrs = attr;
     probe.numAttrs = 1;
@@ -253,9 +270,8 @@ template <int BN, int STAGES>
 cudaError_t run_pair(const uint8_t* a, int64_t lda, const uint8_t* b, int64_t ldb, GemmParams p,
                      const GemmArgs& g, const DeviceInfo& dev, cudaStream_t stream) {
   using C = PairCfg<BN, STAGES>;
-  auto kernel = gemm_fp8_pair_kernel<BN, STAGES>;
   int max_pairs = 0;
-  cudaError_t e = pair_setup<BN, STAGES>(dev, &max_pairs);
+  cudaError_t e = pair_setup<BN, STAGES, 8>(dev, &max_pairs);
   if (e != cudaSuccess) return e;
   CUtensorMap ma, mb, md;
   if (!make_map_k_major(&ma, a, p.M, p.K, lda, kBM)) return map_failed("pair GEMM operand A map");
@@ -267,18 +283,28 @@ cudaError_t run_pair(const uint8_t* a, int64_t lda, const uint8_t* b, int64_t ld
   set_error_site("pair GEMM launch");
   const int units = p.t_full + (tiles - p.t_full) * p.s_tail;
   const int pairs = units < max_pairs ? units : max_pairs;
-  return launch_kernel(kernel, dim3(2 * pairs), dim3(kGemmThreads), C::kSmemBytes, stream, 2, false,
-                       ma, mb, md, p);
+  if constexpr (BN == 256) {  // (the 128-wide tiles, for N <= 128, keep 8 warps)
+    if (pair_epi(p.t_full, max_pairs, (p.K + kBK - 1) / kBK) == 4) {
+      int slots4 = 0;
+      if ((e = pair_setup<BN, STAGES, 4>(dev, &slots4)) != cudaSuccess) return e;
+      if (slots4 >= pairs)  // (the same shared memory: as many pairs fit)
+          return launch_kernel(gemm_fp8_pair_kernel<BN, STAGES, 4>, dim3(2 * pairs),
+                             dim3(pair_threads<4>()), C::kSmemBytes, stream, 2, false, ma, mb,
+                             md, p);
+    }
+  }
+  return launch_kernel(gemm_fp8_pair_kernel<BN, STAGES, 8>, dim3(2 * pairs),
+                       dim3(pair_threads<8>()), C::kSmemBytes, stream, 2, false, ma, mb, md, p);
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int EPI>
 cudaError_t pair2_setup(const DeviceInfo& dev) {
   static std::mutex mu;
   static bool done[kMaxDevices] = {};
   if (dev.device < 0 || dev.device >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
   if (done[dev.device]) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(gemm_fp8_pair2_kernel<BN, STAGES>,
+  cudaError_t e = cudaFuncSetAttribute(gemm_fp8_pair2_kernel<BN, STAGES, EPI>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(PairCfg<BN, STAGES>::kSmemBytes));
   if (e == cudaSuccess) done[dev.device] = true;
@@ -491,13 +517,13 @@ void describe_plan(int64_t M, int64_t N, int64_t K, int num_sms, int pair_slots,
     case Variant::kOne128: name = "gemm_fp8_kernel<128, 6, 0>"; bn = 128; break;
     case Variant::kOne256: name = "gemm_fp8_kernel<256, 4, 0>"; break;
     case Variant::kPair128:
-      name = "gemm_fp8_pair_kernel<128, 8>";
+      name = "gemm_fp8_pair_kernel<128, 8, 8>";
       bn = 128;
       rows = 2 * kBM;
       slots = pair_slots;
       break;
     case Variant::kPair256:
-      name = "gemm_fp8_pair_kernel<256, 6>";
+      name = "gemm_fp8_pair_kernel<256, 6, 8>";
       rows = 2 * kBM;
       slots = pair_slots;
       break;
@@ -508,6 +534,8 @@ void describe_plan(int64_t M, int64_t N, int64_t K, int num_sms, int pair_slots,
   const int num_kb = static_cast<int>((K + kBK - 1) / kBK);
   const SplitPlan sp =
       plan_split(tiles, slots, num_kb, rows, bn, gemm_split_workspace_bytes(num_sms));
+  if (v == Variant::kPair256 && pair_epi(sp.t_full, slots, num_kb) == 4)
+    name = "gemm_fp8_pair_kernel<256, 6, 4>";
   const int units = sp.t_full + (tiles - sp.t_full) * sp.ways;
   const int used = units < slots ? units : slots;
   char sched[64] = "whole tiles";
@@ -527,8 +555,8 @@ cudaError_t describe_gemm(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev
   int pair_slots = dev.num_sms / 2;
   cudaError_t e = cudaSuccess;
   switch (choose_variant(M, N)) {
-    case Variant::kPair128: e = pair_setup<128, 8>(dev, &pair_slots); break;
-    case Variant::kPair256: e = pair_setup<256, 6>(dev, &pair_slots); break;
+    case Variant::kPair128: e = pair_setup<128, 8, 8>(dev, &pair_slots); break;
+    case Variant::kPair256: e = pair_setup<256, 6, 8>(dev, &pair_slots); break;
     default: break;
   }
   if (e != cudaSuccess) return e;
@@ -556,7 +584,7 @@ cudaError_t pair2_plan(const GemmArgs& ga, const GemmArgs& gb, const DeviceInfo&
   out->use = false;
   if (group_mode() == 0 || !group_qualifies(ga, gb)) return cudaSuccess;
   int max_pairs = 0;
-  cudaError_t e = pair_setup<256, 6>(dev, &max_pairs);
+  cudaError_t e = pair_setup<256, 6, 8>(dev, &max_pairs);
   if (e != cudaSuccess) return e;
   out->swap = (gb.K + kBK - 1) / kBK > (ga.K + kBK - 1) / kBK;
   const GemmArgs& g0 = out->swap ? gb : ga;
@@ -589,7 +617,6 @@ cudaError_t launch_gemm_pair2(const GemmArgs& ga, const GemmArgs& gb, const Devi
   cudaError_t e = pair2_plan(ga, gb, dev, &pl);
   if (e != cudaSuccess) return e;
   if (!pl.use) return cudaErrorInvalidValue;
-  if ((e = pair2_setup<256, 6>(dev)) != cudaSuccess) return e;
   const GemmArgs& g0 = pl.swap ? gb : ga;
   const GemmArgs& g1 = pl.swap ? ga : gb;
   GemmParams p0 = base_params(g0), p1 = base_params(g1);
@@ -611,7 +638,15 @@ cudaError_t launch_gemm_pair2(const GemmArgs& ga, const GemmArgs& gb, const Devi
   const int pairs = units < pl.max_pairs ? units : pl.max_pairs;
   GroupSched gs = pl.gs;
   if (pairs < pl.max_pairs) gs = {pl.tiles0, pl.tiles1, 0};  // one round: a pair per unit
-  return launch_kernel(gemm_fp8_pair2_kernel<256, 6>, dim3(2 * pairs), dim3(kGemmThreads),
+  const int kb0 = (p0.K + kBK - 1) / kBK, kb1 = (p1.K + kBK - 1) / kBK;
+  if (group_epi(units, pl.max_pairs, kb0, kb1) == 4) {
+    if ((e = pair2_setup<256, 6, 4>(dev)) != cudaSuccess) return e;
+    return launch_kernel(gemm_fp8_pair2_kernel<256, 6, 4>, dim3(2 * pairs),
+                         dim3(pair_threads<4>()), PairCfg<256, 6>::kSmemBytes, stream, 2, false,
+                         ma0, mb0, md0, p0, ma1, mb1, md1, p1, gs);
+  }
+  if ((e = pair2_setup<256, 6, 8>(dev)) != cudaSuccess) return e;
+  return launch_kernel(gemm_fp8_pair2_kernel<256, 6, 8>, dim3(2 * pairs), dim3(pair_threads<8>()),
                        PairCfg<256, 6>::kSmemBytes, stream, 2, false, ma0, mb0, md0, p0, ma1, mb1,
                        md1, p1, gs);
 }
@@ -648,9 +683,10 @@ void describe_group_plan(int64_t Ma, int64_t Na, int64_t Ka, int64_t Mb, int64_t
   }
   for (int c : seen) ok = ok && c == 1;
   std::snprintf(buf, len, "%s: %d + %d tiles (K blocks %d, %d), d = %d; busiest pair %d K blocks "
-                "grouped, %d alone%s",
+                "grouped, %d alone; %d epilogue warps%s",
                 plan.use ? "grouped" : "separate", tiles0, tiles1, kb0, kb1, plan.gs.d,
-                plan.grouped, plan.alone, ok ? "" : "; DEAL BROKEN");
+                plan.grouped, plan.alone, group_epi(units, pair_slots, kb0, kb1),
+                ok ? "" : "; DEAL BROKEN");
 }
 
 }  // namespace fp8lin

@@ -153,11 +153,11 @@ def test_gemm_without_split_workspace_matches(ws):
     ((128, 4096, 4096), "gemm_fp8_kernel<256, 4, 0>", "K split 8 ways"),
     ((128, 1600, 512), "gemm_fp8_kernel<256, 4, 0>", "whole tiles"),
     ((96, 128, 512), "gemm_fp8_kernel<128, 6, 0>", "whole tiles"),
-    ((384, 1600, 1600), "gemm_fp8_pair_kernel<256, 6>", "whole tiles"),
-    ((512, 128, 1024), "gemm_fp8_pair_kernel<128, 8>", "whole tiles"),
-    ((4096, 4096, 65536), "gemm_fp8_pair_kernel<256, 6>", "last 28 tiles K split 2 ways"),
-    ((4096, 4096, 4096), "gemm_fp8_pair_kernel<256, 6>", "whole tiles"),
-    ((4096, 4096, 1024), "gemm_fp8_pair_kernel<256, 6>", "whole tiles"),
+    ((384, 1600, 1600), "gemm_fp8_pair_kernel<256, 6, 8>", "whole tiles"),
+    ((512, 128, 1024), "gemm_fp8_pair_kernel<128, 8, 8>", "whole tiles"),
+    ((4096, 4096, 65536), "gemm_fp8_pair_kernel<256, 6, 4>", "last 28 tiles K split 2 ways"),
+    ((4096, 4096, 4096), "gemm_fp8_pair_kernel<256, 6, 4>", "whole tiles"),
+    ((4096, 4096, 1024), "gemm_fp8_pair_kernel<256, 6, 8>", "whole tiles"),
 ])
 def test_gemm_describe_names_the_launched_kernel(mnk, kernel, sched, ws):
     """gemm_describe() reports the kernel and schedule gemm() runs; the

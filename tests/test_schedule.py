@@ -32,12 +32,12 @@ LINE = re.compile(
     ((128, 4096, 4096), "gemm_fp8_kernel<256, 4, 0>", "K split 8 ways"),
     ((128, 1600, 512), "gemm_fp8_kernel<256, 4, 0>", "whole tiles"),
     ((96, 128, 512), "gemm_fp8_kernel<128, 6, 0>", "whole tiles"),
-    ((384, 1600, 1600), "gemm_fp8_pair_kernel<256, 6>", "whole tiles"),
-    ((512, 128, 1024), "gemm_fp8_pair_kernel<128, 8>", "whole tiles"),
-    ((4096, 4096, 65536), "gemm_fp8_pair_kernel<256, 6>", "last 28 tiles K split 2 ways"),
-    ((4096, 4096, 4096), "gemm_fp8_pair_kernel<256, 6>", "whole tiles"),
-    ((4096, 4096, 1024), "gemm_fp8_pair_kernel<256, 6>", "whole tiles"),
-    ((512, 10240, 12288), "gemm_fp8_pair_kernel<256, 6>", "last 4 tiles K split 8 ways"),
+    ((384, 1600, 1600), "gemm_fp8_pair_kernel<256, 6, 8>", "whole tiles"),
+    ((512, 128, 1024), "gemm_fp8_pair_kernel<128, 8, 8>", "whole tiles"),
+    ((4096, 4096, 65536), "gemm_fp8_pair_kernel<256, 6, 4>", "last 28 tiles K split 2 ways"),
+    ((4096, 4096, 4096), "gemm_fp8_pair_kernel<256, 6, 4>", "whole tiles"),
+    ((4096, 4096, 1024), "gemm_fp8_pair_kernel<256, 6, 8>", "whole tiles"),
+    ((512, 10240, 12288), "gemm_fp8_pair_kernel<256, 6, 4>", "last 4 tiles K split 8 ways"),
 ])
 def test_kernel_and_schedule_on_gb300(mnk, kernel, sched):
     desc = q.gemm_describe_for(*mnk, GB300_SMS)
@@ -47,10 +47,10 @@ def test_kernel_and_schedule_on_gb300(mnk, kernel, sched):
 def test_headline_products_exactly():
     # the three products of the 65536-token step of the 4096 x 4096 Linear
     assert q.gemm_describe_for(65536, 4096, 4096, GB300_SMS) == (
-        "gemm_fp8_pair_kernel<256, 6>: 256x256 tiles, 4096 tiles on 76 of 76 CTA pairs, "
+        "gemm_fp8_pair_kernel<256, 6, 4>: 256x256 tiles, 4096 tiles on 76 of 76 CTA pairs, "
         "whole tiles")
     assert q.gemm_describe_for(4096, 4096, 65536, GB300_SMS) == (
-        "gemm_fp8_pair_kernel<256, 6>: 256x256 tiles, 256 tiles on 76 of 76 CTA pairs, "
+        "gemm_fp8_pair_kernel<256, 6, 4>: 256x256 tiles, 256 tiles on 76 of 76 CTA pairs, "
         "last 28 tiles K split 2 ways")
 
 
@@ -121,7 +121,8 @@ def test_describe_for_rejects_bad_arguments():
 
 GROUP = re.compile(
     r"^(?P<use>grouped|separate): (?P<t0>\d+) \+ (?P<t1>\d+) tiles \(K blocks (?P<kb0>\d+), "
-    r"(?P<kb1>\d+)\), d = (?P<d>\d+); busiest pair (?P<g>\d+) K blocks grouped, (?P<a>\d+) alone$")
+    r"(?P<kb1>\d+)\), d = (?P<d>\d+); busiest pair (?P<g>\d+) K blocks grouped, (?P<a>\d+) alone; "
+    r"(?P<epi>4|8) epilogue warps$")
 
 
 def _backward_group(M, K, N, sms=GB300_SMS):
@@ -168,6 +169,8 @@ def test_group_deal_covers_every_tile_once():
                 assert desc.startswith("separate: not both"), desc
                 continue
             assert int(m["kb0"]) >= int(m["kb1"]), desc              # problem 0: the longer loop
+            units, kb_min = int(m["t0"]) + int(m["t1"]), int(m["kb1"])
+            assert m["epi"] == ("4" if units >= sms // 2 and kb_min >= 12 else "8"), desc
             assert (m["use"] == "grouped") == (int(m["g"]) * 100 < int(m["a"]) * 92), desc
             # the busiest pair does at least its share of all K blocks
             total = int(m["t0"]) * int(m["kb0"]) + int(m["t1"]) * int(m["kb1"])
@@ -181,3 +184,16 @@ def test_group_describe_rejects_bad_arguments():
     assert lib.fp8lin_gemm_group_describe_for(16, 16, 16, 16, 16, 16, 1, buf, len(buf)) == 1
     assert lib.fp8lin_gemm_group_describe_for(16, 16, 16, 16, 16, 16, 152, None, 64) == 1
     assert lib.fp8lin_gemm_group_describe_for(16, 16, 16, 16, 16, 16, 152, buf, 0) == 1
+
+
+@pytest.mark.parametrize("mnk,epi", [
+    ((65536, 4096, 4096), 4),    # 54 rounds of 32 K blocks: the epilogue hides
+    ((4096, 4096, 2048), 4),     # 16 K blocks a tile
+    ((4096, 4096, 1024), 8),     # 8: the epilogue shows
+    ((4096, 4096, 256), 8),
+    ((256, 4096, 4096), 8),      # a few tiles split along K
+    ((384, 1600, 1600), 8),      # under one round
+])
+def test_pair_kernel_epilogue_warps(mnk, epi):
+    desc = q.gemm_describe_for(*mnk, GB300_SMS)
+    assert desc.startswith("gemm_fp8_pair_kernel<256, 6, %d>:" % epi), desc
