@@ -48,6 +48,8 @@ CASES = [
     (4096, 4096, 1024),     # 256 pair tiles: 3.4 waves
     (128, 40960, 512),      # 160 one-CTA tiles: more tiles than CTAs
     (16, 20480, 256),       # swapped operands, 160 tiles, transposed stores
+    (2064, 2576, 1552),     # pair tiles, four epilogue warps: 99 tiles, ragged M, N, K
+    (1024, 5120, 12288),    # four epilogue warps, the last 4 tiles K split 8 ways
 ]
 
 
@@ -202,6 +204,7 @@ def _bf16_bits(t: torch.Tensor) -> np.ndarray:
     (384, 1600, 1600),     # CTA pairs, N edge inside the last 256-wide tile
     (512, 128, 1024),      # CTA pairs, 128-wide tiles
     (2048, 2560, 256),     # CTA pairs, more than one wave
+    (2064, 2576, 1552),    # CTA pairs, four epilogue warps
 ])
 def test_gemm_output_amax(mnk, ws):
     """max |D| from the epilogue equals the amax of the bf16 D it stored (the
