@@ -36,14 +36,19 @@ def _operand(rows, k, fmt, seed):
     return q8, s, inv
 
 
-@pytest.mark.parametrize("M", [16, 256])
-def test_split_gemm_wait_runs_out_and_the_workspace_recovers(M):
+@pytest.mark.parametrize("M,N,K,sched", [
+    (16, 4096, 4096, "K split 4 ways"),
+    (256, 4096, 4096, "K split 4 ways"),
+    (1024, 5120, 12288, "last 4 tiles K split 8 ways"),
+])
+def test_split_gemm_wait_runs_out_and_the_workspace_recovers(M, N, K, sched):
     """M = 16: the one-CTA kernel; M = 256: the CTA-pair kernel, whose
     closing path then has both CTAs exchange their failure state and the even
-    CTA confirm every stage's last load before either CTA leaves."""
-    N, K = 4096, 4096
+    CTA confirm every stage's last load before either CTA leaves; M = 1024:
+    the pair kernel with four epilogue warps, whose whole tiles finish and
+    whose split tail tiles give up."""
     desc = q.gemm_describe(M, N, K)
-    assert desc.endswith("K split 4 ways"), desc
+    assert desc.endswith(sched), desc
     assert ("pair" in desc) == (M > 128), desc
     a8, sa, inva = _operand(M, K, oracle.E4M3, seed=71)
     b8, sb, invb = _operand(N, K, oracle.E4M3, seed=72)
