@@ -225,6 +225,19 @@ fp8lin_status fp8lin_amax_noalloc(const void* x, int64_t rows, int64_t cols, int
  * BF16" (pytorch/ao issue 1297), repro script. */
 fp8lin_status fp8lin_scale(const fp8lin_scaling_state* st, cudaStream_t stream);
 
+/* fp8lin_scale of each of n states (0 <= n <= 8) in ONE launch, one thread a
+ * state: the history updates and rescales of a Linear's x, W and dY states
+ * after its backward, which sync_float8_amax_and_scale_history performs one
+ * tensor at a time in "[float8] FP8 GPT 1.5B Delayed Scaling 2x Slower than
+ * BF16" (pytorch/ao issue 1297), repro script.  `states` points to n states
+ * in host memory (read during the call only), each checked as fp8lin_scale
+ * checks it; their device buffers must not overlap one another.  The
+ * results are those of n fp8lin_scale calls, bit for bit.  EINVAL for n < 0
+ * or n > 8, for states NULL with n > 0, and for any state fp8lin_scale
+ * rejects (nothing enqueued); n == 0 enqueues nothing. */
+fp8lin_status fp8lin_scale_many(const fp8lin_scaling_state* states, int32_t n,
+                                cudaStream_t stream);
+
 /* cast (row a3): out[i, j] = sat_rne_fp8(fl32(x[i, j] * (*scale))) into the
  * dense [rows, cols] byte array out; if out_t is not NULL also
  * out_t[j, i] = out[i, j] (dense [cols, rows]).  If amax_out is not NULL the

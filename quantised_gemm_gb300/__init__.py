@@ -197,6 +197,17 @@ def scale(state: ScalingState, stream=None):
                "fp8lin_scale")
 
 
+def scale_many(states, stream=None):
+    """scale() of each of up to 8 states in one launch (the same results)."""
+    states = list(states)
+    arr = (_lib.ScalingStateC * max(1, len(states)))()
+    for i, st in enumerate(states):
+        ctypes.memmove(ctypes.byref(arr, i * ctypes.sizeof(_lib.ScalingStateC)),
+                       ctypes.byref(st.c_struct()), ctypes.sizeof(_lib.ScalingStateC))
+    _lib.check(library().fp8lin_scale_many(arr, len(states), _stream(stream)),
+               "fp8lin_scale_many")
+
+
 def cast(x: torch.Tensor, fmt: int, scale_t: torch.Tensor, out: torch.Tensor | None,
          out_t: torch.Tensor | None = None, amax_out: torch.Tensor | None = None, stream=None):
     px, rows, cols, ld = _bf16_2d(x, "x")

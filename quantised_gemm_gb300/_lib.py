@@ -79,6 +79,7 @@ _SIGNATURES = {
     "fp8lin_amax": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I32, _P, _P]),
     "fp8lin_amax_noalloc": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P]),
     "fp8lin_scale": (ctypes.c_int, [_ST, _P]),
+    "fp8lin_scale_many": (ctypes.c_int, [_ST, _I32, _P]),
     "fp8lin_cast": (ctypes.c_int, [_P, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P]),
     "fp8lin_cast_dynamic": (ctypes.c_int, [_P, _I64, _I64, _I64, _ST, _P, _P, _P, _P]),
     "fp8lin_cast_delayed": (ctypes.c_int, [_P, _I64, _I64, _I64, _ST, _P, _P, _P, _P]),

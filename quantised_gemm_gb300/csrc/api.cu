@@ -473,6 +473,24 @@ fp8lin_status fp8lin_scale(const fp8lin_scaling_state* st, cudaStream_t stream) 
   return run_scale(st, stream);
 }
 
+fp8lin_status fp8lin_scale_many(const fp8lin_scaling_state* states, int32_t n,
+                                cudaStream_t stream) {
+  if (n < 0 || n > 8 || (n > 0 && states == nullptr)) return FP8LIN_EINVAL;
+  ScaleArgs a[8];
+  for (int i = 0; i < n; ++i) {
+    const fp8lin_scaling_state* st = &states[i];
+    fp8lin_status s = check_state(st, true);
+    if (s != FP8LIN_OK) return s;
+    const bool delayed = st->kind == FP8LIN_DELAYED;
+    a[i] = {st->amax, st->scale, st->inv_scale, st->amax_history, st->head,
+            delayed ? st->history_len : 1, delayed, st->fmt, st->eps};
+  }
+  if (n == 0) return FP8LIN_OK;
+  ProfScope ps(FP8LIN_PROF_SCALE, stream);
+  cudaError_t e = launch_scale_batch(a, n, stream);
+  return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);
+}
+
 fp8lin_status fp8lin_cast(const void* x, int64_t rows, int64_t cols, int64_t ld, int32_t fmt,
                           const float* scale, uint8_t* out, uint8_t* out_t, float* amax_out,
                           cudaStream_t stream) {

@@ -90,6 +90,24 @@ cudaError_t launch_scale(const float* amax, float* scale, float* inv, float* rin
                        head, history_len, delayed ? 1 : 0, F, eps);
 }
 
+cudaError_t launch_scale_batch(const ScaleArgs* a, int n, cudaStream_t stream) {
+  if (n < 1 || n > kScaleBatch) return cudaErrorInvalidValue;
+  ScaleBatch b = {};
+  b.n = n;
+  for (int i = 0; i < n; ++i) {
+    b.amax[i] = a[i].amax;
+    b.scale[i] = a[i].scale;
+    b.inv[i] = a[i].inv;
+    b.ring[i] = a[i].ring;
+    b.head[i] = a[i].head;
+    b.H[i] = a[i].history_len;
+    b.delayed[i] = a[i].delayed ? 1 : 0;
+    b.F[i] = a[i].fmt == 0 ? 448.0f : 57344.0f;
+    b.eps[i] = a[i].eps;
+  }
+  return launch_kernel(scale_batch_kernel, dim3(1), dim3(32), 0, stream, 1, false, b);
+}
+
 namespace {
 
 template <int kFmt, bool kTrans>

@@ -215,12 +215,11 @@ __global__ void __launch_bounds__(kThreads) amax_final_kernel(const uint32_t* __
 
 // ------------------------------------------------------------------ scale
 
-__global__ void scale_kernel(const float* __restrict__ amax, float* __restrict__ scale,
-                             float* __restrict__ inv, float* __restrict__ ring,
-                             int32_t* __restrict__ head, int32_t H, int delayed, float F,
-                             float eps) {
-  griddep_wait();
-  griddep_launch_dependents();
+// One state's scale update: delayed, the ring takes the amax at its head and
+// the scale comes from the ring's maximum; dynamic, from the amax itself.
+__device__ __forceinline__ void scale_update(const float* amax, float* scale, float* inv,
+                                             float* ring, int32_t* head, int32_t H, int delayed,
+                                             float F, float eps) {
   float a = *amax;
   if (delayed) {
     int32_t h = *head;
@@ -234,6 +233,39 @@ __global__ void scale_kernel(const float* __restrict__ amax, float* __restrict__
   const float s = scale_from_amax(a, eps, F);
   *scale = s;
   *inv = __fdiv_rn(1.0f, s);
+}
+
+__global__ void scale_kernel(const float* __restrict__ amax, float* __restrict__ scale,
+                             float* __restrict__ inv, float* __restrict__ ring,
+                             int32_t* __restrict__ head, int32_t H, int delayed, float F,
+                             float eps) {
+  griddep_wait();
+  griddep_launch_dependents();
+  scale_update(amax, scale, inv, ring, head, H, delayed, F, eps);
+}
+
+// Up to kScaleBatch states updated by one launch, one thread each.
+constexpr int kScaleBatch = 8;
+struct ScaleBatch {
+  const float* amax[kScaleBatch];
+  float* scale[kScaleBatch];
+  float* inv[kScaleBatch];
+  float* ring[kScaleBatch];
+  int32_t* head[kScaleBatch];
+  int32_t H[kScaleBatch];
+  int32_t delayed[kScaleBatch];
+  float F[kScaleBatch];
+  float eps[kScaleBatch];
+  int32_t n;
+};
+
+__global__ void scale_batch_kernel(const __grid_constant__ ScaleBatch b) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int i = static_cast<int>(threadIdx.x);
+  if (i < b.n)
+    scale_update(b.amax[i], b.scale[i], b.inv[i], b.ring[i], b.head[i], b.H[i], b.delayed[i],
+                 b.F[i], b.eps[i]);
 }
 
 // ------------------------------------------------------------------ cast

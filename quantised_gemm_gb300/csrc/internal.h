@@ -115,6 +115,20 @@ cudaError_t launch_amax_static_scratch(const uint16_t* x, int64_t rows, int64_t 
                                        float* amax_out, int grid, cudaStream_t stream);
 
 // One-thread scale update (dynamic or delayed ring).
+// One state of a batched scale update (launch_scale's arguments).
+struct ScaleArgs {
+  const float* amax;
+  float* scale;
+  float* inv;
+  float* ring;
+  int32_t* head;
+  int32_t history_len;
+  bool delayed;
+  int fmt;
+  float eps;
+};
+// Up to 8 states in one launch, one thread each.
+cudaError_t launch_scale_batch(const ScaleArgs* a, int n, cudaStream_t stream);
 cudaError_t launch_scale(const float* amax, float* scale, float* inv, float* ring, int32_t* head,
                          int32_t history_len, bool delayed, int fmt, float eps,
                          cudaStream_t stream);

@@ -17,7 +17,7 @@ import torch
 
 from . import _lib
 from . import (AMAX_AUTO, AMAX_PRECOMPUTED, DELAYED, DYNAMIC, E4M3, E5M2, ScalingState,
-               Workspace, _stream, backward, forward, scale)
+               Workspace, _stream, backward, forward, scale, scale_many)
 
 
 class Fp8Linear:
@@ -69,9 +69,9 @@ class Fp8Linear:
         """Delayed scaling: push this step's amaxes into the histories and
         recompute the scales (a no-op for dynamic scaling).  A new delayed
         weight scale makes a cached W8 stale: the next forward casts again."""
-        for st in (self.sx, self.sw, self.sdy):
-            if st.kind == DELAYED:
-                scale(st, stream)
+        delayed = [st for st in (self.sx, self.sw, self.sdy) if st.kind == DELAYED]
+        if delayed:
+            scale_many(delayed, stream)  # one launch for the Linear's states
         if self.sw.kind == DELAYED:
             self._w_key = None
 

@@ -36,7 +36,7 @@ from __future__ import annotations
 import torch
 import torch.distributed as dist
 
-from . import AMAX_ATOMIC, AMAX_PRECOMPUTED, DELAYED, DYNAMIC, amax, scale
+from . import AMAX_ATOMIC, AMAX_PRECOMPUTED, DELAYED, DYNAMIC, amax, scale, scale_many
 from .linear import Fp8Linear
 
 
@@ -116,7 +116,8 @@ class ShardedFp8Linear:
     def sync_scales(self):
         """Delayed scaling: the group's maximum of each recorded amax, then the
         history update of every state (a no-op for dynamic scaling)."""
-        for st in (self.lin.sx, self.lin.sw, self.lin.sdy):
-            if st.kind == DELAYED:
-                global_amax_(st.amax, self.group)
-                scale(st)
+        delayed = [st for st in (self.lin.sx, self.lin.sw, self.lin.sdy) if st.kind == DELAYED]
+        for st in delayed:
+            global_amax_(st.amax, self.group)
+        if delayed:
+            scale_many(delayed)  # one launch for the three states

@@ -125,6 +125,15 @@ def test_forward_backward_argument_errors(lib):
     assert bwd(sd, dwa=p, dw=None) == L.EINVAL                     # dW amax without dW
     assert lib.fp8lin_scale(None, None) == L.EINVAL
     assert lib.fp8lin_scale(ctypes.byref(_state(0, kind=1, H=0)), None) == L.EINVAL
+    # the batched update: 0..8 states, each checked as fp8lin_scale checks it
+    good, bad = _state(0), _state(0, kind=1, H=0)
+    arr = (L.ScalingStateC * 9)(*([good] * 9))
+    assert lib.fp8lin_scale_many(None, 1, None) == L.EINVAL
+    assert lib.fp8lin_scale_many(arr, -1, None) == L.EINVAL
+    assert lib.fp8lin_scale_many(arr, 9, None) == L.EINVAL
+    assert lib.fp8lin_scale_many(None, 0, None) == L.OK             # nothing to do
+    arr[2] = bad
+    assert lib.fp8lin_scale_many(arr, 3, None) == L.EINVAL
 
 
 def test_gemm_describe_argument_errors(lib):

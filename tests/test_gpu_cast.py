@@ -90,6 +90,35 @@ def test_scale_delayed_ring_matches_oracle(fmt):
                               ref.ring.view(np.uint32))
 
 
+def test_scale_many_matches_the_oracle_state_by_state():
+    """fp8lin_scale_many: eight states in one launch -- delayed ones with
+    rings of 1, 3, 16 and 7 (e4m3 and e5m2) and dynamic ones -- each updated
+    exactly as one fp8lin_scale would, over 20 steps."""
+    g = np.random.default_rng(29)
+    specs = [(E4M3, q.DELAYED, 16), (E5M2, q.DELAYED, 16), (E4M3, q.DELAYED, 1),
+             (E5M2, q.DELAYED, 3), (E4M3, q.DYNAMIC, 1), (E5M2, q.DYNAMIC, 1),
+             (E4M3, q.DELAYED, 7), (E5M2, q.DYNAMIC, 1)]
+    sts = [q.ScalingState(f, k, history_len=h) for f, k, h in specs]
+    refs = [oracle.DelayedState(h, f) if k == q.DELAYED else None for f, k, h in specs]
+    for step in range(20):
+        amaxes = np.exp2(g.uniform(-6, 6, len(specs))).astype(np.float32)
+        amaxes[step % len(specs)] = 0.0                    # an all-zero tensor now and then
+        for st, a in zip(sts, amaxes):
+            st.amax.fill_(float(a))
+        q.scale_many(sts)
+        for (f, k, h), st, ref, a in zip(specs, sts, refs, amaxes):
+            if ref is not None:
+                ref.update(float(a))
+                s, inv = ref.scale, ref.inv_scale
+                assert int(st.head.item()) == ref.head
+                assert np.array_equal(st.amax_history.cpu().numpy().view(np.uint32),
+                                      ref.ring.view(np.uint32))
+            else:
+                s, inv = oracle.scale_dynamic(float(a), f)
+            assert dev_f32_bits(st.scale) == f32_bits(s), (step, f, k, h)
+            assert dev_f32_bits(st.inv_scale) == f32_bits(inv), (step, f, k, h)
+
+
 @pytest.mark.parametrize("fmt", [E4M3, E5M2])
 @pytest.mark.parametrize("trans", [False, True])
 @pytest.mark.parametrize("shape", SHAPES)
