@@ -157,6 +157,42 @@ fp8lin_status do_cast(const CastArgs& a, const DeviceInfo& dev, cudaStream_t str
 }
 
 // Dynamic scaling of one tensor: amax -> scale -> cast (+T) per st->amax_algo.
+// FP8LIN_PAIR_CAST=0 casts x and W of the forward in separate launches even
+// where one paired single pass would take both.
+bool pair_cast_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("FP8LIN_PAIR_CAST");
+    return !(v != nullptr && v[0] == '0');
+  }();
+  return on;
+}
+
+bool single_pass_algo(int32_t algo) {
+  return algo == FP8LIN_AMAX_AUTO || algo == FP8LIN_AMAX_SINGLE_PASS;
+}
+
+SinglePassArgs single_pass_args(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                const fp8lin_scaling_state* st, uint8_t* out, uint8_t* out_t,
+                                void* ws) {
+  SinglePassArgs sp;
+  sp.x = static_cast<const uint16_t*>(x);
+  sp.rows = rows;
+  sp.cols = cols;
+  sp.ld = ld;
+  sp.fmt = st->fmt;
+  sp.eps = st->eps;
+  sp.amax_out = st->amax;
+  sp.scale_out = st->scale;
+  sp.inv_out = st->inv_scale;
+  sp.out = out;
+  sp.out_t = out_t;
+  sp.ws_barrier = ws_u32(ws, kWsBarrierOffset);
+  sp.ws_exits = ws_u32(ws, kWsExitsOffset);
+  sp.ws_amax = ws_u32(ws, kWsAmaxOffset);
+  sp.ws_error = ws_error(ws);
+  return sp;
+}
+
 // SINGLE_PASS falls back to ATOMIC when the tensor does not fit on chip and
 // `allow_fallback` is set.  PRECOMPUTED takes *st->amax as given (written by
 // the producer of x, e.g. a GEMM epilogue) and runs scale + cast only.
@@ -762,6 +798,24 @@ fp8lin_status run_forward(const void* x, const void* w, int64_t M, int64_t K, in
       }
       return run_small_m(a, dev, stream);
     }
+  }
+  // W's single pass with x's cast in the same launch, where x has at most one
+  // tile for each of its CTAs (a few hundred tokens): one launch and one grid
+  // barrier fewer.
+  if (w != nullptr && pair_cast_enabled() && sx->kind == FP8LIN_DYNAMIC &&
+      sw->kind == FP8LIN_DYNAMIC && single_pass_algo(sx->amax_algo) &&
+      single_pass_algo(sw->amax_algo) && x8t != nullptr && w8t != nullptr &&
+      single_pass_pair_fits(dev, N, K, M, K)) {
+    SinglePassArgs wa = single_pass_args(w, N, K, K, sw, w8, w8t, ws);
+    SinglePassArgs xa = single_pass_args(x, M, K, K, sx, x8, x8t, ws);
+    xa.ws_amax = ws_u32(ws, kWsAmax2Offset);
+    {
+      ProfScope ps(FP8LIN_PROF_CAST_FUSED, stream);
+      cudaError_t e = launch_cast_single_pass_pair(wa, xa, dev, stream);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return do_gemm(x8, w8, M, N, K, K, K, FP8LIN_E4M3, FP8LIN_E4M3, sx->inv_scale, sw->inv_scale,
+                   y, N, y_amax, ws, ws_bytes, dev, stream);
   }
   fp8lin_status s;
   if (sx->kind == FP8LIN_DYNAMIC)

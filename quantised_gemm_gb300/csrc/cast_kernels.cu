@@ -370,4 +370,114 @@ cudaError_t launch_cast_single_pass(const SinglePassArgs& a, const DeviceInfo& d
                        stream, 1, true, tm, tq, tqt, p);
 }
 
+namespace {
+
+// The paired kernel's shared memory and resident CTAs per SM (once per device).
+cudaError_t pair_prepare(int* ctas_per_sm) {
+  static std::mutex mu;
+  static int per_sm[64] = {};
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) return e;
+  if (d < 0 || d >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (per_sm[d] == 0) {
+    auto k = cast_pair_single_pass_kernel<0, true>;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSinglePassSmem));
+    if (e != cudaSuccess) return e;
+    const int n = resident_ctas(k, kSpThreads, kSinglePassSmem);
+    if (n < 1) {
+      *ctas_per_sm = 0;
+      return cudaSuccess;
+    }
+    per_sm[d] = n;
+  }
+  *ctas_per_sm = per_sm[d];
+  return cudaSuccess;
+}
+
+int64_t tiles_of(int64_t rows, int64_t cols) {
+  return ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
+}
+
+}  // namespace
+
+bool single_pass_pair_fits(const DeviceInfo& dev, int64_t w_rows, int64_t w_cols, int64_t x_rows,
+                           int64_t x_cols) {
+  if (w_rows <= 0 || w_cols <= 0 || x_rows <= 0 || x_cols <= 0) return false;
+  if (cluster_cast_fits(w_rows, w_cols) || !single_pass_fits(dev, w_rows, w_cols)) return false;
+  int per_sm = 0;
+  if (pair_prepare(&per_sm) != cudaSuccess || per_sm < 1) return false;
+  const int64_t max_grid = static_cast<int64_t>(dev.num_sms) * per_sm;
+  const int64_t wt = tiles_of(w_rows, w_cols);
+  const int64_t grid = wt < max_grid ? wt : max_grid;
+  return wt <= max_grid * kSinglePassTilesPerCta && tiles_of(x_rows, x_cols) <= grid;
+}
+
+cudaError_t launch_cast_single_pass_pair(const SinglePassArgs& a, const SinglePassArgs& x,
+                                         const DeviceInfo& dev, cudaStream_t stream) {
+  if (a.fmt != 0 || x.fmt != 0 || a.out_t == nullptr || x.out_t == nullptr)
+    return cudaErrorInvalidValue;
+  if (!single_pass_pair_fits(dev, a.rows, a.cols, x.rows, x.cols)) return cudaErrorInvalidValue;
+  int per_sm = 0;
+  cudaError_t e = pair_prepare(&per_sm);
+  if (e != cudaSuccess) return e;
+  SinglePassParams p;
+  p.rows = a.rows;
+  p.cols = a.cols;
+  p.eps = a.eps;
+  p.amax_out = a.amax_out;
+  p.scale_out = a.scale_out;
+  p.inv_out = a.inv_out;
+  p.out = a.out;
+  p.out_t = a.out_t;
+  p.ws_barrier = a.ws_barrier;
+  p.ws_exits = a.ws_exits;
+  p.ws_amax = a.ws_amax;
+  p.ws_error = a.ws_error;
+  p.x2 = x.x;
+  p.rows2 = x.rows;
+  p.cols2 = x.cols;
+  p.ld2 = x.ld;
+  p.eps2 = x.eps;
+  p.amax2_out = x.amax_out;
+  p.scale2_out = x.scale_out;
+  p.inv2_out = x.inv_out;
+  p.out2 = x.out;
+  p.out2_t = x.out_t;
+  p.ws_amax2 = x.ws_amax;
+  const int64_t wt = tiles_of(a.rows, a.cols);
+  const int64_t max_grid = static_cast<int64_t>(dev.num_sms) * per_sm;
+  const int64_t grid = wt < max_grid ? wt : max_grid;
+  CUtensorMap tm, tq, tqt, tq2, tqt2;
+  if (!make_map_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, static_cast<uint64_t>(a.cols),
+                   static_cast<uint64_t>(a.rows), static_cast<uint64_t>(a.ld) * 2, kTile, kTile,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+    return map_failed("paired single-pass input map");
+  const void* qw = a.out != nullptr ? static_cast<const void*>(a.out) : a.out_t;
+  const void* qx = x.out != nullptr ? static_cast<const void*>(x.out) : x.out_t;
+  if (!make_map_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, qw,
+                   static_cast<uint64_t>(a.out != nullptr ? a.cols : a.rows),
+                   static_cast<uint64_t>(a.out != nullptr ? a.rows : a.cols),
+                   static_cast<uint64_t>(a.out != nullptr ? a.cols : a.rows), kTile, kTile,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map_2d(&tqt, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.out_t, static_cast<uint64_t>(a.rows),
+                   static_cast<uint64_t>(a.cols), static_cast<uint64_t>(a.rows), kTile, kTile,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map_2d(&tq2, CU_TENSOR_MAP_DATA_TYPE_UINT8, qx,
+                   static_cast<uint64_t>(x.out != nullptr ? x.cols : x.rows),
+                   static_cast<uint64_t>(x.out != nullptr ? x.rows : x.cols),
+                   static_cast<uint64_t>(x.out != nullptr ? x.cols : x.rows), kTile, kTile,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map_2d(&tqt2, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.out_t, static_cast<uint64_t>(x.rows),
+                   static_cast<uint64_t>(x.cols), static_cast<uint64_t>(x.rows), kTile, kTile,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+    return map_failed("paired single-pass output map");
+  set_error_site("paired single-pass cooperative launch");
+  return launch_kernel(cast_pair_single_pass_kernel<0, true>, dim3(static_cast<unsigned>(grid)),
+                       dim3(kSpThreads), kSinglePassSmem, stream, 1, true, tm, tq, tqt, p, tq2,
+                       tqt2);
+}
+
 }  // namespace fp8lin

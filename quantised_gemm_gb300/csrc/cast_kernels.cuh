@@ -598,6 +598,19 @@ struct SinglePassParams {
   uint32_t* ws_exits;     // leavers   } past the barrier clears all three
   uint32_t* ws_amax;      // amax bits }
   int* ws_error;
+  // The paired launch only: a second tensor of at most one 128 x 128 tile a
+  // CTA (x of the forward, cast with W), loaded into registers by group 0 of
+  // CTA b < its tile count, its amax taken at the same grid barrier (its own
+  // word ws_amax2, cleared with the others), cast after the CTA's own tiles.
+  const uint16_t* x2;
+  int64_t rows2, cols2, ld2;
+  float eps2;
+  float* amax2_out;
+  float* scale2_out;
+  float* inv2_out;
+  uint8_t* out2;
+  uint8_t* out2_t;
+  uint32_t* ws_amax2;
 };
 
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
@@ -623,16 +636,17 @@ __device__ __forceinline__ void group_sync(int group) {
   asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(kThreads) : "memory");
 }
 
-template <int kFmt, bool kTrans>
-__global__ void __launch_bounds__(kSpThreads, 1)
-    cast_single_pass_kernel(const __grid_constant__ CUtensorMap tmX,
-                            const __grid_constant__ CUtensorMap tmQ,
-                            const __grid_constant__ CUtensorMap tmQT, const SinglePassParams p) {
+template <int kFmt, bool kTrans, bool kPair>
+__device__ __forceinline__ void single_pass_body(const CUtensorMap* tmX, const CUtensorMap* tmQ,
+                                                 const CUtensorMap* tmQT,
+                                                 const SinglePassParams& p,
+                                                 const CUtensorMap* tmQ2,
+                                                 const CUtensorMap* tmQT2) {
   extern __shared__ __align__(1024) uint8_t tiles_raw[];
   uint8_t* tiles = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(tiles_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   __shared__ __align__(8) uint64_t loaded[kSinglePassTilesPerCta];  // one per tile
-  __shared__ uint32_t s_amax_bits;
+  __shared__ uint32_t s_amax_bits, s_amax2_bits;
   __shared__ uint32_t s_red[kSpThreads / 32];
   __shared__ int s_abort;
   const int group = threadIdx.x / kThreads, tid = threadIdx.x % kThreads;
@@ -651,11 +665,33 @@ __global__ void __launch_bounds__(kSpThreads, 1)
     for (int k = 0; k < mine; ++k) {
       const int64_t t = blockIdx.x + static_cast<int64_t>(k) * gridDim.x;
       mbar_arrive_expect_tx(&loaded[k], kTile * kTile * 2);
-      tma_load_2d(tiles + k * (kTile * kTile * 2), &tmX, &loaded[k],
+      tma_load_2d(tiles + k * (kTile * kTile * 2), tmX, &loaded[k],
                   static_cast<int32_t>((t % ntc) * kTile), static_cast<int32_t>((t / ntc) * kTile));
     }
   }
   __syncthreads();
+  // kPair: group 0 of CTA b < ntiles2 loads tile b of the second tensor into
+  // registers (8 vectors a thread, as the casts below read a tile), in flight
+  // with the TMA loads.
+  uint4 v2[kPair ? 8 : 1];
+  AbsMax x0;
+  int64_t ntc2 = 1, ntiles2 = 0;
+  if constexpr (kPair) {
+    ntc2 = (p.cols2 + kTile - 1) / kTile;
+    ntiles2 = ((p.rows2 + kTile - 1) / kTile) * ntc2;
+    if (static_cast<int64_t>(blockIdx.x) < ntiles2 && group == 0) {
+      const int64_t r0 = (blockIdx.x / ntc2) * kTile, c0 = (blockIdx.x % ntc2) * kTile;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int vi = tid + kThreads * u;
+        const int64_t row = r0 + (vi >> 4), col = c0 + (vi & 15) * 8;
+        v2[u] = row < p.rows2 && col < p.cols2 ? ld_stream_v4(p.x2 + row * p.ld2 + col)
+                                               : make_uint4(0u, 0u, 0u, 0u);
+        x0.add(v2[u]);
+      }
+    }
+  }
+  const bool has2 = kPair && static_cast<int64_t>(blockIdx.x) < ntiles2;  // CTA-uniform
   // The amax of each tile as soon as it lands.  Two independent accumulators
   // of the short-step kind: the tile is on chip, so this loop is a latency
   // chain, not a bandwidth stream.
@@ -682,6 +718,13 @@ __global__ void __launch_bounds__(kSpThreads, 1)
     m = __reduce_max_sync(0xFFFFFFFFu, m);
     if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = m;
   }
+  __shared__ uint32_t s_red2[kThreads / 32];
+  if constexpr (kPair) {  // group 0's maximum of the second tensor's tile
+    const uint32_t acc = x0.packed();
+    uint32_t m = max(acc & 0xFFFFu, acc >> 16);
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if (group == 0 && (tid & 31) == 0) s_red2[tid >> 5] = m;
+  }
   if (__syncthreads_and(landed ? 1 : 0) == 0) {  // one decision for the CTA
     if (threadIdx.x == 0) {
       atomicCAS(p.ws_error, 0, kErrGridBarrier);
@@ -694,7 +737,12 @@ __global__ void __launch_bounds__(kSpThreads, 1)
     uint32_t m = 0;
     for (int w = 0; w < kSpThreads / 32; ++w) m = max(m, s_red[w]);
     atomicMax(p.ws_amax, m << 16);
-    red_release_add(p.ws_barrier, 1u);  // the max above is visible to whoever sees this
+    if (has2) {
+      uint32_t m2 = 0;
+      for (int w = 0; w < kThreads / 32; ++w) m2 = max(m2, s_red2[w]);
+      atomicMax(p.ws_amax2, m2 << 16);
+    }
+    red_release_add(p.ws_barrier, 1u);  // the maxima above are visible to whoever sees this
     const uint64_t t0 = global_timer_ns();
     while (ld_acquire_u32(p.ws_barrier) < gridDim.x) {
       if (global_timer_ns() - t0 > kWaitLimitNs) {
@@ -704,7 +752,10 @@ __global__ void __launch_bounds__(kSpThreads, 1)
       }
     }
     // Ordered after every arrival by the acquiring poll above.
-    if (!s_abort) s_amax_bits = *reinterpret_cast<volatile uint32_t*>(p.ws_amax);
+    if (!s_abort) {
+      s_amax_bits = *reinterpret_cast<volatile uint32_t*>(p.ws_amax);
+      if (kPair) s_amax2_bits = *reinterpret_cast<volatile uint32_t*>(p.ws_amax2);
+    }
   }
   __syncthreads();
   if (s_abort) return;
@@ -716,6 +767,16 @@ __global__ void __launch_bounds__(kSpThreads, 1)
     *p.amax_out = amax;
     *p.scale_out = s;
     *p.inv_out = __fdiv_rn(1.0f, s);
+  }
+  float s2 = 1.0f;
+  if constexpr (kPair) {
+    const float amax2 = __uint_as_float(s_amax2_bits);
+    s2 = scale_from_amax(amax2, p.eps2, fp8_max<kFmt>());
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+      *p.amax2_out = amax2;
+      *p.scale2_out = s2;
+      *p.inv2_out = __fdiv_rn(1.0f, s2);
+    }
   }
   // Phase 2, per tile: cast from shared memory into registers, then stage the
   // fp8 tile (first 16 KB of the tile's own 32 KB buffer, free once read)
@@ -743,10 +804,34 @@ __global__ void __launch_bounds__(kSpThreads, 1)
     group_sync(group);
     if (issuer) {
       if (p.out != nullptr)
-        tma_store_2d(&tmQ, sqt, static_cast<int32_t>(c0), static_cast<int32_t>(r0));
+        tma_store_2d(tmQ, sqt, static_cast<int32_t>(c0), static_cast<int32_t>(r0));
       if (kTrans)
-        tma_store_2d(&tmQT, stt, static_cast<int32_t>(r0), static_cast<int32_t>(c0));
+        tma_store_2d(tmQT, stt, static_cast<int32_t>(r0), static_cast<int32_t>(c0));
       bulk_commit_group();
+    }
+  }
+  if constexpr (kPair) {
+    // The second tensor's tile, by group 0, staged in slot 0 (group 0's
+    // first tile) once that tile's stores have read it.
+    if (has2 && group == 0) {
+      if (issuer) bulk_wait_group_read<0>();
+      group_sync(0);
+      const int64_t r0 = (blockIdx.x / ntc2) * kTile, c0 = (blockIdx.x % ntc2) * kTile;
+      uint2 q[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) q[u] = cast8<kFmt>(v2[u], s2);
+      uint8_t* sqt = tiles;
+      uint8_t* stt = tiles + kTile * kTile;
+      stage_tile_fp8<kTrans>(q, sqt, stt, tid, [&] { group_sync(0); });
+      fence_proxy_async_shared();
+      group_sync(0);
+      if (issuer) {
+        if (p.out2 != nullptr)
+          tma_store_2d(tmQ2, sqt, static_cast<int32_t>(c0), static_cast<int32_t>(r0));
+        if (kTrans)
+          tma_store_2d(tmQT2, stt, static_cast<int32_t>(r0), static_cast<int32_t>(c0));
+        bulk_commit_group();
+      }
     }
   }
   // Count this CTA out (it has read the amax; after its casts, so that the
@@ -756,8 +841,31 @@ __global__ void __launch_bounds__(kSpThreads, 1)
     atomicExch(p.ws_barrier, 0u);
     atomicExch(p.ws_exits, 0u);
     atomicExch(p.ws_amax, 0u);
+    if (kPair) atomicExch(p.ws_amax2, 0u);
   }
   if (issuer) bulk_wait_group<0>();  // stores done before the shared memory goes away
+}
+
+template <int kFmt, bool kTrans>
+__global__ void __launch_bounds__(kSpThreads, 1)
+    cast_single_pass_kernel(const __grid_constant__ CUtensorMap tmX,
+                            const __grid_constant__ CUtensorMap tmQ,
+                            const __grid_constant__ CUtensorMap tmQT,
+                            const __grid_constant__ SinglePassParams p) {
+  single_pass_body<kFmt, kTrans, false>(&tmX, &tmQ, &tmQT, p, &tmQ, &tmQT);
+}
+
+// The single pass of W with x's cast in the same launch (x: at most one tile
+// a CTA); one grid barrier for both maxima.
+template <int kFmt, bool kTrans>
+__global__ void __launch_bounds__(kSpThreads, 1)
+    cast_pair_single_pass_kernel(const __grid_constant__ CUtensorMap tmX,
+                                 const __grid_constant__ CUtensorMap tmQ,
+                                 const __grid_constant__ CUtensorMap tmQT,
+                                 const __grid_constant__ SinglePassParams p,
+                                 const __grid_constant__ CUtensorMap tmQ2,
+                                 const __grid_constant__ CUtensorMap tmQT2) {
+  single_pass_body<kFmt, kTrans, true>(&tmX, &tmQ, &tmQT, p, &tmQ2, &tmQT2);
 }
 
 // ------------------------------------------------------------------ cluster single pass

@@ -19,6 +19,7 @@ constexpr size_t kWsAtomicTicketOffset = 196;  // uint32: ticketed amax arrivals
 constexpr size_t kWsGemmAmaxAccOffset = 200;     // uint32: GEMM output amax accumulator
 constexpr size_t kWsGemmAmaxTicketOffset = 204;  // uint32: GEMM epilogue warps arrived
 constexpr size_t kWsSmallBAmaxOffset = 208;      // uint32: few-token product, token-side amax
+constexpr size_t kWsAmax2Offset = 212;           // uint32: paired single pass, x's amax bits
 constexpr size_t kWsScratchBegin = 64;    // [64, 256): self-cleaning counters
 constexpr size_t kWsPartialOffset = 256;  // uint32[kMaxPartials]: REDUCTION partial maxima
 constexpr int kMaxPartials = 4096;
@@ -175,6 +176,14 @@ struct SinglePassArgs {
   int* ws_error;
 };
 int64_t single_pass_capacity_elems(const DeviceInfo& dev);
+// W's single pass with x's cast in the same launch (the forward, both e4m3
+// with transposed copies): W must take the cooperative single pass and x have
+// at most one 128 x 128 tile for each of its CTAs.  x's amax goes through the
+// workspace word of x_args.ws_amax.
+bool single_pass_pair_fits(const DeviceInfo& dev, int64_t w_rows, int64_t w_cols,
+                           int64_t x_rows, int64_t x_cols);
+cudaError_t launch_cast_single_pass_pair(const SinglePassArgs& w, const SinglePassArgs& x,
+                                         const DeviceInfo& dev, cudaStream_t stream);
 bool single_pass_fits(const DeviceInfo& dev, int64_t rows, int64_t cols);
 // Small tensors: the same single pass in one thread-block cluster (no grid
 // barrier, no workspace).  Results are identical to the cooperative kernel's.

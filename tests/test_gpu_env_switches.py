@@ -1,10 +1,11 @@
-"""The environment switches that choose between the few-token fused products
-and the separate kernels (read once per process, so each setting runs in a
-child process): a 16-token step with FP8LIN_SMALL_M=0 (casts and GEMMs as
-separate kernels), with FP8LIN_SMALL_M_DW=0 (the fused products, dW as its own
-GEMM) and with neither gives the same fp8 bytes and scales, and every output
-within the oracle's bound; dW with and without its fusion is equal value for
-value."""
+"""The environment switches that choose between fused and separate launches
+(read once per process, so each setting runs in a child process).  A 16-token
+step with FP8LIN_SMALL_M=0 (casts and GEMMs as separate kernels), with
+FP8LIN_SMALL_M_DW=0 (the fused products, dW as its own GEMM) and with neither
+gives the same fp8 bytes and scales, and every output within the oracle's
+bound; dW with and without its fusion is equal value for value.  A
+few-hundred-token forward with FP8LIN_PAIR_CAST=0 casts x and W in two
+launches instead of one paired single pass: the same bits, one launch more."""
 import os
 import subprocess
 import sys
@@ -25,7 +26,7 @@ CHILD = r"""
 import sys, numpy as np, torch
 sys.path.insert(0, sys.argv[1])
 import quantised_gemm_gb300 as q, synth_inputs as si
-M, K, N = %d, %d, %d
+M, K, N = (int(v) for v in sys.argv[3].split(",")) if len(sys.argv) > 3 else (%d, %d, %d)
 x, w, dy = si.linear_inputs(M, K, N, w_init="uniform64", outlier_frac=1e-2, seed=83)
 dev = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
 lin = q.Fp8Linear(M, K, N)
@@ -44,11 +45,12 @@ np.savez(sys.argv[2], **out)
 """ % (M, K, N)
 
 
-def _run(tmp_path, name, env):
+def _run(tmp_path, name, env, mkn=None):
     path = os.path.join(tmp_path, name + ".npz")
     e = dict(os.environ)
     e.update(env)
-    subprocess.run([sys.executable, "-c", CHILD, ROOT, path], env=e, check=True, timeout=600)
+    args = [sys.executable, "-c", CHILD, ROOT, path] + ([",".join(map(str, mkn))] if mkn else [])
+    subprocess.run(args, env=e, check=True, timeout=600)
     return dict(np.load(path))
 
 
@@ -82,3 +84,12 @@ def test_few_token_switches(tmp_path):
     # Only the fusion of dW differs between these two: y and dX are the same bits.
     for name in ("y", "dx"):
         assert np.array_equal(runs["fused"][name], runs["no_dw_fusion"][name]), name
+
+
+@pytest.mark.parametrize("mkn", [(256, 4096, 4096), (208, 1552, 784)])
+def test_paired_forward_cast_switch(tmp_path, mkn):
+    paired = _run(tmp_path, "paired", {"FP8LIN_PAIR_CAST": "1"}, mkn)
+    apart = _run(tmp_path, "apart", {"FP8LIN_PAIR_CAST": "0"}, mkn)
+    assert int(apart["launches"][0]) == int(paired["launches"][0]) + 1
+    for name in ("x8", "x8t", "w8", "w8t", "dy8", "dy8t", "y", "dx", "dw", "sx", "sw", "sdy"):
+        assert np.array_equal(paired[name], apart[name]), name
