@@ -351,7 +351,11 @@ fp8lin_status fp8lin_gemm_group_describe_for(int64_t Ma, int64_t Na, int64_t Ka,
  * SINGLE_PASS): x's cast, W's cast and y run as one fused launch (same
  * results: casts and scales bit for bit, y within the GEMM's bound; only the
  * order in which y's fp32 partial sums are added differs).
- * FP8LIN_SMALL_M=0 in the environment turns this off. */
+ * FP8LIN_SMALL_M=0 in the environment turns this off.
+ * More tokens, with both states dynamic (AUTO or SINGLE_PASS) and W cast by
+ * the cooperative single pass: where x has at most one 128 x 128 tile for
+ * each CTA of W's launch, x's cast runs inside W's (one launch; the same
+ * bits).  FP8LIN_PAIR_CAST=0 in the environment casts them apart. */
 fp8lin_status fp8lin_forward(const void* x, const void* w, int64_t M, int64_t K, int64_t N,
                              fp8lin_scaling_state* sx, fp8lin_scaling_state* sw,
                              void* y, float* y_amax, uint8_t* x8, uint8_t* x8t, uint8_t* w8,
