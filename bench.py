@@ -439,8 +439,9 @@ def chain_sweep_entry(q, torch, dev, name, steps, warmup, flush, rounds=3):
             "graph": graphed(torch, step), "lins": (l1, l2), "ms": [],
             "kernel_us_per_step": {k: round(v * 1e3, 1) for k, v in kk.items()}}
     torch.cuda.synchronize()
-    for _ in range(rounds):
-        for v in variants.values():
+    order = list(variants.values())
+    for r in range(rounds):  # ABBA: neither variant always runs first
+        for v in (order if r % 2 == 0 else order[::-1]):
             v["ms"].append(time_region(v["graph"], steps, flush) / steps)
     res = {"workload": "2 x %s chained" % name, "l2": "flushed between steps" if flush else
            "inputs larger than L2", "cuda_graph": True, "rounds": rounds}
@@ -836,7 +837,7 @@ def run_native(args):
         chains = [chain_sweep_entry(q, torch, dev, "linear4096_m4096", steps=50, warmup=5,
                                     flush=flush),
                   chain_sweep_entry(q, torch, dev, "linear4096_m65536", steps=10, warmup=3,
-                                    flush=None)]
+                                    flush=None, rounds=6)]
         detail["chains"] = chains
         del flush_buf
         torch.cuda.empty_cache()
