@@ -303,7 +303,7 @@ def linear_sweep_entry(q, torch, dev, name, steps, warmup, flush, peak_fp8, peak
     import synth_inputs as si
     wl = si.WORKLOADS[name]
     delayed = wl.get("delayed", False)
-    total_ms = flop = gemm_ms = nbytes = 0.0
+    total_ms = flop = gemm_ms = nbytes = warm_ms = 0.0
     kinds = {}
     for idx, (M, K, N) in enumerate(wl["shapes"]):
         x, w, dy = make_inputs(name, idx)
@@ -323,6 +323,8 @@ def linear_sweep_entry(q, torch, dev, name, steps, warmup, flush, peak_fp8, peak
         fn = graphed(torch, step)
         torch.cuda.synchronize()
         ms = time_region(fn, steps, flush) / steps
+        if flush is not None:  # the same replays back to back: L2 warm
+            warm_ms += time_region(fn, steps) / steps
         kk, gemm_each, _ = profiled(q, torch, step, 5, flush)
         q.check(lin.ws)
         total_ms += ms
@@ -346,6 +348,7 @@ def linear_sweep_entry(q, torch, dev, name, steps, warmup, flush, peak_fp8, peak
             "kernel_us": {k: round(v * 1e3, 2) for k, v in kinds.items()},
             "scaling": "delayed" if delayed else "dynamic",
             "l2": "flushed between steps" if flush else "inputs larger than L2",
+            "us_warm": round(warm_ms * 1e3, 2) if flush is not None else None,
             "cuda_graph": True}
 
 
@@ -562,6 +565,46 @@ def cpu_baseline_sample(name, budget_s=12.0):
     desc = ("oracle fwd+bwd (C casts, numpy fp64 GEMMs), %dx%d Linear, first %d of %d tokens, "
             "%.2f s" % (K, N, Ms, M, elapsed))
     return flop / elapsed / 1e12, desc, oracle.num_threads()
+
+
+def host_cpu():
+    """The host CPU's model name and its logical CPU count."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith("model name"):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    import platform
+    return "%s (%d logical CPUs, %s)" % (model or "unknown model", os.cpu_count() or 0,
+                                         platform.machine())
+
+
+def cpu_baseline_one_core(name, budget_s=5.0):
+    """cpu_baseline_sample on one core: a child process whose OpenMP and BLAS
+    pools have one thread (set before the oracle and numpy load).  Returns
+    (TFLOP/s, description, threads) or None if the child failed."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import json, sys; sys.path.insert(0, %r); import bench; "
+            "print(json.dumps(bench.cpu_baseline_sample(%r, %r)))" % (ROOT, name, budget_s))
+    try:
+        r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
+                           env=env, cwd=ROOT, timeout=300)
+        return tuple(json.loads(r.stdout.strip().splitlines()[-1])) if r.returncode == 0 else None
+    except (OSError, subprocess.SubprocessError, ValueError, IndexError):
+        return None
 
 
 def end_to_end(q, lin, x, w, dy, M, K, N, world, flop_step):
@@ -828,6 +871,8 @@ def run_native(args):
         configs = {}
         for key, e in entries:
             c = {"us": e["us"], "tf": e["tf"]}
+            if e["us_warm"] is not None:
+                c["us_warm"] = e["us_warm"]   # no flush between the replays
             if key.startswith(("m16", "m256")):
                 c["hbm"] = e["hbm"]           # HBM-bound: the step against its bytes
             else:
@@ -856,7 +901,12 @@ def run_native(args):
     if rank == 0 and not args.no_cpu_baseline:
         v, desc, cores = cpu_baseline_sample(args.workload)
         cpu = {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-               "sample": desc}
+               "sample": desc, "cpu": host_cpu()}
+        one = cpu_baseline_one_core(args.workload)
+        if one is not None:  # (its sample, fewer tokens, in the detail file)
+            cpu["one_core"] = {"value": round(one[0], 6), "threads": one[2]}
+            detail["cpu_baseline_one_core"] = {"value": one[0], "threads": one[2],
+                                               "sample": one[1]}
 
     if rank == 0:
         e2e_line = None
@@ -966,7 +1016,8 @@ def run_reference(args):
             "config": {"workload": "%s: Linear 4096->4096, M=%d tokens (sampled %d)" %
                                    (args.workload, M, Ms), "M": M, "K": K, "N": N},
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "kind": "oracle",
-                             "cores": oracle.num_threads(), "sample": sample},
+                             "cores": oracle.num_threads(), "sample": sample,
+                             "cpu": host_cpu()},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
