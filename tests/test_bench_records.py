@@ -90,3 +90,15 @@ def test_gemm_roofline_counts_the_step_flops_once():
     assert "pair2" in two["kernel"] and "pair2" not in three["kernel"]
     assert two["frac"] == pytest.approx(two["achieved"] / 4000.0, abs=1e-3)
     assert two["traffic"] == 123 and two["bound"] == "tensor"
+
+
+def test_cpu_baseline_reports_the_host_and_one_thread():
+    """cpu_baseline's `cpu` names the host, and its one-core figure comes from
+    a child whose OpenMP and BLAS pools really have one thread."""
+    desc = bench.host_cpu()
+    assert "logical CPUs" in desc and str(os.cpu_count()) in desc
+    one = bench.cpu_baseline_one_core("linear4096_m65536", budget_s=0.3)
+    assert one is not None
+    value, sample, threads = one
+    assert threads == 1 and value > 0
+    assert "first" in sample and "of 65536 tokens" in sample
