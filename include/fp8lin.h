@@ -231,10 +231,12 @@ fp8lin_status fp8lin_scale(const fp8lin_scaling_state* st, cudaStream_t stream);
  * tensor at a time in "[float8] FP8 GPT 1.5B Delayed Scaling 2x Slower than
  * BF16" (pytorch/ao issue 1297), repro script.  `states` points to n states
  * in host memory (read during the call only), each checked as fp8lin_scale
- * checks it; their device buffers must not overlap one another.  The
- * results are those of n fp8lin_scale calls, bit for bit.  EINVAL for n < 0
- * or n > 8, for states NULL with n > 0, and for any state fp8lin_scale
- * rejects (nothing enqueued); n == 0 enqueues nothing. */
+ * checks it.  No buffer a state's update writes (scale, inv_scale and,
+ * delayed, amax_history[0..H) and head) may overlap any buffer of another
+ * state; states may share an amax, which is only read.  The results are
+ * those of n fp8lin_scale calls, bit for bit.  EINVAL for n < 0 or n > 8,
+ * for states NULL with n > 0, for any state fp8lin_scale rejects and for
+ * overlapping states (nothing enqueued); n == 0 enqueues nothing. */
 fp8lin_status fp8lin_scale_many(const fp8lin_scaling_state* states, int32_t n,
                                 cudaStream_t stream);
 

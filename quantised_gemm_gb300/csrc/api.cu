@@ -509,6 +509,50 @@ fp8lin_status fp8lin_scale(const fp8lin_scaling_state* st, cudaStream_t stream) 
   return run_scale(st, stream);
 }
 
+// The device byte ranges the scale update of one state writes (scale, inverse
+// and, delayed, the ring and its head); it reads only these and *amax.
+struct ByteRange {
+  uintptr_t lo, hi;
+};
+
+int scale_written_ranges(const fp8lin_scaling_state* st, ByteRange* r) {
+  auto at = [](const void* p, size_t bytes) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return ByteRange{lo, lo + bytes};
+  };
+  int n = 0;
+  r[n++] = at(st->scale, sizeof(float));
+  r[n++] = at(st->inv_scale, sizeof(float));
+  if (st->kind == FP8LIN_DELAYED) {
+    r[n++] = at(st->amax_history, sizeof(float) * static_cast<size_t>(st->history_len));
+    r[n++] = at(st->head, sizeof(int32_t));
+  }
+  return n;
+}
+
+bool ranges_overlap(const ByteRange& a, const ByteRange& b) { return a.lo < b.hi && b.lo < a.hi; }
+
+// True if a buffer that one of the n states' updates writes overlaps any
+// buffer of another state (one thread per state would race on it).  States
+// may share an amax, which the update only reads.
+bool scale_states_overlap(const fp8lin_scaling_state* states, int n) {
+  for (int i = 0; i < n; ++i) {
+    ByteRange wi[4];
+    const int ni = scale_written_ranges(&states[i], wi);
+    for (int j = 0; j < n; ++j) {
+      if (j == i) continue;
+      ByteRange bj[5];
+      int nj = scale_written_ranges(&states[j], bj);
+      const uintptr_t amax = reinterpret_cast<uintptr_t>(states[j].amax);
+      bj[nj++] = {amax, amax + sizeof(float)};
+      for (int x = 0; x < ni; ++x)
+        for (int y = 0; y < nj; ++y)
+          if (ranges_overlap(wi[x], bj[y])) return true;
+    }
+  }
+  return false;
+}
+
 fp8lin_status fp8lin_scale_many(const fp8lin_scaling_state* states, int32_t n,
                                 cudaStream_t stream) {
   if (n < 0 || n > 8 || (n > 0 && states == nullptr)) return FP8LIN_EINVAL;
@@ -522,6 +566,7 @@ fp8lin_status fp8lin_scale_many(const fp8lin_scaling_state* states, int32_t n,
             delayed ? st->history_len : 1, delayed, st->fmt, st->eps};
   }
   if (n == 0) return FP8LIN_OK;
+  if (scale_states_overlap(states, n)) return FP8LIN_EINVAL;
   ProfScope ps(FP8LIN_PROF_SCALE, stream);
   cudaError_t e = launch_scale_batch(a, n, stream);
   return e == cudaSuccess ? FP8LIN_OK : cuda_fail(e);

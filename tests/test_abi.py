@@ -134,6 +134,25 @@ def test_forward_backward_argument_errors(lib):
     assert lib.fp8lin_scale_many(None, 0, None) == L.OK             # nothing to do
     arr[2] = bad
     assert lib.fp8lin_scale_many(arr, 3, None) == L.EINVAL
+    # states whose written buffers overlap another state's buffers (checked
+    # before any launch; no valid case is launched here, the pointers are fake)
+    def state(base, kind=0, H=1):
+        s = _state(0, kind=kind, H=H)
+        s.amax, s.scale, s.inv_scale = base, base + 4, base + 8
+        if kind == 1:
+            s.amax_history, s.head = base + 64, base + 64 + 4 * H
+        return s
+    two = (L.ScalingStateC * 2)
+    assert lib.fp8lin_scale_many(two(state(0x30000), state(0x30000)), 2, None) == L.EINVAL
+    a, b = state(0x30000, kind=1, H=16), state(0x31000)
+    b.scale = 0x30000 + 64 + 4 * 15                    # inside a's ring
+    assert lib.fp8lin_scale_many(two(a, b), 2, None) == L.EINVAL
+    a, b = state(0x30000), state(0x31000)
+    b.inv_scale = 0x30000                              # written over a's amax
+    assert lib.fp8lin_scale_many(two(a, b), 2, None) == L.EINVAL
+    a, b = state(0x30000, kind=1, H=4), state(0x31000, kind=1, H=4)
+    b.head = 0x30000 + 64 + 4 * 4                      # a's head
+    assert lib.fp8lin_scale_many(two(a, b), 2, None) == L.EINVAL
 
 
 def test_gemm_describe_argument_errors(lib):

@@ -119,6 +119,25 @@ def test_scale_many_matches_the_oracle_state_by_state():
             assert dev_f32_bits(st.inv_scale) == f32_bits(inv), (step, f, k, h)
 
 
+def test_scale_many_states_may_share_an_amax():
+    """Two states reading one amax (the update only reads it) are accepted
+    and each gets its own format's scale; a state given twice is refused
+    before anything is enqueued."""
+    a, b = q.ScalingState(E4M3, q.DYNAMIC), q.ScalingState(E5M2, q.DELAYED, history_len=4)
+    b.amax = a.amax
+    a.amax.fill_(3.0)
+    q.scale_many([a, b])
+    for st, fmt in ((a, E4M3), (b, E5M2)):
+        s, inv = oracle.scale_dynamic(3.0, fmt)   # (a delayed ring of one amax: the same)
+        assert dev_f32_bits(st.scale) == f32_bits(s)
+        assert dev_f32_bits(st.inv_scale) == f32_bits(inv)
+    before = a.scale.clone()
+    with pytest.raises(RuntimeError):
+        q.scale_many([a, a])
+    torch.cuda.synchronize()
+    assert torch.equal(a.scale, before)
+
+
 @pytest.mark.parametrize("fmt", [E4M3, E5M2])
 @pytest.mark.parametrize("trans", [False, True])
 @pytest.mark.parametrize("shape", SHAPES)
