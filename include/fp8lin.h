@@ -254,8 +254,14 @@ fp8lin_status fp8lin_cast(const void* x, int64_t rows, int64_t cols, int64_t ld,
 /* Dynamic scaling in one call: amax -> scale -> cast (+ transpose) with
  * st->amax_algo (ATOMIC, REDUCTION, SINGLE_PASS or AUTO); writes *st->amax,
  * *st->scale, *st->inv_scale, out and (if not NULL) out_t.  st->kind must
- * be FP8LIN_DYNAMIC.  SINGLE_PASS returns FP8LIN_EUNSUPPORTED (nothing
- * enqueued) for tensors above fp8lin_single_pass_max_elems(). */
+ * be FP8LIN_DYNAMIC.  ws is the caller's workspace (fp8lin_workspace_bytes
+ * of any shape): REDUCTION's partial maxima and the single pass's barrier
+ * words live there.  SINGLE_PASS returns FP8LIN_EUNSUPPORTED (nothing
+ * enqueued) for tensors above fp8lin_single_pass_max_elems().  Source:
+ * "Integrate float8nocompile ..." (torchtitan PR 778), Summary (tensorwise
+ * dynamic scaling with hand-written conversion kernels) and "Benchmarking
+ * single linear layer forward+backward performance" (the ATOMIC_MAX and
+ * REDUCTION amax algorithms). */
 fp8lin_status fp8lin_cast_dynamic(const void* x, int64_t rows, int64_t cols, int64_t ld,
                                   const fp8lin_scaling_state* st, uint8_t* out,
                                   uint8_t* out_t, void* ws, cudaStream_t stream);
