@@ -44,6 +44,47 @@ def test_linear_dynamic_full_compare(mkn, algo):
     _check_full(lin, x, w, dy, sx, sw, sd)
 
 
+def _paired_cast_shapes(n, seed=47):
+    """Seeded shapes whose forward casts x with W in one launch: more than 32
+    tokens, W above the one-cluster cast and within the single pass (in
+    128 x 128 tiles), x at most one tile for each CTA of W's launch (the
+    smaller of W's tile count and 152); sizes multiples of 16, mostly ragged."""
+    g = np.random.default_rng(seed)
+    tiles = lambda r, c: -(-r // 128) * -(-c // 128)  # noqa: E731
+    out = []
+    while len(out) < n:
+        M, K, N = (int(v) * 16 for v in (g.integers(3, 38), g.integers(1, 129), g.integers(1, 257)))
+        if (M > 32 and N * K >= 1 << 20 and tiles(N, K) <= 152 * 7
+                and tiles(M, K) <= min(tiles(N, K), 152)):
+            out.append((M, K, N))
+    return out
+
+
+@pytest.mark.parametrize("mkn", _paired_cast_shapes(8))
+def test_paired_forward_cast_random_shapes(mkn):
+    """The paired single pass (W's tiles in shared memory, x's one tile per
+    CTA in registers, both maxima at one grid barrier) on random ragged
+    shapes: the forward is two launches, and every fp8 byte, scale and GEMM
+    output matches the oracle."""
+    M, K, N = mkn
+    x, w, dy = si.linear_inputs(M, K, N, w_init="uniform64", outlier_frac=1e-3, seed=M + K + N)
+    lin = q.Fp8Linear(M, K, N)
+    torch.cuda.synchronize()
+    n0 = q.launch_count()
+    lin.forward(to_dev_bf16(x), to_dev_bf16(w))
+    torch.cuda.synchronize()
+    assert q.launch_count() - n0 == 2, mkn
+    lin.backward(to_dev_bf16(dy))
+    q.check(lin.ws)
+    sx, invx = oracle.scale_dynamic(oracle.amax(x), E4M3)
+    sw, invw = oracle.scale_dynamic(oracle.amax(w), E4M3)
+    sd, _ = oracle.scale_dynamic(oracle.amax(dy), E5M2)
+    for st, s, inv in ((lin.sx, sx, invx), (lin.sw, sw, invw)):
+        assert dev_f32_bits(st.scale) == f32_bits(s) and dev_f32_bits(st.inv_scale) == f32_bits(inv)
+    assert dev_f32_bits(lin.sdy.scale) == f32_bits(sd)
+    _check_full(lin, x, w, dy, sx, sw, sd)
+
+
 @pytest.mark.parametrize("mkn", [(16, 272, 208), (32, 784, 1040), (16, 16, 16), (32, 4096, 4096),
                                  (16, 2048, 6144)])
 @pytest.mark.parametrize("given_amax", [False, True])
