@@ -7,7 +7,8 @@ and dW the same bits wherever the separate launch runs whole tiles (no K
 split: the same accumulation order).  The grouped launch also delivers
 max |dX| from its epilogue; with both amaxes asked for, the two GEMMs run as
 two launches.  The shapes cover one round, several rounds with the long
-tiles' pairs taking d short ones, and ragged edges."""
+tiles' pairs taking d short ones, and ragged edges, plus three seeded random
+ones."""
 import os
 import subprocess
 import sys
@@ -23,6 +24,10 @@ pytestmark = pytest.mark.gpu
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SHAPES = [(4096, 2048, 1024), (2064, 1552, 784), (1040, 784, 2000), (3008, 1200, 4992)]
+# and three seeded random ones, every size a multiple of 16 above 128 (both
+# products on 256-wide pair tiles), mostly ragged
+_g = np.random.default_rng(53)
+SHAPES += [tuple(int(v) * 16 for v in _g.integers(9, 200, 3)) for _ in range(3)]
 
 CHILD = r"""
 import sys, numpy as np, torch
