@@ -85,6 +85,43 @@ def test_paired_forward_cast_random_shapes(mkn):
     _check_full(lin, x, w, dy, sx, sw, sd)
 
 
+def _few_token_shapes(n, seed=59):
+    """Seeded shapes of the few-token fused products: 16 or 32 tokens, K and N
+    multiples of 16 up to 4096 with the weight in at most 152 x 7 tiles."""
+    g = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        M, K, N = int(g.choice([16, 32])), int(g.integers(1, 257)) * 16, int(g.integers(1, 257)) * 16
+        if -(-K // 128) * -(-N // 128) <= 152 * 7:
+            out.append((M, K, N))
+    return out
+
+
+@pytest.mark.parametrize("mkn", _few_token_shapes(4))
+def test_few_token_fused_random_shapes(mkn):
+    """The two fused few-token products on random ragged shapes: one launch
+    each way, every fp8 byte and scale exact, y, dX and dW within the bound."""
+    M, K, N = mkn
+    x, w, dy = si.linear_inputs(M, K, N, w_init="uniform64", outlier_frac=1e-2, seed=M * K + N)
+    lin = q.Fp8Linear(M, K, N)
+    launches = []
+    for call in (lambda: lin.forward(to_dev_bf16(x), to_dev_bf16(w)),
+                 lambda: lin.backward(to_dev_bf16(dy))):
+        torch.cuda.synchronize()
+        n0 = q.launch_count()
+        call()
+        torch.cuda.synchronize()
+        launches.append(q.launch_count() - n0)
+    q.check(lin.ws)
+    assert launches == [1, 1], (mkn, launches)
+    sx, _ = oracle.scale_dynamic(oracle.amax(x), E4M3)
+    sw, _ = oracle.scale_dynamic(oracle.amax(w), E4M3)
+    sd, _ = oracle.scale_dynamic(oracle.amax(dy), E5M2)
+    for st, s in ((lin.sx, sx), (lin.sw, sw), (lin.sdy, sd)):
+        assert dev_f32_bits(st.scale) == f32_bits(s)
+    _check_full(lin, x, w, dy, sx, sw, sd)
+
+
 @pytest.mark.parametrize("mkn", [(16, 272, 208), (32, 784, 1040), (16, 16, 16), (32, 4096, 4096),
                                  (16, 2048, 6144)])
 @pytest.mark.parametrize("given_amax", [False, True])
