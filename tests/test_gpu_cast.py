@@ -196,6 +196,42 @@ def test_cast_dynamic_all_algorithms(fmt, algo, shape, ws):
     assert np.array_equal(out_t.cpu().numpy(), qtr)
 
 
+def _random_cast_shapes(n, seed=61):
+    """Seeded [rows, cols], multiples of 16 up to 8192 each, within the single
+    pass's capacity (at most 152 x 7 tiles of 128 x 128): small ones go to the
+    one-cluster kernel, the rest to the cooperative one; mostly ragged."""
+    g = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        hi = 33 if len(out) % 2 == 0 else 513   # every other shape at most 512 x 512
+        r, c = (int(v) * 16 for v in g.integers(1, hi, 2))
+        if -(-r // 128) * -(-c // 128) <= 152 * 7:
+            out.append((r, c))
+    return out
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+@pytest.mark.parametrize("algo", [q.AMAX_ATOMIC, q.AMAX_REDUCTION, q.AMAX_SINGLE_PASS, q.AMAX_AUTO])
+@pytest.mark.parametrize("shape", _random_cast_shapes(6))
+def test_cast_dynamic_random_shapes(fmt, algo, shape, ws):
+    """Every amax algorithm of the dynamic cast on random ragged shapes: amax,
+    scale, inverse and every byte of q and q^T as the oracle has them."""
+    x = _tensor(shape, seed=shape[0] + 3 * shape[1])
+    a = oracle.amax(x)
+    s, inv = oracle.scale_dynamic(a, fmt)
+    qr, qtr, _ = oracle.cast(x, s, fmt, transpose=True)
+    st = q.ScalingState(fmt, q.DYNAMIC, amax_algo=algo)
+    out = torch.empty(shape, dtype=torch.uint8, device="cuda")
+    out_t = torch.empty(shape[::-1], dtype=torch.uint8, device="cuda")
+    q.cast_dynamic(to_dev_bf16(x), st, out, out_t, ws)
+    q.check(ws)
+    assert dev_f32_bits(st.amax) == f32_bits(a)
+    assert dev_f32_bits(st.scale) == f32_bits(s)
+    assert dev_f32_bits(st.inv_scale) == f32_bits(inv)
+    assert np.array_equal(out.cpu().numpy(), qr)
+    assert np.array_equal(out_t.cpu().numpy(), qtr)
+
+
 def test_single_pass_capacity_and_refusal(ws):
     cap = q.single_pass_max_elems()
     assert cap >= 4096 * 4096, cap             # holds a 4096 x 4096 weight
