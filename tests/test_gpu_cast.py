@@ -232,6 +232,30 @@ def test_cast_dynamic_random_shapes(fmt, algo, shape, ws):
     assert np.array_equal(out_t.cpu().numpy(), qtr)
 
 
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+@pytest.mark.parametrize("shape", _random_cast_shapes(6, seed=67))
+def test_cast_delayed_random_shapes(fmt, shape, ws):
+    """Delayed scaling's one-read cast on random ragged shapes: the first call
+    takes its scale from its own amax (amax init), the second keeps the stored
+    scale; every byte of q and q^T and the recorded amax as the oracle has
+    them."""
+    x0 = _tensor(shape, seed=shape[0] + shape[1])
+    x1 = si.normal_bf16(shape, 3.0, shape[0] * 7 + shape[1], 1)   # a larger spread: saturates
+    st = q.ScalingState(fmt, q.DELAYED, history_len=4)
+    out = torch.empty(shape, dtype=torch.uint8, device="cuda")
+    out_t = torch.empty(shape[::-1], dtype=torch.uint8, device="cuda")
+    s0, _ = oracle.scale_dynamic(oracle.amax(x0), fmt)
+    for xh in (x0, x1):
+        q.cast_delayed(to_dev_bf16(xh), st, out, out_t, ws)
+        q.check(ws)
+        assert st.needs_init == 0
+        assert dev_f32_bits(st.scale) == f32_bits(s0)
+        assert dev_f32_bits(st.amax) == f32_bits(oracle.amax(xh))
+        qr, qtr, _ = oracle.cast(xh, s0, fmt, transpose=True)
+        assert np.array_equal(out.cpu().numpy(), qr)
+        assert np.array_equal(out_t.cpu().numpy(), qtr)
+
+
 def test_single_pass_capacity_and_refusal(ws):
     cap = q.single_pass_max_elems()
     assert cap >= 4096 * 4096, cap             # holds a 4096 x 4096 weight
