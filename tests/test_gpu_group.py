@@ -23,7 +23,8 @@ from helpers import assert_within_bound
 pytestmark = pytest.mark.gpu
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-SHAPES = [(4096, 2048, 1024), (2064, 1552, 784), (1040, 784, 2000), (3008, 1200, 4992)]
+SHAPES = [(4096, 2048, 1024), (2064, 1552, 784), (1040, 784, 2000), (3008, 1200, 4992),
+          (2064, 2064, 1552)]  # the last: 144 tiles of 13 and 17 K blocks, four epilogue warps
 # and three seeded random ones, every size a multiple of 16 above 128 (both
 # products on 256-wide pair tiles), mostly ragged
 _g = np.random.default_rng(53)
